@@ -1,0 +1,174 @@
+"""fp64 CPU oracle (test infrastructure) for index-selection sparse attention.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+reference legs of ``bench.py`` may import this package.  It wraps the plain C
+library ``oracle.c`` (compiled here with gcc, ``-ffp-contract=off``) through
+ctypes and shares no code with the CUDA path.
+
+Functions take a :class:`workloads.Case`-like object (or explicit arrays) and
+return NumPy arrays:
+
+* :func:`index_scores` -- ``S[t, s]`` for every causal ``s <= q_pos[t]`` (NaN
+  beyond), the indexer score of the lightweight indexer (Ascend CANN page
+  §2.1 "Core Pipeline Operator Fusion").
+* :func:`indexer_topk` -- ``idx[t, :K]`` in (score desc, position asc) order,
+  ``-1`` padded, plus ``{S_(K), S_(K+1)}`` per row (Day-0 accelerator page
+  §3.1 "Integration of the Index Selection Operator").
+* :func:`sparse_attn` -- fp64 ``out[t, h, :d_v]``, ``lse[t, h]`` and the sum of
+  the softmax weights, over the rows ``idx`` selects (lightweight indexer page
+  §1, "sparse flash attention").
+
+Parity pins for every function live in ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+MODES = {"f32": 0, "bf16": 1, "bf16_kfp8": 2}
+
+
+class ODims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("mode", "B", "max_blocks", "num_blocks", "block_size", "H_I", "d_I", "H", "d", "d_v", "K")]
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` (next to the source)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                               "-Wall", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _bind(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def _bind(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    P = ctypes.c_void_p
+    lib.oracle_bf16_to_f64.restype = ctypes.c_double
+    lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+    lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_index_scores.restype = ctypes.c_int
+    lib.oracle_index_scores.argtypes = [ctypes.POINTER(ODims), P, P, P, P, P, P, P, P, ctypes.c_int,
+                                        ctypes.c_int64, P, ctypes.c_int]
+    lib.oracle_indexer_topk.restype = ctypes.c_int
+    lib.oracle_indexer_topk.argtypes = [ctypes.POINTER(ODims), P, P, P, P, P, P, P, P, ctypes.c_int, P, P,
+                                        ctypes.c_int]
+    lib.oracle_sparse_attn.restype = ctypes.c_int
+    lib.oracle_sparse_attn.argtypes = [ctypes.POINTER(ODims), P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_double, P, P, P, ctypes.c_int]
+    return lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def dims_of(case, K=None) -> ODims:
+    s = case.spec
+    return ODims(MODES[s.mode], s.B, case.max_blocks, case.num_blocks, s.block_size, s.H_I, s.d_I, s.H, s.d,
+                 s.d_v, s.K if K is None else K)
+
+
+def bf16_to_f64(bits: int) -> float:
+    return _load().oracle_bf16_to_f64(int(bits))
+
+
+def e4m3_to_f64(code: int) -> float:
+    return _load().oracle_e4m3_to_f64(int(code))
+
+
+def _rows(case, rows):
+    """Query-side arrays restricted to the query rows ``rows`` (all rows if None)."""
+    if rows is None:
+        return case.q_I, case.w, case.q, case.q_seq, case.q_pos
+    rows = np.asarray(rows, dtype=np.int64)
+    return case.q_I[rows], case.w[rows], case.q[rows], case.q_seq[rows], case.q_pos[rows]
+
+
+def index_scores(case, rows=None, threads=None) -> np.ndarray:
+    """fp64 indexer scores ``S[r, s]`` for the query rows ``rows`` (NaN where s > q_pos)."""
+    lib = _load()
+    q_I, w, _, q_seq, q_pos = _rows(case, rows)
+    T = len(q_seq)
+    stride = int(q_pos.max()) + 1 if T else 1
+    S = np.full((T, stride), np.nan, dtype=np.float64)
+    D = dims_of(case)
+    kdt = {"f32": np.float32, "bf16": np.uint16, "bf16_kfp8": np.uint8}[case.spec.mode]
+    adt = np.float32 if case.spec.mode == "f32" else np.uint16
+    rc = lib.oracle_index_scores(ctypes.byref(D), _ptr(_c(q_I, adt)), _ptr(_c(w, np.float32)),
+                                 _ptr(_c(case.k_I, kdt)), _ptr(_c(case.k_I_scale, np.float32)),
+                                 _ptr(_c(case.block_table, np.int32)), _ptr(_c(case.seq_lens, np.int32)),
+                                 _ptr(_c(q_seq, np.int32)), _ptr(_c(q_pos, np.int32)), T, stride, _ptr(S),
+                                 threads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle_index_scores failed: {rc}")
+    return S
+
+
+def indexer_topk(case, rows=None, K=None, threads=None):
+    """(idx[r, K] int32 in (score desc, pos asc) order, kth[r, 2] = {S_(K), S_(K+1)})."""
+    lib = _load()
+    q_I, w, _, q_seq, q_pos = _rows(case, rows)
+    T = len(q_seq)
+    D = dims_of(case, K)
+    idx = np.full((T, D.K), -1, dtype=np.int32)
+    kth = np.full((T, 2), np.nan, dtype=np.float64)
+    kdt = {"f32": np.float32, "bf16": np.uint16, "bf16_kfp8": np.uint8}[case.spec.mode]
+    adt = np.float32 if case.spec.mode == "f32" else np.uint16
+    keep = [_c(q_I, adt), _c(w, np.float32), _c(case.k_I, kdt), _c(case.k_I_scale, np.float32),
+            _c(case.block_table, np.int32), _c(case.seq_lens, np.int32), _c(q_seq, np.int32), _c(q_pos, np.int32)]
+    rc = lib.oracle_indexer_topk(ctypes.byref(D), *[_ptr(a) for a in keep], T, _ptr(idx), _ptr(kth),
+                                 threads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle_indexer_topk failed: {rc}")
+    return idx, kth
+
+
+def sparse_attn(case, idx, rows=None, sm_scale=None, threads=None):
+    """(out[r, H, d_v] f64, lse[r, H] f64, psum[r, H] f64) over the positions in ``idx[r]``."""
+    lib = _load()
+    _, _, q, q_seq, _ = _rows(case, rows)
+    T = len(q_seq)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    assert idx.shape[0] == T
+    s = case.spec
+    D = dims_of(case)
+    out = np.zeros((T, s.H, s.d_v), dtype=np.float64)
+    lse = np.zeros((T, s.H), dtype=np.float64)
+    psum = np.zeros((T, s.H), dtype=np.float64)
+    adt = np.float32 if s.mode == "f32" else np.uint16
+    keep = [_c(q, adt), _c(case.kv, adt), _c(case.block_table, np.int32), _c(case.seq_lens, np.int32),
+            _c(q_seq, np.int32)]
+    rc = lib.oracle_sparse_attn(ctypes.byref(D), *[_ptr(a) for a in keep], _ptr(idx), idx.shape[1], T,
+                                s.sm_scale if sm_scale is None else float(sm_scale), _ptr(out), _ptr(lse),
+                                _ptr(psum), threads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle_sparse_attn failed: {rc}")
+    return out, lse, psum

@@ -1,0 +1,66 @@
+"""The oracle's pins have teeth: plausible mistakes planted in a copy of the
+oracle (compiled on the CPU into a temporary library) must each fail at least
+one pin from test_oracle_pins.py.  Nothing here touches a GPU."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = open(oracle._SRC).read()
+
+MUTANTS = {
+    "drop_head_weight": ("total += (double)C->w[(size_t)t * D->H_I + j] * relu;", "total += relu;"),
+    "relu_wrong_side": ("double relu = dot > 0.0 ? dot : 0.0;", "double relu = dot < 0.0 ? -dot : 0.0;"),
+    "no_relu": ("double relu = dot > 0.0 ? dot : 0.0;", "double relu = dot;"),
+    "ties_to_higher": ("return (x->pos > y->pos) - (x->pos < y->pos);", "return (x->pos < y->pos) - (x->pos > y->pos);"),
+    "ignore_block_table": ("return (int64_t)blk * D->block_size + s % D->block_size;",
+                           "return (int64_t)b * D->max_blocks * D->block_size + s;"),
+    "transposed_query": ("dot += q[(size_t)j * D->d_I + e] * k[e];", "dot += q[(size_t)e * D->H_I + j] * k[e];"),
+    "e4m3_bias_8": ("else v = ldexp(1.0 + (double)m / 8.0, e - 7);", "else v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "e4m3_no_subnormal": ("if (e == 0) v = ldexp((double)m, -9);", "if (e == 0) v = ldexp(1.0 + (double)m / 8.0, -7);"),
+    "no_block_scale": ("double scale = (D->mode == 2) ? (double)C->k_I_scale[blk] : 1.0;", "double scale = 1.0;"),
+    "not_causal_inclusive": ("if (s1 > pos + 1) s1 = pos + 1;", "if (s1 > pos) s1 = pos;"),
+    "drop_sm_scale": ("z[i] = C->sm_scale * dot;", "z[i] = dot;"),
+    "value_width_d_v": ("o[c] += p * rows[(size_t)i * D->d + c];", "o[c] += p * rows[(size_t)i * D->d_v + c];"),
+    "no_max_shift": ("for (int i = 0; i < n; ++i) { z[i] = exp(z[i] - m); l += z[i]; }",
+                     "for (int i = 0; i < n; ++i) { z[i] = exp(z[i]); l += z[i]; }"),
+    "kth_off_by_one": ("C->kth[2 * t + 0] = (K - 1 < n) ? a[K - 1].s : NAN;", "C->kth[2 * t + 0] = (K < n) ? a[K].s : NAN;"),
+}
+
+PIN_TESTS = [
+    pins.test_e4m3_decoder_all_codes_vs_torch,
+    pins.test_hand_example_indexer,
+    pins.test_hand_example_attention,
+    lambda: [pins.test_topk_matches_brute_force(*p) for p in pins.TINY],
+    pins.test_prefill_rows_are_causal,
+    pins.test_exact_ties_go_to_lower_position,
+    lambda: [pins.test_attention_full_selection_equals_dense_sdpa(m) for m in ("f32", "bf16")],
+    pins.test_attention_zero_query_is_mean_of_values,
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    assert SRC.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    src = tmp_path / "mutant.c"
+    src.write_text(SRC.replace(old, new))
+    lib_path = str(tmp_path / "libmutant.so")
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread", "-o",
+                           lib_path, str(src), "-lm"])
+    saved = oracle._lib
+    oracle._lib = oracle._bind(ctypes.CDLL(lib_path))
+    caught = []
+    try:
+        for fn in PIN_TESTS:
+            try:
+                fn()
+            except (AssertionError, RuntimeError, ValueError):
+                caught.append(getattr(fn, "__name__", "lambda"))
+    finally:
+        oracle._lib = saved
+    assert caught, f"no pin caught mutant {name}"
