@@ -1,0 +1,411 @@
+"""Benchmark of the decode step of index-selection sparse attention (indexer + Top-K + sparse
+attention over a paged KV cache) on GB300, through the library's C ABI.
+
+Default workload: decode, bf16, batch 32, context lengths uniform in [16384, 32768], 64 indexer
+heads of 128, Top-K 2048, 128 query heads over a 576-wide latent cache (V = first 512 columns),
+64-token blocks, shuffled block table. One step = one dsa_decode call on a batch resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own batch (weak scaling, no collective on the data path);
+timing is bracketed by a barrier + synchronize and the maximum over ranks is reported.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "decode indexer+sparse-attn µs/step & HBM GB/s (%roofline); prefill tokens/s"
+WORKLOAD = ("decode_bf16_b32: batch 32, context U{16384..32768}, indexer 64x128 bf16, Top-K 2048, "
+            "128 heads x 576 latent (V = 512 cols), 64-token blocks, shuffled block table")
+L2_FLUSH_BYTES = 256 << 20
+PROFILE = os.path.join(ROOT, "profiles", "indexer_tc_decode_bf16_b32.md")
+
+
+# ------------------------------------------------------------------------------------------------
+# algorithmic traffic of one decode step (the method's own bytes: every causal key once, the
+# selected rows once, queries, weights, block-table entries, indices and outputs)
+# ------------------------------------------------------------------------------------------------
+
+def indexer_bytes(case) -> int:
+    s = case.spec
+    key_b = {"f32": 4, "bf16": 2, "bf16_kfp8": 1}[s.mode] * s.d_I
+    L = case.seq_lens.astype(np.int64)
+    blocks = (L + 63) // 64
+    b = int(L.sum()) * key_b
+    if s.mode == "bf16_kfp8":
+        b += int(blocks.sum()) * 4
+    act = 4 if s.mode == "f32" else 2
+    b += s.T * s.H_I * s.d_I * act + s.T * s.H_I * 4           # q_I, w
+    b += int(blocks.sum()) * 4 + s.B * 4                        # block-table entries, seq_lens
+    b += s.T * s.K * 4                                          # idx written
+    return b
+
+
+def attn_bytes(case) -> int:
+    s = case.spec
+    act = 4 if s.mode == "f32" else 2
+    n_sel = int(np.minimum(case.seq_lens.astype(np.int64), s.K).sum())
+    b = n_sel * s.d * act                                       # gathered rows
+    b += s.T * s.K * 4 + n_sel * 4                              # idx read + table entries
+    b += s.T * s.H * s.d * act + s.T * s.H * s.d_v * act        # q, out
+    b += s.T * s.H * 4                                          # lse
+    return b
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    for f in ("indexer_tc.cu", "common.cuh", "ptx.cuh"):
+        h.update(open(os.path.join(ROOT, "indexer_top_sparse_paged_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per indexer launch from the committed ncu summary, if it is for this kernel source."""
+    if not os.path.exists(PROFILE):
+        return None
+    vals = {}
+    for line in open(PROFILE):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_digest") != kernel_digest():
+        return None
+    try:
+        return int(vals["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------------------------------------
+# clock sampling during the timed region
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,utilization.gpu,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm, smax, util = float(r[0]), float(r[1]), float(r[2])
+            except ValueError:
+                continue
+            mx = smax
+            if util > 0:
+                mhz.append(sm)
+            for n, v in zip(names, r[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples_under_load": len(mhz)}
+
+
+# ------------------------------------------------------------------------------------------------
+# our implementation
+# ------------------------------------------------------------------------------------------------
+
+def to_dev(a, dev):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
+
+
+def run_ours(args, rank, world):
+    import indexer_top_sparse_paged_gb300 as dsa
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    spec, seed = W.named(2)
+    case = W.generate(spec, seed + 1000 * rank)
+    s = case.spec
+    dims = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K)
+    q_I, w, k_I = to_dev(case.q_I, dev), to_dev(case.w, dev), to_dev(case.k_I, dev)
+    q, kv = to_dev(case.q, dev), to_dev(case.kv, dev)
+    bt, sl = to_dev(case.block_table, dev), to_dev(case.seq_lens, dev)
+    ws = dsa.workspace(dims, s.T, dev)
+    idx = torch.empty((s.T, s.K), dtype=torch.int32, device=dev)
+    out = torch.empty((s.T, s.H, s.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((s.T, s.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        dsa.decode(dims, q_I, w, k_I, None, bt, sl, q, kv, s.sm_scale, ws=ws, idx=idx, out=out, lse=lse)
+        return dsa.last_launch_count()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if dsa.read_error(ws) != 0:
+        raise RuntimeError("device fault bits set during warm-up")
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    t_burst = time.time()
+    while time.time() - t_burst < 0.6:   # load the GPU so the sampler sees clocks under load
+        for _ in range(20):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize(dev)
+
+    # --- timed region: K steps, L2 flushed before each, CUDA events on the launching stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches = 0
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        launches += step()
+        ev[i][1].record(stream)
+    barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # --- per-stage breakdown (same work, split into its two ABI calls) for the roofline
+    ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev3[i][0].record(stream)
+        dsa.indexer_topk(dims, q_I, w, k_I, None, bt, sl, ws=ws, idx=idx)
+        ev3[i][1].record(stream)
+        dsa.sparse_attn(dims, q, kv, bt, sl, idx, s.sm_scale, ws=ws, out=out, lse=lse)
+        ev3[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    idx_ms = [a.elapsed_time(b) for a, b, _ in ev3]
+    att_ms = [b.elapsed_time(c) for _, b, c in ev3]
+
+    # --- end to end through the public API with host buffers (pinned), copies inside the region
+    h_in = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v)).pin_memory()
+            for k, v in (("q_I", case.q_I), ("w", case.w), ("q", case.q), ("bt", case.block_table),
+                         ("sl", case.seq_lens))}
+    h_out = torch.empty((s.T, s.H, s.d_v), dtype=torch.bfloat16).pin_memory()
+    h_idx = torch.empty((s.T, s.K), dtype=torch.int32).pin_memory()
+    d_in = {"q_I": q_I.view(torch.int16), "w": w, "q": q.view(torch.int16), "bt": bt, "sl": sl}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = h_out.numel() * 2 + h_idx.numel() * 4
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        for k in h_in:
+            d_in[k].copy_(h_in[k], non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_idx.copy_(idx, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    barrier()
+    e2e_ms = [a.elapsed_time(b) for a, b in e2e_ev]
+
+    if dsa.read_error(ws) != 0:
+        raise RuntimeError("device fault bits set during the timed region")
+
+    total_ms = sum(step_ms)
+    e2e_total = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_total], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, e2e_total = float(t[0]), float(t[1])
+
+    ib, ab = indexer_bytes(case), attn_bytes(case)
+    step_bytes = ib + ab
+    ms_per_step = total_ms / args.steps
+    value = step_bytes * world * args.steps / (total_ms * 1e-3) / 1e9
+    e2e_value = step_bytes * world * args.steps / (e2e_total * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    idx_avg = statistics.mean(idx_ms)
+    achieved = ib / (idx_avg * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "hbm_frac_of_" + peak_kind: round(value / world / peak, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) values, U(0,1) head weights, shuffled block table)",
+        "config": {"workload": WORKLOAD, "global_batch": s.B * world, "seq_len": "16384..32768",
+                   "parallelism": f"replicas x{world}", "l2": "flushed (256 MiB write) before every timed step",
+                   "step_bytes": step_bytes, "indexer_bytes": ib, "attention_bytes": ab},
+        "breakdown_us": {"indexer_topk": round(idx_avg * 1e3, 2), "sparse_attn": round(statistics.mean(att_ms) * 1e3, 2)},
+        "roofline": {"kernel": "dsa_indexer_topk (plan + indexer_tc_kernel + topk_merge)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                     "algorithmic_bytes_per_launch": ib},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_total / args.steps, 5)},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(case)
+    return res
+
+
+# ------------------------------------------------------------------------------------------------
+# oracle (CPU) baseline
+# ------------------------------------------------------------------------------------------------
+
+def sample_case(case, n_seq: int):
+    """The first n_seq sequences of a decode case (a bounded sample of the same workload)."""
+    sub = W.Case(case.spec, case.seed, case.block_table[:n_seq], case.seq_lens[:n_seq], case.q_seq[:n_seq],
+                 case.q_pos[:n_seq], case.q_I[:n_seq], case.w[:n_seq], case.k_I, case.k_I_scale, case.q[:n_seq],
+                 case.kv)
+    sub.spec = W.Spec(case.spec.name, case.spec.mode, list(case.spec.seq_lens[:n_seq]), [1] * n_seq,
+                      case.spec.H_I, case.spec.d_I, case.spec.H, case.spec.d, case.spec.d_v, case.spec.K)
+    return sub
+
+
+def time_oracle(sub, threads: int) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    idx, _ = oracle.indexer_topk(sub, threads=threads)
+    oracle.sparse_attn(sub, idx, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(case, n_seq: int = 4):
+    threads = os.cpu_count() or 1
+    sub = sample_case(case, n_seq)
+    dt = time_oracle(sub, threads)
+    b = indexer_bytes(sub) + attn_bytes(sub)
+    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_seq} of the 32 decode sequences (indexer + Top-K + attention, fp64), {dt:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    spec, seed = W.named(2)
+    case = W.generate(spec, seed)
+    threads = os.cpu_count() or 1
+    sub = sample_case(case, 2)
+    for _ in range(max(0, min(args.warmup, 1))):
+        time_oracle(sub, threads)
+    times = [time_oracle(sub, threads) for _ in range(args.steps)]
+    b = indexer_bytes(sub) + attn_bytes(sub)
+    total = sum(times)
+    value = b * args.steps / total / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) values, U(0,1) head weights, shuffled block table)",
+        "config": {"workload": WORKLOAD, "global_batch": s_b(case), "seq_len": "16384..32768",
+                   "parallelism": "cpu oracle, rank 0 only"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "2 of the 32 decode sequences per step (indexer + Top-K + attention, fp64)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def s_b(case):
+    return case.spec.B
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) index-selection sparse attention library (libdsa.so).
+ *
+ * The operation (one query row t of sequence b = q_seq[t] at absolute position pos = q_pos[t]):
+ *
+ *   paged fetch   logical position s of sequence b is physical cache row
+ *                 block_table[b][s / 64] * 64 + s % 64
+ *                 ("Engineering Path for Day-0 Adaptation ... on Domestic AI Accelerators" §3.2:
+ *                 fixed-size blocks, an index maps to block number and in-block offset)
+ *   indexer       S[t,s] = sum_j w[t,j] * max(0, q_I[t,j,:] . k_I[s,:])   for s in [0, pos]
+ *                 with k_I[s,:] = e4m3 code * block scale for FP8 indexer keys
+ *                 ("Day0 Inference Support ... on Huawei Ascend CANN Architecture" §2.1: relevance
+ *                 scoring, head-weight weighting and Top-K selection fused over the paged cache; §3:
+ *                 FP8 quantized indexer data; formula fixed by the problem statement)
+ *   Top-K         the K largest S[t,s], ties to the lower s; fewer than K positions -> all of them
+ *                 ("Engineering Path ..." §3.1: index selection is scoring plus Top-K filtering and
+ *                 yields a discrete index set)
+ *   attention     z_i = sm_scale * q[t,h,:] . row_i ; out[t,h,:] = sum_i softmax(z)_i * row_i[0:d_v]
+ *                 over the rows row_i = kv_cache[phys(idx[t][i])] of one shared latent cache
+ *                 ("Day0 Inference Support ..." §1: a sparse flash attention module reads the KV
+ *                 pairs at the selected positions; V is the first d_v columns of the same row)
+ *
+ * Conventions for every entry point:
+ *  - All tensor arguments are DEVICE pointers owned by the caller, row-major and densely packed
+ *    in the shapes given below. Inputs are only read; idx / out / lse / ws are written.
+ *  - The library allocates, frees and synchronises nothing (except dsa_read_error, which says so).
+ *    All work is enqueued on `stream` (NULL = the legacy default stream) in launch order.
+ *  - A return value other than DSA_OK means nothing was launched, except DSA_ERR_LAUNCH, which
+ *    means a launch failed part way (the stream then holds a partial result).
+ *  - Faults the host cannot see (a block-table entry outside [0, num_blocks), an idx entry outside
+ *    [0, seq_len) other than -1, a pipeline wait that timed out) set bits of an error word in the
+ *    workspace; the offending rows are skipped (read as zeros) and dsa_read_error reports them.
+ *  - The workspace `ws` (>= dsa_workspace_size bytes, 256-byte aligned) is scratch owned by one
+ *    call at a time: calls that share a workspace must be ordered on one stream.
+ *  - No shared mutable state besides a per-thread launch counter: calls on different streams with
+ *    distinct workspaces may run concurrently.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1, /* null pointer, inconsistent sizes, misaligned pointer */
+    DSA_ERR_UNSUPPORTED = 2, /* shape or mode outside the compiled set (see dsa_dims) */
+    DSA_ERR_WORKSPACE = 3,   /* ws == NULL or ws_bytes < dsa_workspace_size(...) */
+    DSA_ERR_LAUNCH = 4,      /* a CUDA launch or tensor-map encode failed */
+    DSA_ERR_DEVICE = 5,      /* dsa_read_error found a device-side fault bit (see DSA_FAULT_*) */
+    DSA_ERR_TIMEOUT = 6      /* dsa_read_error found a pipeline wait that gave up */
+} dsa_status;
+
+/* bits of the device error word */
+#define DSA_FAULT_BLOCK_TABLE 0x1 /* block_table entry outside [0, num_blocks) */
+#define DSA_FAULT_INDEX 0x2       /* idx entry outside [0, seq_len) and not -1 */
+#define DSA_FAULT_TIMEOUT 0x4     /* a bounded wait inside a kernel expired */
+
+typedef enum {
+    DSA_F32 = 0,       /* q_I, k_I, q, kv, out: fp32 */
+    DSA_BF16 = 1,      /* q_I, k_I, q, kv, out: bf16 */
+    DSA_BF16_KFP8 = 2  /* as DSA_BF16, but k_I is OCP e4m3 with one fp32 scale per 64-token block */
+} dsa_mode;
+
+/*
+ * Problem dimensions.
+ *   block_size must be 64 (tokens per physical cache block).
+ *   DSA_F32:              H_I <= 64, d_I <= 256, d_I % 4 == 0, H <= 128, d <= 1024, d % 4 == 0, d_v <= d
+ *   DSA_BF16 / _KFP8:     indexer (H_I, d_I) == (64, 128) [tensor cores] or H_I <= 64, d_I <= 256, d_I % 8 == 0;
+ *                         attention (H, d, d_v) == (128, 576, 512) [tensor cores] or H <= 128, d <= 1024,
+ *                         d % 8 == 0, d_v <= d, d_v % 8 == 0
+ *   1 <= K <= 2048.
+ */
+typedef struct {
+    int32_t mode;       /* dsa_mode */
+    int32_t B;          /* number of sequences (rows of block_table, entries of seq_lens) */
+    int32_t max_blocks; /* block_table row length */
+    int32_t num_blocks; /* physical blocks in k_I_cache and kv_cache */
+    int32_t block_size; /* 64 */
+    int32_t H_I, d_I;   /* indexer heads, indexer head dim */
+    int32_t H, d, d_v;  /* attention heads, latent row width, value width (V = row[0:d_v]) */
+    int32_t K;          /* Top-K */
+} dsa_dims;
+
+/* Clears the error word of a freshly allocated workspace (enqueued on `stream`). Call once after
+ * allocating `ws`; dsa_read_error clears it again after each read. */
+dsa_status dsa_workspace_init(void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* Bytes of workspace needed by any of the calls below for T query rows with these dims on the
+ * current device. T > B means some sequence has several query rows (prefill) and includes the
+ * prefill score buffer. Returns 0 for invalid dims. */
+size_t dsa_workspace_size(const dsa_dims* dims, int32_t T);
+
+/*
+ * Indexer + Top-K ("lightning indexer": scores -> top_k_indices).
+ *   q_I        [T][H_I][d_I]        fp32 or bf16 (per mode)
+ *   w          [T][H_I]             fp32 head weights (any sign)
+ *   k_I_cache  [num_blocks][64][d_I] fp32 / bf16 / e4m3 codes (per mode)
+ *   k_I_scale  [num_blocks]         fp32 per-block scale; required for DSA_BF16_KFP8, else ignored
+ *   block_table[B][max_blocks]      int32 physical block ids (entries past a sequence's end unread)
+ *   seq_lens   [B]                  int32 cached positions per sequence, new tokens included
+ *   q_seq      [T]                  int32 sequence of each query row; NULL means row t is sequence t (T == B)
+ *   q_pos      [T]                  int32 absolute position of each query row (< seq_len of its
+ *                                   sequence); NULL means decode: q_pos[t] = seq_lens[q_seq[t]] - 1
+ *   idx        [T][K]               int32 out: the selected logical positions of each row in
+ *                                   ascending order, then -1 for the slots past min(K, pos + 1)
+ * Decode-shaped calls (each sequence has at most one query row) stream the keys once with the
+ * Top-K fused (no score tensor leaves the chip); calls with several rows per sequence (prefill)
+ * score each tile of queries x keys on tensor cores into the workspace, then select per row.
+ */
+dsa_status dsa_indexer_topk(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+                            const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                            const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx, void* ws,
+                            size_t ws_bytes, dsa_stream_t stream);
+
+/*
+ * Sparse attention over the positions idx selects ("sparse flash attention").
+ *   q          [T][H][d]            fp32 or bf16
+ *   kv_cache   [num_blocks][64][d]  fp32 or bf16 shared latent rows (K = row, V = row[0:d_v])
+ *   idx        [T][K]               int32 logical positions, -1 = empty slot (any order)
+ *   sm_scale   softmax scale (usually 1/sqrt(d))
+ *   out        [T][H][d_v]          fp32 (DSA_F32) or bf16 out
+ *   lse        [T][H]               fp32 natural-log sum of exp of the logits, or NULL; rows with no
+ *                                   valid index give out = 0 and lse = -inf
+ */
+dsa_status dsa_sparse_attn(const dsa_dims* dims, const void* q, const void* kv_cache, const int32_t* block_table,
+                           const int32_t* seq_lens, const int32_t* q_seq, const int32_t* idx, int32_t T,
+                           float sm_scale, void* out, float* lse, void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/*
+ * Fused decode step: one query row per sequence (T = B, q_seq = NULL, q_pos = NULL), the indexer +
+ * Top-K followed by sparse attention on one stream. idx may be NULL (the indices then live in the
+ * workspace only). Arguments as in dsa_indexer_topk / dsa_sparse_attn.
+ */
+dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+                      const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens, const void* q,
+                      const void* kv_cache, float sm_scale, int32_t* idx, void* out, float* lse, void* ws,
+                      size_t ws_bytes, dsa_stream_t stream);
+
+/* Synchronises `stream`, copies the device error word of `ws` to *fault_bits (may be NULL) and
+ * clears it. Returns DSA_OK when no bit was set, DSA_ERR_TIMEOUT when DSA_FAULT_TIMEOUT was set,
+ * DSA_ERR_DEVICE for any other bit, DSA_ERR_LAUNCH if the copy failed. */
+dsa_status dsa_read_error(void* ws, int32_t* fault_bits, dsa_stream_t stream);
+
+/* Number of kernels the last successful call on this thread launched (0 before any call). */
+int32_t dsa_last_launch_count(void);
+
+/* Static string for a status code. */
+const char* dsa_status_string(dsa_status status);
+
+/* ABI version (major * 100 + minor). */
+int32_t dsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H */

@@ -1,0 +1,163 @@
+"""Index-selection sparse attention over a paged KV cache on GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``libdsa.so`` (C ABI in ``include/dsa.h``). It only marshals
+arguments: torch tensors are passed as device pointers together with the current CUDA stream,
+and every step of the computation runs in the library's kernels. There is no fallback: if the
+library is missing or fails to load, :func:`lib` raises.
+
+Entry points (same names as the C ABI):
+
+* :func:`indexer_topk` -- lightning indexer + Top-K: ``idx[T][K]`` of the selected positions.
+* :func:`sparse_attn` -- sparse attention over the rows ``idx`` selects.
+* :func:`decode` -- both, fused on one stream, for one query row per sequence.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa.so")
+_lib = None
+
+MODES = {"f32": 0, "bf16": 1, "bf16_kfp8": 2}
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "launch", 5: "device fault",
+          6: "timeout"}
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("mode", "B", "max_blocks", "num_blocks", "block_size", "H_I", "d_I", "H", "d", "d_v", "K")]
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {lib().dsa_status_string(status).decode()} (status {status})")
+
+
+def lib():
+    """The loaded libdsa.so (built by ``__graft_entry__.build()``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m indexer_top_sparse_paged_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        D = ctypes.POINTER(Dims)
+        L.dsa_workspace_size.restype = SZ
+        L.dsa_workspace_size.argtypes = [D, I32]
+        L.dsa_workspace_init.restype = ctypes.c_int
+        L.dsa_workspace_init.argtypes = [P, SZ, P]
+        L.dsa_indexer_topk.restype = ctypes.c_int
+        L.dsa_indexer_topk.argtypes = [D, P, P, P, P, P, P, P, P, I32, P, P, SZ, P]
+        L.dsa_sparse_attn.restype = ctypes.c_int
+        L.dsa_sparse_attn.argtypes = [D, P, P, P, P, P, P, I32, ctypes.c_float, P, P, P, SZ, P]
+        L.dsa_decode.restype = ctypes.c_int
+        L.dsa_decode.argtypes = [D, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, SZ, P]
+        L.dsa_read_error.restype = ctypes.c_int
+        L.dsa_read_error.argtypes = [P, ctypes.POINTER(I32), P]
+        L.dsa_last_launch_count.restype = I32
+        L.dsa_last_launch_count.argtypes = []
+        L.dsa_status_string.restype = ctypes.c_char_p
+        L.dsa_status_string.argtypes = [ctypes.c_int]
+        L.dsa_version.restype = I32
+        L.dsa_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def make_dims(mode: str, B: int, max_blocks: int, num_blocks: int, H_I: int, d_I: int, H: int, d: int, d_v: int,
+              K: int, block_size: int = 64) -> Dims:
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    return Dims(m, B, max_blocks, num_blocks, block_size, H_I, d_I, H, d, d_v, K)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise DsaError(fn, status)
+
+
+def workspace_size(dims: Dims, T: int) -> int:
+    return int(lib().dsa_workspace_size(ctypes.byref(dims), T))
+
+
+def workspace(dims: Dims, T: int, device="cuda", stream=None) -> torch.Tensor:
+    """Allocates (with torch) and initialises a workspace for calls with T query rows."""
+    n = workspace_size(dims, T)
+    if n == 0:
+        raise ValueError("invalid dims")
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off: off + n]
+    _check("dsa_workspace_init", lib().dsa_workspace_init(_p(ws), n, _stream(stream)))
+    return ws
+
+
+def indexer_topk(dims: Dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, q_seq=None, q_pos=None, *, ws,
+                 idx=None, stream=None) -> torch.Tensor:
+    """idx[T][K] int32: the Top-K causal positions of every query row (ascending, -1 padded)."""
+    T = q_I.shape[0]
+    if idx is None:
+        idx = torch.empty((T, dims.K), dtype=torch.int32, device=q_I.device)
+    st = lib().dsa_indexer_topk(ctypes.byref(dims), _p(q_I), _p(w), _p(k_I_cache), _p(k_I_scale), _p(block_table),
+                                _p(seq_lens), _p(q_seq), _p(q_pos), T, _p(idx), _p(ws), ws.numel(), _stream(stream))
+    _check("dsa_indexer_topk", st)
+    return idx
+
+
+def sparse_attn(dims: Dims, q, kv_cache, block_table, seq_lens, idx, sm_scale: float, q_seq=None, *, ws, out=None,
+                lse=None, stream=None):
+    """(out[T][H][d_v], lse[T][H]) of softmax attention over the rows idx selects."""
+    T = q.shape[0]
+    odt = torch.float32 if dims.mode == MODES["f32"] else torch.bfloat16
+    if out is None:
+        out = torch.empty((T, dims.H, dims.d_v), dtype=odt, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, dims.H), dtype=torch.float32, device=q.device)
+    st = lib().dsa_sparse_attn(ctypes.byref(dims), _p(q), _p(kv_cache), _p(block_table), _p(seq_lens), _p(q_seq),
+                               _p(idx), T, float(sm_scale), _p(out), _p(lse), _p(ws), ws.numel(), _stream(stream))
+    _check("dsa_sparse_attn", st)
+    return out, lse
+
+
+def decode(dims: Dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, q, kv_cache, sm_scale: float, *, ws,
+           idx=None, out=None, lse=None, want_idx: bool = True, stream=None):
+    """Fused decode step (one query row per sequence): (idx or None, out, lse)."""
+    T = dims.B
+    odt = torch.float32 if dims.mode == MODES["f32"] else torch.bfloat16
+    if idx is None and want_idx:
+        idx = torch.empty((T, dims.K), dtype=torch.int32, device=q.device)
+    if out is None:
+        out = torch.empty((T, dims.H, dims.d_v), dtype=odt, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, dims.H), dtype=torch.float32, device=q.device)
+    st = lib().dsa_decode(ctypes.byref(dims), _p(q_I), _p(w), _p(k_I_cache), _p(k_I_scale), _p(block_table),
+                          _p(seq_lens), _p(q), _p(kv_cache), float(sm_scale), _p(idx), _p(out), _p(lse), _p(ws),
+                          ws.numel(), _stream(stream))
+    _check("dsa_decode", st)
+    return idx, out, lse
+
+
+def read_error(ws, stream=None) -> int:
+    """Synchronises the stream and returns (then clears) the device fault bits of ``ws``."""
+    bits = ctypes.c_int32(0)
+    st = lib().dsa_read_error(_p(ws), ctypes.byref(bits), _stream(stream))
+    if st not in (0, 5, 6):
+        raise DsaError("dsa_read_error", st)
+    return int(bits.value)
+
+
+def last_launch_count() -> int:
+    return int(lib().dsa_last_launch_count())

@@ -1,0 +1,136 @@
+// Sparse attention on CUDA cores for small head shapes (the fp32 workload: 8 heads of 128). One
+// CTA per (query row, head): the selected positions are mapped through the block table once, the
+// logits z_i = sm_scale * q . row_i are reduced per warp (each warp reads whole 16-byte-coalesced
+// rows), then p = softmax(z) and out = sum_i p_i * row_i[0:d_v] with one thread per output column
+// ("Day0 Inference Support ... on Huawei Ascend CANN Architecture" §1 and §2.1: the sparse
+// attention reads the main KV exactly at the selected indices).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace dsa {
+
+constexpr int kAttnSimtThreads = 256;
+
+__device__ __forceinline__ float act_f(const void* p, int64_t i, bool bf16) {
+    return bf16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(p)[i]) << 16)
+                : static_cast<const float*>(p)[i];
+}
+
+__device__ __forceinline__ uint16_t to_bf16_rn(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+template <bool BF16>
+__global__ void __launch_bounds__(kAttnSimtThreads) attn_simt_kernel(AttnArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int d = a.d, K = a.K;
+    float* q_s = reinterpret_cast<float*>(smem);  // [d]
+    float* z_s = q_s + d;                          // [K]
+    int64_t* row_s = reinterpret_cast<int64_t*>(
+        (reinterpret_cast<uintptr_t>(z_s + K) + 7) & ~static_cast<uintptr_t>(7));  // [K] physical rows
+    __shared__ float red[kAttnSimtThreads / 32];
+    __shared__ float m_s, l_s;
+
+    const int h = blockIdx.x, t = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = a.q_seq ? a.q_seq[t] : t;
+    const bool seq_ok = b >= 0 && b < a.B;
+    const int L = seq_ok ? a.seq_lens[b] : 0;
+
+    for (int e = tid; e < d; e += kAttnSimtThreads)
+        q_s[e] = act_f(a.q, (static_cast<int64_t>(t) * a.H + h) * d + e, BF16);
+    for (int i = tid; i < K; i += kAttnSimtThreads) {
+        const int s = a.idx[static_cast<int64_t>(t) * K + i];
+        int64_t r = -1;
+        if (s != -1) {
+            if (s < 0 || s >= L) {
+                atomicOr(a.err, DSA_FAULT_INDEX);
+            } else {
+                const int blk = a.block_table[static_cast<int64_t>(b) * a.max_blocks + (s >> 6)];
+                if (blk < 0 || blk >= a.num_blocks) atomicOr(a.err, DSA_FAULT_BLOCK_TABLE);
+                else r = static_cast<int64_t>(blk) * kBlock + (s & 63);
+            }
+        }
+        row_s[i] = r;
+    }
+    __syncthreads();
+
+    // logits: one warp per selected row
+    for (int i = warp; i < K; i += kAttnSimtThreads / 32) {
+        const int64_t r = row_s[i];
+        float dot = 0.0f;
+        if (r >= 0) {
+            for (int e = lane; e < d; e += 32) dot = fmaf(q_s[e], act_f(a.kv, r * d + e, BF16), dot);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
+        }
+        if (lane == 0) z_s[i] = (r >= 0) ? dot * a.sm_scale : -INFINITY;
+    }
+    __syncthreads();
+
+    float m = -INFINITY;
+    for (int i = tid; i < K; i += kAttnSimtThreads) m = fmaxf(m, z_s[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (tid == 0) {
+        float mm = -INFINITY;
+        for (int w = 0; w < kAttnSimtThreads / 32; ++w) mm = fmaxf(mm, red[w]);
+        m_s = mm;
+    }
+    __syncthreads();
+    m = m_s;
+    float l = 0.0f;
+    for (int i = tid; i < K; i += kAttnSimtThreads) {
+        const float p = (z_s[i] == -INFINITY) ? 0.0f : expf(z_s[i] - m);
+        z_s[i] = p;
+        l += p;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = l;
+    __syncthreads();
+    if (tid == 0) {
+        float ll = 0.0f;
+        for (int w = 0; w < kAttnSimtThreads / 32; ++w) ll += red[w];
+        l_s = ll;
+    }
+    __syncthreads();
+    l = l_s;
+    const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+
+    const int64_t obase = (static_cast<int64_t>(t) * a.H + h) * a.d_v;
+    for (int c = tid; c < a.d_v; c += kAttnSimtThreads) {
+        float acc = 0.0f;
+        for (int i = 0; i < K; ++i) {
+            const int64_t r = row_s[i];
+            if (r >= 0) acc = fmaf(z_s[i], act_f(a.kv, r * d + c, BF16), acc);
+        }
+        const float o = acc * inv;
+        if (BF16) static_cast<uint16_t*>(a.out)[obase + c] = to_bf16_rn(o);
+        else static_cast<float*>(a.out)[obase + c] = o;
+    }
+    if (tid == 0 && a.lse) a.lse[static_cast<int64_t>(t) * a.H + h] = (l > 0.0f) ? m + logf(l) : -INFINITY;
+}
+
+bool launch_attn_simt(const AttnArgs& a, cudaStream_t s, int* launches) {
+    if (a.T == 0) return true;
+    const size_t smem = static_cast<size_t>(a.d + a.K) * 4 + 8 + static_cast<size_t>(a.K) * 8;
+    dim3 grid(a.H, a.T);
+    if (a.mode == DSA_F32) {
+        if (cudaFuncSetAttribute(attn_simt_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return false;
+        attn_simt_kernel<false><<<grid, kAttnSimtThreads, smem, s>>>(a);
+    } else {
+        if (cudaFuncSetAttribute(attn_simt_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return false;
+        attn_simt_kernel<true><<<grid, kAttnSimtThreads, smem, s>>>(a);
+    }
+    ++*launches;
+    return cudaGetLastError() == cudaSuccess;
+}
+
+}  // namespace dsa

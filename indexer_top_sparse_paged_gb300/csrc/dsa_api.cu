@@ -1,0 +1,331 @@
+// Host side of the C ABI (include/dsa.h): argument checks, workspace layout, kernel selection and
+// launch order. Nothing here allocates, frees or synchronises (dsa_read_error excepted).
+//
+// Kernel selection follows the shape of the call ("Adapting GPU Software Stacks ..." §3.3:
+// separate implementations per path, chosen at run time from batch size and sequence length):
+// tensor-core kernels for the 64x128 indexer and the 128-head x 576 latent attention, CUDA-core
+// kernels for small shapes (the fp32 workload).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace dsa {
+
+static thread_local int g_last_launches = 0;
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+bool indexer_uses_tc(const dsa_dims& d) { return d.mode == DSA_BF16 && d.H_I == 64 && d.d_I == 128; }
+
+bool attn_uses_tc(const dsa_dims& d) {
+    return (d.mode == DSA_BF16 || d.mode == DSA_BF16_KFP8) && d.H == 128 && d.d == 576 && d.d_v == 512;
+}
+
+int indexer_ctas(const dsa_dims& d) {
+    const int sms = device_sm_count();
+    const int G = indexer_uses_tc(d) ? sms : 2 * sms;
+    return G < kMaxIndexerCtas ? G : kMaxIndexerCtas;
+}
+
+int attn_splits(const dsa_dims& d, int T) {
+    if (!attn_uses_tc(d) || T <= 0) return 1;
+    const int sms = device_sm_count();
+    int S = sms / (2 * T);
+    int smax = d.K / 64;
+    if (smax > kMaxSplits) smax = kMaxSplits;
+    if (S > smax) S = smax;
+    return S < 1 ? 1 : S;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+WsLayout ws_layout(const dsa_dims& d, int T) {
+    WsLayout w{};
+    w.G = indexer_ctas(d);
+    w.S = attn_splits(d, T);
+    size_t off = 0;
+    w.err = off;
+    off += 256;
+    w.tile_prefix = off;
+    off = align256(off + sizeof(int32_t) * (static_cast<size_t>(T) + 1));
+    w.slot_count = off;
+    off = align256(off + sizeof(int32_t) * (static_cast<size_t>(w.G) + T));
+    w.slots = off;
+    off = align256(off + sizeof(uint64_t) * (static_cast<size_t>(w.G) + T) * d.K);
+    w.idx = off;
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(T) * d.K);
+    w.part_o = off;
+    if (w.S > 1) off = align256(off + sizeof(float) * static_cast<size_t>(T) * w.S * d.H * d.d_v);
+    w.part_ml = off;
+    if (w.S > 1) off = align256(off + sizeof(float) * static_cast<size_t>(T) * w.S * d.H * 2);
+    w.scores = off;
+    w.total = off;
+    return w;
+}
+
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+static EncodeTiled encode_fn() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t cols, uint64_t rows,
+                  uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiled fn = encode_fn();
+    if (!fn || rows == 0) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------------------------------------
+// argument checks
+// ------------------------------------------------------------------------------------------------
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static dsa_status check_common(const dsa_dims* d) {
+    if (!d) return DSA_ERR_INVALID_ARG;
+    if (d->mode < DSA_F32 || d->mode > DSA_BF16_KFP8) return DSA_ERR_UNSUPPORTED;
+    if (d->block_size != kBlock) return DSA_ERR_UNSUPPORTED;
+    if (d->B <= 0 || d->max_blocks <= 0 || d->num_blocks <= 0) return DSA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(d->num_blocks) * kBlock >= (1ll << 31)) return DSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(d->max_blocks) * kBlock >= (1ll << 31)) return DSA_ERR_UNSUPPORTED;
+    if (d->K <= 0 || d->K > 2048) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+static dsa_status check_indexer_dims(const dsa_dims* d) {
+    dsa_status st = check_common(d);
+    if (st != DSA_OK) return st;
+    if (d->H_I <= 0 || d->d_I <= 0) return DSA_ERR_INVALID_ARG;
+    if (indexer_uses_tc(*d)) return DSA_OK;
+    if (d->H_I > 64 || d->d_I > 256) return DSA_ERR_UNSUPPORTED;
+    const int unit = d->mode == DSA_F32 ? 4 : (d->mode == DSA_BF16 ? 8 : 16);
+    if (d->d_I % unit) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+static dsa_status check_attn_dims(const dsa_dims* d) {
+    dsa_status st = check_common(d);
+    if (st != DSA_OK) return st;
+    if (d->H <= 0 || d->d <= 0 || d->d_v <= 0 || d->d_v > d->d) return DSA_ERR_INVALID_ARG;
+    if (attn_uses_tc(*d)) return DSA_OK;
+    if (d->H > 128 || d->d > 1024) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+static dsa_status check_ws(const dsa_dims* d, int T, void* ws, size_t ws_bytes) {
+    if (!ws) return DSA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return DSA_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(*d, T).total) return DSA_ERR_WORKSPACE;
+    return DSA_OK;
+}
+
+static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w, const void* k_I_cache,
+                              const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                              const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx, void* ws,
+                              cudaStream_t stream, int* launches) {
+    const WsLayout L = ws_layout(*d, T);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    IndexerArgs a{};
+    a.mode = d->mode;
+    a.B = d->B;
+    a.max_blocks = d->max_blocks;
+    a.num_blocks = d->num_blocks;
+    a.H_I = d->H_I;
+    a.d_I = d->d_I;
+    a.K = d->K;
+    a.T = T;
+    a.q_I = q_I;
+    a.w = w;
+    a.k_I = k_I_cache;
+    a.k_I_scale = k_I_scale;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.q_seq = q_seq;
+    a.q_pos = q_pos;
+    a.tile_prefix = reinterpret_cast<int32_t*>(base + L.tile_prefix);
+    a.slot_count = reinterpret_cast<int32_t*>(base + L.slot_count);
+    a.slots = reinterpret_cast<uint64_t*>(base + L.slots);
+    a.idx = idx;
+    a.err = reinterpret_cast<int*>(base + L.err);
+    a.G = L.G;
+    if (!launch_plan(a, stream, launches)) return DSA_ERR_LAUNCH;
+    const bool ok = indexer_uses_tc(*d) ? launch_indexer_tc(a, stream, launches) : launch_indexer_simt(a, stream, launches);
+    if (!ok) return DSA_ERR_LAUNCH;
+    if (!launch_merge(a, stream, launches)) return DSA_ERR_LAUNCH;
+    return DSA_OK;
+}
+
+static dsa_status run_attn(const dsa_dims* d, const void* q, const void* kv_cache, const int32_t* block_table,
+                           const int32_t* seq_lens, const int32_t* q_seq, const int32_t* idx, int32_t T,
+                           float sm_scale, void* out, float* lse, void* ws, cudaStream_t stream, int* launches) {
+    const WsLayout L = ws_layout(*d, T);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    AttnArgs a{};
+    a.mode = d->mode;
+    a.B = d->B;
+    a.max_blocks = d->max_blocks;
+    a.num_blocks = d->num_blocks;
+    a.H = d->H;
+    a.d = d->d;
+    a.d_v = d->d_v;
+    a.K = d->K;
+    a.T = T;
+    a.sm_scale = sm_scale;
+    a.q = q;
+    a.kv = kv_cache;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.q_seq = q_seq;
+    a.idx = idx;
+    a.out = out;
+    a.lse = lse;
+    a.part_o = reinterpret_cast<float*>(base + L.part_o);
+    a.part_ml = reinterpret_cast<float*>(base + L.part_ml);
+    a.S = L.S;
+    a.err = reinterpret_cast<int*>(base + L.err);
+    const bool ok = attn_uses_tc(*d) ? launch_attn_tc(a, stream, launches) : launch_attn_simt(a, stream, launches);
+    return ok ? DSA_OK : DSA_ERR_LAUNCH;
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+size_t dsa_workspace_size(const dsa_dims* dims, int32_t T) {
+    if (!dims || T < 0 || check_common(dims) != DSA_OK) return 0;
+    return ws_layout(*dims, T).total;
+}
+
+dsa_status dsa_workspace_init(void* ws, size_t ws_bytes, dsa_stream_t stream) {
+    if (!ws || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DSA_ERR_WORKSPACE;
+    return cudaMemsetAsync(ws, 0, 256, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? DSA_OK
+                                                                                              : DSA_ERR_LAUNCH;
+}
+
+dsa_status dsa_indexer_topk(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+                            const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                            const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx, void* ws,
+                            size_t ws_bytes, dsa_stream_t stream) {
+    dsa_status st = check_indexer_dims(dims);
+    if (st != DSA_OK) return st;
+    if (T < 0) return DSA_ERR_INVALID_ARG;
+    if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
+    if (T > 0 && (!q_I || !w || !k_I_cache || !block_table || !seq_lens || !idx)) return DSA_ERR_INVALID_ARG;
+    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_I) || !aligned16(w) || !aligned16(k_I_cache)) return DSA_ERR_INVALID_ARG;
+    st = check_ws(dims, T, ws, ws_bytes);
+    if (st != DSA_OK) return st;
+    int launches = 0;
+    if (T > 0)
+        st = run_indexer(dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, q_seq, q_pos, T, idx, ws,
+                         reinterpret_cast<cudaStream_t>(stream), &launches);
+    g_last_launches = launches;
+    return st;
+}
+
+dsa_status dsa_sparse_attn(const dsa_dims* dims, const void* q, const void* kv_cache, const int32_t* block_table,
+                           const int32_t* seq_lens, const int32_t* q_seq, const int32_t* idx, int32_t T,
+                           float sm_scale, void* out, float* lse, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+    dsa_status st = check_attn_dims(dims);
+    if (st != DSA_OK) return st;
+    if (T < 0) return DSA_ERR_INVALID_ARG;
+    if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !kv_cache || !block_table || !seq_lens || !idx || !out)) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+    st = check_ws(dims, T, ws, ws_bytes);
+    if (st != DSA_OK) return st;
+    int launches = 0;
+    if (T > 0)
+        st = run_attn(dims, q, kv_cache, block_table, seq_lens, q_seq, idx, T, sm_scale, out, lse, ws,
+                      reinterpret_cast<cudaStream_t>(stream), &launches);
+    g_last_launches = launches;
+    return st;
+}
+
+dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+                      const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens, const void* q,
+                      const void* kv_cache, float sm_scale, int32_t* idx, void* out, float* lse, void* ws,
+                      size_t ws_bytes, dsa_stream_t stream) {
+    dsa_status st = check_indexer_dims(dims);
+    if (st != DSA_OK) return st;
+    st = check_attn_dims(dims);
+    if (st != DSA_OK) return st;
+    const int T = dims->B;
+    if (!q_I || !w || !k_I_cache || !block_table || !seq_lens || !q || !kv_cache || !out) return DSA_ERR_INVALID_ARG;
+    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_I) || !aligned16(w) || !aligned16(k_I_cache) || !aligned16(q) || !aligned16(kv_cache) ||
+        !aligned16(out))
+        return DSA_ERR_INVALID_ARG;
+    st = check_ws(dims, T, ws, ws_bytes);
+    if (st != DSA_OK) return st;
+    const WsLayout L = ws_layout(*dims, T);
+    int32_t* idx_buf = idx ? idx : reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + L.idx);
+    int launches = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = run_indexer(dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, nullptr, nullptr, T, idx_buf, ws, s,
+                     &launches);
+    if (st == DSA_OK)
+        st = run_attn(dims, q, kv_cache, block_table, seq_lens, nullptr, idx_buf, T, sm_scale, out, lse, ws, s,
+                      &launches);
+    g_last_launches = launches;
+    return st;
+}
+
+dsa_status dsa_read_error(void* ws, int32_t* fault_bits, dsa_stream_t stream) {
+    if (!ws) return DSA_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DSA_ERR_LAUNCH;
+    if (cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_LAUNCH;
+    if (cudaMemset(ws, 0, sizeof v) != cudaSuccess) return DSA_ERR_LAUNCH;
+    if (fault_bits) *fault_bits = v;
+    if (v & DSA_FAULT_TIMEOUT) return DSA_ERR_TIMEOUT;
+    return v ? DSA_ERR_DEVICE : DSA_OK;
+}
+
+int32_t dsa_last_launch_count(void) { return g_last_launches; }
+
+const char* dsa_status_string(dsa_status status) {
+    switch (status) {
+        case DSA_OK: return "ok";
+        case DSA_ERR_INVALID_ARG: return "invalid argument";
+        case DSA_ERR_UNSUPPORTED: return "unsupported shape or mode";
+        case DSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case DSA_ERR_LAUNCH: return "kernel launch failed";
+        case DSA_ERR_DEVICE: return "device-side fault (bad block-table entry or index)";
+        case DSA_ERR_TIMEOUT: return "a pipeline wait inside a kernel timed out";
+    }
+    return "unknown status";
+}
+
+int32_t dsa_version(void) { return 100; }
+
+}  // extern "C"

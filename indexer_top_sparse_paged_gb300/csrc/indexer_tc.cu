@@ -1,0 +1,258 @@
+// Decode indexer + streaming Top-K on the 5th-generation tensor cores (tcgen05), for 64 indexer
+// heads of width 128 with bf16 keys.
+//
+// Per 128-key tile (two 64-token cache blocks fetched by TMA through the block table) the tile
+// is one M=128 x N=64 x K=128 contraction: A = the tile's keys (one key per row, K-major, 128-byte
+// swizzled), B = the query row's 64 heads (K-major), D = 128 x 64 fp32 in tensor memory. Each
+// epilogue thread owns one TMEM lane = one key, so the head-weighted ReLU sum
+//     S[s] = sum_j w_j * max(0, D[s, j])
+// runs in-thread with no shuffles, and the key goes straight into the CTA's Top-K buffer: no
+// score tensor is written to global memory ("Day0 Inference Support ... on Huawei Ascend CANN
+// Architecture" §2.1: scoring, head-weight weighting and Top-K fused in one operator reading the
+// paged cache; "Engineering Path for Day-0 Adaptation ..." §3.1: the scoring reuses a matrix
+// multiplication).
+//
+// Roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
+// warps 2..5 = epilogue (TMEM lane quarter = warp % 4). Pipelines: 4 smem stages of 32 KB,
+// 2 TMEM accumulators of 64 columns, 2 query buffers (one per segment in flight).
+#include "internal.h"
+
+namespace dsa {
+namespace tcidx {
+
+constexpr int kHeads = 64;
+constexpr int kDim = 128;
+constexpr int kStages = 4;
+constexpr int kHalfBytes = kTileKeys * 128;   // [128 keys x 64 bf16] = 16 KB
+constexpr int kStageBytes = 2 * kHalfBytes;   // both K halves = 32 KB
+constexpr int kQHalfBytes = kHeads * 128;     // [64 heads x 64 bf16] = 8 KB
+constexpr int kQBytes = 2 * kQHalfBytes;      // 16 KB
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kTmemCols = 128;
+constexpr uint32_t kIdesc = idesc_f16(128, kHeads, 1u, 0u, 0u);
+
+struct Smem {
+    uint64_t full[kStages], empty[kStages];
+    uint64_t qfull[2], qempty[2];
+    uint64_t tfull[2], tempty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    uint32_t hist[256];
+    TopkCtl ctl;
+};
+
+constexpr size_t kOffA = 0;
+constexpr size_t kOffQ = kOffA + static_cast<size_t>(kStages) * kStageBytes;
+constexpr size_t kOffBuf = kOffQ + 2 * kQBytes;
+
+__host__ __device__ constexpr uint32_t topk_cap(int K) { return static_cast<uint32_t>(2 * K + kEpiThreads); }
+
+__host__ __device__ constexpr size_t smem_bytes(int K) {
+    return 1024 /*alignment slack*/ + kOffBuf + static_cast<size_t>(topk_cap(K)) * 8 + sizeof(Smem) + 64;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_tc_kernel(IndexerArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sA = smem_u32(smem + kOffA);
+    const uint32_t sQ = smem_u32(smem + kOffQ);
+    uint64_t* buf = reinterpret_cast<uint64_t*>(smem + kOffBuf);
+    Smem& S = *reinterpret_cast<Smem*>(smem + kOffBuf + static_cast<size_t>(topk_cap(a.K)) * 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    volatile int* abort_flag = &S.abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(smem_u32(&S.full[i]), 1);
+            mbar_init(smem_u32(&S.empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&S.qfull[i]), 1);
+            mbar_init(smem_u32(&S.qempty[i]), 1);
+            mbar_init(smem_u32(&S.tfull[i]), 1);
+            mbar_init(smem_u32(&S.tempty[i]), kEpiThreads);
+        }
+        mbar_init(smem_u32(&S.mma_done), 1);
+        S.abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_k);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+
+    SegmentIter it;
+    it.init(a.tile_prefix, a.T, blockIdx.x, a.G);
+    Segment seg;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t sg = 0, n_it = 0;
+            bool ok = true;
+            while (ok && it.next(seg)) {
+                const int t = seg.row;
+                const int b = row_seq(a, t);
+                const int n = row_len(a, t);
+                const uint32_t qb = sg & 1u;
+                ok = mbar_wait(smem_u32(&S.qempty[qb]), ((sg >> 1) & 1u) ^ 1u, abort_flag, a.err);
+                if (!ok) break;
+                mbar_arrive_expect_tx(smem_u32(&S.qfull[qb]), kQBytes);
+                tma_load_2d(sQ + qb * kQBytes, &map_q, 0, t * kHeads, smem_u32(&S.qfull[qb]));
+                tma_load_2d(sQ + qb * kQBytes + kQHalfBytes, &map_q, 64, t * kHeads, smem_u32(&S.qfull[qb]));
+                for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
+                    const uint32_t st = n_it % kStages, use = n_it / kStages;
+                    ok = mbar_wait(smem_u32(&S.empty[st]), (use & 1u) ^ 1u, abort_flag, a.err);
+                    if (!ok) break;
+                    int blk[2];
+                    uint32_t bytes = 0;
+                    for (int p = 0; p < 2; ++p) {
+                        const int lb = 2 * j + p;
+                        blk[p] = (lb * kBlock < n) ? phys_block(a, b, lb) : -1;
+                        if (blk[p] >= 0) bytes += 2 * (kBlock * 128);
+                    }
+                    const uint32_t fb = smem_u32(&S.full[st]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    for (int p = 0; p < 2; ++p) {
+                        if (blk[p] < 0) continue;
+                        const uint32_t dst = sA + st * kStageBytes + p * (kBlock * 128);
+                        tma_load_2d(dst, &map_k, 0, blk[p] * kBlock, fb);
+                        tma_load_2d(dst + kHalfBytes, &map_k, 64, blk[p] * kBlock, fb);
+                    }
+                }
+                ++sg;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t sg = 0, n_it = 0;
+            bool ok = true;
+            while (ok && it.next(seg)) {
+                const uint32_t qb = sg & 1u;
+                ok = mbar_wait(smem_u32(&S.qfull[qb]), (sg >> 1) & 1u, abort_flag, a.err);
+                if (!ok) break;
+                for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
+                    const uint32_t st = n_it % kStages, use = n_it / kStages;
+                    const uint32_t acc = n_it & 1u, ause = n_it >> 1;
+                    ok = mbar_wait(smem_u32(&S.full[st]), use & 1u, abort_flag, a.err);
+                    if (!ok) break;
+                    ok = mbar_wait(smem_u32(&S.tempty[acc]), (ause & 1u) ^ 1u, abort_flag, a.err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t d = tmem + acc * kHeads;
+#pragma unroll
+                    for (int k = 0; k < kDim / 16; ++k) {
+                        const uint32_t half = k >> 2, kk = k & 3;
+                        const uint64_t ad = sw128_desc(sA + st * kStageBytes + half * kHalfBytes + kk * 32, 16, 1024);
+                        const uint64_t bd = sw128_desc(sQ + qb * kQBytes + half * kQHalfBytes + kk * 32, 16, 1024);
+                        mma_ss(d, ad, bd, kIdesc, k > 0 ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&S.empty[st]));
+                    tc_commit(smem_u32(&S.tfull[acc]));
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&S.qempty[qb]));
+                ++sg;
+            }
+            // every MMA issued so far must be complete before TMEM is released
+            tc_commit(smem_u32(&S.mma_done));
+            mbar_wait_drain(smem_u32(&S.mma_done), 0, a.err);
+        }
+    } else {
+        // ------------------------------------------------------------- epilogue + Top-K
+        const uint32_t etid = threadIdx.x - 64;        // 0..127
+        const uint32_t quarter = warp & 3;             // TMEM lane quarter of this warp
+        const uint32_t row = quarter * 32 + lane;      // key within the tile
+        TopkGroup<kEpiThreads> topk{buf, S.hist, &S.ctl, topk_cap(a.K), static_cast<uint32_t>(a.K), etid, 1};
+        uint32_t n_it = 0;
+        while (it.next(seg)) {
+            const int t = seg.row;
+            const int n = row_len(a, t);
+            float wv[kHeads];
+            const float4* w4 = reinterpret_cast<const float4*>(a.w + static_cast<int64_t>(t) * kHeads);
+#pragma unroll
+            for (int i = 0; i < kHeads / 4; ++i) {
+                const float4 v = w4[i];
+                wv[4 * i] = v.x;
+                wv[4 * i + 1] = v.y;
+                wv[4 * i + 2] = v.z;
+                wv[4 * i + 3] = v.w;
+            }
+            topk.reset();
+            bool ok = true;
+            for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
+                const uint32_t acc = n_it & 1u, ause = n_it >> 1;
+                const bool got = mbar_wait(smem_u32(&S.tfull[acc]), ause & 1u, abort_flag, a.err);
+                if (named_bar_or(1, kEpiThreads, !got)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t v0[32], v1[32];
+                const uint32_t taddr = tmem + acc * kHeads + ((quarter * 32) << 16);
+                tmem_ld32(taddr, v0);
+                tmem_ld32(taddr + 32, v1);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&S.tempty[acc]));
+                float score = 0.0f;
+#pragma unroll
+                for (int h = 0; h < 32; ++h) score = fmaf(wv[h], fmaxf(__uint_as_float(v0[h]), 0.0f), score);
+#pragma unroll
+                for (int h = 0; h < 32; ++h) score = fmaf(wv[32 + h], fmaxf(__uint_as_float(v1[h]), 0.0f), score);
+                const int s = j * kTileKeys + static_cast<int>(row);
+                bool valid = s < n;
+                if (valid) {
+                    // a tile block whose table entry was invalid was never loaded
+                    const int lb = s >> 6;
+                    const int blk = a.block_table[static_cast<int64_t>(row_seq(a, t)) * a.max_blocks + lb];
+                    valid = blk >= 0 && blk < a.num_blocks;
+                }
+                topk.push(make_key(score, static_cast<uint32_t>(s)), valid);
+            }
+            if (!ok) break;
+            const int64_t slot = static_cast<int64_t>(blockIdx.x) + t;
+            topk.flush(a.slots + slot * a.K, a.slot_count + slot);
+            topk.sync();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace tcidx
+
+bool launch_indexer_tc(const IndexerArgs& a, cudaStream_t s, int* launches) {
+    CUtensorMap map_q, map_k;
+    if (!make_tmap_2d(&map_q, a.q_I, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcidx::kDim,
+                      static_cast<uint64_t>(a.T) * tcidx::kHeads, tcidx::kDim * 2, 64, 64))
+        return false;
+    if (!make_tmap_2d(&map_k, a.k_I, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcidx::kDim,
+                      static_cast<uint64_t>(a.num_blocks) * kBlock, tcidx::kDim * 2, 64, 64))
+        return false;
+    const size_t smem = tcidx::smem_bytes(a.K);
+    if (cudaFuncSetAttribute(tcidx::indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return false;
+    tcidx::indexer_tc_kernel<<<a.G, tcidx::kThreads, smem, s>>>(a, map_q, map_k);
+    ++*launches;
+    return cudaGetLastError() == cudaSuccess;
+}
+
+size_t indexer_tc_smem(int K) { return tcidx::smem_bytes(K); }
+
+}  // namespace dsa

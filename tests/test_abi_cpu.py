@@ -1,0 +1,102 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol include/dsa.h declares, and
+rejects bad arguments on the host before any launch (no GPU needed: nothing here computes)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import indexer_top_sparse_paged_gb300 as dsa
+from indexer_top_sparse_paged_gb300.build import build_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_library()
+    return dsa.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for n in ("dsa_indexer_topk", "dsa_sparse_attn", "dsa_decode", "dsa_workspace_size", "dsa_read_error",
+              "dsa_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for n in declared_symbols():
+        assert hasattr(L, n), f"{n} declared in dsa.h but not exported"
+
+
+def test_status_strings_and_version(L):
+    for code in range(7):
+        assert L.dsa_status_string(code)
+    assert L.dsa_version() >= 100
+    assert L.dsa_last_launch_count() == 0
+
+
+def _dims(**kw):
+    d = dict(mode="bf16", B=2, max_blocks=4, num_blocks=8, H_I=64, d_I=128, H=128, d=576, d_v=512, K=256)
+    d.update(kw)
+    return dsa.make_dims(**d)
+
+
+def test_workspace_size_rejects_bad_dims(L):
+    assert L.dsa_workspace_size(None, 2) == 0
+    assert L.dsa_workspace_size(ctypes.byref(_dims(block_size=32)), 2) == 0
+    assert L.dsa_workspace_size(ctypes.byref(_dims(K=0)), 2) == 0
+    assert L.dsa_workspace_size(ctypes.byref(_dims(K=4096)), 2) == 0
+    assert L.dsa_workspace_size(ctypes.byref(_dims()), 2) > 0
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation first
+
+
+def test_indexer_rejects_null_and_unsupported(L):
+    d = _dims()
+    args = [FAKE] * 8
+    # null q_I
+    st = L.dsa_indexer_topk(ctypes.byref(d), None, *args[1:8], 2, FAKE, FAKE, 1 << 30, None)
+    assert st == 1
+    # unsupported block size and K
+    for bad in (_dims(block_size=16), _dims(K=3000), _dims(mode=7)):
+        assert L.dsa_indexer_topk(ctypes.byref(bad), *args, 2, FAKE, FAKE, 1 << 30, None) == 2
+    # unsupported small shape (d_I not a multiple of 8 in bf16)
+    assert L.dsa_indexer_topk(ctypes.byref(_dims(H_I=4, d_I=12)), *args, 2, FAKE, FAKE, 1 << 30, None) == 2
+    # FP8 keys need their scales
+    st = L.dsa_indexer_topk(ctypes.byref(_dims(mode="bf16_kfp8")), FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE,
+                            2, FAKE, FAKE, 1 << 30, None)
+    assert st == 1
+    # T != B without q_seq
+    assert L.dsa_indexer_topk(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 3, FAKE, FAKE,
+                              1 << 30, None) == 1
+    # misaligned pointer
+    assert L.dsa_indexer_topk(ctypes.byref(d), ctypes.c_void_p((1 << 20) + 4), *args[1:8], 2, FAKE, FAKE, 1 << 30,
+                              None) == 1
+    # missing / misaligned / small workspace
+    assert L.dsa_indexer_topk(ctypes.byref(d), *args, 2, FAKE, None, 1 << 30, None) == 3
+    assert L.dsa_indexer_topk(ctypes.byref(d), *args, 2, FAKE, ctypes.c_void_p((1 << 20) + 16), 1 << 30, None) == 3
+    assert L.dsa_indexer_topk(ctypes.byref(d), *args, 2, FAKE, FAKE, 100, None) == 3
+
+
+def test_attention_and_decode_reject_bad_args(L):
+    d = _dims()
+    st = L.dsa_sparse_attn(ctypes.byref(d), None, FAKE, FAKE, FAKE, FAKE, FAKE, 2, ctypes.c_float(0.04), FAKE, None,
+                           FAKE, 1 << 30, None)
+    assert st == 1
+    assert L.dsa_sparse_attn(ctypes.byref(_dims(d_v=600)), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2,
+                             ctypes.c_float(0.04), FAKE, None, FAKE, 1 << 30, None) == 1
+    st = L.dsa_decode(ctypes.byref(d), FAKE, FAKE, FAKE, None, FAKE, FAKE, None, FAKE, ctypes.c_float(0.04), None,
+                      FAKE, None, FAKE, 1 << 30, None)
+    assert st == 1
+    assert L.dsa_read_error(None, None, None) == 3
+    assert L.dsa_workspace_init(None, 256, None) == 3
