@@ -336,7 +336,7 @@ def time_oracle(sub, threads: int) -> float:
     return time.perf_counter() - t0
 
 
-def cpu_baseline(case, n_seq: int = 4):
+def cpu_baseline(case, n_seq: int = 32):
     threads = os.cpu_count() or 1
     sub = sample_case(case, n_seq)
     dt = time_oracle(sub, threads)
@@ -378,6 +378,25 @@ def run_reference(args, rank, world):
     }
 
 
+def run_profile(args):
+    """warmup + 1 decode steps of the default workload and nothing else (for ncu)."""
+    import indexer_top_sparse_paged_gb300 as dsa
+
+    dev = torch.device("cuda", 0)
+    spec, seed = W.named(2)
+    case = W.generate(spec, seed)
+    s = case.spec
+    dims = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K)
+    q_I, w, k_I = to_dev(case.q_I, dev), to_dev(case.w, dev), to_dev(case.k_I, dev)
+    q, kv = to_dev(case.q, dev), to_dev(case.kv, dev)
+    bt, sl = to_dev(case.block_table, dev), to_dev(case.seq_lens, dev)
+    ws = dsa.workspace(dims, s.T, dev)
+    for _ in range(args.warmup + 1):
+        dsa.decode(dims, q_I, w, k_I, None, bt, sl, q, kv, s.sm_scale, ws=ws)
+    torch.cuda.synchronize(dev)
+    assert dsa.read_error(ws) == 0
+
+
 def s_b(case):
     return case.spec.B
 
@@ -389,7 +408,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="only run --warmup + 1 decode steps (a short command for ncu captures)")
     args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

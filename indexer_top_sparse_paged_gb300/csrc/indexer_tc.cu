@@ -172,10 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------- epilogue + Top-K
-        const uint32_t etid = threadIdx.x - 64;        // 0..127
         const uint32_t quarter = warp & 3;             // TMEM lane quarter of this warp
         const uint32_t row = quarter * 32 + lane;      // key within the tile
-        TopkGroup<kEpiThreads> topk{buf, S.hist, &S.ctl, topk_cap(a.K), static_cast<uint32_t>(a.K), etid, 1};
+        // the group's thread index is the key row, so stable compaction keeps position order
+        TopkGroup<kEpiThreads> topk{buf, S.hist, &S.ctl, topk_cap(a.K), static_cast<uint32_t>(a.K), row, 1};
         uint32_t n_it = 0;
         while (it.next(seg)) {
             const int t = seg.row;

@@ -127,7 +127,7 @@ def test_duplicated_keys_break_ties_to_lower_position():
     bs = spec.block_size
     # one strong key copied to 400 random positions: exact ties, Top-K = its 256 lowest positions
     u = (case.w[0][:, None].astype(np.float64) * np_bf16(case.q_I[0])).sum(0)
-    strong = W.to_bf16_bits((3.0 * u / np.linalg.norm(u)).astype(np.float32))
+    strong = W.to_bf16_bits((40.0 * u / np.linalg.norm(u)).astype(np.float32))
     P = np.sort(rng.choice(1500, size=400, replace=False))
     for s in P:
         case.k_I[case.block_table[0, s // bs], s % bs] = strong
@@ -190,9 +190,7 @@ def test_bad_block_table_entry_is_reported_not_faulted():
     case.block_table[1, 3] = case.num_blocks + 5
     dev = Dev(case)
     idx = dev.indexer()
-    from indexer_top_sparse_paged_gb300 import read_error
-    bits = read_error(dev.ws)
-    assert bits & 0x1
+    assert dev.faults() & 0x1
     assert np.all(idx[0] >= -1)
 
 
