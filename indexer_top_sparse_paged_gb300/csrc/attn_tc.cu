@@ -38,14 +38,16 @@ constexpr int kKvChunkBytes = kRows * 128;              // [16 rows x 64 bf16]
 constexpr int kKvStageBytes = kChunks * kKvChunkBytes;  // 18 KB
 constexpr int kMaxRows = 2048;
 constexpr int kThreads = 288;
+constexpr int kNB = 4;          // S / P buffers (tiles the tensor core may run ahead of softmax)
+constexpr int kPrefetch = 8;    // tiles of gathered rows prefetched into L2 ahead of their cp.async
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 288;
+constexpr uint32_t kColO = 0, kColS = 256, kColP = kColS + kNB * kRows;
 constexpr uint32_t kIdescQK = idesc_f16(128, kRows, 1u, 0u, 0u);
 constexpr uint32_t kIdescPV = idesc_f16(128, kDVH, 1u, 0u, 1u);
 
 struct Smem {
     uint64_t full[kStages], empty[kStages];
-    uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
+    uint64_t s_full[kNB], s_empty[kNB], p_full[kNB], p_empty[kNB];
     uint64_t qfull, o_full, mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -86,13 +88,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(smem_u32(&S.full[i]), 128);
+            mbar_init(smem_u32(&S.full[i]), 1);
             mbar_init(smem_u32(&S.empty[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kNB; ++i) {
             mbar_init(smem_u32(&S.s_full[i]), 1);
-            mbar_init(smem_u32(&S.s_empty[i]), 128);
-            mbar_init(smem_u32(&S.p_full[i]), 128);
+            mbar_init(smem_u32(&S.s_empty[i]), 4);  // one elected arrive per softmax warp
+            mbar_init(smem_u32(&S.p_full[i]), 4);
             mbar_init(smem_u32(&S.p_empty[i]), 1);
         }
         mbar_init(smem_u32(&S.qfull), 1);
@@ -134,59 +136,97 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
 
     if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------- gather producers
-        const int ptid = threadIdx.x - 128;
-        const int r = ptid >> 3, sub = ptid & 7;
+        // Producer warp w fills stage w with tiles w, w + 4, ...: its 32 lanes copy the tile's
+        // 16 rows x 72 16-byte units with cp.async, wait for their own copies, and one lane
+        // arrives on the stage's barrier. Rows of later tiles are prefetched into L2 first.
+        const int pw = warp - 4;
         const uint8_t* kv = static_cast<const uint8_t*>(a.kv);
-        for (int i = 0; i < ntiles; ++i) {
-            const int st = i % kStages;
-            if (!mbar_wait(smem_u32(&S.empty[st]), ((i / kStages) & 1) ^ 1, abort_flag, a.err)) break;
-            const int row = i * kRows + r;
-            const int p = (row < nrows) ? phys_s[row] : -1;
-            const uint8_t* src = (p >= 0) ? kv + static_cast<int64_t>(p) * (kD * 2) + sub * 16 : kv;
-            const uint32_t dst = sKv + st * kKvStageBytes + r * 128 + ((sub ^ (r & 7)) << 4);
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-                cp_async16(dst + c * kKvChunkBytes, (p >= 0) ? src + c * 128 : kv, (p >= 0) ? 16u : 0u);
-            cp_async_arrive_noinc(smem_u32(&S.full[st]));
+        auto prefetch_tile = [&](int i) {
+            const int row = i * kRows + lane;
+            if (lane < kRows && i < ntiles && row < nrows) {
+                const int p = phys_s[row];
+                if (p >= 0)
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kv + static_cast<int64_t>(p) * (kD * 2)),
+                                 "r"(kD * 2)
+                                 : "memory");
+            }
+        };
+        prefetch_tile(pw);
+        prefetch_tile(pw + kStages);
+        for (int i = pw; i < ntiles; i += kStages) {
+            prefetch_tile(i + 2 * kStages);
+            const int st = pw, use = i / kStages;
+            const bool got = mbar_wait(smem_u32(&S.empty[st]), (use & 1) ^ 1, abort_flag, a.err);
+            if (!__all_sync(0xFFFFFFFFu, got)) break;
+            const uint32_t base = sKv + st * kKvStageBytes;
+#pragma unroll 4
+            for (int e = lane; e < kRows * (kD / 8); e += 32) {
+                const int r = e / (kD / 8), u = e % (kD / 8);
+                const int c = u >> 3, sub = u & 7;
+                const int row = i * kRows + r;
+                const int p = (row < nrows) ? phys_s[row] : -1;
+                const uint32_t dst = base + c * kKvChunkBytes + r * 128 + ((sub ^ (r & 7)) << 4);
+                cp_async16(dst, (p >= 0) ? kv + static_cast<int64_t>(p) * (kD * 2) + u * 16 : kv, (p >= 0) ? 16u : 0u);
+            }
+            cp_async_wait_all();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&S.full[st]));
         }
         cp_async_wait_all();
     } else if (warp == 8) {
         // ------------------------------------------------------------- MMA issuer
+        // Polls instead of blocking: QK of a tile is issued as soon as its rows have landed and an
+        // S buffer is free; PV as soon as softmax has written P. The tensor core thus computes S
+        // for the next tiles while softmax works on the current one.
         if (lane == 0 && ntiles > 0) {
             bool ok = mbar_wait(smem_u32(&S.qfull), 0, abort_flag, a.err);
-            auto pv = [&](int j) -> bool {
-                const int pb = j & 1;
-                if (!mbar_wait(smem_u32(&S.p_full[pb]), (j >> 1) & 1, abort_flag, a.err)) return false;
-                tc_fence_after();
-                const uint64_t vd =
-                    sw128_desc(sKv + (j % kStages) * kKvStageBytes + (4 * half) * kKvChunkBytes, kKvChunkBytes, 1024);
-                mma_ts(tmem + kColO, tmem + kColP + pb * 8, vd, kIdescPV, j > 0 ? 1u : 0u);
-                tc_commit(smem_u32(&S.empty[j % kStages]));
-                tc_commit(smem_u32(&S.p_empty[pb]));
-                return true;
-            };
-            for (int i = 0; ok && i < ntiles; ++i) {
-                const int st = i % kStages, sb = i & 1;
-                ok = mbar_wait(smem_u32(&S.full[st]), (i / kStages) & 1, abort_flag, a.err);
-                if (!ok) break;
-                fence_proxy_async_smem();  // rows written by cp.async -> visible to the tensor core
-                ok = mbar_wait(smem_u32(&S.s_empty[sb]), ((i >> 1) & 1) ^ 1, abort_flag, a.err);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t d = tmem + kColS + sb * kRows;
+            const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
+            const uint64_t dkv0 = sw128_desc(sKv, 16, 1024);
+            const uint64_t dv0 = sw128_desc(sKv + (4 * half) * kKvChunkBytes, kKvChunkBytes, 1024);
+            int qk = 0, pv = 0;
+            long long t_idle = 0;
+            while (ok && pv < ntiles) {
+                bool did = false;
+                if (pv < qk && mbar_test(smem_u32(&S.p_full[pv % kNB]), (pv / kNB) & 1)) {
+                    tc_fence_after();
+                    const uint64_t vd = dv0 + static_cast<uint64_t>(((pv % kStages) * kKvStageBytes) >> 4);
+                    mma_ts(tmem + kColO, tmem + kColP + (pv % kNB) * (kRows / 2), vd, kIdescPV, pv > 0 ? 1u : 0u);
+                    tc_commit(smem_u32(&S.empty[pv % kStages]));
+                    tc_commit(smem_u32(&S.p_empty[pv % kNB]));
+                    ++pv;
+                    did = true;
+                } else if (qk < ntiles && qk - pv < kNB &&
+                           mbar_test(smem_u32(&S.full[qk % kStages]), (qk / kStages) & 1) &&
+                           mbar_test(smem_u32(&S.s_empty[qk % kNB]), ((qk / kNB) & 1) ^ 1)) {
+                    tc_fence_after();
+                    const uint32_t d = tmem + kColS + (qk % kNB) * kRows;
+                    const uint64_t kvb = dkv0 + static_cast<uint64_t>(((qk % kStages) * kKvStageBytes) >> 4);
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
+                    for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sw128_desc(sQ + c * kQChunkBytes + kk * 32, 16, 1024);
-                        const uint64_t bd = sw128_desc(sKv + st * kKvStageBytes + c * kKvChunkBytes + kk * 32, 16, 1024);
-                        mma_ss(d, ad, bd, kIdescQK, (c | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = dq0 + static_cast<uint64_t>((c * kQChunkBytes + kk * 32) >> 4);
+                            const uint64_t bd = kvb + static_cast<uint64_t>((c * kKvChunkBytes + kk * 32) >> 4);
+                            mma_ss(d, ad, bd, kIdescQK, (c | kk) != 0 ? 1u : 0u);
+                        }
                     }
+                    tc_commit(smem_u32(&S.s_full[qk % kNB]));
+                    ++qk;
+                    did = true;
                 }
-                tc_commit(smem_u32(&S.s_full[sb]));
-                if (i >= 1) ok = pv(i - 1);
+                if (did) {
+                    t_idle = 0;
+                } else if (t_idle == 0) {
+                    t_idle = clock64();
+                } else if (*abort_flag) {
+                    ok = false;
+                } else if (clock64() - t_idle > kWaitCycles) {
+                    *abort_flag = 1;
+                    atomicOr(a.err, DSA_FAULT_TIMEOUT);
+                    ok = false;
+                }
             }
-            if (ok) ok = pv(ntiles - 1);
             if (ok) tc_commit(smem_u32(&S.o_full));
             tc_commit(smem_u32(&S.mma_done));
             mbar_wait_drain(smem_u32(&S.mma_done), 0, a.err);
@@ -199,15 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
         float m_ref = -INFINITY, l = 0.0f;
         bool dead = false;
         for (int i = 0; i < ntiles; ++i) {
-            const int sb = i & 1;
-            bool got = mbar_wait(smem_u32(&S.s_full[sb]), (i >> 1) & 1, abort_flag, a.err);
+            const int sb = i % kNB;
+            bool got = mbar_wait(smem_u32(&S.s_full[sb]), (i / kNB) & 1, abort_flag, a.err);
             if (named_bar_or(2, 128, dead || !got)) { dead = true; break; }
             tc_fence_after();
             uint32_t sv[16];
             tmem_ld16(tmem + lane_base + kColS + sb * kRows, sv);
             tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(smem_u32(&S.s_empty[sb]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&S.s_empty[sb]));
             float z[kRows];
             float mt = -INFINITY;
 #pragma unroll
@@ -221,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
             if (__any_sync(0xFFFFFFFFu, need)) {
                 const float m_new = need ? mt : m_ref;
                 if (i > 0) {
-                    got = mbar_wait(smem_u32(&S.p_empty[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort_flag, a.err);
+                    got = mbar_wait(smem_u32(&S.p_empty[(i - 1) % kNB]), ((i - 1) / kNB) & 1, abort_flag, a.err);
                     if (__any_sync(0xFFFFFFFFu, !got)) dead = true;
                     if (!dead) {
                         tc_fence_after();
@@ -251,17 +292,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
                 packed[j / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) |
                                 (static_cast<uint32_t>(__bfloat16_as_ushort(b1)) << 16);
             }
-            if (i >= 2) {
-                got = mbar_wait(smem_u32(&S.p_empty[i & 1]), ((i - 2) >> 1) & 1, abort_flag, a.err);
+            if (i >= kNB) {
+                got = mbar_wait(smem_u32(&S.p_empty[i % kNB]), ((i - kNB) / kNB) & 1, abort_flag, a.err);
                 if (__any_sync(0xFFFFFFFFu, !got)) dead = true;
             }
             if (!dead) {
                 tc_fence_after();
-                tmem_st8(tmem + lane_base + kColP + (i & 1) * 8, packed);
+                tmem_st8(tmem + lane_base + kColP + (i % kNB) * (kRows / 2), packed);
                 tmem_st_wait();
                 tc_fence_before();
             }
-            mbar_arrive(smem_u32(&S.p_full[i & 1]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&S.p_full[i % kNB]));
         }
         if (ntiles > 0) {  // every softmax thread takes this barrier, dead or not
             const bool got = dead ? false : mbar_wait(smem_u32(&S.o_full), 0, abort_flag, a.err);

@@ -100,153 +100,312 @@ struct SegmentIter {
 };
 
 // ------------------------------------------------------------------------------------------------
-// streaming Top-K buffer in shared memory, driven collectively by NT threads (one named barrier)
+// Top-K selection: control block, warp-aggregated histograms, radix threshold
 // ------------------------------------------------------------------------------------------------
 
 struct TopkCtl {
     uint32_t count;
     uint32_t theta_lo, theta_hi;  // admission threshold: keys below it cannot be in the Top-K
     uint32_t digit, above, bucket;
-    uint32_t warp_cnt[32];
+    unsigned long long diff;      // OR of (key ^ first key): the bits where candidates differ
+    uint32_t warp_cnt[32];        // two arrays of 16 per-warp counts (alternating)
 };
 
+// Adds 1 to hist[bin] for every active lane of the warp. `hist` is the warp's private histogram,
+// so only lanes of one warp can collide on a bin (shared-memory atomics serialise those lanes).
+__device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool active) {
+    if (active) atomicAdd(&hist[bin], 1u);
+}
+
+// Collective over NT threads (named barrier bar_id): the threshold thr such that exactly K of the
+// keys in the spans are >= thr (keys are distinct; the total count must exceed K). MSB-first radix
+// select with 8-bit digits, starting below the bits all keys share, stopping as soon as the
+// boundary bucket is taken whole. `hist` holds NT/32 private 256-bin histograms (one per warp, so
+// warps never contend on a hot bin); they are summed into the first one after every pass.
 template <int NT>
+__device__ uint64_t radix_threshold(const uint64_t* const* span_ptr, const uint32_t* span_cnt, int ns, uint32_t K,
+                                    uint32_t* hist, TopkCtl* ctl, uint32_t tid, uint32_t bar_id) {
+    constexpr uint32_t NW = NT / 32;
+    const uint32_t lane = tid & 31u, warp = tid >> 5;
+    uint32_t* my_hist = hist + warp * 256;
+    // 1. bits shared by every key
+    if (tid == 0) ctl->diff = 0ull;
+    named_bar_sync(bar_id, NT);
+    const uint64_t k0 = span_ptr[0][0];
+    uint64_t d = 0;
+    for (int s = 0; s < ns; ++s) {
+        const uint64_t* sp = span_ptr[s];
+        for (uint32_t i = tid; i < span_cnt[s]; i += NT) d |= sp[i] ^ k0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d |= __shfl_xor_sync(0xFFFFFFFFu, d, o);
+    if (lane == 0 && d) atomicOr(&ctl->diff, static_cast<unsigned long long>(d));
+    named_bar_sync(bar_id, NT);
+    const uint64_t diff = ctl->diff;
+    const int hi = 63 - __clzll(static_cast<long long>(diff | 1ull));
+    int shift = (hi >> 3) << 3;
+    uint64_t prefix = (shift >= 56) ? 0ull : (k0 & (~0ull << (shift + 8)));
+    uint32_t rem = K;
+    // 2. radix passes
+    for (; shift >= 0; shift -= 8) {
+        for (uint32_t i = lane; i < 256; i += 32) my_hist[i] = 0;
+        __syncwarp();
+        for (int s = 0; s < ns; ++s) {
+            const uint64_t* sp = span_ptr[s];
+            const uint32_t cnt = span_cnt[s];
+            for (uint32_t base = 0; base < cnt; base += NT) {
+                const uint32_t i = base + tid;
+                const uint64_t k = (i < cnt) ? sp[i] : 0ull;
+                const bool match = (i < cnt) && ((shift == 56) || ((k >> (shift + 8)) == (prefix >> (shift + 8))));
+                hist_add_warp(my_hist, static_cast<uint32_t>(k >> shift) & 255u, match);
+            }
+        }
+        named_bar_sync(bar_id, NT);
+        for (uint32_t b = tid; b < 256; b += NT) {  // sum the private histograms into the first
+            uint32_t c = hist[b];
+#pragma unroll
+            for (uint32_t w = 1; w < NW; ++w) c += hist[w * 256 + b];
+            hist[b] = c;
+        }
+        named_bar_sync(bar_id, NT);
+        if (tid < 32) {
+            uint32_t c = 0;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) c += hist[lane * 8 + b];
+            uint32_t S = c;  // inclusive suffix sum over lanes
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, S, o);
+                if (lane + o < 32) S += v;
+            }
+            const uint32_t mask = __ballot_sync(0xFFFFFFFFu, S >= rem);
+            const int L = 31 - __clz(mask);
+            if (static_cast<int>(lane) == L) {
+                uint32_t running = S - c;
+                for (int b = 7; b >= 0; --b) {
+                    const uint32_t h = hist[lane * 8 + b];
+                    if (running + h >= rem) {
+                        ctl->digit = lane * 8 + b;
+                        ctl->above = running;
+                        ctl->bucket = h;
+                        break;
+                    }
+                    running += h;
+                }
+            }
+        }
+        named_bar_sync(bar_id, NT);
+        rem -= ctl->above;
+        prefix |= static_cast<uint64_t>(ctl->digit) << shift;
+        const bool done = ctl->bucket == rem;
+        named_bar_sync(bar_id, NT);  // ctl and hist are rewritten by the next pass
+        if (done) break;
+    }
+    return prefix;
+}
+
+// Collective over NT threads (named barrier bar_id): exclusive prefix of v over the threads in
+// thread order, and the total. Two barriers; warp_tot is free again when it returns.
+template <int NT>
+__device__ __forceinline__ uint32_t group_excl_scan(uint32_t v, uint32_t* warp_tot, uint32_t tid, uint32_t bar_id,
+                                                    uint32_t& total) {
+    const uint32_t lane = tid & 31u, warp = tid >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= static_cast<uint32_t>(o)) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    named_bar_sync(bar_id, NT);
+    uint32_t before = 0;
+    total = 0;
+#pragma unroll
+    for (uint32_t w = 0; w < NT / 32; ++w) {
+        const uint32_t c = warp_tot[w];
+        before += (w < warp) ? c : 0u;
+        total += c;
+    }
+    named_bar_sync(bar_id, NT);
+    return before + x - v;
+}
+
+// Collective over NT threads: radix threshold (as radix_threshold) over keys held in registers,
+// keys[j] valid for j < cnt; thread 0 must hold at least one key. hist: NT/32 x 256 words.
+template <int NT, int PER>
+__device__ uint64_t reg_radix_threshold(const uint64_t (&keys)[PER], uint32_t cnt, uint32_t K, uint32_t* hist,
+                                        TopkCtl* ctl, uint32_t tid, uint32_t bar_id) {
+    constexpr uint32_t NW = NT / 32;
+    const uint32_t lane = tid & 31u, warp = tid >> 5;
+    uint32_t* my_hist = hist + warp * 256;
+    if (tid == 0) {  // reference key for the bits every key shares
+        ctl->theta_lo = static_cast<uint32_t>(keys[0]);
+        ctl->theta_hi = static_cast<uint32_t>(keys[0] >> 32);
+        ctl->diff = 0ull;
+    }
+    named_bar_sync(bar_id, NT);
+    const uint64_t ref = (static_cast<uint64_t>(ctl->theta_hi) << 32) | ctl->theta_lo;
+    uint64_t d = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+        if (static_cast<uint32_t>(j) < cnt) d |= keys[j] ^ ref;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d |= __shfl_xor_sync(0xFFFFFFFFu, d, o);
+    if (lane == 0 && d) atomicOr(&ctl->diff, static_cast<unsigned long long>(d));
+    named_bar_sync(bar_id, NT);
+    const int hi = 63 - __clzll(static_cast<long long>(ctl->diff | 1ull));
+    int shift = (hi >> 3) << 3;
+    uint64_t prefix = (shift >= 56) ? 0ull : (ref & (~0ull << (shift + 8)));
+    uint32_t rem = K;
+    for (; shift >= 0; shift -= 8) {
+        for (uint32_t i = lane; i < 256; i += 32) my_hist[i] = 0;
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const uint64_t k = keys[j];
+            const bool match =
+                static_cast<uint32_t>(j) < cnt && ((shift == 56) || ((k >> (shift + 8)) == (prefix >> (shift + 8))));
+            if (match) atomicAdd(&my_hist[static_cast<uint32_t>(k >> shift) & 255u], 1u);
+        }
+        named_bar_sync(bar_id, NT);
+        for (uint32_t b = tid; b < 256; b += NT) {
+            uint32_t c = hist[b];
+#pragma unroll
+            for (uint32_t w = 1; w < NW; ++w) c += hist[w * 256 + b];
+            hist[b] = c;
+        }
+        named_bar_sync(bar_id, NT);
+        if (tid < 32) {
+            uint32_t c = 0;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) c += hist[lane * 8 + b];
+            uint32_t S = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, S, o);
+                if (lane + o < 32) S += v;
+            }
+            const uint32_t mask = __ballot_sync(0xFFFFFFFFu, S >= rem);
+            const int L = 31 - __clz(mask);
+            if (static_cast<int>(lane) == L) {
+                uint32_t running = S - c;
+                for (int b = 7; b >= 0; --b) {
+                    const uint32_t h = hist[lane * 8 + b];
+                    if (running + h >= rem) {
+                        ctl->digit = lane * 8 + b;
+                        ctl->above = running;
+                        ctl->bucket = h;
+                        break;
+                    }
+                    running += h;
+                }
+            }
+        }
+        named_bar_sync(bar_id, NT);
+        rem -= ctl->above;
+        prefix |= static_cast<uint64_t>(ctl->digit) << shift;
+        const bool done = ctl->bucket == rem;
+        named_bar_sync(bar_id, NT);
+        if (done) break;
+    }
+    return prefix;
+}
+
+// ------------------------------------------------------------------------------------------------
+// streaming Top-K buffer in shared memory, driven collectively by NT threads (one named barrier)
+// ------------------------------------------------------------------------------------------------
+
+template <int NT, int PER>
 struct TopkGroup {
-    uint64_t* buf;   // [cap]
-    uint32_t* hist;  // [256]
+    uint64_t* buf;   // [cap], cap <= NT * PER
+    uint32_t* hist;  // [NT/32][256]
     TopkCtl* ctl;
     uint32_t cap;    // >= K + NT
     uint32_t K;
     uint32_t tid;    // 0..NT-1
     uint32_t bar_id;
+    // uniform across the group (every thread computes the same values)
+    uint32_t count = 0;
+    uint64_t theta = 0;  // admission threshold: keys below it cannot be in the Top-K
+    uint32_t parity = 0;
 
     __device__ __forceinline__ void sync() const { named_bar_sync(bar_id, NT); }
 
+    // Collective. Starts a new candidate set (after the previous flush has been read).
     __device__ void reset() {
-        if (tid == 0) {
-            ctl->count = 0;
-            ctl->theta_lo = 0;
-            ctl->theta_hi = 0;
-        }
+        count = 0;
+        theta = 0;
         sync();
     }
 
-    // Stable compaction of buf[0, count) keeping keys >= thr; returns the kept count (uniform).
-    __device__ uint32_t compact(uint32_t count, uint64_t thr) {
+    // Collective: exclusive offset of this thread's predicate among the group and the total.
+    // One barrier; the per-warp counts alternate between two arrays so that the next call
+    // cannot overwrite counts another thread is still reading.
+    __device__ __forceinline__ uint32_t scan(bool p, uint32_t& total) {
         const uint32_t lane = tid & 31u, warp = tid >> 5;
-        uint32_t out = 0;
-        for (uint32_t base = 0; base < count; base += NT) {
-            const uint32_t i = base + tid;
-            const uint64_t k = (i < count) ? buf[i] : 0ull;
-            const bool p = (i < count) && (k >= thr);
-            const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, p);
-            if (lane == 0) ctl->warp_cnt[warp] = __popc(ballot);
-            sync();
-            uint32_t off = 0, total = 0;
+        const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, p);
+        uint32_t* wc = ctl->warp_cnt + parity * 16;
+        if (lane == 0) wc[warp] = __popc(ballot);
+        sync();
+        uint32_t off = 0;
+        total = 0;
 #pragma unroll
-            for (uint32_t w = 0; w < NT / 32; ++w) {
-                const uint32_t c = ctl->warp_cnt[w];
-                off += (w < warp) ? c : 0u;
-                total += c;
-            }
-            if (p) buf[out + off + __popc(ballot & ((1u << lane) - 1u))] = k;
-            sync();
-            out += total;
+        for (uint32_t w = 0; w < NT / 32; ++w) {
+            const uint32_t c = wc[w];
+            off += (w < warp) ? c : 0u;
+            total += c;
         }
-        return out;
+        parity ^= 1u;
+        return off + __popc(ballot & ((1u << lane) - 1u));
     }
 
-    // Keeps exactly the K largest of buf[0, count) (count > K), in their original order, and
-    // raises the admission threshold to the smallest kept key's radix prefix.
-    __device__ void select(uint32_t count) {
-        uint64_t prefix = 0;
-        uint32_t rem = K;
-        const uint32_t lane = tid & 31u;
-        for (int shift = 56; shift >= 0; shift -= 8) {
-            for (uint32_t i = tid; i < 256; i += NT) hist[i] = 0;
-            sync();
-            for (uint32_t i = tid; i < count; i += NT) {
-                const uint64_t k = buf[i];
-                const bool match = (shift == 56) || ((k >> (shift + 8)) == (prefix >> (shift + 8)));
-                if (match) atomicAdd(&hist[(k >> shift) & 255u], 1u);
-            }
-            sync();
-            if (tid < 32) {
-                uint32_t s = 0;
+    // Collective: writes the min(count, K) largest keys of buf, in buffer (= position) order, to
+    // dst (shared or global; may be buf itself) and returns how many. Each thread loads its
+    // contiguous chunk into registers first, so writing over buf is safe.
+    __device__ uint32_t select_to(uint64_t* dst) {
+        sync();  // every push's writes to buf are visible
+        const uint32_t n = count;
+        const uint32_t per = (n + NT - 1) / NT;
+        const uint32_t c0 = min(n, tid * per), c1 = min(n, c0 + per);
+        const uint32_t cnt = c1 - c0;
+        uint64_t keys[PER];
 #pragma unroll
-                for (int b = 0; b < 8; ++b) s += hist[lane * 8 + b];
-                uint32_t S = s;
+        for (int j = 0; j < PER; ++j) keys[j] = (static_cast<uint32_t>(j) < cnt) ? buf[c0 + j] : 0ull;
+        uint64_t thr = 0ull;
+        if (n > K) thr = reg_radix_threshold<NT, PER>(keys, cnt, K, hist, ctl, tid, bar_id);
+        uint32_t mine = 0;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, S, o);
-                    if (lane + o < 32) S += v;
-                }
-                const uint32_t mask = __ballot_sync(0xFFFFFFFFu, S >= rem);
-                const int L = 31 - __clz(mask);
-                if (static_cast<int>(lane) == L) {
-                    uint32_t running = S - s;
-                    for (int b = 7; b >= 0; --b) {
-                        const uint32_t h = hist[lane * 8 + b];
-                        if (running + h >= rem) {
-                            ctl->digit = lane * 8 + b;
-                            ctl->above = running;
-                            ctl->bucket = h;
-                            break;
-                        }
-                        running += h;
-                    }
-                }
-            }
-            sync();
-            const uint32_t dg = ctl->digit;
-            rem -= ctl->above;
-            prefix |= static_cast<uint64_t>(dg) << shift;
-            if (ctl->bucket == rem) break;  // the whole bucket is selected
+        for (int j = 0; j < PER; ++j) mine += (static_cast<uint32_t>(j) < cnt && keys[j] >= thr) ? 1u : 0u;
+        uint32_t kept;
+        uint32_t o = group_excl_scan<NT>(mine, ctl->warp_cnt, tid, bar_id, kept);  // all loads done before
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            if (static_cast<uint32_t>(j) < cnt && keys[j] >= thr) dst[o++] = keys[j];
         }
-        const uint32_t kept = compact(count, prefix);
-        if (tid == 0) {
-            ctl->count = kept;
-            ctl->theta_lo = static_cast<uint32_t>(prefix);
-            ctl->theta_hi = static_cast<uint32_t>(prefix >> 32);
-        }
+        if (n > K) theta = thr;
+        return kept;
+    }
+
+    // Keeps the K largest keys of buf (in order) and raises the admission threshold.
+    __device__ void select() {
+        count = select_to(buf);
         sync();
     }
 
     // Collective: every thread offers at most one key per call.
     __device__ void push(uint64_t key, bool valid) {
-        uint32_t count = ctl->count;
-        if (count + NT > cap) {
-            select(count);
-            count = ctl->count;
-        }
-        const uint64_t theta = (static_cast<uint64_t>(ctl->theta_hi) << 32) | ctl->theta_lo;
+        if (count + NT > cap) select();
         const bool p = valid && key >= theta;
-        const uint32_t lane = tid & 31u, warp = tid >> 5;
-        const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, p);
-        if (lane == 0) ctl->warp_cnt[warp] = __popc(ballot);
-        sync();
-        uint32_t off = 0, total = 0;
-#pragma unroll
-        for (uint32_t w = 0; w < NT / 32; ++w) {
-            const uint32_t c = ctl->warp_cnt[w];
-            off += (w < warp) ? c : 0u;
-            total += c;
-        }
-        if (p) buf[count + off + __popc(ballot & ((1u << lane) - 1u))] = key;
-        sync();
-        if (tid == 0) ctl->count = count + total;
-        sync();
+        uint32_t total;
+        const uint32_t o = scan(p, total);
+        if (p) buf[count + o] = key;
+        count += total;
     }
 
-    // Collective: reduces to at most K keys (in position order) and writes them to `out`.
+    // Collective: writes at most K keys (in position order) to `out`, their number to count_out.
     __device__ void flush(uint64_t* out, int32_t* count_out) {
-        uint32_t count = ctl->count;
-        if (count > K) {
-            select(count);
-            count = ctl->count;
-        }
-        for (uint32_t i = tid; i < count; i += NT) out[i] = buf[i];
-        if (tid == 0) *count_out = static_cast<int32_t>(count);
+        const uint32_t kept = select_to(out);
+        if (tid == 0) *count_out = static_cast<int32_t>(kept);
     }
 };
 

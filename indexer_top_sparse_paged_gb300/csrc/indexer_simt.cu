@@ -84,12 +84,12 @@ __global__ void __launch_bounds__(kSimtThreads) indexer_simt_kernel(IndexerArgs 
     float* scale_s = k_s + kTileKeys * kstride;                          // [2] per block of the tile
     uint64_t* buf = reinterpret_cast<uint64_t*>(
         (reinterpret_cast<uintptr_t>(scale_s + 2) + 15) & ~static_cast<uintptr_t>(15));  // [cap]
-    __shared__ uint32_t hist[256];
+    __shared__ uint32_t hist[kSimtThreads / 32 * 256];
     __shared__ TopkCtl ctl;
     __shared__ int blk_s[2];
 
     const int tid = threadIdx.x;
-    TopkGroup<kSimtThreads> topk{buf, hist, &ctl, cap, static_cast<uint32_t>(a.K), static_cast<uint32_t>(tid), 1};
+    TopkGroup<kSimtThreads, 33> topk{buf, hist, &ctl, cap, static_cast<uint32_t>(a.K), static_cast<uint32_t>(tid), 1};
     constexpr int per = Widen<KT>::kPer16B;
     const int units_per_row = d_I / per;
     constexpr size_t key_bytes = 16 / per;

@@ -13,8 +13,9 @@
 // multiplication).
 //
 // Roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
-// warps 2..5 = epilogue (TMEM lane quarter = warp % 4). Pipelines: 4 smem stages of 32 KB,
-// 2 TMEM accumulators of 64 columns, 2 query buffers (one per segment in flight).
+// warps 2..5 = epilogue (TMEM lane quarter = warp % 4). Pipelines: 5 smem stages of 32 KB (the
+// HBM round trip under full load is ~3.7 us: 160 KB in flight per SM keeps it busy), 2 TMEM
+// accumulators of 64 columns, one query buffer.
 #include "internal.h"
 
 namespace dsa {
@@ -22,7 +23,7 @@ namespace tcidx {
 
 constexpr int kHeads = 64;
 constexpr int kDim = 128;
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kHalfBytes = kTileKeys * 128;   // [128 keys x 64 bf16] = 16 KB
 constexpr int kStageBytes = 2 * kHalfBytes;   // both K halves = 32 KB
 constexpr int kQHalfBytes = kHeads * 128;     // [64 heads x 64 bf16] = 8 KB
@@ -34,24 +35,28 @@ constexpr uint32_t kIdesc = idesc_f16(128, kHeads, 1u, 0u, 0u);
 
 struct Smem {
     uint64_t full[kStages], empty[kStages];
-    uint64_t qfull[2], qempty[2];
+    uint64_t qfull, qempty;
     uint64_t tfull[2], tempty[2];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
-    uint32_t hist[256];
+    uint32_t hist[kEpiThreads / 32 * 256];
     TopkCtl ctl;
 };
 
 constexpr size_t kOffA = 0;
 constexpr size_t kOffQ = kOffA + static_cast<size_t>(kStages) * kStageBytes;
-constexpr size_t kOffBuf = kOffQ + 2 * kQBytes;
+constexpr size_t kOffBuf = kOffQ + kQBytes;
 
+constexpr int kTopkPer = 33;  // candidate keys per epilogue thread held in registers while selecting
+constexpr size_t kSmemLimit = 232448;
 __host__ __device__ constexpr uint32_t topk_cap(int K) { return static_cast<uint32_t>(2 * K + kEpiThreads); }
 
 __host__ __device__ constexpr size_t smem_bytes(int K) {
     return 1024 /*alignment slack*/ + kOffBuf + static_cast<size_t>(topk_cap(K)) * 8 + sizeof(Smem) + 64;
 }
+static_assert(topk_cap(2048) <= static_cast<uint32_t>(kEpiThreads * kTopkPer), "candidate buffer exceeds registers");
+static_assert(smem_bytes(2048) <= kSmemLimit, "indexer shared memory over the limit");
 
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_tc_kernel(IndexerArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
@@ -71,11 +76,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&S.full[i]), 1);
             mbar_init(smem_u32(&S.empty[i]), 1);
         }
+        mbar_init(smem_u32(&S.qfull), 1);
+        mbar_init(smem_u32(&S.qempty), 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&S.qfull[i]), 1);
-            mbar_init(smem_u32(&S.qempty[i]), 1);
             mbar_init(smem_u32(&S.tfull[i]), 1);
-            mbar_init(smem_u32(&S.tempty[i]), kEpiThreads);
+            mbar_init(smem_u32(&S.tempty[i]), kEpiThreads / 32);  // one elected arrive per epilogue warp
         }
         mbar_init(smem_u32(&S.mma_done), 1);
         S.abort_flag = 0;
@@ -97,33 +102,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     Segment seg;
 
     if (warp == 0) {
-        // ------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            uint32_t sg = 0, n_it = 0;
-            bool ok = true;
-            while (ok && it.next(seg)) {
-                const int t = seg.row;
-                const int b = row_seq(a, t);
-                const int n = row_len(a, t);
-                const uint32_t qb = sg & 1u;
-                ok = mbar_wait(smem_u32(&S.qempty[qb]), ((sg >> 1) & 1u) ^ 1u, abort_flag, a.err);
+        // ------------------------------------------------------------- TMA producer (whole warp)
+        // The block-table entries of a segment are read 32 pages at a time by the 32 lanes, one
+        // window ahead of use, so no table load sits between two TMA issues.
+        uint32_t sg = 0, n_it = 0;
+        bool ok = true;
+        while (ok && it.next(seg)) {
+            const int t = seg.row;
+            const int b = row_seq(a, t);
+            const int n = row_len(a, t);
+            const int npages = (n + kBlock - 1) / kBlock;
+            const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
+            auto load_window = [&](int w0) -> int {  // entry of page w0 + lane, -1 if past the row
+                const int pg = w0 + lane;
+                if (pg >= npages) return -1;
+                const int v = bt[pg];
+                return v;
+            };
+            // one query buffer: reload it once the previous segment's MMAs are done with it
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&S.qempty), (sg & 1u) ^ 1u, abort_flag, a.err));
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(smem_u32(&S.qfull), kQBytes);
+                tma_load_2d(sQ, &map_q, 0, t * kHeads, smem_u32(&S.qfull));
+                tma_load_2d(sQ + kQHalfBytes, &map_q, 64, t * kHeads, smem_u32(&S.qfull));
+            }
+            int w0 = (2 * seg.tile0) & ~31;
+            int cur = load_window(w0), nxt = load_window(w0 + 32);
+            for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
+                if (2 * j >= w0 + 32) {  // advance the window (pages come in pairs: never straddles)
+                    w0 += 32;
+                    cur = nxt;
+                    nxt = load_window(w0 + 32);
+                }
+                const uint32_t st = n_it % kStages, use = n_it / kStages;
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&S.empty[st]), (use & 1u) ^ 1u, abort_flag, a.err));
                 if (!ok) break;
-                mbar_arrive_expect_tx(smem_u32(&S.qfull[qb]), kQBytes);
-                tma_load_2d(sQ + qb * kQBytes, &map_q, 0, t * kHeads, smem_u32(&S.qfull[qb]));
-                tma_load_2d(sQ + qb * kQBytes + kQHalfBytes, &map_q, 64, t * kHeads, smem_u32(&S.qfull[qb]));
-                for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
-                    const uint32_t st = n_it % kStages, use = n_it / kStages;
-                    ok = mbar_wait(smem_u32(&S.empty[st]), (use & 1u) ^ 1u, abort_flag, a.err);
-                    if (!ok) break;
-                    int blk[2];
-                    uint32_t bytes = 0;
-                    for (int p = 0; p < 2; ++p) {
-                        const int lb = 2 * j + p;
-                        blk[p] = (lb * kBlock < n) ? phys_block(a, b, lb) : -1;
-                        if (blk[p] >= 0) bytes += 2 * (kBlock * 128);
-                    }
+                int blk[2];
+                uint32_t bytes = 0;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int lb = 2 * j + p;
+                    const int v = __shfl_sync(0xFFFFFFFFu, cur, lb - w0);
+                    const bool inside = lb * kBlock < n;
+                    const bool good = v >= 0 && v < a.num_blocks;
+                    if (inside && !good && lane == 0) atomicOr(a.err, DSA_FAULT_BLOCK_TABLE);
+                    blk[p] = (inside && good) ? v : -1;
+                    if (blk[p] >= 0) bytes += 2 * (kBlock * 128);
+                }
+                if (lane == 0) {
                     const uint32_t fb = smem_u32(&S.full[st]);
                     mbar_arrive_expect_tx(fb, bytes);
+#pragma unroll
                     for (int p = 0; p < 2; ++p) {
                         if (blk[p] < 0) continue;
                         const uint32_t dst = sA + st * kStageBytes + p * (kBlock * 128);
@@ -131,8 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d(dst + kHalfBytes, &map_k, 64, blk[p] * kBlock, fb);
                     }
                 }
-                ++sg;
+                __syncwarp();
             }
+            ++sg;
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issuer
@@ -140,8 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sg = 0, n_it = 0;
             bool ok = true;
             while (ok && it.next(seg)) {
-                const uint32_t qb = sg & 1u;
-                ok = mbar_wait(smem_u32(&S.qfull[qb]), (sg >> 1) & 1u, abort_flag, a.err);
+                ok = mbar_wait(smem_u32(&S.qfull), sg & 1u, abort_flag, a.err);
                 if (!ok) break;
                 for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
                     const uint32_t st = n_it % kStages, use = n_it / kStages;
@@ -156,14 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < kDim / 16; ++k) {
                         const uint32_t half = k >> 2, kk = k & 3;
                         const uint64_t ad = sw128_desc(sA + st * kStageBytes + half * kHalfBytes + kk * 32, 16, 1024);
-                        const uint64_t bd = sw128_desc(sQ + qb * kQBytes + half * kQHalfBytes + kk * 32, 16, 1024);
+                        const uint64_t bd = sw128_desc(sQ + half * kQHalfBytes + kk * 32, 16, 1024);
                         mma_ss(d, ad, bd, kIdesc, k > 0 ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&S.empty[st]));
                     tc_commit(smem_u32(&S.tfull[acc]));
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(&S.qempty[qb]));
+                tc_commit(smem_u32(&S.qempty));
                 ++sg;
             }
             // every MMA issued so far must be complete before TMEM is released
@@ -175,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t quarter = warp & 3;             // TMEM lane quarter of this warp
         const uint32_t row = quarter * 32 + lane;      // key within the tile
         // the group's thread index is the key row, so stable compaction keeps position order
-        TopkGroup<kEpiThreads> topk{buf, S.hist, &S.ctl, topk_cap(a.K), static_cast<uint32_t>(a.K), row, 1};
+        TopkGroup<kEpiThreads, kTopkPer> topk{buf, S.hist, &S.ctl, topk_cap(a.K), static_cast<uint32_t>(a.K), row, 1};
         uint32_t n_it = 0;
         while (it.next(seg)) {
             const int t = seg.row;
@@ -192,8 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             topk.reset();
             bool ok = true;
+            const int32_t* bt = a.block_table + static_cast<int64_t>(row_seq(a, t)) * a.max_blocks;
             for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
                 const uint32_t acc = n_it & 1u, ause = n_it >> 1;
+                const int s = j * kTileKeys + static_cast<int>(row);
+                const int blk = (s < n) ? bt[s >> 6] : -1;  // issued before the wait: latency hidden
                 const bool got = mbar_wait(smem_u32(&S.tfull[acc]), ause & 1u, abort_flag, a.err);
                 if (named_bar_or(1, kEpiThreads, !got)) { ok = false; break; }
                 tc_fence_after();
@@ -203,20 +236,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(taddr + 32, v1);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(smem_u32(&S.tempty[acc]));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.tempty[acc]));
                 float score = 0.0f;
 #pragma unroll
                 for (int h = 0; h < 32; ++h) score = fmaf(wv[h], fmaxf(__uint_as_float(v0[h]), 0.0f), score);
 #pragma unroll
                 for (int h = 0; h < 32; ++h) score = fmaf(wv[32 + h], fmaxf(__uint_as_float(v1[h]), 0.0f), score);
-                const int s = j * kTileKeys + static_cast<int>(row);
-                bool valid = s < n;
-                if (valid) {
-                    // a tile block whose table entry was invalid was never loaded
-                    const int lb = s >> 6;
-                    const int blk = a.block_table[static_cast<int64_t>(row_seq(a, t)) * a.max_blocks + lb];
-                    valid = blk >= 0 && blk < a.num_blocks;
-                }
+                // a block whose table entry is invalid was never loaded: its keys do not count
+                const bool valid = s < n && blk >= 0 && blk < a.num_blocks;
                 topk.push(make_key(score, static_cast<uint32_t>(s)), valid);
             }
             if (!ok) break;

@@ -13,7 +13,7 @@
 namespace dsa {
 
 constexpr int kMaxSplits = 32;   // split-K pieces per attention row
-constexpr int kMaxIndexerCtas = 2048;
+constexpr int kMaxIndexerCtas = 1024;
 
 // Byte offsets of the workspace regions for one call shape.
 struct WsLayout {

@@ -14,7 +14,8 @@ namespace dsa {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kMergeThreads = 1024;
-constexpr int kMergeSmemKeys = 24576;  // 192 KB of staged candidates
+constexpr int kMergeSmemKeys = 16384;  // candidates held in registers (16 per thread)
+constexpr int kMergeHistBytes = kMergeThreads / 32 * 256 * 4;  // one 256-bin histogram per warp
 constexpr int kMaxSpans = kMaxIndexerCtas + 1;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(IndexerArgs a) {
@@ -54,45 +55,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(IndexerArgs a) {
     if (tid == 0) a.tile_prefix[a.T] = carry;
 }
 
-// Stable compaction of one span of keys into positions: writes key_pos of every key >= thr.
-__device__ __forceinline__ uint32_t emit_span(const uint64_t* span, uint32_t cnt, uint64_t thr, int32_t* out,
-                                              uint32_t out_n, uint32_t* warp_cnt, bool take_all, uint32_t limit) {
-    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    for (uint32_t base = 0; base < cnt; base += kMergeThreads) {
-        const uint32_t i = base + tid;
-        const uint64_t k = (i < cnt) ? span[i] : 0ull;
-        const bool p = (i < cnt) && (take_all || k >= thr);
-        const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, p);
-        if (lane == 0) warp_cnt[warp] = __popc(ballot);
-        __syncthreads();
-        uint32_t off = 0, total = 0;
-#pragma unroll
-        for (uint32_t w = 0; w < kMergeThreads / 32; ++w) {
-            const uint32_t c = warp_cnt[w];
-            off += (w < warp) ? c : 0u;
-            total += c;
-        }
-        const uint32_t o = out_n + off + __popc(ballot & ((1u << lane) - 1u));
-        if (p && o < limit) out[o] = key_pos(k);
-        __syncthreads();
-        out_n += total;
-    }
-    return out_n;
-}
+constexpr int kPer = kMergeSmemKeys / kMergeThreads;  // candidates per thread held in registers
 
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a) {
     extern __shared__ __align__(16) uint8_t merge_smem[];
-    uint64_t* stage = reinterpret_cast<uint64_t*>(merge_smem);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(merge_smem);  // [32 warps][256]
     __shared__ const uint64_t* span_ptr[kMaxSpans];
-    __shared__ uint32_t span_cnt[kMaxSpans];
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t warp_cnt[32];
-    __shared__ uint32_t ctl_digit, ctl_above, ctl_bucket;
+    __shared__ uint32_t span_off[kMaxSpans + 1];
+    __shared__ uint32_t warp_tot[32];
+    __shared__ TopkCtl ctl;
     __shared__ int n_spans;
     __shared__ uint32_t n_total;
 
     const int t = blockIdx.x;
-    const uint32_t tid = threadIdx.x, lane = tid & 31u;
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
     const uint32_t K = static_cast<uint32_t>(a.K);
     int32_t* out = a.idx + static_cast<int64_t>(t) * a.K;
     const int64_t p0 = a.tile_prefix[t], p1 = a.tile_prefix[t + 1], total = a.tile_prefix[a.T];
@@ -101,109 +77,122 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a
         for (uint32_t i = tid; i < K; i += kMergeThreads) out[i] = -1;
         return;
     }
-    if (tid == 0) {
+    // 1. the segments of row t: CTAs whose tile range meets [p0, p1), 32 at a time by warp 0
+    if (tid < 32) {
         const int64_t G = a.G;
-        int64_t c = (p0 * G) / total;
-        if (c > G - 1) c = G - 1;
-        while (c + 1 < G && tile_begin(c + 1, total, G) <= p0) ++c;
-        while (c > 0 && tile_begin(c, total, G) > p0) --c;
+        int64_t cf = 0;
+        if (tid == 0) {
+            cf = (p0 * G) / total;
+            if (cf > G - 1) cf = G - 1;
+            while (cf + 1 < G && tile_begin(cf + 1, total, G) <= p0) ++cf;
+            while (cf > 0 && tile_begin(cf, total, G) > p0) --cf;
+        }
+        cf = __shfl_sync(0xFFFFFFFFu, cf, 0);
         int ns = 0;
         uint32_t n = 0;
-        for (; c < G && tile_begin(c, total, G) < p1; ++c) {
-            if (tile_begin(c + 1, total, G) == tile_begin(c, total, G)) continue;  // empty CTA range
-            const int64_t slot = c + t;
-            const uint32_t cnt = static_cast<uint32_t>(a.slot_count[slot]);
-            if (ns < kMaxSpans && cnt > 0) {
-                span_ptr[ns] = a.slots + slot * a.K;
-                span_cnt[ns] = cnt;
-                ++ns;
-                n += cnt;
+        for (int64_t base = cf;; base += 32) {
+            const int64_t c = base + tid;
+            const bool in = c < G && tile_begin(c, total, G) < p1;
+            const bool seg = in && tile_begin(c + 1, total, G) > tile_begin(c, total, G);
+            const uint32_t cnt = seg ? static_cast<uint32_t>(a.slot_count[c + t]) : 0u;
+            const bool keep = cnt > 0;
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
+            uint32_t x = cnt;  // inclusive scan of the counts of this group of 32
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (tid >= static_cast<uint32_t>(o)) x += y;
             }
+            const int pos = ns + __popc(bal & ((1u << tid) - 1u));
+            if (keep && pos < kMaxSpans) {
+                span_ptr[pos] = a.slots + (c + t) * a.K;
+                span_off[pos] = n + x - cnt;
+            }
+            ns += __popc(bal);
+            n += __shfl_sync(0xFFFFFFFFu, x, 31);
+            if (!__any_sync(0xFFFFFFFFu, in)) break;
         }
-        n_spans = ns;
-        n_total = n;
+        if (tid == 0) {
+            if (ns > kMaxSpans) ns = kMaxSpans;
+            n_spans = ns;
+            span_off[ns] = n;
+            n_total = n;
+        }
     }
     __syncthreads();
-    int ns = n_spans;
+    const int ns = n_spans;
     const uint32_t n = n_total;
 
-    if (n <= K) {
+    const uint32_t per = (n + kMergeThreads - 1) / kMergeThreads;
+
+    if (per > static_cast<uint32_t>(kPer)) {
+        // Long rows (more candidates than the registers hold): radix select streaming the lists
+        // from global memory, then emit them list by list.
+        __shared__ uint32_t span_cnt[kMaxSpans];
+        for (int q = tid; q < ns; q += kMergeThreads) span_cnt[q] = span_off[q + 1] - span_off[q];
+        __syncthreads();
+        const uint64_t thr = radix_threshold<kMergeThreads>(span_ptr, span_cnt, ns, K, hist, &ctl, tid, 1);
         uint32_t out_n = 0;
-        for (int s = 0; s < ns; ++s) out_n = emit_span(span_ptr[s], span_cnt[s], 0ull, out, out_n, warp_cnt, true, K);
+        for (int q = 0; q < ns; ++q) {
+            const uint64_t* sp = span_ptr[q];
+            for (uint32_t base = 0; base < span_cnt[q]; base += kMergeThreads) {
+                const uint32_t i = base + tid;
+                const uint64_t k = (i < span_cnt[q]) ? sp[i] : 0ull;
+                const bool p = i < span_cnt[q] && k >= thr;
+                uint32_t tot;
+                const uint32_t o = out_n + group_excl_scan<kMergeThreads>(p ? 1u : 0u, warp_tot, tid, 1, tot);
+                if (p && o < K) out[o] = key_pos(k);
+                out_n += tot;
+            }
+        }
         for (uint32_t i = out_n + tid; i < K; i += kMergeThreads) out[i] = -1;
         return;
     }
 
-    // stage into shared memory when the candidates fit (one read of global memory)
-    if (n <= static_cast<uint32_t>(kMergeSmemKeys)) {
-        uint32_t off = 0;
-        for (int s = 0; s < ns; ++s) {
-            const uint64_t* src = span_ptr[s];
-            for (uint32_t i = tid; i < span_cnt[s]; i += kMergeThreads) stage[off + i] = src[i];
-            off += span_cnt[s];
+    // 2. load: thread tid owns the contiguous candidates [c0, c1) of the concatenated lists
+    const uint32_t c0 = min(n, tid * per), c1 = min(n, c0 + per);
+    const uint32_t cnt = c1 - c0;
+    uint64_t keys[kPer];
+    {
+        int sp = 0;
+        if (cnt) {
+            int lo = 0, hi = ns - 1;  // last list starting at or before c0
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (span_off[mid] <= c0) lo = mid;
+                else hi = mid - 1;
+            }
+            sp = lo;
         }
-        __syncthreads();
-        if (tid == 0) {
-            span_ptr[0] = stage;
-            span_cnt[0] = n;
-            n_spans = 1;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const uint32_t g = c0 + j;
+            keys[j] = 0ull;
+            if (static_cast<uint32_t>(j) < cnt) {
+                while (g >= span_off[sp + 1]) ++sp;
+                keys[j] = span_ptr[sp][g - span_off[sp]];
+            }
         }
-        __syncthreads();
-        ns = 1;
     }
 
-    // MSB-first radix select of the K-th largest key over the spans
-    uint64_t prefix = 0;
-    uint32_t rem = K;
-    for (int shift = 56; shift >= 0; shift -= 8) {
-        for (uint32_t i = tid; i < 256; i += kMergeThreads) hist[i] = 0;
-        __syncthreads();
-        for (int s = 0; s < ns; ++s) {
-            const uint64_t* sp = span_ptr[s];
-            const uint32_t cnt = span_cnt[s];
-            for (uint32_t i = tid; i < cnt; i += kMergeThreads) {
-                const uint64_t k = sp[i];
-                const bool match = (shift == 56) || ((k >> (shift + 8)) == (prefix >> (shift + 8)));
-                if (match) atomicAdd(&hist[(k >> shift) & 255u], 1u);
-            }
-        }
-        __syncthreads();
-        if (tid < 32) {
-            uint32_t s = 0;
+    // 3. threshold: exactly K keys are >= thr (thr = 0 keeps every candidate when n <= K)
+    uint64_t thr = 0ull;
+    if (n > K) thr = reg_radix_threshold<kMergeThreads, kPer>(keys, cnt, K, hist, &ctl, tid, 1);
+
+    // 4. emit the positions of the kept keys in candidate order (= ascending position)
+    uint32_t mine = 0;
 #pragma unroll
-            for (int b = 0; b < 8; ++b) s += hist[lane * 8 + b];
-            uint32_t S = s;
+    for (int j = 0; j < kPer; ++j) mine += (static_cast<uint32_t>(j) < cnt && keys[j] >= thr) ? 1u : 0u;
+    uint32_t kept;
+    uint32_t o = group_excl_scan<kMergeThreads>(mine, warp_tot, tid, 1, kept);
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, S, o);
-                if (lane + o < 32) S += v;
-            }
-            const uint32_t mask = __ballot_sync(0xFFFFFFFFu, S >= rem);
-            const int L = 31 - __clz(mask);
-            if (static_cast<int>(lane) == L) {
-                uint32_t running = S - s;
-                for (int b = 7; b >= 0; --b) {
-                    const uint32_t h = hist[lane * 8 + b];
-                    if (running + h >= rem) {
-                        ctl_digit = lane * 8 + b;
-                        ctl_above = running;
-                        ctl_bucket = h;
-                        break;
-                    }
-                    running += h;
-                }
-            }
+    for (int j = 0; j < kPer; ++j) {
+        if (static_cast<uint32_t>(j) < cnt && keys[j] >= thr) {
+            if (o < K) out[o] = key_pos(keys[j]);
+            ++o;
         }
-        __syncthreads();
-        rem -= ctl_above;
-        prefix |= static_cast<uint64_t>(ctl_digit) << shift;
-        const bool done = (ctl_bucket == rem);
-        __syncthreads();
-        if (done) break;
     }
-    uint32_t out_n = 0;
-    for (int s = 0; s < ns; ++s) out_n = emit_span(span_ptr[s], span_cnt[s], prefix, out, out_n, warp_cnt, false, K);
-    for (uint32_t i = out_n + tid; i < K; i += kMergeThreads) out[i] = -1;
+    for (uint32_t i = kept + tid; i < K; i += kMergeThreads) out[i] = -1;
 }
 
 bool launch_plan(const IndexerArgs& a, cudaStream_t s, int* launches) {
@@ -214,7 +203,7 @@ bool launch_plan(const IndexerArgs& a, cudaStream_t s, int* launches) {
 
 bool launch_merge(const IndexerArgs& a, cudaStream_t s, int* launches) {
     if (a.T == 0) return true;
-    const size_t smem = static_cast<size_t>(kMergeSmemKeys) * sizeof(uint64_t);
+    const size_t smem = kMergeHistBytes;
     if (cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return false;
