@@ -1,23 +1,28 @@
 // Sparse MQA attention over gathered latent rows on tcgen05 tensor cores, for 128 query heads and
-// 576-wide rows with the first 512 columns as values ("Day0 Inference Support ... on Huawei
-// Ascend CANN Architecture" §1: sparse flash attention reads the KV pairs at the Top-K positions;
-// §2.1: it reads the main KV exactly at the selected indices).
+// 576-wide rows whose first 512 columns are the values ("Day0 Inference Support ... on Huawei
+// Ascend CANN Architecture" §1: a sparse flash attention module reads the KV pairs at the Top-K
+// positions; §2.1: it reads the main KV exactly at the selected indices).
 //
-// One CTA = (query row t, value half, split of the K selected rows). With the 128 heads stacked
-// as M, every 16-row tile of gathered rows is two dense contractions:
-//   S[128 x 16]  = Q[128 x 576] . R^T          (tcgen05, A = Q in smem, B = rows, K-major)
-//   O[128 x 256] += P[128 x 16] . R[:, half]    (tcgen05, A = P in TMEM, B = rows, MN-major)
-// with an online softmax between them (one thread per head, lazy rescaling of O in TMEM only when
-// a head's running maximum grows by more than 2^8). The value columns are split across two CTAs
-// because O for all 512 columns would need the whole tensor memory; each CTA computes S itself.
+// Work unit: a cluster of two CTAs per (query row t, split of its K selected rows). The pair
+// divides the latent dimension: CTA 0 owns columns 0..255, CTA 1 owns columns 256..575. For every
+// tile of 64 gathered rows each CTA
+//   1. gathers only its columns of the 64 rows (the index list drives TMA tile::gather4 row
+//      gathers into the 128-byte-swizzled layout the tensor core reads),
+//   2. computes its partial logits S_r[128 heads x 64 rows] = Q[:, cols_r] . R[:, cols_r]^T with
+//      tcgen05 (M = 128 heads, N = 64 rows; an MMA of N < 64 would leave the tensor pipe idle),
+//   3. sends S_r to the other CTA through distributed shared memory and adds the one it receives
+//      (S_0 + S_1 in both CTAs: fp32 addition commutes, so both see the same logits),
+//   4. runs the online softmax (one thread per head, lazy rescaling of O when a head's running
+//      maximum grows by more than 2^8) and writes P as bf16 over its S in tensor memory,
+//   5. accumulates O_r[128 x 256] += P . V_r with V_r = its 256 value columns (CTA 0: values
+//      0..255, CTA 1: values 256..511 -- both inside the columns it already holds).
+// No row byte is loaded twice and no product is computed twice. The O accumulator (256 fp32
+// columns) plus two S/P buffers fit the 512 tensor-memory columns; CTA 1 keeps the last 64 query
+// columns in tensor memory (A operand from TMEM) so that its shared memory holds 3 row stages.
 //
-// The index list drives the staging: the physical row of every selected position is resolved
-// through the block table once per CTA, then 128 producer threads gather each tile's rows with
-// 16-byte cp.async into the 128-byte-swizzled layout the MMA reads, arriving on the tile's
-// mbarrier when their copies land.
-//
-// Roles (288 threads): warps 0-3 softmax / epilogue (one head per thread), warps 4-7 producers,
-// warp 8 TMEM allocator + MMA issuer (+ the TMA load of Q).
+// Roles (288 threads per CTA): warps 0-3 softmax / epilogue (thread = head = TMEM lane), warps
+// 4-6 gather producers (warp 4 + s owns row stage s), warp 7 idle, warp 8 TMEM allocator + MMA
+// issuer (+ the TMA load of the query).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -28,36 +33,39 @@ namespace tcattn {
 constexpr int kHeads = 128;
 constexpr int kD = 576;
 constexpr int kDV = 512;
-constexpr int kDVH = 256;
-constexpr int kRows = 16;  // gathered rows per tile
-constexpr int kChunks = kD / 64;
-constexpr int kStages = 4;
-constexpr int kQChunkBytes = kHeads * 128;              // [128 heads x 64 bf16]
-constexpr int kQBytes = kChunks * kQChunkBytes;         // 144 KB
-constexpr int kKvChunkBytes = kRows * 128;              // [16 rows x 64 bf16]
-constexpr int kKvStageBytes = kChunks * kKvChunkBytes;  // 18 KB
+constexpr int kDVH = 256;              // value columns per CTA
+constexpr int kRows = 64;              // gathered rows per tile
+constexpr int kStages = 3;
+constexpr int kChunkBytes = kRows * 128;      // [64 rows x 64 bf16]
+constexpr int kQChunkBytes = kHeads * 128;    // [128 heads x 64 bf16]
+constexpr int kQSmemChunks = 4;               // query chunks in shared memory (both CTAs)
+constexpr int kMaxChunks = 5;                 // row chunks per CTA (CTA 0: 4, CTA 1: 5)
+constexpr int kStageBytes = kMaxChunks * kChunkBytes;
+constexpr int kXBytes = kHeads * kRows * 4;   // one partial-logit tile (fp32)
 constexpr int kMaxRows = 2048;
 constexpr int kThreads = 288;
-constexpr int kNB = 4;          // S / P buffers (tiles the tensor core may run ahead of softmax)
-constexpr int kPrefetch = 8;    // tiles of gathered rows prefetched into L2 ahead of their cp.async
+constexpr int kPrefetchTiles = 9;  // tiles of rows prefetched into L2 ahead of their copy (a multiple of kStages)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColP = kColS + kNB * kRows;
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // S/P buffers at 256 and 320
 constexpr uint32_t kIdescQK = idesc_f16(128, kRows, 1u, 0u, 0u);
 constexpr uint32_t kIdescPV = idesc_f16(128, kDVH, 1u, 0u, 1u);
 
 struct Smem {
     uint64_t full[kStages], empty[kStages];
-    uint64_t s_full[kNB], s_empty[kNB], p_full[kNB], p_empty[kNB];
+    uint64_t s_full[2], p_full[2], s_free[2];
     uint64_t qfull, o_full, mma_done;
+    uint64_t xfull, xempty;  // arrived on by the other CTA of the pair
     uint32_t tmem_base;
     int abort_flag;
 };
 
 constexpr size_t kOffQ = 0;
-constexpr size_t kOffKv = kOffQ + kQBytes;
-constexpr size_t kOffPhys = kOffKv + static_cast<size_t>(kStages) * kKvStageBytes;
+constexpr size_t kOffKv = kOffQ + static_cast<size_t>(kQSmemChunks) * kQChunkBytes;
+constexpr size_t kOffX = kOffKv + static_cast<size_t>(kStages) * kStageBytes;
+constexpr size_t kOffPhys = kOffX + kXBytes;
 constexpr size_t kOffCtl = kOffPhys + kMaxRows * sizeof(int32_t);
 constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(Smem);
+static_assert(kSmemBytes <= 232448, "attention shared memory over the limit");
 
 __host__ __device__ inline int split_rows(int K, int S) {
     const int per = (K + S - 1) / S;
@@ -66,17 +74,29 @@ __host__ __device__ inline int split_rows(int K, int S) {
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap map_q) {
+// Exchange-buffer byte offset of head h's 16-byte group g (64 fp32 per head, 16 groups), swizzled
+// by the head index so that the 32 heads of a warp hit distinct banks.
+__device__ __forceinline__ uint32_t xoff(int h, int g) {
+    return static_cast<uint32_t>(h * (kRows * 4) + ((g ^ (h & 15)) << 4));
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
+    attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem + kOffQ);
     const uint32_t sKv = smem_u32(smem + kOffKv);
+    const uint32_t sX = smem_u32(smem + kOffX);
     int32_t* phys_s = reinterpret_cast<int32_t*>(smem + kOffPhys);
     Smem& S = *reinterpret_cast<Smem*>(smem + kOffCtl);
     volatile int* abort_flag = &S.abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int half = blockIdx.x & 1, split = blockIdx.x >> 1, t = blockIdx.y;
+    const uint32_t rank = cluster_ctarank();  // 0: columns 0..255, 1: columns 256..575
+    const uint32_t peer = rank ^ 1u;
+    const int nchunks = rank ? 5 : 4;         // row chunks of 64 columns this CTA gathers
+    const int c0 = rank ? 4 : 0;              // first global chunk
+    const int split = blockIdx.x >> 1, t = blockIdx.y;
     const int R = split_rows(a.K, a.S);
     const int r0 = split * R;
     const int r1 = min(a.K, r0 + R);
@@ -91,15 +111,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
             mbar_init(smem_u32(&S.full[i]), 1);
             mbar_init(smem_u32(&S.empty[i]), 1);
         }
-        for (int i = 0; i < kNB; ++i) {
+        for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&S.s_full[i]), 1);
-            mbar_init(smem_u32(&S.s_empty[i]), 4);  // one elected arrive per softmax warp
-            mbar_init(smem_u32(&S.p_full[i]), 4);
-            mbar_init(smem_u32(&S.p_empty[i]), 1);
+            mbar_init(smem_u32(&S.p_full[i]), 4);  // one elected arrive per softmax warp
+            mbar_init(smem_u32(&S.s_free[i]), 1);
         }
         mbar_init(smem_u32(&S.qfull), 1);
         mbar_init(smem_u32(&S.o_full), 1);
         mbar_init(smem_u32(&S.mma_done), 1);
+        mbar_init(smem_u32(&S.xfull), 4);   // the peer's four softmax warps
+        mbar_init(smem_u32(&S.xempty), 4);
         S.abort_flag = 0;
         fence_mbar_init();
     }
@@ -108,14 +129,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
 
     if (warp == 8 && lane == 0 && ntiles > 0) {
-        mbar_arrive_expect_tx(smem_u32(&S.qfull), kQBytes);
-        for (int c = 0; c < kChunks; ++c)
-            tma_load_2d(sQ + c * kQChunkBytes, &map_q, c * 64, t * kHeads, smem_u32(&S.qfull));
+        mbar_arrive_expect_tx(smem_u32(&S.qfull), kQSmemChunks * kQChunkBytes);
+        for (int c = 0; c < kQSmemChunks; ++c)
+            tma_load_2d(sQ + c * kQChunkBytes, &map_q, (c0 + c) * 64, t * kHeads, smem_u32(&S.qfull));
+    }
+    if (rank == 1 && warp < 4 && ntiles > 0) {
+        // query columns 512..575 (the fifth chunk of CTA 1) go to tensor memory, packed in pairs
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
+                                                           (static_cast<int64_t>(t) * kHeads + threadIdx.x) * kD + 512);
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 v = src[i];
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+        tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + kColQ, w);
+        tmem_st_wait();
     }
     // resolve every selected position of this split to its physical cache row once
     for (int i = threadIdx.x; i < nrows; i += kThreads) {
@@ -132,137 +169,175 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
         }
         phys_s[i] = p;
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
 
-    if (warp >= 4 && warp < 8) {
+    if (warp >= 4 && warp < 4 + kStages) {
         // ------------------------------------------------------------- gather producers
-        // Producer warp w fills stage w with tiles w, w + 4, ...: its 32 lanes copy the tile's
-        // 16 rows x 72 16-byte units with cp.async, wait for their own copies, and one lane
-        // arrives on the stage's barrier. Rows of later tiles are prefetched into L2 first.
+        // Producer warp w owns stage w and fills tiles w, w + 3, ...: successive fills of a stage
+        // come from one warp, so each waits for exactly the previous use's release. The index
+        // list drives TMA row gathers: one tile::gather4 per 4 rows x one 64-column chunk, straight
+        // into the 128-byte-swizzled layout (rows with no position read as zeros).
         const int pw = warp - 4;
         const uint8_t* kv = static_cast<const uint8_t*>(a.kv);
         auto prefetch_tile = [&](int i) {
-            const int row = i * kRows + lane;
-            if (lane < kRows && i < ntiles && row < nrows) {
-                const int p = phys_s[row];
+            if (i >= ntiles) return;
+            for (int rr = lane; rr < kRows; rr += 32) {
+                const int row = i * kRows + rr;
+                const int p = (row < nrows) ? phys_s[row] : -1;
                 if (p >= 0)
-                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kv + static_cast<int64_t>(p) * (kD * 2)),
-                                 "r"(kD * 2)
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                     kv + static_cast<int64_t>(p) * (kD * 2) + c0 * 128),
+                                 "r"(nchunks * 128)
                                  : "memory");
             }
         };
-        prefetch_tile(pw);
-        prefetch_tile(pw + kStages);
+        if (lane == 0) tma_prefetch_desc(&map_kv);
+        for (int i = pw; i < kPrefetchTiles; i += kStages) prefetch_tile(i);
         for (int i = pw; i < ntiles; i += kStages) {
-            prefetch_tile(i + 2 * kStages);
+            prefetch_tile(i + kPrefetchTiles - (kPrefetchTiles % kStages));
             const int st = pw, use = i / kStages;
             const bool got = mbar_wait(smem_u32(&S.empty[st]), (use & 1) ^ 1, abort_flag, a.err);
             if (!__all_sync(0xFFFFFFFFu, got)) break;
-            const uint32_t base = sKv + st * kKvStageBytes;
-#pragma unroll 4
-            for (int e = lane; e < kRows * (kD / 8); e += 32) {
-                const int r = e / (kD / 8), u = e % (kD / 8);
-                const int c = u >> 3, sub = u & 7;
-                const int row = i * kRows + r;
-                const int p = (row < nrows) ? phys_s[row] : -1;
-                const uint32_t dst = base + c * kKvChunkBytes + r * 128 + ((sub ^ (r & 7)) << 4);
-                cp_async16(dst, (p >= 0) ? kv + static_cast<int64_t>(p) * (kD * 2) + u * 16 : kv, (p >= 0) ? 16u : 0u);
-            }
-            cp_async_wait_all();
-            fence_proxy_async_smem();
+            const uint32_t fb = smem_u32(&S.full[st]);
+            if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kRows * nchunks * 128));
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&S.full[st]));
+            const uint32_t base = sKv + st * kStageBytes;
+            if (lane < kRows / 4) {  // lane g gathers rows 4g..4g+3 of the tile, all chunks
+                int rw[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int row = i * kRows + 4 * lane + j;
+                    rw[j] = (row < nrows) ? phys_s[row] : -1;  // -1: outside the tensor -> zeros
+                }
+                for (int cc = 0; cc < nchunks; ++cc)
+                    tma_gather4(base + cc * kChunkBytes + lane * 4 * 128, &map_kv, (c0 + cc) * 64, rw[0], rw[1],
+                                rw[2], rw[3], fb);
+            }
         }
-        cp_async_wait_all();
     } else if (warp == 8) {
         // ------------------------------------------------------------- MMA issuer
-        // Polls instead of blocking: QK of a tile is issued as soon as its rows have landed and an
-        // S buffer is free; PV as soon as softmax has written P. The tensor core thus computes S
-        // for the next tiles while softmax works on the current one.
         if (lane == 0 && ntiles > 0) {
             bool ok = mbar_wait(smem_u32(&S.qfull), 0, abort_flag, a.err);
             const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
             const uint64_t dkv0 = sw128_desc(sKv, 16, 1024);
-            const uint64_t dv0 = sw128_desc(sKv + (4 * half) * kKvChunkBytes, kKvChunkBytes, 1024);
-            int qk = 0, pv = 0;
-            long long t_idle = 0;
-            while (ok && pv < ntiles) {
-                bool did = false;
-                if (pv < qk && mbar_test(smem_u32(&S.p_full[pv % kNB]), (pv / kNB) & 1)) {
-                    tc_fence_after();
-                    const uint64_t vd = dv0 + static_cast<uint64_t>(((pv % kStages) * kKvStageBytes) >> 4);
-                    mma_ts(tmem + kColO, tmem + kColP + (pv % kNB) * (kRows / 2), vd, kIdescPV, pv > 0 ? 1u : 0u);
-                    tc_commit(smem_u32(&S.empty[pv % kStages]));
-                    tc_commit(smem_u32(&S.p_empty[pv % kNB]));
-                    ++pv;
-                    did = true;
-                } else if (qk < ntiles && qk - pv < kNB &&
-                           mbar_test(smem_u32(&S.full[qk % kStages]), (qk / kStages) & 1) &&
-                           mbar_test(smem_u32(&S.s_empty[qk % kNB]), ((qk / kNB) & 1) ^ 1)) {
-                    tc_fence_after();
-                    const uint32_t d = tmem + kColS + (qk % kNB) * kRows;
-                    const uint64_t kvb = dkv0 + static_cast<uint64_t>(((qk % kStages) * kKvStageBytes) >> 4);
+            const uint64_t dv0 = sw128_desc(sKv, kChunkBytes, 1024);  // V: MN-major, atoms 8 KB apart
+            auto qk = [&](int i) -> bool {
+                const int st = i % kStages;
+                if (!mbar_wait(smem_u32(&S.full[st]), (i / kStages) & 1, abort_flag, a.err)) return false;
+                tc_fence_after();
+                const uint32_t d = tmem + kColS + (i & 1) * kRows;
+                const uint64_t kvb = dkv0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
+                for (int c = 0; c < kQSmemChunks; ++c) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = dq0 + static_cast<uint64_t>((c * kQChunkBytes + kk * 32) >> 4);
-                            const uint64_t bd = kvb + static_cast<uint64_t>((c * kKvChunkBytes + kk * 32) >> 4);
-                            mma_ss(d, ad, bd, kIdescQK, (c | kk) != 0 ? 1u : 0u);
-                        }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = dq0 + static_cast<uint64_t>((c * kQChunkBytes + kk * 32) >> 4);
+                        const uint64_t bd = kvb + static_cast<uint64_t>((c * kChunkBytes + kk * 32) >> 4);
+                        mma_ss(d, ad, bd, kIdescQK, (c | kk) != 0 ? 1u : 0u);
                     }
-                    tc_commit(smem_u32(&S.s_full[qk % kNB]));
-                    ++qk;
-                    did = true;
                 }
-                if (did) {
-                    t_idle = 0;
-                } else if (t_idle == 0) {
-                    t_idle = clock64();
-                } else if (*abort_flag) {
-                    ok = false;
-                } else if (clock64() - t_idle > kWaitCycles) {
-                    *abort_flag = 1;
-                    atomicOr(a.err, DSA_FAULT_TIMEOUT);
-                    ok = false;
+                if (nchunks == 5) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t bd = kvb + static_cast<uint64_t>((4 * kChunkBytes + kk * 32) >> 4);
+                        mma_ts(d, tmem + kColQ + kk * 8, bd, kIdescQK, 1u);
+                    }
                 }
+                tc_commit(smem_u32(&S.s_full[i & 1]));
+                return true;
+            };
+            if (ok) ok = qk(0);
+            if (ok && ntiles > 1) ok = qk(1);
+            for (int i = 0; ok && i < ntiles; ++i) {
+                ok = mbar_wait(smem_u32(&S.p_full[i & 1]), (i >> 1) & 1, abort_flag, a.err);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t vb = dv0 + static_cast<uint64_t>(((i % kStages) * kStageBytes) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < kRows / 16; ++kk) {
+                    const uint64_t vd = vb + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+                    mma_ts(tmem + kColO, tmem + kColS + (i & 1) * kRows + kk * 8, vd, kIdescPV,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(smem_u32(&S.empty[i % kStages]));
+                tc_commit(smem_u32(&S.s_free[i & 1]));
+                if (i + 2 < ntiles) ok = qk(i + 2);  // same S buffer: the pipe runs PV(i) first
             }
             if (ok) tc_commit(smem_u32(&S.o_full));
             tc_commit(smem_u32(&S.mma_done));
             mbar_wait_drain(smem_u32(&S.mma_done), 0, a.err);
         }
-    } else {
+    } else if (warp < 4) {
         // ------------------------------------------------------------- softmax + epilogue
         const int h = threadIdx.x;  // head = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const float scale2 = a.sm_scale * 1.4426950408889634f;  // logits in log2 units
+        const uint32_t peer_x = mapa_shared(sX, peer);
+        const uint32_t peer_xfull = mapa_shared(smem_u32(&S.xfull), peer);
+        const uint32_t peer_xempty = mapa_shared(smem_u32(&S.xempty), peer);
         float m_ref = -INFINITY, l = 0.0f;
         bool dead = false;
         for (int i = 0; i < ntiles; ++i) {
-            const int sb = i % kNB;
-            bool got = mbar_wait(smem_u32(&S.s_full[sb]), (i / kNB) & 1, abort_flag, a.err);
+            const int sb = i & 1;
+            bool got = mbar_wait(smem_u32(&S.s_full[sb]), (i >> 1) & 1, abort_flag, a.err);
             if (named_bar_or(2, 128, dead || !got)) { dead = true; break; }
             tc_fence_after();
-            uint32_t sv[16];
-            tmem_ld16(tmem + lane_base + kColS + sb * kRows, sv);
+            uint32_t v0[32], v1[32];
+            const uint32_t sa = tmem + lane_base + kColS + sb * kRows;
+            tmem_ld32(sa, v0);
+            tmem_ld32(sa + 32, v1);
             tmem_ld_wait();
-            tc_fence_before();
+            // send this CTA's partial logits to the peer ...
+            got = mbar_wait_cluster(smem_u32(&S.xempty), (i & 1) ^ 1, abort_flag, a.err);
+            if (__any_sync(0xFFFFFFFFu, !got)) dead = true;
+            if (!dead) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    st_cluster_v4(peer_x + xoff(h, g), __uint_as_float(v0[4 * g]), __uint_as_float(v0[4 * g + 1]),
+                                  __uint_as_float(v0[4 * g + 2]), __uint_as_float(v0[4 * g + 3]));
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    st_cluster_v4(peer_x + xoff(h, 8 + g), __uint_as_float(v1[4 * g]), __uint_as_float(v1[4 * g + 1]),
+                                  __uint_as_float(v1[4 * g + 2]), __uint_as_float(v1[4 * g + 3]));
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&S.s_empty[sb]));
+            if (lane == 0) mbar_arrive_remote(peer_xfull);
+            // ... and add the peer's
+            got = mbar_wait_cluster(smem_u32(&S.xfull), i & 1, abort_flag, a.err);
+            if (__any_sync(0xFFFFFFFFu, !got)) dead = true;
             float z[kRows];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                z[j] = __uint_as_float(v0[j]);
+                z[32 + j] = __uint_as_float(v1[j]);
+            }
+            if (!dead) {
+#pragma unroll
+                for (int g = 0; g < 16; ++g) {
+                    const float4 o = *reinterpret_cast<const float4*>(smem + kOffX + xoff(h, g));
+                    z[4 * g] += o.x;
+                    z[4 * g + 1] += o.y;
+                    z[4 * g + 2] += o.z;
+                    z[4 * g + 3] += o.w;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(peer_xempty);  // the peer may refill our buffer
             float mt = -INFINITY;
 #pragma unroll
             for (int j = 0; j < kRows; ++j) {
                 const int row = i * kRows + j;
                 const bool valid = row < nrows && phys_s[row] >= 0;
-                z[j] = valid ? __uint_as_float(sv[j]) * scale2 : -INFINITY;
+                z[j] = valid ? z[j] * scale2 : -INFINITY;
                 mt = fmaxf(mt, z[j]);
             }
             const bool need = mt > m_ref + 8.0f;
             if (__any_sync(0xFFFFFFFFu, need)) {
                 const float m_new = need ? mt : m_ref;
                 if (i > 0) {
-                    got = mbar_wait(smem_u32(&S.p_empty[(i - 1) % kNB]), ((i - 1) / kNB) & 1, abort_flag, a.err);
+                    got = mbar_wait(smem_u32(&S.s_free[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort_flag, a.err);
                     if (__any_sync(0xFFFFFFFFu, !got)) dead = true;
                     if (!dead) {
                         tc_fence_after();
@@ -292,18 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
                 packed[j / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) |
                                 (static_cast<uint32_t>(__bfloat16_as_ushort(b1)) << 16);
             }
-            if (i >= kNB) {
-                got = mbar_wait(smem_u32(&S.p_empty[i % kNB]), ((i - kNB) / kNB) & 1, abort_flag, a.err);
-                if (__any_sync(0xFFFFFFFFu, !got)) dead = true;
-            }
-            if (!dead) {
-                tc_fence_after();
-                tmem_st8(tmem + lane_base + kColP + (i % kNB) * (kRows / 2), packed);
+            if (!dead) {  // P (bf16) over the first 32 columns of this tile's S
+                tmem_st32(sa, packed);
                 tmem_st_wait();
                 tc_fence_before();
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&S.p_full[i % kNB]));
+            if (lane == 0) mbar_arrive(smem_u32(&S.p_full[sb]));
         }
         if (ntiles > 0) {  // every softmax thread takes this barrier, dead or not
             const bool got = dead ? false : mbar_wait(smem_u32(&S.o_full), 0, abort_flag, a.err);
@@ -314,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
         const int64_t prow = (static_cast<int64_t>(t) * a.S + split) * kHeads + h;
         if (a.S == 1) {
             const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
-            uint16_t* out = static_cast<uint16_t*>(a.out) + (static_cast<int64_t>(t) * kHeads + h) * kDV + half * kDVH;
+            uint16_t* out =
+                static_cast<uint16_t*>(a.out) + (static_cast<int64_t>(t) * kHeads + h) * kDV + rank * kDVH;
 #pragma unroll 1
             for (int cc = 0; cc < kDVH / 32; ++cc) {
                 uint32_t v[32];
@@ -334,11 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
 #pragma unroll
                 for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             }
-            if (half == 0 && a.lse)
+            if (rank == 0 && a.lse)
                 a.lse[static_cast<int64_t>(t) * kHeads + h] =
                     (l > 0.0f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
         } else {
-            float* po = a.part_o + prow * kDV + half * kDVH;
+            float* po = a.part_o + prow * kDV + rank * kDVH;
 #pragma unroll 1
             for (int cc = 0; cc < kDVH / 32; ++cc) {
                 uint32_t v[32];
@@ -347,15 +418,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
                     tmem_ld_wait();
                 }
                 float4* dst = reinterpret_cast<float4*>(po + cc * 32);
+                const bool zero = !(have_o && l > 0.0f);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const bool z = !(have_o && l > 0.0f);
-                    dst[q] = z ? make_float4(0.f, 0.f, 0.f, 0.f)
-                               : make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-                }
+                for (int q = 0; q < 8; ++q)
+                    dst[q] = zero ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                  : make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
             }
-            if (half == 0) {
+            if (rank == 0) {
                 a.part_ml[prow * 2] = (l > 0.0f) ? m_ref : -INFINITY;
                 a.part_ml[prow * 2 + 1] = l;
             }
@@ -363,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, const 
     }
 
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();  // no remote access to this CTA's shared memory may follow its exit
     if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -411,11 +481,15 @@ bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches) {
     if (!make_tmap_2d(&map_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcattn::kD,
                       static_cast<uint64_t>(a.T) * tcattn::kHeads, tcattn::kD * 2, 64, 128))
         return false;
+    CUtensorMap map_kv;  // [num_blocks * 64 rows][576 cols], gathered one row x 64 columns at a time
+    if (!make_tmap_2d(&map_kv, a.kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcattn::kD,
+                      static_cast<uint64_t>(a.num_blocks) * kBlock, tcattn::kD * 2, 64, 1))
+        return false;
     if (cudaFuncSetAttribute(tcattn::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(tcattn::kSmemBytes)) != cudaSuccess)
         return false;
     dim3 grid(2 * a.S, a.T);
-    tcattn::attn_tc_kernel<<<grid, tcattn::kThreads, tcattn::kSmemBytes, s>>>(a, map_q);
+    tcattn::attn_tc_kernel<<<grid, tcattn::kThreads, tcattn::kSmemBytes, s>>>(a, map_q, map_kv);
     ++*launches;
     if (cudaGetLastError() != cudaSuccess) return false;
     if (a.S > 1) {
