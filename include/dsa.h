@@ -54,7 +54,8 @@ typedef enum {
     DSA_ERR_WORKSPACE = 3,   /* ws == NULL or ws_bytes < dsa_workspace_size(...) */
     DSA_ERR_LAUNCH = 4,      /* a CUDA launch or tensor-map encode failed */
     DSA_ERR_DEVICE = 5,      /* dsa_read_error found a device-side fault bit (see DSA_FAULT_*) */
-    DSA_ERR_TIMEOUT = 6      /* dsa_read_error found a pipeline wait that gave up */
+    DSA_ERR_TIMEOUT = 6,     /* dsa_read_error found a pipeline wait that gave up */
+    DSA_ERR_TOO_LARGE = 7    /* dsa_indexer_topk_noalloc: the call needs more than its static scratch */
 } dsa_status;
 
 /* bits of the device error word */
@@ -142,6 +143,36 @@ dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, con
                       const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens, const void* q,
                       const void* kv_cache, float sm_scale, int32_t* idx, void* out, float* lse, void* ws,
                       size_t ws_bytes, dsa_stream_t stream);
+
+/*
+ * Indexer + Top-K that allocates nothing and takes no workspace: the same computation and kernels
+ * as dsa_indexer_topk (arguments as there), with the scratch in one statically sized device
+ * buffer inside libdsa.so (DSA_NOALLOC_SCRATCH_BYTES per device).
+ *
+ * The method's pages have no counterpart of this call: it serves callers that cannot allocate
+ * device memory or hand over a workspace -- code running inside another framework's caching
+ * allocator or memory pool that forbids raw allocations, plugins whose host owns all device
+ * memory, and launch sequences that must not change the device's memory map between calls.
+ *
+ *   fault_word  optional DEVICE int32 (may be NULL) that receives this call's DSA_FAULT_* bits,
+ *               copied on `stream` after the kernels; bad rows are skipped as in dsa_indexer_topk.
+ *
+ * The first call on each device (with that device current) resolves the device address of the
+ * static buffer (cudaGetSymbolAddress); make that first call before any stream capture. Every
+ * call then clears the buffer's error word on `stream` and launches the same kernels as
+ * dsa_indexer_topk. All calls on one device share the one buffer: calls that overlap in time
+ * (different streams or threads without ordering between them) race and give wrong indices;
+ * order them on one stream.
+ * Returns DSA_ERR_TOO_LARGE, launching nothing, when the indexer's scratch (error word, work plan
+ * and candidate lists: about (indexer CTAs + T) * K * 8 bytes) exceeds DSA_NOALLOC_SCRATCH_BYTES
+ * (for K = 2048: T <= 871 rows with the 64 x 128 bf16 indexer on 152 SMs);
+ * DSA_ERR_LAUNCH when the set-up or a launch fails.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES (16u << 20)
+dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+                                    const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                                    const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx,
+                                    int32_t* fault_word, dsa_stream_t stream);
 
 /* Synchronises `stream`, copies the device error word of `ws` to *fault_bits (may be NULL) and
  * clears it. Returns DSA_OK when no bit was set, DSA_ERR_TIMEOUT when DSA_FAULT_TIMEOUT was set,

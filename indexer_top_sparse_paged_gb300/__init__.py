@@ -10,6 +10,8 @@ Entry points (same names as the C ABI):
 * :func:`indexer_topk` -- lightning indexer + Top-K: ``idx[T][K]`` of the selected positions.
 * :func:`sparse_attn` -- sparse attention over the rows ``idx`` selects.
 * :func:`decode` -- both, fused on one stream, for one query row per sequence.
+* :func:`indexer_topk_noalloc` -- :func:`indexer_topk` with the library's static scratch instead of
+  a workspace, for callers that cannot allocate device memory.
 """
 from __future__ import annotations
 
@@ -24,7 +26,7 @@ _lib = None
 
 MODES = {"f32": 0, "bf16": 1, "bf16_kfp8": 2}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "launch", 5: "device fault",
-          6: "timeout"}
+          6: "timeout", 7: "too large for the static scratch"}
 
 
 class Dims(ctypes.Structure):
@@ -57,6 +59,8 @@ def lib():
         L.dsa_sparse_attn.argtypes = [D, P, P, P, P, P, P, I32, ctypes.c_float, P, P, P, SZ, P]
         L.dsa_decode.restype = ctypes.c_int
         L.dsa_decode.argtypes = [D, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, SZ, P]
+        L.dsa_indexer_topk_noalloc.restype = ctypes.c_int
+        L.dsa_indexer_topk_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, I32, P, P, P]
         L.dsa_read_error.restype = ctypes.c_int
         L.dsa_read_error.argtypes = [P, ctypes.POINTER(I32), P]
         L.dsa_last_launch_count.restype = I32
@@ -114,6 +118,23 @@ def indexer_topk(dims: Dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens
     st = lib().dsa_indexer_topk(ctypes.byref(dims), _p(q_I), _p(w), _p(k_I_cache), _p(k_I_scale), _p(block_table),
                                 _p(seq_lens), _p(q_seq), _p(q_pos), T, _p(idx), _p(ws), ws.numel(), _stream(stream))
     _check("dsa_indexer_topk", st)
+    return idx
+
+
+def indexer_topk_noalloc(dims: Dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, q_seq=None, q_pos=None,
+                         *, idx=None, fault_word=None, stream=None) -> torch.Tensor:
+    """As :func:`indexer_topk`, without a workspace: the library's static scratch is used.
+
+    ``fault_word`` (optional int32 device tensor of one element) receives the call's fault bits.
+    Calls must be ordered on one stream (they share the scratch).
+    """
+    T = q_I.shape[0]
+    if idx is None:
+        idx = torch.empty((T, dims.K), dtype=torch.int32, device=q_I.device)
+    st = lib().dsa_indexer_topk_noalloc(ctypes.byref(dims), _p(q_I), _p(w), _p(k_I_cache), _p(k_I_scale),
+                                        _p(block_table), _p(seq_lens), _p(q_seq), _p(q_pos), T, _p(idx),
+                                        _p(fault_word), _stream(stream))
+    _check("dsa_indexer_topk_noalloc", st)
     return idx
 
 

@@ -213,6 +213,32 @@ static dsa_status run_attn(const dsa_dims* d, const void* q, const void* kv_cach
     return ok ? DSA_OK : DSA_ERR_LAUNCH;
 }
 
+// ------------------------------------------------------------------------------------------------
+// scratch of dsa_indexer_topk_noalloc: one static device buffer per device, resolved once
+// ------------------------------------------------------------------------------------------------
+
+constexpr size_t kNoAllocScratchBytes = DSA_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_base[kMaxDevices];
+
+// Device address of the static scratch on the current device; the first call per device looks it
+// up (this may load the module on that device, so it belongs before any stream capture).
+static void* noalloc_scratch() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_base[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        if (reinterpret_cast<uintptr_t>(p) & 255u) return nullptr;
+        g_noalloc_base[dev] = p;
+    }
+    return g_noalloc_base[dev];
+}
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -299,6 +325,37 @@ dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, con
     return st;
 }
 
+dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+                                    const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                                    const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx,
+                                    int32_t* fault_word, dsa_stream_t stream) {
+    dsa_status st = check_indexer_dims(dims);
+    if (st != DSA_OK) return st;
+    if (T < 0) return DSA_ERR_INVALID_ARG;
+    if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
+    if (T > 0 && (!q_I || !w || !k_I_cache || !block_table || !seq_lens || !idx)) return DSA_ERR_INVALID_ARG;
+    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_I) || !aligned16(w) || !aligned16(k_I_cache)) return DSA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(fault_word) & 3u) return DSA_ERR_INVALID_ARG;
+    // the indexer uses the workspace regions up to the attention's (error word, plan, candidates)
+    if (ws_layout(*dims, T).idx > kNoAllocScratchBytes) return DSA_ERR_TOO_LARGE;
+    void* ws = noalloc_scratch();
+    if (!ws) return DSA_ERR_LAUNCH;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int launches = 0;
+    // the error word is the only scratch that must start at zero (every other region is written
+    // before it is read within the call)
+    if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return DSA_ERR_LAUNCH;
+    if (T > 0)
+        st = run_indexer(dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, q_seq, q_pos, T, idx, ws, s,
+                         &launches);
+    if (st == DSA_OK && fault_word &&
+        cudaMemcpyAsync(fault_word, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        st = DSA_ERR_LAUNCH;
+    g_last_launches = launches;
+    return st;
+}
+
 dsa_status dsa_read_error(void* ws, int32_t* fault_bits, dsa_stream_t stream) {
     if (!ws) return DSA_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -322,6 +379,7 @@ const char* dsa_status_string(dsa_status status) {
         case DSA_ERR_LAUNCH: return "kernel launch failed";
         case DSA_ERR_DEVICE: return "device-side fault (bad block-table entry or index)";
         case DSA_ERR_TIMEOUT: return "a pipeline wait inside a kernel timed out";
+        case DSA_ERR_TOO_LARGE: return "call needs more scratch than the static buffer of dsa_indexer_topk_noalloc";
     }
     return "unknown status";
 }

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings_and_version(L):
-    for code in range(7):
+    for code in range(8):
         assert L.dsa_status_string(code)
     assert L.dsa_version() >= 100
     assert L.dsa_last_launch_count() == 0
@@ -100,3 +100,17 @@ def test_attention_and_decode_reject_bad_args(L):
     assert st == 1
     assert L.dsa_read_error(None, None, None) == 3
     assert L.dsa_workspace_init(None, 256, None) == 3
+
+
+def test_noalloc_rejects_before_any_device_work(L):
+    d = _dims()
+    # null input, misaligned fault word
+    assert L.dsa_indexer_topk_noalloc(ctypes.byref(d), None, FAKE, FAKE, None, FAKE, FAKE, None, None, 2, FAKE,
+                                      None, None) == 1
+    assert L.dsa_indexer_topk_noalloc(ctypes.byref(d), FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None, 2, FAKE,
+                                      ctypes.c_void_p((1 << 20) + 2), None) == 1
+    # more rows than the static scratch holds (K = 2048: (G + T) * 16 KiB > 16 MiB)
+    big = _dims(B=4096, K=2048)
+    assert L.dsa_workspace_size(ctypes.byref(big), 4096) > 16 << 20
+    assert L.dsa_indexer_topk_noalloc(ctypes.byref(big), FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None, 4096, FAKE,
+                                      None, None) == 7
