@@ -74,10 +74,16 @@ __host__ __device__ inline int split_rows(int K, int S) {
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Exchange-buffer byte offset of head h's 16-byte group g (64 fp32 per head, 16 groups), swizzled
-// by the head index so that the 32 heads of a warp hit distinct banks.
-__device__ __forceinline__ uint32_t xoff(int h, int g) {
-    return static_cast<uint32_t>(h * (kRows * 4) + ((g ^ (h & 15)) << 4));
+// Exchange-buffer byte offset of head h's 16-byte group g (64 fp32 per head, 16 groups): groups
+// are the outer index, so the 32 heads of a warp write one contiguous 512-byte run per store
+// (remote stores travel as whole segments) and read it back without bank conflicts.
+__device__ __forceinline__ uint32_t xoff(int h, int g) { return static_cast<uint32_t>((g * kHeads + h) * 16); }
+
+// 2^x on the special-function unit (flushes subnormal results to zero; 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
@@ -325,14 +331,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(peer_xempty);  // the peer may refill our buffer
-            float mt = -INFINITY;
+            // rows without a position (past the split's end, or idx -1) take no weight
+            const int rlo = i * kRows + lane, rhi = rlo + 32;
+            const uint32_t vm0 = __ballot_sync(0xFFFFFFFFu, rlo < nrows && phys_s[rlo] >= 0);
+            const uint32_t vm1 = __ballot_sync(0xFFFFFFFFu, rhi < nrows && phys_s[rhi] >= 0);
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int j = 0; j < kRows; ++j) {
-                const int row = i * kRows + j;
-                const bool valid = row < nrows && phys_s[row] >= 0;
-                z[j] = valid ? z[j] * scale2 : -INFINITY;
-                mt = fmaxf(mt, z[j]);
+                const uint32_t vm = j < 32 ? vm0 : vm1;
+                z[j] = ((vm >> (j & 31)) & 1u) ? z[j] : -INFINITY;
+                mx[j & 3] = fmaxf(mx[j & 3], z[j]);
             }
+            // scale2 > 0 and rounding is monotone, so max(z) * scale2 is the max of the scaled logits
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale2;
             const bool need = mt > m_ref + 8.0f;
             if (__any_sync(0xFFFFFFFFu, need)) {
                 const float m_new = need ? mt : m_ref;
@@ -357,16 +368,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                 }
                 m_ref = m_new;
             }
+            // p = 2^(z * scale2 - m_ref), rounded to bf16 in pairs; l sums the rounded values that
+            // the P.V product uses (masked rows: 2^-inf = 0)
             uint32_t packed[kRows / 2];
+            float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;  // no valid row yet: all p = 0
 #pragma unroll
             for (int j = 0; j < kRows; j += 2) {
-                const float p0 = (z[j] == -INFINITY) ? 0.0f : exp2f(z[j] - m_ref);
-                const float p1 = (z[j + 1] == -INFINITY) ? 0.0f : exp2f(z[j + 1] - m_ref);
-                const __nv_bfloat16 b0 = __float2bfloat16_rn(p0), b1 = __float2bfloat16_rn(p1);
-                l += __bfloat162float(b0) + __bfloat162float(b1);
-                packed[j / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) |
-                                (static_cast<uint32_t>(__bfloat16_as_ushort(b1)) << 16);
+                const float p0 = ex2_approx(fmaf(z[j], scale2, neg_m));
+                const float p1 = ex2_approx(fmaf(z[j + 1], scale2, neg_m));
+                const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);  // .x (low half) = p0
+                const uint32_t u = *reinterpret_cast<const uint32_t*>(&pb);
+                packed[j / 2] = u;
+                ls[(j >> 1) & 3] += __uint_as_float(u << 16) + __uint_as_float(u & 0xFFFF0000u);
             }
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             if (!dead) {  // P (bf16) over the first 32 columns of this tile's S
                 tmem_st32(sa, packed);
                 tmem_st_wait();
