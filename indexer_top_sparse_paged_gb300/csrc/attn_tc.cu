@@ -4,26 +4,30 @@
 // positions; §2.1: it reads the main KV exactly at the selected indices).
 //
 // Work unit: a cluster of two CTAs per (query row t, split of its K selected rows). The pair
-// divides the latent dimension: CTA 0 owns columns 0..255, CTA 1 owns columns 256..575. For every
-// tile of 64 gathered rows each CTA
-//   1. gathers only its columns of the 64 rows (the index list drives TMA tile::gather4 row
-//      gathers into the 128-byte-swizzled layout the tensor core reads),
+// divides the latent dimension: CTA 0 owns columns 0..255, CTA 1 owns columns 256..575, so every
+// selected row is gathered from memory exactly once. For every tile of 64 gathered rows each CTA
+//   1. gathers only its columns of the 64 rows (the index list drives 16-byte cp.async row
+//      copies by four producer warps into the 128-byte-swizzled layout the tensor core reads),
 //   2. computes its partial logits S_r[128 heads x 64 rows] = Q[:, cols_r] . R[:, cols_r]^T with
 //      tcgen05 (M = 128 heads, N = 64 rows; an MMA of N < 64 would leave the tensor pipe idle),
-//   3. sends S_r to the other CTA through distributed shared memory and adds the one it receives
-//      (S_0 + S_1 in both CTAs: fp32 addition commutes, so both see the same logits),
+//   3. sends S_r to the other CTA with one bulk shared-memory copy (the copy engine moves it, so
+//      the transfer does not compete with the tensor core's operand reads) and adds the one it
+//      receives (S_0 + S_1 in both CTAs: fp32 addition commutes, so both see the same logits); the
+//      partial of tile i + 1 is sent before tile i is completed whenever it is already computed,
+//      so the transfer overlaps the softmax (two exchange slots per direction),
 //   4. runs the online softmax (one thread per head, lazy rescaling of O when a head's running
 //      maximum grows by more than 2^8) and writes P as bf16 over its S in tensor memory,
 //   5. accumulates O_r[128 x 256] += P . V_r with V_r = its 256 value columns (CTA 0: values
 //      0..255, CTA 1: values 256..511 -- both inside the columns it already holds).
-// No row byte is loaded twice and no product is computed twice. The O accumulator (256 fp32
-// columns) plus two S/P buffers fit the 512 tensor-memory columns; CTA 1 keeps the last 64 query
-// columns in tensor memory (A operand from TMEM) so that its shared memory holds 3 row stages.
+// Tensor memory holds the O accumulator (256 fp32 columns), two S/P buffers and all but the first
+// 64 query columns of the CTA (A operand from TMEM); shared memory holds the first query chunk,
+// two row stages, the two exchange slots in each direction and a validity bit per selected row.
 //
-// Roles (288 threads per CTA): warps 0-3 softmax / epilogue (thread = head = TMEM lane), warps
-// 4-6 gather producers (warp 4 + s owns row stage s), warp 7 idle, warp 8 TMEM allocator + MMA
-// issuer (+ the TMA load of the query).
+// Roles (320 threads per CTA): warps 0-3 softmax / epilogue (thread = head = TMEM lane), warps
+// 4-7 gather producers, warp 8 TMEM allocator + MMA issuer (+ the TMA load of the first query
+// chunk), warp 9 prefetches the CTA's columns of every selected row into L2 at the start.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 
@@ -33,20 +37,20 @@ namespace tcattn {
 constexpr int kHeads = 128;
 constexpr int kD = 576;
 constexpr int kDV = 512;
-constexpr int kDVH = 256;              // value columns per CTA
-constexpr int kRows = 64;              // gathered rows per tile
+constexpr int kDVH = 256;                     // value columns per CTA
+constexpr int kRows = 64;                     // gathered rows per tile
 constexpr int kStages = 3;
 constexpr int kChunkBytes = kRows * 128;      // [64 rows x 64 bf16]
 constexpr int kQChunkBytes = kHeads * 128;    // [128 heads x 64 bf16]
-constexpr int kQSmemChunks = 4;               // query chunks in shared memory (both CTAs)
 constexpr int kMaxChunks = 5;                 // row chunks per CTA (CTA 0: 4, CTA 1: 5)
 constexpr int kStageBytes = kMaxChunks * kChunkBytes;
-constexpr int kXBytes = kHeads * kRows * 4;   // one partial-logit tile (fp32)
+constexpr int kXBytes = kHeads * kRows * 2;   // one partial-logit tile (fp16, prescaled by 2^-8)
+constexpr float kXScale = 1.0f / 256.0f;      // partial logits travel as fp16(S_r * 2^-8)
 constexpr int kMaxRows = 2048;
-constexpr int kThreads = 288;
-constexpr int kPrefetchTiles = 9;  // tiles of rows prefetched into L2 ahead of their copy (a multiple of kStages)
+constexpr int kThreads = 320;
+constexpr int kProducers = 4;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // S/P buffers at 256 and 320
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // S/P buffers at 256 and 320; Q chunks 32 apart
 constexpr uint32_t kIdescQK = idesc_f16(128, kRows, 1u, 0u, 0u);
 constexpr uint32_t kIdescPV = idesc_f16(128, kDVH, 1u, 0u, 1u);
 
@@ -54,16 +58,17 @@ struct Smem {
     uint64_t full[kStages], empty[kStages];
     uint64_t s_full[2], p_full[2], s_free[2];
     uint64_t qfull, o_full, mma_done;
-    uint64_t xfull, xempty;  // arrived on by the other CTA of the pair
+    uint64_t xfull[2], xempty[2];  // xfull: the peer's copy landed; xempty: arrived on by the peer
     uint32_t tmem_base;
     int abort_flag;
 };
 
 constexpr size_t kOffQ = 0;
-constexpr size_t kOffKv = kOffQ + static_cast<size_t>(kQSmemChunks) * kQChunkBytes;
-constexpr size_t kOffX = kOffKv + static_cast<size_t>(kStages) * kStageBytes;
-constexpr size_t kOffPhys = kOffX + kXBytes;
-constexpr size_t kOffCtl = kOffPhys + kMaxRows * sizeof(int32_t);
+constexpr size_t kOffKv = kOffQ + kQChunkBytes;
+constexpr size_t kOffX = kOffKv + static_cast<size_t>(kStages) * kStageBytes;  // received partials
+constexpr size_t kOffStage = kOffX + 2 * kXBytes;                                // partials to send
+constexpr size_t kOffValid = kOffStage + 2 * kXBytes;                            // 1 bit per selected row
+constexpr size_t kOffCtl = kOffValid + kMaxRows / 8;
 constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(Smem);
 static_assert(kSmemBytes <= 232448, "attention shared memory over the limit");
 
@@ -72,11 +77,9 @@ __host__ __device__ inline int split_rows(int K, int S) {
     return (per + kRows - 1) / kRows * kRows;
 }
 
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// Exchange-buffer byte offset of head h's 16-byte group g (64 fp32 per head, 16 groups): groups
-// are the outer index, so the 32 heads of a warp write one contiguous 512-byte run per store
-// (remote stores travel as whole segments) and read it back without bank conflicts.
+// Exchange-slot byte offset of head h's 16-byte group g (64 fp16 per head, 8 groups): groups are
+// the outer index, so the 32 heads of a warp touch one contiguous 512-byte run per access (no bank
+// conflicts on either side).
 __device__ __forceinline__ uint32_t xoff(int h, int g) { return static_cast<uint32_t>((g * kHeads + h) * 16); }
 
 // 2^x on the special-function unit (flushes subnormal results to zero; 2^-inf = +0).
@@ -87,13 +90,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
-    attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv) {
+    attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap map_q) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem + kOffQ);
     const uint32_t sKv = smem_u32(smem + kOffKv);
     const uint32_t sX = smem_u32(smem + kOffX);
-    int32_t* phys_s = reinterpret_cast<int32_t*>(smem + kOffPhys);
+    const uint32_t sStage = smem_u32(smem + kOffStage);
+    uint32_t* valid_bits = reinterpret_cast<uint32_t*>(smem + kOffValid);
     Smem& S = *reinterpret_cast<Smem*>(smem + kOffCtl);
     volatile int* abort_flag = &S.abort_flag;
 
@@ -111,22 +115,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
     const int b = a.q_seq ? a.q_seq[t] : t;
     const bool seq_ok = b >= 0 && b < a.B;
     const int L = seq_ok ? a.seq_lens[b] : 0;
+    const int32_t* idx_row = a.idx + static_cast<int64_t>(t) * a.K + r0;
+    const int32_t* bt_row = a.block_table + static_cast<int64_t>(seq_ok ? b : 0) * a.max_blocks;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(smem_u32(&S.full[i]), 1);
+            mbar_init(smem_u32(&S.full[i]), kProducers * 32);  // every producer thread's cp.async
             mbar_init(smem_u32(&S.empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&S.s_full[i]), 1);
             mbar_init(smem_u32(&S.p_full[i]), 4);  // one elected arrive per softmax warp
             mbar_init(smem_u32(&S.s_free[i]), 1);
+            mbar_init(smem_u32(&S.xfull[i]), 1);   // arrive.expect_tx here + the peer's copy bytes
+            mbar_init(smem_u32(&S.xempty[i]), 4);  // the peer's four softmax warps
         }
         mbar_init(smem_u32(&S.qfull), 1);
         mbar_init(smem_u32(&S.o_full), 1);
         mbar_init(smem_u32(&S.mma_done), 1);
-        mbar_init(smem_u32(&S.xfull), 4);   // the peer's four softmax warps
-        mbar_init(smem_u32(&S.xempty), 4);
         S.abort_flag = 0;
         fence_mbar_init();
     }
@@ -135,91 +141,123 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         tmem_relinquish();
     }
     tc_fence_before();
-    cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
+    cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive or copy
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
 
     if (warp == 8 && lane == 0 && ntiles > 0) {
-        mbar_arrive_expect_tx(smem_u32(&S.qfull), kQSmemChunks * kQChunkBytes);
-        for (int c = 0; c < kQSmemChunks; ++c)
-            tma_load_2d(sQ + c * kQChunkBytes, &map_q, (c0 + c) * 64, t * kHeads, smem_u32(&S.qfull));
+        mbar_arrive_expect_tx(smem_u32(&S.qfull), kQChunkBytes);
+        tma_load_2d(sQ, &map_q, c0 * 64, t * kHeads, smem_u32(&S.qfull));
     }
-    if (rank == 1 && warp < 4 && ntiles > 0) {
-        // query columns 512..575 (the fifth chunk of CTA 1) go to tensor memory, packed in pairs
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
-                                                           (static_cast<int64_t>(t) * kHeads + threadIdx.x) * kD + 512);
-        uint32_t w[32];
+    if (warp < 4 && ntiles > 0) {
+        // the CTA's query chunks after the first go to tensor memory (head = lane, bf16 pairs)
+        const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(t) * kHeads + threadIdx.x) * kD;
+        for (int k = 0; k + 1 < nchunks; ++k) {
+            const uint4* src = reinterpret_cast<const uint4*>(qrow + (c0 + 1 + k) * 64);
+            uint32_t w[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint4 v = src[i];
-            w[4 * i] = v.x;
-            w[4 * i + 1] = v.y;
-            w[4 * i + 2] = v.z;
-            w[4 * i + 3] = v.w;
+            for (int i = 0; i < 8; ++i) {
+                const uint4 v = src[i];
+                w[4 * i] = v.x;
+                w[4 * i + 1] = v.y;
+                w[4 * i + 2] = v.z;
+                w[4 * i + 3] = v.w;
+            }
+            tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + kColQ + k * 32, w);
         }
-        tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + kColQ, w);
         tmem_st_wait();
     }
-    // resolve every selected position of this split to its physical cache row once
-    for (int i = threadIdx.x; i < nrows; i += kThreads) {
-        const int s = a.idx[static_cast<int64_t>(t) * a.K + r0 + i];
-        int32_t p = -1;
-        if (s != -1) {
-            if (s < 0 || s >= L) {
-                atomicOr(a.err, DSA_FAULT_INDEX);
-            } else {
-                const int blk = a.block_table[static_cast<int64_t>(b) * a.max_blocks + (s >> 6)];
-                if (blk < 0 || blk >= a.num_blocks) atomicOr(a.err, DSA_FAULT_BLOCK_TABLE);
-                else p = blk * kBlock + (s & 63);
+    // one validity bit per selected row (the softmax gives rows without a position no weight); the
+    // faults of bad entries are recorded once, by CTA 0
+    for (int w0 = warp * 32; w0 < ntiles * kRows; w0 += kThreads) {
+        const int i = w0 + lane;
+        bool ok = false;
+        if (i < nrows) {
+            const int s = idx_row[i];
+            if (s != -1) {
+                if (s < 0 || s >= L) {
+                    if (rank == 0) atomicOr(a.err, DSA_FAULT_INDEX);
+                } else {
+                    const int blk = bt_row[s >> 6];
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        if (rank == 0) atomicOr(a.err, DSA_FAULT_BLOCK_TABLE);
+                    } else {
+                        ok = true;
+                    }
+                }
             }
         }
-        phys_s[i] = p;
+        const uint32_t word = __ballot_sync(0xFFFFFFFFu, ok);
+        if (lane == 0) valid_bits[w0 >> 5] = word;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    if (warp >= 4 && warp < 4 + kStages) {
+    if (warp >= 4 && warp < 4 + kProducers) {
         // ------------------------------------------------------------- gather producers
-        // Producer warp w owns stage w and fills tiles w, w + 3, ...: successive fills of a stage
-        // come from one warp, so each waits for exactly the previous use's release. The index
-        // list drives TMA row gathers: one tile::gather4 per 4 rows x one 64-column chunk, straight
-        // into the 128-byte-swizzled layout (rows with no position read as zeros).
+        // The index list drives 16-byte cp.async row copies (the load/store path, leaving the
+        // copy engine to the partial-logit exchange), written straight into the 128-byte-swizzled
+        // layout the tensor core reads: the 16-byte group g of row r goes to position g ^ (r & 7)
+        // of the row. Producer warp pw copies rows pw, pw + 4, ... of every tile, one row per step
+        // across its 32 lanes (lane = chunk * 8 + group); rows with no position are zero-filled.
+        // Lane k < 16 resolves row 4k + pw of the next tile to its physical cache row while the
+        // current tile is issued (the index loads run two tiles ahead).
         const int pw = warp - 4;
         const uint8_t* kv = static_cast<const uint8_t*>(a.kv);
-        auto prefetch_tile = [&](int i) {
-            if (i >= ntiles) return;
-            for (int rr = lane; rr < kRows; rr += 32) {
-                const int row = i * kRows + rr;
-                const int p = (row < nrows) ? phys_s[row] : -1;
-                if (p >= 0)
-                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                                     kv + static_cast<int64_t>(p) * (kD * 2) + c0 * 128),
-                                 "r"(nchunks * 128)
-                                 : "memory");
-            }
+        auto load_idx = [&](int tile) -> int {
+            const int row = tile * kRows + 4 * lane + pw;
+            const bool ok = lane < 16 && tile < ntiles && row < nrows && ((valid_bits[row >> 5] >> (row & 31)) & 1u);
+            return ok ? idx_row[row] : -1;
         };
-        if (lane == 0) tma_prefetch_desc(&map_kv);
-        for (int i = pw; i < kPrefetchTiles; i += kStages) prefetch_tile(i);
-        for (int i = pw; i < ntiles; i += kStages) {
-            prefetch_tile(i + kPrefetchTiles - (kPrefetchTiles % kStages));
-            const int st = pw, use = i / kStages;
-            const bool got = mbar_wait(smem_u32(&S.empty[st]), (use & 1) ^ 1, abort_flag, a.err);
+        auto to_phys = [&](int sidx) -> int { return sidx >= 0 ? bt_row[sidx >> 6] * kBlock + (sidx & 63) : -1; };
+        int s1 = load_idx(0);
+        int ph = to_phys(s1);
+        s1 = load_idx(1);
+        const int c = lane >> 3, g = lane & 7;  // chunk and 16-byte group this lane copies
+        for (int i = 0; i < ntiles; ++i) {
+            const int s2 = load_idx(i + 2);
+            const int nph = to_phys(s1);
+            const int st = i % kStages;
+            const bool got = mbar_wait(smem_u32(&S.empty[st]), ((i / kStages) & 1) ^ 1, abort_flag, a.err);
             if (!__all_sync(0xFFFFFFFFu, got)) break;
-            const uint32_t fb = smem_u32(&S.full[st]);
-            if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kRows * nchunks * 128));
-            __syncwarp();
             const uint32_t base = sKv + st * kStageBytes;
-            if (lane < kRows / 4) {  // lane g gathers rows 4g..4g+3 of the tile, all chunks
-                int rw[4];
+#pragma unroll 4
+            for (int k = 0; k < 16; ++k) {
+                const int p = __shfl_sync(0xFFFFFFFFu, ph, k);
+                const int r = 4 * k + pw;
+                const uint8_t* src = p >= 0 ? kv + static_cast<int64_t>(p) * (kD * 2) + c0 * 128 : kv;
+                const uint32_t nb = p >= 0 ? 16u : 0u;  // 0: zero-fill
+                const uint32_t rowoff = static_cast<uint32_t>(r * 128);
+                cp_async16(base + c * kChunkBytes + rowoff + ((g ^ (r & 7)) << 4), src + (p >= 0 ? c * 128 + g * 16 : 0), nb);
+                if (nchunks == 5 && lane < 8)
+                    cp_async16(base + 4 * kChunkBytes + rowoff + ((lane ^ (r & 7)) << 4),
+                               src + (p >= 0 ? 4 * 128 + lane * 16 : 0), nb);
+            }
+            cp_async_arrive_noinc(smem_u32(&S.full[st]));  // once this thread's copies have landed
+            ph = nph;
+            s1 = s2;
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------- L2 prefetch
+        // Every valid selected row's columns of this CTA (4 or 5 lines of 128 B), requested up
+        // front so that the gathers find them in L2.
+        const uint8_t* kv = static_cast<const uint8_t*>(a.kv) + c0 * 128;
+        for (int base = 0; base < nrows; base += 4 * 32) {
+            int sv[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int row = i * kRows + 4 * lane + j;
-                    rw[j] = (row < nrows) ? phys_s[row] : -1;  // -1: outside the tensor -> zeros
-                }
-                for (int cc = 0; cc < nchunks; ++cc)
-                    tma_gather4(base + cc * kChunkBytes + lane * 4 * 128, &map_kv, (c0 + cc) * 64, rw[0], rw[1],
-                                rw[2], rw[3], fb);
+            for (int j = 0; j < 4; ++j) {
+                const int row = base + j * 32 + lane;
+                sv[j] = (row < nrows && ((valid_bits[row >> 5] >> (row & 31)) & 1u)) ? idx_row[row] : -1;
+            }
+            int pv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pv[j] = sv[j] >= 0 ? bt_row[sv[j] >> 6] * kBlock + (sv[j] & 63) : -1;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (pv[j] < 0) continue;
+                const uint8_t* rp = kv + static_cast<int64_t>(pv[j]) * (kD * 2);
+                for (int c = 0; c < nchunks; ++c) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + c * 128));
             }
         }
     } else if (warp == 8) {
@@ -232,23 +270,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             auto qk = [&](int i) -> bool {
                 const int st = i % kStages;
                 if (!mbar_wait(smem_u32(&S.full[st]), (i / kStages) & 1, abort_flag, a.err)) return false;
+                fence_proxy_async_smem();  // rows written by cp.async -> visible to the tensor core
                 tc_fence_after();
                 const uint32_t d = tmem + kColS + (i & 1) * kRows;
                 const uint64_t kvb = dkv0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
 #pragma unroll
-                for (int c = 0; c < kQSmemChunks; ++c) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = dq0 + static_cast<uint64_t>((c * kQChunkBytes + kk * 32) >> 4);
-                        const uint64_t bd = kvb + static_cast<uint64_t>((c * kChunkBytes + kk * 32) >> 4);
-                        mma_ss(d, ad, bd, kIdescQK, (c | kk) != 0 ? 1u : 0u);
-                    }
+                for (int kk = 0; kk < 4; ++kk) {  // first chunk: query from shared memory
+                    const uint64_t ad = dq0 + static_cast<uint64_t>((kk * 32) >> 4);
+                    const uint64_t bd = kvb + static_cast<uint64_t>((kk * 32) >> 4);
+                    mma_ss(d, ad, bd, kIdescQK, kk != 0 ? 1u : 0u);
                 }
-                if (nchunks == 5) {
+                for (int cc = 1; cc < nchunks; ++cc) {  // the rest: query from tensor memory
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bd = kvb + static_cast<uint64_t>((4 * kChunkBytes + kk * 32) >> 4);
-                        mma_ts(d, tmem + kColQ + kk * 8, bd, kIdescQK, 1u);
+                        const uint64_t bd = kvb + static_cast<uint64_t>((cc * kChunkBytes + kk * 32) >> 4);
+                        mma_ts(d, tmem + kColQ + (cc - 1) * 32 + kk * 8, bd, kIdescQK, 1u);
                     }
                 }
                 tc_commit(smem_u32(&S.s_full[i & 1]));
@@ -279,62 +315,100 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         // ------------------------------------------------------------- softmax + epilogue
         const int h = threadIdx.x;  // head = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const float scale2 = a.sm_scale * 1.4426950408889634f;  // logits in log2 units
+        const float scale2 = a.sm_scale * 1.4426950408889634f / kXScale;  // exchanged units -> log2 units
         const uint32_t peer_x = mapa_shared(sX, peer);
-        const uint32_t peer_xfull = mapa_shared(smem_u32(&S.xfull), peer);
-        const uint32_t peer_xempty = mapa_shared(smem_u32(&S.xempty), peer);
+        const uint32_t peer_xfull = mapa_shared(smem_u32(&S.xfull[0]), peer);    // [1] at +8
+        const uint32_t peer_xempty = mapa_shared(smem_u32(&S.xempty[0]), peer);  // [1] at +8
         float m_ref = -INFINITY, l = 0.0f;
-        bool dead = false;
-        for (int i = 0; i < ntiles; ++i) {
-            const int sb = i & 1;
-            bool got = mbar_wait(smem_u32(&S.s_full[sb]), (i >> 1) & 1, abort_flag, a.err);
-            if (named_bar_or(2, 128, dead || !got)) { dead = true; break; }
+        // Sends this CTA's partial logits of tile j to the peer's exchange slot j & 1: once the
+        // tile's S is in tensor memory and the peer has consumed tile j - 2 from that slot (which
+        // also means the copy out of the local staging slot j & 1 is complete), the 128 threads
+        // stage the partial and one thread starts the bulk copy. Arms the local slot j & 1 for the
+        // peer's tile j. Returns false for all 128 threads alike if any is dead or a wait gave up.
+        auto send_partial = [&](int j, bool dead_in) -> bool {
+            const int sb = j & 1;
+            const bool got = !dead_in && mbar_wait(smem_u32(&S.s_full[sb]), (j >> 1) & 1, abort_flag, a.err);
+            if (named_bar_or(2, 128, dead_in || !got)) return false;
             tc_fence_after();
             uint32_t v0[32], v1[32];
             const uint32_t sa = tmem + lane_base + kColS + sb * kRows;
             tmem_ld32(sa, v0);
             tmem_ld32(sa + 32, v1);
             tmem_ld_wait();
-            // send this CTA's partial logits to the peer ...
-            got = mbar_wait_cluster(smem_u32(&S.xempty), (i & 1) ^ 1, abort_flag, a.err);
-            if (__any_sync(0xFFFFFFFFu, !got)) dead = true;
-            if (!dead) {
+            const bool free_ok = mbar_wait_cluster(smem_u32(&S.xempty[sb]), ((j >> 1) & 1) ^ 1, abort_flag, a.err);
+            // fp16(S_r * 2^-8), packed in pairs of rows; this CTA completes the tile from the same
+            // rounded values it sends, so both CTAs add identical operands
+            uint32_t hp[32];
 #pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    st_cluster_v4(peer_x + xoff(h, g), __uint_as_float(v0[4 * g]), __uint_as_float(v0[4 * g + 1]),
-                                  __uint_as_float(v0[4 * g + 2]), __uint_as_float(v0[4 * g + 3]));
-#pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    st_cluster_v4(peer_x + xoff(h, 8 + g), __uint_as_float(v1[4 * g]), __uint_as_float(v1[4 * g + 1]),
-                                  __uint_as_float(v1[4 * g + 2]), __uint_as_float(v1[4 * g + 3]));
+            for (int e = 0; e < 16; ++e) {
+                const __half2 x0 = __floats2half2_rn(__uint_as_float(v0[2 * e]) * kXScale, __uint_as_float(v0[2 * e + 1]) * kXScale);
+                const __half2 x1 = __floats2half2_rn(__uint_as_float(v1[2 * e]) * kXScale, __uint_as_float(v1[2 * e + 1]) * kXScale);
+                hp[e] = *reinterpret_cast<const uint32_t*>(&x0);
+                hp[16 + e] = *reinterpret_cast<const uint32_t*>(&x1);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(peer_xfull);
-            // ... and add the peer's
-            got = mbar_wait_cluster(smem_u32(&S.xfull), i & 1, abort_flag, a.err);
+            uint8_t* stg = smem + kOffStage + sb * kXBytes;
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+                *reinterpret_cast<uint4*>(stg + xoff(h, g)) = make_uint4(hp[4 * g], hp[4 * g + 1], hp[4 * g + 2], hp[4 * g + 3]);
+            fence_proxy_async_smem();  // generic-proxy writes -> visible to the copy engine
+            if (named_bar_or(2, 128, !free_ok)) return false;
+            if (threadIdx.x == 0) {
+                mbar_arrive_expect_tx(smem_u32(&S.xfull[sb]), kXBytes);  // the peer's tile j lands here
+                bulk_copy_to_peer(peer_x + sb * kXBytes, sStage + sb * kXBytes, kXBytes, peer_xfull + sb * 8);
+            }
+            return true;
+        };
+        bool dead = false;
+        int sent = 0;  // tiles [0, sent) have been sent to the peer
+        for (int i = 0; i < ntiles; ++i) {  // every softmax thread takes the same barriers, dead or not
+            const int sb = i & 1;
+            if (sent <= i) {  // tile i itself must go out before it can complete
+                if (!send_partial(i, dead)) {
+                    dead = true;
+                    break;
+                }
+                sent = i + 1;
+            }
+            // Send tile i + 1 ahead if its S is already in tensor memory (never wait for it here:
+            // its rows may still be in flight behind this tile's product). The OR makes the
+            // decision uniform; a phase seen complete by one thread is complete for all.
+            const bool ahead = i + 1 < ntiles && mbar_test(smem_u32(&S.s_full[(i + 1) & 1]), ((i + 1) >> 1) & 1);
+            if (named_bar_or(2, 128, ahead && !dead)) {
+                if (!send_partial(i + 1, dead)) {
+                    dead = true;
+                    break;
+                }
+                sent = i + 2;
+            } else if (named_bar_or(2, 128, dead)) {
+                dead = true;
+                break;
+            }
+            // complete tile i: this CTA's rounded partial (still in its staging slot) plus the peer's,
+            // both in units of 2^8 (the scale is folded into scale2)
+            const bool got = mbar_wait_cluster(smem_u32(&S.xfull[sb]), (i >> 1) & 1, abort_flag, a.err);
             if (__any_sync(0xFFFFFFFFu, !got)) dead = true;
             float z[kRows];
+            {
+                const uint8_t* mine = smem + kOffStage + sb * kXBytes;
+                const uint8_t* theirs = smem + kOffX + sb * kXBytes;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                z[j] = __uint_as_float(v0[j]);
-                z[32 + j] = __uint_as_float(v1[j]);
-            }
-            if (!dead) {
+                for (int g = 0; g < 8; ++g) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(mine + xoff(h, g));
+                    const uint4 w = dead ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(theirs + xoff(h, g));
+                    const uint32_t us[4] = {u.x, u.y, u.z, u.w}, ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int g = 0; g < 16; ++g) {
-                    const float4 o = *reinterpret_cast<const float4*>(smem + kOffX + xoff(h, g));
-                    z[4 * g] += o.x;
-                    z[4 * g + 1] += o.y;
-                    z[4 * g + 2] += o.z;
-                    z[4 * g + 3] += o.w;
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&us[q]));
+                        const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&ws[q]));
+                        z[8 * g + 2 * q] = a2.x + b2.x;
+                        z[8 * g + 2 * q + 1] = a2.y + b2.y;
+                    }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(peer_xempty);  // the peer may refill our buffer
-            // rows without a position (past the split's end, or idx -1) take no weight
-            const int rlo = i * kRows + lane, rhi = rlo + 32;
-            const uint32_t vm0 = __ballot_sync(0xFFFFFFFFu, rlo < nrows && phys_s[rlo] >= 0);
-            const uint32_t vm1 = __ballot_sync(0xFFFFFFFFu, rhi < nrows && phys_s[rhi] >= 0);
+            if (lane == 0) mbar_arrive_remote(peer_xempty + sb * 8);  // the peer may refill this slot
+            // rows without a position (past the split's end, idx -1, bad entries) take no weight
+            const uint32_t vm0 = valid_bits[2 * i], vm1 = valid_bits[2 * i + 1];
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int j = 0; j < kRows; ++j) {
@@ -348,8 +422,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             if (__any_sync(0xFFFFFFFFu, need)) {
                 const float m_new = need ? mt : m_ref;
                 if (i > 0) {
-                    got = mbar_wait(smem_u32(&S.s_free[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort_flag, a.err);
-                    if (__any_sync(0xFFFFFFFFu, !got)) dead = true;
+                    const bool freed = mbar_wait(smem_u32(&S.s_free[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort_flag, a.err);
+                    if (__any_sync(0xFFFFFFFFu, !freed)) dead = true;
                     if (!dead) {
                         tc_fence_after();
                         const float alpha = (m_new == m_ref) ? 1.0f : exp2f(m_ref - m_new);
@@ -384,7 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             if (!dead) {  // P (bf16) over the first 32 columns of this tile's S
-                tmem_st32(sa, packed);
+                tmem_st32(tmem + lane_base + kColS + sb * kRows, packed);
                 tmem_st_wait();
                 tc_fence_before();
             }
@@ -497,15 +571,11 @@ bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches) {
     if (!make_tmap_2d(&map_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcattn::kD,
                       static_cast<uint64_t>(a.T) * tcattn::kHeads, tcattn::kD * 2, 64, 128))
         return false;
-    CUtensorMap map_kv;  // [num_blocks * 64 rows][576 cols], gathered one row x 64 columns at a time
-    if (!make_tmap_2d(&map_kv, a.kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcattn::kD,
-                      static_cast<uint64_t>(a.num_blocks) * kBlock, tcattn::kD * 2, 64, 1))
-        return false;
     if (cudaFuncSetAttribute(tcattn::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(tcattn::kSmemBytes)) != cudaSuccess)
         return false;
     dim3 grid(2 * a.S, a.T);
-    tcattn::attn_tc_kernel<<<grid, tcattn::kThreads, tcattn::kSmemBytes, s>>>(a, map_q, map_kv);
+    tcattn::attn_tc_kernel<<<grid, tcattn::kThreads, tcattn::kSmemBytes, s>>>(a, map_q);
     ++*launches;
     if (cudaGetLastError() != cudaSuccess) return false;
     if (a.S > 1) {

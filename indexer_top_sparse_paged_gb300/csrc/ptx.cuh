@@ -146,6 +146,22 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from this CTA's shared
+// memory to another CTA's shared memory in the cluster, performed by the copy engine; the
+// destination CTA's mbarrier (cluster address) receives the byte count as complete_tx. The source
+// writes must have been made visible to the async proxy (fence_proxy_async_smem) beforehand.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                  uint32_t mbar_cluster) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(src), "r"(bytes), "r"(mbar_cluster)
+                 : "memory");
+}
+
 // Arrive on an mbarrier of another CTA of the cluster, releasing this thread's prior writes
 // (including its distributed-shared-memory stores) at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
