@@ -39,7 +39,7 @@ constexpr int kD = 576;
 constexpr int kDV = 512;
 constexpr int kDVH = 256;                     // value columns per CTA
 constexpr int kRows = 64;                     // gathered rows per tile
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kChunkBytes = kRows * 128;      // [64 rows x 64 bf16]
 constexpr int kQChunkBytes = kHeads * 128;    // [128 heads x 64 bf16]
 constexpr int kMaxChunks = 5;                 // row chunks per CTA (CTA 0: 4, CTA 1: 5)
@@ -58,7 +58,8 @@ struct Smem {
     uint64_t full[kStages], empty[kStages];
     uint64_t s_full[2], p_full[2], s_free[2];
     uint64_t qfull, o_full, mma_done;
-    uint64_t xfull[2], xempty[2];  // xfull: the peer's copy landed; xempty: arrived on by the peer
+    uint64_t xfull[2], xempty[2];  // both arrived on by the peer: its partial landed / it consumed ours
+    uint64_t s_sent[2];            // the producers have read S out of tensor memory
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -66,9 +67,9 @@ struct Smem {
 constexpr size_t kOffQ = 0;
 constexpr size_t kOffKv = kOffQ + kQChunkBytes;
 constexpr size_t kOffX = kOffKv + static_cast<size_t>(kStages) * kStageBytes;  // received partials
-constexpr size_t kOffStage = kOffX + 2 * kXBytes;                                // partials to send
-constexpr size_t kOffValid = kOffStage + 2 * kXBytes;                            // 1 bit per selected row
-constexpr size_t kOffCtl = kOffValid + kMaxRows / 8;
+constexpr size_t kOffValid = kOffX + 2 * kXBytes;                                // 1 bit per selected row
+constexpr size_t kOffPhys = kOffValid + kMaxRows / 8;                             // physical row per selected row
+constexpr size_t kOffCtl = kOffPhys + kMaxRows * sizeof(int32_t);
 constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(Smem);
 static_assert(kSmemBytes <= 232448, "attention shared memory over the limit");
 
@@ -90,14 +91,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
-    attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap map_q) {
+    attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem + kOffQ);
     const uint32_t sKv = smem_u32(smem + kOffKv);
     const uint32_t sX = smem_u32(smem + kOffX);
-    const uint32_t sStage = smem_u32(smem + kOffStage);
     uint32_t* valid_bits = reinterpret_cast<uint32_t*>(smem + kOffValid);
+    int32_t* phys_s = reinterpret_cast<int32_t*>(smem + kOffPhys);
     Smem& S = *reinterpret_cast<Smem*>(smem + kOffCtl);
     volatile int* abort_flag = &S.abort_flag;
 
@@ -120,21 +121,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(smem_u32(&S.full[i]), kProducers * 32);  // every producer thread's cp.async
+            mbar_init(smem_u32(&S.full[i]), kProducers);  // one arrive.expect_tx per producer warp
             mbar_init(smem_u32(&S.empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&S.s_full[i]), 1);
             mbar_init(smem_u32(&S.p_full[i]), 4);  // one elected arrive per softmax warp
             mbar_init(smem_u32(&S.s_free[i]), 1);
-            mbar_init(smem_u32(&S.xfull[i]), 1);   // arrive.expect_tx here + the peer's copy bytes
+            mbar_init(smem_u32(&S.xfull[i]), 1);   // arrive.expect_tx here + the peer's st.async bytes
             mbar_init(smem_u32(&S.xempty[i]), 4);  // the peer's four softmax warps
+            mbar_init(smem_u32(&S.s_sent[i]), 4);  // this CTA's four producer warps
         }
         mbar_init(smem_u32(&S.qfull), 1);
         mbar_init(smem_u32(&S.o_full), 1);
         mbar_init(smem_u32(&S.mma_done), 1);
         S.abort_flag = 0;
         fence_mbar_init();
+        // exchange slots 0 and 1 expect the peer's tiles 0 and 1 (re-armed as tiles are consumed)
+        mbar_arrive_expect_tx(smem_u32(&S.xfull[0]), kXBytes);
+        mbar_arrive_expect_tx(smem_u32(&S.xfull[1]), kXBytes);
     }
     if (warp == 8) {
         tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
@@ -167,11 +172,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         }
         tmem_st_wait();
     }
-    // one validity bit per selected row (the softmax gives rows without a position no weight); the
-    // faults of bad entries are recorded once, by CTA 0
+    // every selected row resolved once to its physical cache row (-1: no position, or a bad entry,
+    // whose fault CTA 0 records) plus a validity bit per row for the softmax
     for (int w0 = warp * 32; w0 < ntiles * kRows; w0 += kThreads) {
         const int i = w0 + lane;
-        bool ok = false;
+        int32_t p = -1;
         if (i < nrows) {
             const int s = idx_row[i];
             if (s != -1) {
@@ -182,12 +187,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                     if (blk < 0 || blk >= a.num_blocks) {
                         if (rank == 0) atomicOr(a.err, DSA_FAULT_BLOCK_TABLE);
                     } else {
-                        ok = true;
+                        p = blk * kBlock + (s & 63);
                     }
                 }
             }
         }
-        const uint32_t word = __ballot_sync(0xFFFFFFFFu, ok);
+        phys_s[i] = p;
+        const uint32_t word = __ballot_sync(0xFFFFFFFFu, p >= 0);
         if (lane == 0) valid_bits[w0 >> 5] = word;
     }
     tc_fence_before();
@@ -195,70 +201,97 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
     tc_fence_after();
 
     if (warp >= 4 && warp < 4 + kProducers) {
-        // ------------------------------------------------------------- gather producers
-        // The index list drives 16-byte cp.async row copies (the load/store path, leaving the
-        // copy engine to the partial-logit exchange), written straight into the 128-byte-swizzled
-        // layout the tensor core reads: the 16-byte group g of row r goes to position g ^ (r & 7)
-        // of the row. Producer warp pw copies rows pw, pw + 4, ... of every tile, one row per step
-        // across its 32 lanes (lane = chunk * 8 + group); rows with no position are zero-filled.
-        // Lane k < 16 resolves row 4k + pw of the next tile to its physical cache row while the
-        // current tile is issued (the index loads run two tiles ahead).
+        // ------------------------------------------------------------- producers: gather + send
+        // Producer warp pw (TMEM lane quarter pw) alternates two jobs, in an order that matches the
+        // tensor pipe's (QK(j + 1) is issued right after PV(j - 1), which frees the stage of tile
+        // j + 3), so neither job waits behind the other:
+        //  send(j):   once S(j) is in tensor memory, read the partial logits of heads 32pw..32pw+31,
+        //             round them to fp16(S * 2^-8) and store them into the peer's exchange slot
+        //             j & 1 (distributed shared memory; the peer's softmax frees the slot);
+        //  gather(t): once stage t % 4 is free, resolve rows 4g..4g+3 of tile t (lane g) to
+        //             physical cache rows and issue one TMA tile::gather4 per 64-column chunk
+        //             (chunk pw; CTA 1's chunk 4 also goes to pw = 0) into the 128-byte-swizzled
+        //             layout (rows with no position read as zeros).
         const int pw = warp - 4;
-        const uint8_t* kv = static_cast<const uint8_t*>(a.kv);
-        auto load_idx = [&](int tile) -> int {
-            const int row = tile * kRows + 4 * lane + pw;
-            const bool ok = lane < 16 && tile < ntiles && row < nrows && ((valid_bits[row >> 5] >> (row & 31)) & 1u);
-            return ok ? idx_row[row] : -1;
+        const int h = pw * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(pw * 32) << 16;
+        const uint32_t peer_x = mapa_shared(sX, peer);
+        const uint32_t peer_xfull = mapa_shared(smem_u32(&S.xfull[0]), peer);  // [1] at +8
+        const int my_chunks = (pw == 0 && nchunks == 5) ? 2 : 1;
+        auto rows_of = [&](int tile, int (&rw)[4]) {  // physical cache rows of rows 4g..4g+3, or -1
+#pragma unroll
+            for (int j = 0; j < 4; ++j) rw[j] = (lane < 16 && tile < ntiles) ? phys_s[tile * kRows + 4 * lane + j] : -1;
         };
-        auto to_phys = [&](int sidx) -> int { return sidx >= 0 ? bt_row[sidx >> 6] * kBlock + (sidx & 63) : -1; };
-        int s1 = load_idx(0);
-        int ph = to_phys(s1);
-        s1 = load_idx(1);
-        const int c = lane >> 3, g = lane & 7;  // chunk and 16-byte group this lane copies
-        for (int i = 0; i < ntiles; ++i) {
-            const int s2 = load_idx(i + 2);
-            const int nph = to_phys(s1);
-            const int st = i % kStages;
-            const bool got = mbar_wait(smem_u32(&S.empty[st]), ((i / kStages) & 1) ^ 1, abort_flag, a.err);
-            if (!__all_sync(0xFFFFFFFFu, got)) break;
+        auto gather = [&](int tile, const int (&rw)[4]) -> bool {
+            const int st = tile % kStages;
+            const bool got = mbar_wait(smem_u32(&S.empty[st]), ((tile / kStages) & 1) ^ 1, abort_flag, a.err);
+            if (!__all_sync(0xFFFFFFFFu, got)) return false;
+            const uint32_t fb = smem_u32(&S.full[st]);
+            if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kRows * 128 * my_chunks));
+            __syncwarp();
             const uint32_t base = sKv + st * kStageBytes;
-#pragma unroll 4
-            for (int k = 0; k < 16; ++k) {
-                const int p = __shfl_sync(0xFFFFFFFFu, ph, k);
-                const int r = 4 * k + pw;
-                const uint8_t* src = p >= 0 ? kv + static_cast<int64_t>(p) * (kD * 2) + c0 * 128 : kv;
-                const uint32_t nb = p >= 0 ? 16u : 0u;  // 0: zero-fill
-                const uint32_t rowoff = static_cast<uint32_t>(r * 128);
-                cp_async16(base + c * kChunkBytes + rowoff + ((g ^ (r & 7)) << 4), src + (p >= 0 ? c * 128 + g * 16 : 0), nb);
-                if (nchunks == 5 && lane < 8)
-                    cp_async16(base + 4 * kChunkBytes + rowoff + ((lane ^ (r & 7)) << 4),
-                               src + (p >= 0 ? 4 * 128 + lane * 16 : 0), nb);
+            if (lane < kRows / 4) {
+                tma_gather4(base + pw * kChunkBytes + lane * 4 * 128, &map_kv, (c0 + pw) * 64, rw[0], rw[1], rw[2],
+                            rw[3], fb);
+                if (my_chunks == 2)
+                    tma_gather4(base + 4 * kChunkBytes + lane * 4 * 128, &map_kv, (c0 + 4) * 64, rw[0], rw[1], rw[2],
+                                rw[3], fb);
             }
-            cp_async_arrive_noinc(smem_u32(&S.full[st]));  // once this thread's copies have landed
-            ph = nph;
-            s1 = s2;
+            return true;
+        };
+        auto send = [&](int j) -> bool {
+            const int sb = j & 1;
+            const bool got = mbar_wait(smem_u32(&S.s_full[sb]), (j >> 1) & 1, abort_flag, a.err);
+            if (!__all_sync(0xFFFFFFFFu, got)) return false;
+            tc_fence_after();
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tmem + lane_base + kColS + sb * kRows, v0);
+            tmem_ld32(tmem + lane_base + kColS + sb * kRows + 32, v1);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&S.s_sent[sb]));  // the softmax may overwrite S(j) with P
+            uint32_t hp[32];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const __half2 x0 = __floats2half2_rn(__uint_as_float(v0[2 * e]) * kXScale, __uint_as_float(v0[2 * e + 1]) * kXScale);
+                const __half2 x1 = __floats2half2_rn(__uint_as_float(v1[2 * e]) * kXScale, __uint_as_float(v1[2 * e + 1]) * kXScale);
+                hp[e] = *reinterpret_cast<const uint32_t*>(&x0);
+                hp[16 + e] = *reinterpret_cast<const uint32_t*>(&x1);
+            }
+            const bool free_ok = mbar_wait_cluster(smem_u32(&S.xempty[sb]), ((j >> 1) & 1) ^ 1, abort_flag, a.err);
+            if (!__all_sync(0xFFFFFFFFu, free_ok)) return false;
+            const uint32_t dst = peer_x + sb * kXBytes;
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+                st_async_v4(dst + xoff(h, g), hp[4 * g], hp[4 * g + 1], hp[4 * g + 2], hp[4 * g + 3], peer_xfull + sb * 8);
+            return true;
+        };
+        if (lane == 0) tma_prefetch_desc(&map_kv);
+        bool ok = true;
+        for (int t = 0; ok && t < kStages - 1 && t < ntiles; ++t) {
+            int rw[4];
+            rows_of(t, rw);
+            ok = gather(t, rw);
+        }
+        for (int j = 0; ok && j < ntiles; ++j) {
+            ok = send(j);
+            if (ok && j + kStages - 1 < ntiles) {
+                int rw[4];
+                rows_of(j + kStages - 1, rw);
+                ok = gather(j + kStages - 1, rw);
+            }
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------- L2 prefetch
         // Every valid selected row's columns of this CTA (4 or 5 lines of 128 B), requested up
         // front so that the gathers find them in L2.
         const uint8_t* kv = static_cast<const uint8_t*>(a.kv) + c0 * 128;
-        for (int base = 0; base < nrows; base += 4 * 32) {
-            int sv[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int row = base + j * 32 + lane;
-                sv[j] = (row < nrows && ((valid_bits[row >> 5] >> (row & 31)) & 1u)) ? idx_row[row] : -1;
-            }
-            int pv[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) pv[j] = sv[j] >= 0 ? bt_row[sv[j] >> 6] * kBlock + (sv[j] & 63) : -1;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (pv[j] < 0) continue;
-                const uint8_t* rp = kv + static_cast<int64_t>(pv[j]) * (kD * 2);
-                for (int c = 0; c < nchunks; ++c) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + c * 128));
-            }
+        for (int row = lane; row < nrows; row += 32) {
+            const int p = phys_s[row];
+            if (p < 0) continue;
+            const uint8_t* rp = kv + static_cast<int64_t>(p) * (kD * 2);
+            for (int c = 0; c < nchunks; ++c) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + c * 128));
         }
     } else if (warp == 8) {
         // ------------------------------------------------------------- MMA issuer
@@ -270,7 +303,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             auto qk = [&](int i) -> bool {
                 const int st = i % kStages;
                 if (!mbar_wait(smem_u32(&S.full[st]), (i / kStages) & 1, abort_flag, a.err)) return false;
-                fence_proxy_async_smem();  // rows written by cp.async -> visible to the tensor core
                 tc_fence_after();
                 const uint32_t d = tmem + kColS + (i & 1) * kRows;
                 const uint64_t kvb = dkv0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
@@ -316,97 +348,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         const int h = threadIdx.x;  // head = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const float scale2 = a.sm_scale * 1.4426950408889634f / kXScale;  // exchanged units -> log2 units
-        const uint32_t peer_x = mapa_shared(sX, peer);
-        const uint32_t peer_xfull = mapa_shared(smem_u32(&S.xfull[0]), peer);    // [1] at +8
         const uint32_t peer_xempty = mapa_shared(smem_u32(&S.xempty[0]), peer);  // [1] at +8
         float m_ref = -INFINITY, l = 0.0f;
-        // Sends this CTA's partial logits of tile j to the peer's exchange slot j & 1: once the
-        // tile's S is in tensor memory and the peer has consumed tile j - 2 from that slot (which
-        // also means the copy out of the local staging slot j & 1 is complete), the 128 threads
-        // stage the partial and one thread starts the bulk copy. Arms the local slot j & 1 for the
-        // peer's tile j. Returns false for all 128 threads alike if any is dead or a wait gave up.
-        auto send_partial = [&](int j, bool dead_in) -> bool {
-            const int sb = j & 1;
-            const bool got = !dead_in && mbar_wait(smem_u32(&S.s_full[sb]), (j >> 1) & 1, abort_flag, a.err);
-            if (named_bar_or(2, 128, dead_in || !got)) return false;
-            tc_fence_after();
-            uint32_t v0[32], v1[32];
-            const uint32_t sa = tmem + lane_base + kColS + sb * kRows;
-            tmem_ld32(sa, v0);
-            tmem_ld32(sa + 32, v1);
-            tmem_ld_wait();
-            const bool free_ok = mbar_wait_cluster(smem_u32(&S.xempty[sb]), ((j >> 1) & 1) ^ 1, abort_flag, a.err);
-            // fp16(S_r * 2^-8), packed in pairs of rows; this CTA completes the tile from the same
-            // rounded values it sends, so both CTAs add identical operands
-            uint32_t hp[32];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const __half2 x0 = __floats2half2_rn(__uint_as_float(v0[2 * e]) * kXScale, __uint_as_float(v0[2 * e + 1]) * kXScale);
-                const __half2 x1 = __floats2half2_rn(__uint_as_float(v1[2 * e]) * kXScale, __uint_as_float(v1[2 * e + 1]) * kXScale);
-                hp[e] = *reinterpret_cast<const uint32_t*>(&x0);
-                hp[16 + e] = *reinterpret_cast<const uint32_t*>(&x1);
-            }
-            uint8_t* stg = smem + kOffStage + sb * kXBytes;
-#pragma unroll
-            for (int g = 0; g < 8; ++g)
-                *reinterpret_cast<uint4*>(stg + xoff(h, g)) = make_uint4(hp[4 * g], hp[4 * g + 1], hp[4 * g + 2], hp[4 * g + 3]);
-            fence_proxy_async_smem();  // generic-proxy writes -> visible to the copy engine
-            if (named_bar_or(2, 128, !free_ok)) return false;
-            if (threadIdx.x == 0) {
-                mbar_arrive_expect_tx(smem_u32(&S.xfull[sb]), kXBytes);  // the peer's tile j lands here
-                bulk_copy_to_peer(peer_x + sb * kXBytes, sStage + sb * kXBytes, kXBytes, peer_xfull + sb * 8);
-            }
-            return true;
-        };
         bool dead = false;
-        int sent = 0;  // tiles [0, sent) have been sent to the peer
-        for (int i = 0; i < ntiles; ++i) {  // every softmax thread takes the same barriers, dead or not
+        for (int i = 0; i < ntiles; ++i) {
             const int sb = i & 1;
-            if (sent <= i) {  // tile i itself must go out before it can complete
-                if (!send_partial(i, dead)) {
-                    dead = true;
-                    break;
-                }
-                sent = i + 1;
-            }
-            // Send tile i + 1 ahead if its S is already in tensor memory (never wait for it here:
-            // its rows may still be in flight behind this tile's product). The OR makes the
-            // decision uniform; a phase seen complete by one thread is complete for all.
-            const bool ahead = i + 1 < ntiles && mbar_test(smem_u32(&S.s_full[(i + 1) & 1]), ((i + 1) >> 1) & 1);
-            if (named_bar_or(2, 128, ahead && !dead)) {
-                if (!send_partial(i + 1, dead)) {
-                    dead = true;
-                    break;
-                }
-                sent = i + 2;
-            } else if (named_bar_or(2, 128, dead)) {
+            const bool got = mbar_wait(smem_u32(&S.s_full[sb]), (i >> 1) & 1, abort_flag, a.err) &&
+                             mbar_wait_cluster(smem_u32(&S.xfull[sb]), (i >> 1) & 1, abort_flag, a.err);
+            if (__any_sync(0xFFFFFFFFu, !got)) {
                 dead = true;
                 break;
             }
-            // complete tile i: this CTA's rounded partial (still in its staging slot) plus the peer's,
-            // both in units of 2^8 (the scale is folded into scale2)
-            const bool got = mbar_wait_cluster(smem_u32(&S.xfull[sb]), (i >> 1) & 1, abort_flag, a.err);
-            if (__any_sync(0xFFFFFFFFu, !got)) dead = true;
+            tc_fence_after();
+            // this CTA's partial, rounded exactly as the producers sent it, plus the peer's; both
+            // in units of 2^8 (the scale is folded into scale2)
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tmem + lane_base + kColS + sb * kRows, v0);
+            tmem_ld32(tmem + lane_base + kColS + sb * kRows + 32, v1);
+            tmem_ld_wait();
             float z[kRows];
-            {
-                const uint8_t* mine = smem + kOffStage + sb * kXBytes;
-                const uint8_t* theirs = smem + kOffX + sb * kXBytes;
+            const uint8_t* theirs = smem + kOffX + sb * kXBytes;
 #pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    const uint4 u = *reinterpret_cast<const uint4*>(mine + xoff(h, g));
-                    const uint4 w = dead ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(theirs + xoff(h, g));
-                    const uint32_t us[4] = {u.x, u.y, u.z, u.w}, ws[4] = {w.x, w.y, w.z, w.w};
+            for (int g = 0; g < 8; ++g) {
+                const uint4 w = *reinterpret_cast<const uint4*>(theirs + xoff(h, g));
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&us[q]));
-                        const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&ws[q]));
-                        z[8 * g + 2 * q] = a2.x + b2.x;
-                        z[8 * g + 2 * q + 1] = a2.y + b2.y;
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    const int r = 8 * g + 2 * q;  // rows r, r + 1
+                    const float o0 = __uint_as_float(r < 32 ? v0[r] : v1[r - 32]);
+                    const float o1 = __uint_as_float(r < 32 ? v0[r + 1] : v1[r - 31]);
+                    const float2 a2 = __half22float2(__floats2half2_rn(o0 * kXScale, o1 * kXScale));
+                    const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&ws[q]));
+                    z[r] = a2.x + b2.x;
+                    z[r + 1] = a2.y + b2.y;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(peer_xempty + sb * 8);  // the peer may refill this slot
             // rows without a position (past the split's end, idx -1, bad entries) take no weight
             const uint32_t vm0 = valid_bits[2 * i], vm1 = valid_bits[2 * i + 1];
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -457,13 +433,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                 ls[(j >> 1) & 3] += __uint_as_float(u << 16) + __uint_as_float(u & 0xFFFF0000u);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            if (!dead) {  // P (bf16) over the first 32 columns of this tile's S
+            // P (bf16) over the first 32 columns of this tile's S, once the producers have read S
+            const bool read_ok = mbar_wait(smem_u32(&S.s_sent[sb]), (i >> 1) & 1, abort_flag, a.err);
+            if (__any_sync(0xFFFFFFFFu, !read_ok)) dead = true;
+            if (!dead) {
                 tmem_st32(tmem + lane_base + kColS + sb * kRows, packed);
                 tmem_st_wait();
                 tc_fence_before();
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&S.p_full[sb]));
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&S.p_full[sb]));
+                // the peer may refill this exchange slot: every value read from it has been consumed
+                mbar_arrive_remote_relaxed(peer_xempty + sb * 8);
+            }
+            // the slot now expects the peer's tile i + 2 (its phase for tile i is complete)
+            if (threadIdx.x == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(smem_u32(&S.xfull[sb]), kXBytes);
         }
         if (ntiles > 0) {  // every softmax thread takes this barrier, dead or not
             const bool got = dead ? false : mbar_wait(smem_u32(&S.o_full), 0, abort_flag, a.err);
@@ -571,11 +556,15 @@ bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches) {
     if (!make_tmap_2d(&map_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcattn::kD,
                       static_cast<uint64_t>(a.T) * tcattn::kHeads, tcattn::kD * 2, 64, 128))
         return false;
+    CUtensorMap map_kv;  // [num_blocks * 64 rows][576 cols], gathered one row x 64 columns at a time
+    if (!make_tmap_2d(&map_kv, a.kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcattn::kD,
+                      static_cast<uint64_t>(a.num_blocks) * kBlock, tcattn::kD * 2, 64, 1))
+        return false;
     if (cudaFuncSetAttribute(tcattn::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(tcattn::kSmemBytes)) != cudaSuccess)
         return false;
     dim3 grid(2 * a.S, a.T);
-    tcattn::attn_tc_kernel<<<grid, tcattn::kThreads, tcattn::kSmemBytes, s>>>(a, map_q);
+    tcattn::attn_tc_kernel<<<grid, tcattn::kThreads, tcattn::kSmemBytes, s>>>(a, map_q, map_kv);
     ++*launches;
     if (cudaGetLastError() != cudaSuccess) return false;
     if (a.S > 1) {

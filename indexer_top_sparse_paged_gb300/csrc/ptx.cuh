@@ -150,6 +150,17 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory (cluster address, 16-byte aligned);
+// its bytes count as complete_tx on that CTA's mbarrier `remote_bar` (cluster address), which
+// makes them visible to the threads that wait on it. The storing thread does not wait.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+                 : "memory");
+}
+
 // Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from this CTA's shared
 // memory to another CTA's shared memory in the cluster, performed by the copy engine; the
 // destination CTA's mbarrier (cluster address) receives the byte count as complete_tx. The source
@@ -166,6 +177,12 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t
 // (including its distributed-shared-memory stores) at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// As mbar_arrive_remote, without ordering this thread's earlier memory accesses: for hand-offs whose
+// data dependences already order them (the loaded values were consumed before the arrive).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
