@@ -6,26 +6,28 @@
 // Work unit: a cluster of two CTAs per (query row t, split of its K selected rows). The pair
 // divides the latent dimension: CTA 0 owns columns 0..255, CTA 1 owns columns 256..575, so every
 // selected row is gathered from memory exactly once. For every tile of 64 gathered rows each CTA
-//   1. gathers only its columns of the 64 rows (the index list drives 16-byte cp.async row
-//      copies by four producer warps into the 128-byte-swizzled layout the tensor core reads),
+//   1. gathers only its columns of the 64 rows (the index list, resolved once to physical cache
+//      rows, drives 16-byte cp.async row copies by four producer warps straight into the
+//      128-byte-swizzled layout the tensor core reads; four row stages),
 //   2. computes its partial logits S_r[128 heads x 64 rows] = Q[:, cols_r] . R[:, cols_r]^T with
 //      tcgen05 (M = 128 heads, N = 64 rows; an MMA of N < 64 would leave the tensor pipe idle),
-//   3. sends S_r to the other CTA with one bulk shared-memory copy (the copy engine moves it, so
-//      the transfer does not compete with the tensor core's operand reads) and adds the one it
-//      receives (S_0 + S_1 in both CTAs: fp32 addition commutes, so both see the same logits); the
-//      partial of tile i + 1 is sent before tile i is completed whenever it is already computed,
-//      so the transfer overlaps the softmax (two exchange slots per direction),
+//   3. the producer warps, as soon as S_r is in tensor memory, round it to fp16(S_r * 2^-8) and
+//      store it into the other CTA's shared memory with st.async (completion counted in bytes on
+//      the receiver's mbarrier; the sender never waits); the softmax adds the two rounded
+//      partials, which both CTAs do with identical operands, so both see the same logits,
 //   4. runs the online softmax (one thread per head, lazy rescaling of O when a head's running
 //      maximum grows by more than 2^8) and writes P as bf16 over its S in tensor memory,
 //   5. accumulates O_r[128 x 256] += P . V_r with V_r = its 256 value columns (CTA 0: values
 //      0..255, CTA 1: values 256..511 -- both inside the columns it already holds).
-// Tensor memory holds the O accumulator (256 fp32 columns), two S/P buffers and all but the first
-// 64 query columns of the CTA (A operand from TMEM); shared memory holds the first query chunk,
-// two row stages, the two exchange slots in each direction and a validity bit per selected row.
+// Split-K partials (m, l, O) are merged by attn_combine_kernel. Tensor memory holds the O
+// accumulator (256 fp32 columns), two S/P buffers and all but the first 64 query columns of the
+// CTA (A operand from TMEM); shared memory holds the first query chunk, four row stages, two
+// exchange slots and the resolved rows of the split.
 //
 // Roles (320 threads per CTA): warps 0-3 softmax / epilogue (thread = head = TMEM lane), warps
-// 4-7 gather producers, warp 8 TMEM allocator + MMA issuer (+ the TMA load of the first query
-// chunk), warp 9 prefetches the CTA's columns of every selected row into L2 at the start.
+// 4-7 producers (gather rows; send the partial logits of their TMEM lane quarter), warp 8 TMEM
+// allocator + MMA issuer (+ the TMA loads of the query), warp 9 prefetches the CTA's columns of
+// every selected row into L2 at the start.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -91,7 +93,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
-    attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv) {
+    attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap map_q) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem + kOffQ);
@@ -121,7 +123,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(smem_u32(&S.full[i]), kProducers);  // one arrive.expect_tx per producer warp
+            mbar_init(smem_u32(&S.full[i]), kProducers * 32);  // every producer thread's cp.async
             mbar_init(smem_u32(&S.empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -151,50 +153,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
     const uint32_t tmem = S.tmem_base;
 
     if (warp == 8 && lane == 0 && ntiles > 0) {
-        mbar_arrive_expect_tx(smem_u32(&S.qfull), kQChunkBytes);
+        // the CTA's query chunks: the first to its own buffer (A operand from shared memory), the
+        // rest to the still idle row stages, from where they move to tensor memory below
+        mbar_arrive_expect_tx(smem_u32(&S.qfull), static_cast<uint32_t>(nchunks * kQChunkBytes));
         tma_load_2d(sQ, &map_q, c0 * 64, t * kHeads, smem_u32(&S.qfull));
-    }
-    if (warp < 4 && ntiles > 0) {
-        // the CTA's query chunks after the first go to tensor memory (head = lane, bf16 pairs)
-        const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(t) * kHeads + threadIdx.x) * kD;
-        for (int k = 0; k + 1 < nchunks; ++k) {
-            const uint4* src = reinterpret_cast<const uint4*>(qrow + (c0 + 1 + k) * 64);
-            uint32_t w[32];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint4 v = src[i];
-                w[4 * i] = v.x;
-                w[4 * i + 1] = v.y;
-                w[4 * i + 2] = v.z;
-                w[4 * i + 3] = v.w;
-            }
-            tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + kColQ + k * 32, w);
-        }
-        tmem_st_wait();
+        for (int k = 1; k < nchunks; ++k)
+            tma_load_2d(sKv + (k - 1) * kQChunkBytes, &map_q, (c0 + k) * 64, t * kHeads, smem_u32(&S.qfull));
     }
     // every selected row resolved once to its physical cache row (-1: no position, or a bad entry,
-    // whose fault CTA 0 records) plus a validity bit per row for the softmax
-    for (int w0 = warp * 32; w0 < ntiles * kRows; w0 += kThreads) {
-        const int i = w0 + lane;
-        int32_t p = -1;
-        if (i < nrows) {
-            const int s = idx_row[i];
-            if (s != -1) {
-                if (s < 0 || s >= L) {
+    // whose fault CTA 0 records) plus a validity bit per row for the softmax; all index loads are
+    // issued before the dependent block-table loads
+    {
+        constexpr int kPerThread = (kMaxRows + kThreads - 1) / kThreads;
+        int sv[kPerThread];
+#pragma unroll
+        for (int q = 0; q < kPerThread; ++q) {
+            const int i = (q * (kThreads / 32) + warp) * 32 + lane;
+            sv[q] = (i < nrows) ? idx_row[i] : -1;
+        }
+        int blk[kPerThread];
+#pragma unroll
+        for (int q = 0; q < kPerThread; ++q)
+            blk[q] = (sv[q] >= 0 && sv[q] < L && (sv[q] >> 6) < a.max_blocks) ? bt_row[sv[q] >> 6] : -1;
+#pragma unroll
+        for (int q = 0; q < kPerThread; ++q) {
+            const int w0 = (q * (kThreads / 32) + warp) * 32;
+            if (w0 >= ntiles * kRows) break;  // warp-uniform
+            const int i = w0 + lane;
+            int32_t p = -1;
+            if (i < nrows && sv[q] != -1) {
+                if (sv[q] < 0 || sv[q] >= L) {
                     if (rank == 0) atomicOr(a.err, DSA_FAULT_INDEX);
+                } else if (blk[q] < 0 || blk[q] >= a.num_blocks) {
+                    if (rank == 0) atomicOr(a.err, DSA_FAULT_BLOCK_TABLE);
                 } else {
-                    const int blk = bt_row[s >> 6];
-                    if (blk < 0 || blk >= a.num_blocks) {
-                        if (rank == 0) atomicOr(a.err, DSA_FAULT_BLOCK_TABLE);
-                    } else {
-                        p = blk * kBlock + (s & 63);
-                    }
+                    p = blk[q] * kBlock + (sv[q] & 63);
                 }
             }
+            phys_s[i] = p;
+            const uint32_t word = __ballot_sync(0xFFFFFFFFu, p >= 0);
+            if (lane == 0) valid_bits[w0 >> 5] = word;
         }
-        phys_s[i] = p;
-        const uint32_t word = __ballot_sync(0xFFFFFFFFu, p >= 0);
-        if (lane == 0) valid_bits[w0 >> 5] = word;
+    }
+    if (warp < 4 && ntiles > 0) {
+        // query chunks 1.. of head h (row h of the 128-byte-swizzled boxes) -> TMEM lane h, bf16 pairs
+        const bool got = mbar_wait(smem_u32(&S.qfull), 0, abort_flag, a.err);
+        if (__all_sync(0xFFFFFFFFu, got)) {
+            const int h = threadIdx.x;
+            for (int k = 0; k + 1 < nchunks; ++k) {
+                const uint8_t* row = smem + kOffKv + k * kQChunkBytes + (h >> 3) * 1024 + (h & 7) * 128;
+                uint32_t w[32];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(row + ((g ^ (h & 7)) << 4));
+                    w[4 * g] = v.x;
+                    w[4 * g + 1] = v.y;
+                    w[4 * g + 2] = v.z;
+                    w[4 * g + 3] = v.w;
+                }
+                tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + kColQ + k * 32, w);
+            }
+            tmem_st_wait();
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -217,26 +237,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         const uint32_t lane_base = static_cast<uint32_t>(pw * 32) << 16;
         const uint32_t peer_x = mapa_shared(sX, peer);
         const uint32_t peer_xfull = mapa_shared(smem_u32(&S.xfull[0]), peer);  // [1] at +8
-        const int my_chunks = (pw == 0 && nchunks == 5) ? 2 : 1;
-        auto rows_of = [&](int tile, int (&rw)[4]) {  // physical cache rows of rows 4g..4g+3, or -1
-#pragma unroll
-            for (int j = 0; j < 4; ++j) rw[j] = (lane < 16 && tile < ntiles) ? phys_s[tile * kRows + 4 * lane + j] : -1;
-        };
-        auto gather = [&](int tile, const int (&rw)[4]) -> bool {
+        const uint8_t* kv = static_cast<const uint8_t*>(a.kv) + c0 * 128;
+        const int c = lane >> 3, g = lane & 7;  // chunk and 16-byte group this lane copies
+        auto gather = [&](int tile) -> bool {
             const int st = tile % kStages;
             const bool got = mbar_wait(smem_u32(&S.empty[st]), ((tile / kStages) & 1) ^ 1, abort_flag, a.err);
             if (!__all_sync(0xFFFFFFFFu, got)) return false;
-            const uint32_t fb = smem_u32(&S.full[st]);
-            if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kRows * 128 * my_chunks));
-            __syncwarp();
             const uint32_t base = sKv + st * kStageBytes;
-            if (lane < kRows / 4) {
-                tma_gather4(base + pw * kChunkBytes + lane * 4 * 128, &map_kv, (c0 + pw) * 64, rw[0], rw[1], rw[2],
-                            rw[3], fb);
-                if (my_chunks == 2)
-                    tma_gather4(base + 4 * kChunkBytes + lane * 4 * 128, &map_kv, (c0 + 4) * 64, rw[0], rw[1], rw[2],
-                                rw[3], fb);
+#pragma unroll 4
+            for (int k = 0; k < kRows / kProducers; ++k) {
+                const int r = kProducers * k + pw;
+                const int p = phys_s[tile * kRows + r];
+                const uint8_t* src = p >= 0 ? kv + static_cast<int64_t>(p) * (kD * 2) : kv;
+                const uint32_t nb = p >= 0 ? 16u : 0u;  // 0: zero-fill
+                const uint32_t rowoff = static_cast<uint32_t>(r * 128);
+                cp_async16(base + c * kChunkBytes + rowoff + ((g ^ (r & 7)) << 4), src + (p >= 0 ? c * 128 + g * 16 : 0), nb);
+                if (nchunks == 5 && lane < 8)
+                    cp_async16(base + 4 * kChunkBytes + rowoff + ((lane ^ (r & 7)) << 4),
+                               src + (p >= 0 ? 4 * 128 + lane * 16 : 0), nb);
             }
+            cp_async_arrive_noinc(smem_u32(&S.full[st]));  // once this thread's copies have landed
             return true;
         };
         auto send = [&](int j) -> bool {
@@ -267,20 +287,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                 st_async_v4(dst + xoff(h, g), hp[4 * g], hp[4 * g + 1], hp[4 * g + 2], hp[4 * g + 3], peer_xfull + sb * 8);
             return true;
         };
-        if (lane == 0) tma_prefetch_desc(&map_kv);
         bool ok = true;
-        for (int t = 0; ok && t < kStages - 1 && t < ntiles; ++t) {
-            int rw[4];
-            rows_of(t, rw);
-            ok = gather(t, rw);
-        }
+        for (int t = 0; ok && t < kStages - 1 && t < ntiles; ++t) ok = gather(t);
         for (int j = 0; ok && j < ntiles; ++j) {
             ok = send(j);
-            if (ok && j + kStages - 1 < ntiles) {
-                int rw[4];
-                rows_of(j + kStages - 1, rw);
-                ok = gather(j + kStages - 1, rw);
-            }
+            if (ok && j + kStages - 1 < ntiles) ok = gather(j + kStages - 1);
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------- L2 prefetch
@@ -303,6 +314,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             auto qk = [&](int i) -> bool {
                 const int st = i % kStages;
                 if (!mbar_wait(smem_u32(&S.full[st]), (i / kStages) & 1, abort_flag, a.err)) return false;
+                fence_proxy_async_smem();  // rows written by cp.async -> visible to the tensor core
                 tc_fence_after();
                 const uint32_t d = tmem + kColS + (i & 1) * kRows;
                 const uint64_t kvb = dkv0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
@@ -456,54 +468,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         }
         const bool have_o = ntiles > 0 && !dead;
         if (have_o) tc_fence_after();
-        const int64_t prow = (static_cast<int64_t>(t) * a.S + split) * kHeads + h;
+        // O rows leave through a per-warp 32 x 32 transpose in the (now idle) row stages, so that
+        // every store of a warp covers whole 128-byte runs of head rows
+        float* tile = reinterpret_cast<float*>(smem + kOffKv) + warp * (32 * 33);
+        const int h0 = warp * 32;
+        const bool zero = !(have_o && l > 0.0f);  // the row is written as zeros
+        const int col0 = rank * kDVH;
+        auto stage_chunk = [&](int cc) {  // O[h0 + lane][cc*32 .. +32) -> tile[lane][.]
+            uint32_t v[32];
+            if (have_o) {
+                tmem_ld32(tmem + lane_base + kColO + cc * 32, v);
+                tmem_ld_wait();
+            }
+            __syncwarp();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) tile[lane * 33 + e] = zero ? 0.0f : __uint_as_float(v[e]);
+            __syncwarp();
+        };
+        const int tq = lane & 7;  // after the transpose: lane covers columns 4tq..4tq+3 of heads (lane >> 3) + 4j
         if (a.S == 1) {
-            const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
-            uint16_t* out =
-                static_cast<uint16_t*>(a.out) + (static_cast<int64_t>(t) * kHeads + h) * kDV + rank * kDVH;
+            const float inv = zero ? 0.0f : 1.0f / l;
+            float invk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) invk[j] = __shfl_sync(0xFFFFFFFFu, inv, (lane >> 3) + 4 * j);
 #pragma unroll 1
             for (int cc = 0; cc < kDVH / 32; ++cc) {
-                uint32_t v[32];
-                if (have_o) {
-                    tmem_ld32(tmem + lane_base + kColO + cc * 32, v);
-                    tmem_ld_wait();
-                }
-                uint32_t w[16];
+                stage_chunk(cc);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float o0 = have_o ? __uint_as_float(v[2 * e]) * inv : 0.0f;
-                    const float o1 = have_o ? __uint_as_float(v[2 * e + 1]) * inv : 0.0f;
-                    w[e] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o0))) |
-                           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o1))) << 16);
+                for (int j = 0; j < 8; ++j) {
+                    const int k = (lane >> 3) + 4 * j;
+                    const float* tr = tile + k * 33 + 4 * tq;
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(tr[0] * invk[j], tr[1] * invk[j]);
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(tr[2] * invk[j], tr[3] * invk[j]);
+                    uint16_t* out = static_cast<uint16_t*>(a.out) + (static_cast<int64_t>(t) * kHeads + h0 + k) * kDV +
+                                    col0 + cc * 32 + 4 * tq;
+                    *reinterpret_cast<uint2*>(out) =
+                        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
                 }
-                uint4* dst = reinterpret_cast<uint4*>(out + cc * 32);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             }
             if (rank == 0 && a.lse)
                 a.lse[static_cast<int64_t>(t) * kHeads + h] =
                     (l > 0.0f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
         } else {
-            float* po = a.part_o + prow * kDV + rank * kDVH;
+            // split-K: this CTA's partial (O half, m, l) to the workspace; attn_combine_kernel merges
 #pragma unroll 1
             for (int cc = 0; cc < kDVH / 32; ++cc) {
-                uint32_t v[32];
-                if (have_o) {
-                    tmem_ld32(tmem + lane_base + kColO + cc * 32, v);
-                    tmem_ld_wait();
-                }
-                float4* dst = reinterpret_cast<float4*>(po + cc * 32);
-                const bool zero = !(have_o && l > 0.0f);
+                stage_chunk(cc);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    dst[q] = zero ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                  : make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                for (int j = 0; j < 8; ++j) {
+                    const int k = (lane >> 3) + 4 * j;
+                    const float* tr = tile + k * 33 + 4 * tq;
+                    float* po = a.part_o + ((static_cast<int64_t>(t) * a.S + split) * kHeads + h0 + k) * kDV + col0 +
+                                cc * 32 + 4 * tq;
+                    *reinterpret_cast<float4*>(po) = make_float4(tr[0], tr[1], tr[2], tr[3]);
+                }
             }
-            if (rank == 0) {
-                a.part_ml[prow * 2] = (l > 0.0f) ? m_ref : -INFINITY;
-                a.part_ml[prow * 2 + 1] = l;
-            }
+            const int64_t mlrow = ((static_cast<int64_t>(t) * a.S + split) * 2 + rank) * kHeads + h;
+            a.part_ml[mlrow * 2] = (l > 0.0f && !zero) ? m_ref : -INFINITY;
+            a.part_ml[mlrow * 2 + 1] = zero ? 0.0f : l;
         }
     }
 
@@ -520,16 +542,17 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
     const int h = blockIdx.x, t = blockIdx.y;
     const int c = threadIdx.x * 4;
     float M = -INFINITY;
-    for (int s = 0; s < a.S; ++s) M = fmaxf(M, a.part_ml[((static_cast<int64_t>(t) * a.S + s) * kHeads + h) * 2]);
+    for (int s = 0; s < a.S; ++s) M = fmaxf(M, a.part_ml[((static_cast<int64_t>(t) * a.S + s) * 2 * kHeads + h) * 2]);
     float wsum = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
         for (int s = 0; s < a.S; ++s) {
             const int64_t prow = (static_cast<int64_t>(t) * a.S + s) * kHeads + h;
-            const float ms = a.part_ml[prow * 2];
+            const int64_t mlrow = (static_cast<int64_t>(t) * a.S + s) * 2 * kHeads + h;  // CTA 0's (m, l)
+            const float ms = a.part_ml[mlrow * 2];
             if (ms == -INFINITY) continue;
             const float f = exp2f(ms - M);
-            wsum += f * a.part_ml[prow * 2 + 1];
+            wsum += f * a.part_ml[mlrow * 2 + 1];
             const float4 o = *reinterpret_cast<const float4*>(a.part_o + prow * kDV + c);
             acc.x = fmaf(f, o.x, acc.x);
             acc.y = fmaf(f, o.y, acc.y);
@@ -556,15 +579,11 @@ bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches) {
     if (!make_tmap_2d(&map_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcattn::kD,
                       static_cast<uint64_t>(a.T) * tcattn::kHeads, tcattn::kD * 2, 64, 128))
         return false;
-    CUtensorMap map_kv;  // [num_blocks * 64 rows][576 cols], gathered one row x 64 columns at a time
-    if (!make_tmap_2d(&map_kv, a.kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcattn::kD,
-                      static_cast<uint64_t>(a.num_blocks) * kBlock, tcattn::kD * 2, 64, 1))
-        return false;
     if (cudaFuncSetAttribute(tcattn::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(tcattn::kSmemBytes)) != cudaSuccess)
         return false;
     dim3 grid(2 * a.S, a.T);
-    tcattn::attn_tc_kernel<<<grid, tcattn::kThreads, tcattn::kSmemBytes, s>>>(a, map_q, map_kv);
+    tcattn::attn_tc_kernel<<<grid, tcattn::kThreads, tcattn::kSmemBytes, s>>>(a, map_q);
     ++*launches;
     if (cudaGetLastError() != cudaSuccess) return false;
     if (a.S > 1) {

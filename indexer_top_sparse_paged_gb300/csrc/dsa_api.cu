@@ -66,7 +66,7 @@ WsLayout ws_layout(const dsa_dims& d, int T) {
     w.part_o = off;
     if (w.S > 1) off = align256(off + sizeof(float) * static_cast<size_t>(T) * w.S * d.H * d.d_v);
     w.part_ml = off;
-    if (w.S > 1) off = align256(off + sizeof(float) * static_cast<size_t>(T) * w.S * d.H * 2);
+    if (w.S > 1) off = align256(off + sizeof(float) * static_cast<size_t>(T) * w.S * 2 * d.H * 2);
     w.scores = off;
     w.total = off;
     return w;

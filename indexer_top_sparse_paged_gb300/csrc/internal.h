@@ -23,7 +23,7 @@ struct WsLayout {
     size_t slots;        // uint64 [G + T][K]
     size_t idx;          // int32 [T][K] (dsa_decode without a caller idx)
     size_t part_o;       // fp32 [T][S][H][d_v]
-    size_t part_ml;      // fp32 [T][S][H][2]
+    size_t part_ml;      // fp32 [T][S][2 CTAs][H][2] (m, l)
     size_t scores;       // fp32 [T][max_blocks * 64] (prefill only)
     size_t total;
     int G;               // indexer CTAs
