@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(kAttnSimtThreads) attn_simt_kernel(AttnArgs a)
 
     for (int e = tid; e < d; e += kAttnSimtThreads)
         q_s[e] = act_f(a.q, (static_cast<int64_t>(t) * a.H + h) * d + e, BF16);
+    griddep_wait();  // idx may come from the previous kernel of this call
     for (int i = tid; i < K; i += kAttnSimtThreads) {
         const int s = a.idx[static_cast<int64_t>(t) * K + i];
         int64_t r = -1;
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(kAttnSimtThreads) attn_simt_kernel(AttnArgs a)
         }
         row_s[i] = r;
     }
-    __syncthreads();
+    block_sync();
 
     // logits: one warp per selected row
     for (int i = warp; i < K; i += kAttnSimtThreads / 32) {
@@ -65,20 +66,20 @@ __global__ void __launch_bounds__(kAttnSimtThreads) attn_simt_kernel(AttnArgs a)
         }
         if (lane == 0) z_s[i] = (r >= 0) ? dot * a.sm_scale : -INFINITY;
     }
-    __syncthreads();
+    block_sync();
 
     float m = -INFINITY;
     for (int i = tid; i < K; i += kAttnSimtThreads) m = fmaxf(m, z_s[i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if (lane == 0) red[warp] = m;
-    __syncthreads();
+    block_sync();
     if (tid == 0) {
         float mm = -INFINITY;
         for (int w = 0; w < kAttnSimtThreads / 32; ++w) mm = fmaxf(mm, red[w]);
         m_s = mm;
     }
-    __syncthreads();
+    block_sync();
     m = m_s;
     float l = 0.0f;
     for (int i = tid; i < K; i += kAttnSimtThreads) {
@@ -88,15 +89,15 @@ __global__ void __launch_bounds__(kAttnSimtThreads) attn_simt_kernel(AttnArgs a)
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-    __syncthreads();
+    block_sync();
     if (lane == 0) red[warp] = l;
-    __syncthreads();
+    block_sync();
     if (tid == 0) {
         float ll = 0.0f;
         for (int w = 0; w < kAttnSimtThreads / 32; ++w) ll += red[w];
         l_s = ll;
     }
-    __syncthreads();
+    block_sync();
     l = l_s;
     const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
 
@@ -118,19 +119,16 @@ bool launch_attn_simt(const AttnArgs& a, cudaStream_t s, int* launches) {
     if (a.T == 0) return true;
     const size_t smem = static_cast<size_t>(a.d + a.K) * 4 + 8 + static_cast<size_t>(a.K) * 8;
     dim3 grid(a.H, a.T);
+    const bool pdl = a.after_own_kernel != 0;
     if (a.mode == DSA_F32) {
-        if (cudaFuncSetAttribute(attn_simt_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
-            return false;
-        attn_simt_kernel<false><<<grid, kAttnSimtThreads, smem, s>>>(a);
+        if (!set_max_dynamic_smem(reinterpret_cast<const void*>(attn_simt_kernel<false>), smem)) return false;
+        if (!launch_kernel(pdl, attn_simt_kernel<false>, grid, dim3(kAttnSimtThreads), smem, s, a)) return false;
     } else {
-        if (cudaFuncSetAttribute(attn_simt_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
-            return false;
-        attn_simt_kernel<true><<<grid, kAttnSimtThreads, smem, s>>>(a);
+        if (!set_max_dynamic_smem(reinterpret_cast<const void*>(attn_simt_kernel<true>), smem)) return false;
+        if (!launch_kernel(pdl, attn_simt_kernel<true>, grid, dim3(kAttnSimtThreads), smem, s, a)) return false;
     }
     ++*launches;
-    return cudaGetLastError() == cudaSuccess;
+    return true;
 }
 
 }  // namespace dsa

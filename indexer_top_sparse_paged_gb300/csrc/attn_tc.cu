@@ -105,6 +105,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
     volatile int* abort_flag = &S.abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    griddep_launch_dependents();
     const uint32_t rank = cluster_ctarank();  // 0: columns 0..255, 1: columns 256..575
     const uint32_t peer = rank ^ 1u;
     const int nchunks = rank ? 5 : 4;         // row chunks of 64 columns this CTA gathers
@@ -160,6 +161,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         for (int k = 1; k < nchunks; ++k)
             tma_load_2d(sKv + (k - 1) * kQChunkBytes, &map_q, (c0 + k) * 64, t * kHeads, smem_u32(&S.qfull));
     }
+    griddep_wait();  // idx may come from the previous kernel of this call
     // every selected row resolved once to its physical cache row (-1: no position, or a bad entry,
     // whose fault CTA 0 records) plus a validity bit per row for the softmax; all index loads are
     // issued before the dependent block-table loads
@@ -217,7 +219,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         }
     }
     tc_fence_before();
-    __syncthreads();
+    block_sync();
     tc_fence_after();
 
     if (warp >= 4 && warp < 4 + kProducers) {
@@ -532,6 +534,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
     tc_fence_before();
     cluster_sync_all();  // no remote access to this CTA's shared memory may follow its exit
     if (warp == 8) {
+        __syncwarp();  // the issuing lane rejoins its warp: dealloc is a whole-warp (aligned) instruction
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -539,6 +542,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
 
 // out[t][h][:] = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s over the splits of row t.
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
+    griddep_wait();  // the partials of every split are written
     const int h = blockIdx.x, t = blockIdx.y;
     const int c = threadIdx.x * 4;
     float M = -INFINITY;
@@ -579,17 +583,14 @@ bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches) {
     if (!make_tmap_2d(&map_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcattn::kD,
                       static_cast<uint64_t>(a.T) * tcattn::kHeads, tcattn::kD * 2, 64, 128))
         return false;
-    if (cudaFuncSetAttribute(tcattn::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(tcattn::kSmemBytes)) != cudaSuccess)
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(tcattn::attn_tc_kernel), tcattn::kSmemBytes)) return false;
+    if (!launch_kernel(a.after_own_kernel != 0, tcattn::attn_tc_kernel, dim3(2 * a.S, a.T), dim3(tcattn::kThreads),
+                       tcattn::kSmemBytes, s, a, map_q))
         return false;
-    dim3 grid(2 * a.S, a.T);
-    tcattn::attn_tc_kernel<<<grid, tcattn::kThreads, tcattn::kSmemBytes, s>>>(a, map_q);
     ++*launches;
-    if (cudaGetLastError() != cudaSuccess) return false;
     if (a.S > 1) {
-        tcattn::attn_combine_kernel<<<dim3(tcattn::kHeads, a.T), 128, 0, s>>>(a);
+        if (!launch_kernel(true, tcattn::attn_combine_kernel, dim3(tcattn::kHeads, a.T), dim3(128), 0, s, a)) return false;
         ++*launches;
-        if (cudaGetLastError() != cudaSuccess) return false;
     }
     return true;
 }

@@ -9,7 +9,9 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -17,11 +19,35 @@ namespace dsa {
 
 static thread_local int g_last_launches = 0;
 
+constexpr int kMaxDevices = 64;
+
 int device_sm_count() {
+    static std::atomic<int> cache[kMaxDevices];
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < kMaxDevices && (n = cache[dev].load(std::memory_order_relaxed)) > 0) return n;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
     return n;
+}
+
+bool set_max_dynamic_smem(const void* func, size_t bytes) {
+    struct Entry {
+        int dev;
+        const void* func;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : done)
+        if (e.dev == dev && e.func == func && e.bytes >= bytes) return true;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess)
+        return false;
+    done.push_back({dev, func, bytes});
+    return true;
 }
 
 bool indexer_uses_tc(const dsa_dims& d) { return d.mode == DSA_BF16 && d.H_I == 64 && d.d_I == 128; }
@@ -183,7 +209,8 @@ static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w
 
 static dsa_status run_attn(const dsa_dims* d, const void* q, const void* kv_cache, const int32_t* block_table,
                            const int32_t* seq_lens, const int32_t* q_seq, const int32_t* idx, int32_t T,
-                           float sm_scale, void* out, float* lse, void* ws, cudaStream_t stream, int* launches) {
+                           float sm_scale, void* out, float* lse, void* ws, cudaStream_t stream, int* launches,
+                           bool after_own_kernel) {
     const WsLayout L = ws_layout(*d, T);
     uint8_t* base = static_cast<uint8_t*>(ws);
     AttnArgs a{};
@@ -209,6 +236,7 @@ static dsa_status run_attn(const dsa_dims* d, const void* q, const void* kv_cach
     a.part_ml = reinterpret_cast<float*>(base + L.part_ml);
     a.S = L.S;
     a.err = reinterpret_cast<int*>(base + L.err);
+    a.after_own_kernel = after_own_kernel ? 1 : 0;
     const bool ok = attn_uses_tc(*d) ? launch_attn_tc(a, stream, launches) : launch_attn_simt(a, stream, launches);
     return ok ? DSA_OK : DSA_ERR_LAUNCH;
 }
@@ -220,7 +248,6 @@ static dsa_status run_attn(const dsa_dims* d, const void* q, const void* kv_cach
 constexpr size_t kNoAllocScratchBytes = DSA_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
 static std::mutex g_noalloc_mu;
 static void* g_noalloc_base[kMaxDevices];
 
@@ -291,7 +318,7 @@ dsa_status dsa_sparse_attn(const dsa_dims* dims, const void* q, const void* kv_c
     int launches = 0;
     if (T > 0)
         st = run_attn(dims, q, kv_cache, block_table, seq_lens, q_seq, idx, T, sm_scale, out, lse, ws,
-                      reinterpret_cast<cudaStream_t>(stream), &launches);
+                      reinterpret_cast<cudaStream_t>(stream), &launches, false);
     g_last_launches = launches;
     return st;
 }
@@ -320,7 +347,7 @@ dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, con
                      &launches);
     if (st == DSA_OK)
         st = run_attn(dims, q, kv_cache, block_table, seq_lens, nullptr, idx_buf, T, sm_scale, out, lse, ws, s,
-                      &launches);
+                      &launches, true);
     g_last_launches = launches;
     return st;
 }

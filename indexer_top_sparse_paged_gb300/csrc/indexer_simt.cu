@@ -94,6 +94,8 @@ __global__ void __launch_bounds__(kSimtThreads) indexer_simt_kernel(IndexerArgs 
     const int units_per_row = d_I / per;
     constexpr size_t key_bytes = 16 / per;
 
+    griddep_launch_dependents();
+    griddep_wait();  // the work plan (tile prefix) is written
     SegmentIter it;
     it.init(a.tile_prefix, a.T, blockIdx.x, a.G);
     Segment seg;
@@ -162,12 +164,10 @@ static size_t simt_smem_bytes(const IndexerArgs& a) {
 template <typename KT, typename QT>
 static bool launch_typed(const IndexerArgs& a, cudaStream_t s, int* launches) {
     const size_t smem = simt_smem_bytes(a);
-    if (cudaFuncSetAttribute(indexer_simt_kernel<KT, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return false;
-    indexer_simt_kernel<KT, QT><<<a.G, kSimtThreads, smem, s>>>(a);
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(indexer_simt_kernel<KT, QT>), smem)) return false;
+    if (!launch_kernel(true, indexer_simt_kernel<KT, QT>, dim3(a.G), dim3(kSimtThreads), smem, s, a)) return false;
     ++*launches;
-    return cudaGetLastError() == cudaSuccess;
+    return true;
 }
 
 bool launch_indexer_simt(const IndexerArgs& a, cudaStream_t s, int* launches) {

@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int* abort_flag = &S.abort_flag;
+    griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -93,9 +94,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    block_sync();
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
+    griddep_wait();  // the work plan (tile prefix) is written
 
     SegmentIter it;
     it.init(a.tile_prefix, a.T, blockIdx.x, a.G);
@@ -200,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(smem_u32(&S.mma_done));
             mbar_wait_drain(smem_u32(&S.mma_done), 0, a.err);
         }
+        __syncwarp();  // the whole warp reaches the final CTA barrier together
     } else {
         // ------------------------------------------------------------- epilogue + Top-K
         const uint32_t quarter = warp & 3;             // TMEM lane quarter of this warp
@@ -255,8 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     tc_fence_before();
-    __syncthreads();
+    block_sync();
     if (warp == 1) {
+        __syncwarp();  // the issuing lane rejoins its warp: dealloc is a whole-warp (aligned) instruction
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -273,12 +277,11 @@ bool launch_indexer_tc(const IndexerArgs& a, cudaStream_t s, int* launches) {
                       static_cast<uint64_t>(a.num_blocks) * kBlock, tcidx::kDim * 2, 64, 64))
         return false;
     const size_t smem = tcidx::smem_bytes(a.K);
-    if (cudaFuncSetAttribute(tcidx::indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(tcidx::indexer_tc_kernel), smem)) return false;
+    if (!launch_kernel(true, tcidx::indexer_tc_kernel, dim3(a.G), dim3(tcidx::kThreads), smem, s, a, map_q, map_k))
         return false;
-    tcidx::indexer_tc_kernel<<<a.G, tcidx::kThreads, smem, s>>>(a, map_q, map_k);
     ++*launches;
-    return cudaGetLastError() == cudaSuccess;
+    return true;
 }
 
 size_t indexer_tc_smem(int K) { return tcidx::smem_bytes(K); }

@@ -43,6 +43,29 @@ bool attn_uses_tc(const dsa_dims& d);
 bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t cols, uint64_t rows,
                   uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows);
 
+// Raises a kernel's dynamic shared memory limit once per device (cached).
+bool set_max_dynamic_smem(const void* func, size_t bytes);
+
+// Launches `kernel`; with `pdl` the launch may overlap the tail of the previous kernel on the
+// stream (programmatic dependent launch), so the kernel must call griddep_wait() before it reads
+// anything that kernel writes. Only kernels that follow another kernel of the same call use it:
+// the first kernel of a call always waits for all earlier work on the stream.
+template <typename... KArgs, typename... Args>
+inline bool launch_kernel(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess;
+}
+
 // ---- launchers (return false if a launch failed; each adds its launches to *launches) ----------
 
 bool launch_plan(const IndexerArgs& a, cudaStream_t s, int* launches);
@@ -68,6 +91,7 @@ struct AttnArgs {
     float* part_ml;
     int S;
     int* err;
+    int after_own_kernel;  // 1: launched right after this library's kernel (dsa_decode) -> PDL
 };
 
 bool launch_attn_simt(const AttnArgs& a, cudaStream_t s, int* launches);

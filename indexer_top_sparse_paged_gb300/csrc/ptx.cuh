@@ -18,8 +18,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Barriers here count threads, not warps: the non-.aligned forms, since the lanes of a warp may
+// reach them apart (a lane that did extra work, e.g. the one issuing MMAs, arrives later). The
+// block-wide one reconverges the warp first, because __syncthreads is the warp-aligned form.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void block_sync() {
+    __syncwarp();
+    __syncthreads();
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
@@ -30,13 +38,19 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, boo
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "barrier.red.or.pred q, %2, %3, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n}"
         : "=r"(r)
         : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
         : "memory");
     return r != 0;
 }
+
+// Programmatic dependent launch: allow the next kernel of the stream to start launching (its blocks
+// run their prologue while this grid finishes) / wait until the previous kernel of the stream has
+// completed and its memory writes are visible. Both are no-ops for kernels launched without it.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // A bounded wait gives up after this many SM clock cycles (~1 s at 2 GHz), records
 // DSA_FAULT_TIMEOUT in the workspace error word and lets the kernel wind down.
@@ -131,6 +145,7 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 
 // All threads of every CTA of the cluster: release own prior writes, then acquire the others'.
 __device__ __forceinline__ void cluster_sync_all() {
+    __syncwarp();  // the .aligned cluster barrier needs the whole warp converged
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 

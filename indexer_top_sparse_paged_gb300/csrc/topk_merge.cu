@@ -16,14 +16,16 @@ constexpr int kPlanThreads = 1024;
 constexpr int kMergeThreads = 1024;
 constexpr int kMergeSmemKeys = 16384;  // candidates held in registers (16 per thread)
 constexpr int kMergeHistBytes = kMergeThreads / 32 * 256 * 4;  // one 256-bin histogram per warp
+constexpr int kMergeSmemBytes = kMergeHistBytes + kMergeSmemKeys * 8;  // + the row's candidates
 constexpr int kMaxSpans = kMaxIndexerCtas + 1;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(IndexerArgs a) {
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t carry;
+    griddep_launch_dependents();  // the indexer may start its prologue
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) carry = 0;
-    __syncthreads();
+    block_sync();
     for (int base = 0; base < a.T; base += kPlanThreads) {
         const int t = base + tid;
         const int n = (t < a.T) ? row_len(a, t) : 0;
@@ -35,7 +37,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(IndexerArgs a) {
             if (lane >= o) x += v;
         }
         if (lane == 31) warp_sums[warp] = x;
-        __syncthreads();
+        block_sync();
         if (warp == 0) {
             int y = warp_sums[lane];
 #pragma unroll
@@ -45,18 +47,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(IndexerArgs a) {
             }
             warp_sums[lane] = y;  // inclusive over warps
         }
-        __syncthreads();
+        block_sync();
         const int excl = carry + (warp ? warp_sums[warp - 1] : 0) + x - tiles;
         if (t < a.T) a.tile_prefix[t] = excl;
-        __syncthreads();
+        block_sync();
         if (tid == kPlanThreads - 1) carry = excl + tiles;
-        __syncthreads();
+        block_sync();
     }
     if (tid == 0) a.tile_prefix[a.T] = carry;
 }
 
 constexpr int kPer = kMergeSmemKeys / kMergeThreads;  // candidates per thread held in registers
-
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a) {
     extern __shared__ __align__(16) uint8_t merge_smem[];
     uint32_t* hist = reinterpret_cast<uint32_t*>(merge_smem);  // [32 warps][256]
@@ -67,6 +68,8 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a
     __shared__ int n_spans;
     __shared__ uint32_t n_total;
 
+    griddep_launch_dependents();
+    griddep_wait();  // the indexer's candidate lists are complete
     const int t = blockIdx.x;
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
     const uint32_t K = static_cast<uint32_t>(a.K);
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a
             n_total = n;
         }
     }
-    __syncthreads();
+    block_sync();
     const int ns = n_spans;
     const uint32_t n = n_total;
 
@@ -130,7 +133,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a
         // from global memory, then emit them list by list.
         __shared__ uint32_t span_cnt[kMaxSpans];
         for (int q = tid; q < ns; q += kMergeThreads) span_cnt[q] = span_off[q + 1] - span_off[q];
-        __syncthreads();
+        block_sync();
         const uint64_t thr = radix_threshold<kMergeThreads>(span_ptr, span_cnt, ns, K, hist, &ctl, tid, 1);
         uint32_t out_n = 0;
         for (int q = 0; q < ns; ++q) {
@@ -149,31 +152,20 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a
         return;
     }
 
-    // 2. load: thread tid owns the contiguous candidates [c0, c1) of the concatenated lists
+    // 2. load: the lists are copied into shared memory in order (coalesced, every load in flight
+    //    at once), then thread tid takes the contiguous candidates [c0, c1) into registers
+    uint64_t* cand = reinterpret_cast<uint64_t*>(merge_smem + kMergeHistBytes);
+    for (int q = 0; q < ns; ++q) {
+        const uint64_t* sp = span_ptr[q];
+        const uint32_t o = span_off[q], m = span_off[q + 1] - o;
+        for (uint32_t i = tid; i < m; i += kMergeThreads) cand[o + i] = __ldcg(sp + i);
+    }
+    block_sync();
     const uint32_t c0 = min(n, tid * per), c1 = min(n, c0 + per);
     const uint32_t cnt = c1 - c0;
     uint64_t keys[kPer];
-    {
-        int sp = 0;
-        if (cnt) {
-            int lo = 0, hi = ns - 1;  // last list starting at or before c0
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (span_off[mid] <= c0) lo = mid;
-                else hi = mid - 1;
-            }
-            sp = lo;
-        }
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const uint32_t g = c0 + j;
-            keys[j] = 0ull;
-            if (static_cast<uint32_t>(j) < cnt) {
-                while (g >= span_off[sp + 1]) ++sp;
-                keys[j] = span_ptr[sp][g - span_off[sp]];
-            }
-        }
-    }
+    for (int j = 0; j < kPer; ++j) keys[j] = (static_cast<uint32_t>(j) < cnt) ? cand[c0 + j] : 0ull;
 
     // 3. threshold: exactly K keys are >= thr (thr = 0 keeps every candidate when n <= K)
     uint64_t thr = 0ull;
@@ -203,13 +195,11 @@ bool launch_plan(const IndexerArgs& a, cudaStream_t s, int* launches) {
 
 bool launch_merge(const IndexerArgs& a, cudaStream_t s, int* launches) {
     if (a.T == 0) return true;
-    const size_t smem = kMergeHistBytes;
-    if (cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return false;
-    topk_merge_kernel<<<a.T, kMergeThreads, smem, s>>>(a);
+    const size_t smem = kMergeSmemBytes;
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(topk_merge_kernel), smem)) return false;
+    if (!launch_kernel(true, topk_merge_kernel, dim3(a.T), dim3(kMergeThreads), smem, s, a)) return false;
     ++*launches;
-    return cudaGetLastError() == cudaSuccess;
+    return true;
 }
 
 }  // namespace dsa
