@@ -103,6 +103,25 @@ def profiled_traffic():
 
 
 # ------------------------------------------------------------------------------------------------
+# multi-rank aggregation (N independent replicas, one GPU each; no collective on the data path)
+# ------------------------------------------------------------------------------------------------
+
+def reduce_across_ranks(values, op: str, world: int, device):
+    """Element-wise max or sum of `values` over the ranks (every rank calls it; world 1: unchanged)."""
+    if world == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    red = torch.distributed.ReduceOp.MAX if op == "max" else torch.distributed.ReduceOp.SUM
+    torch.distributed.all_reduce(t, op=red)
+    return [float(v) for v in t]
+
+
+def job_throughput(total_bytes: float, slowest_ms: float) -> float:
+    """Whole-job GB/s: the bytes every rank processed over the slowest rank's time."""
+    return total_bytes / (slowest_ms * 1e-3) / 1e9
+
+
+# ------------------------------------------------------------------------------------------------
 # clock sampling during the timed region
 # ------------------------------------------------------------------------------------------------
 
@@ -266,18 +285,13 @@ def run_ours(args, rank, world):
     if dsa.read_error(ws) != 0:
         raise RuntimeError("device fault bits set during the timed region")
 
-    total_ms = sum(step_ms)
-    e2e_total = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_total], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, e2e_total = float(t[0]), float(t[1])
-
     ib, ab = indexer_bytes(case), attn_bytes(case)
     step_bytes = ib + ab
+    total_ms, e2e_total = reduce_across_ranks([sum(step_ms), sum(e2e_ms)], "max", world, dev)
+    (job_bytes,) = reduce_across_ranks([step_bytes * args.steps], "sum", world, dev)
     ms_per_step = total_ms / args.steps
-    value = step_bytes * world * args.steps / (total_ms * 1e-3) / 1e9
-    e2e_value = step_bytes * world * args.steps / (e2e_total * 1e-3) / 1e9
+    value = job_throughput(job_bytes, total_ms)
+    e2e_value = job_throughput(job_bytes, e2e_total)
     peak, peak_kind = measured_peaks()
     idx_avg = statistics.mean(idx_ms)
     achieved = ib / (idx_avg * 1e-3) / 1e9
