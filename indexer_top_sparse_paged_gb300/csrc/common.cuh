@@ -232,9 +232,11 @@ __device__ __forceinline__ uint32_t group_excl_scan(uint32_t v, uint32_t* warp_t
 
 // Collective over NT threads: radix threshold (as radix_threshold) over keys held in registers,
 // keys[j] valid for j < cnt; thread 0 must hold at least one key. hist: NT/32 x 256 words.
+// With max_passes, the select stops early and returns a threshold that keeps the whole boundary
+// bucket: at least K keys (fewer passes, a few keys more than K).
 template <int NT, int PER>
 __device__ uint64_t reg_radix_threshold(const uint64_t (&keys)[PER], uint32_t cnt, uint32_t K, uint32_t* hist,
-                                        TopkCtl* ctl, uint32_t tid, uint32_t bar_id) {
+                                        TopkCtl* ctl, uint32_t tid, uint32_t bar_id, int max_passes = 64) {
     constexpr uint32_t NW = NT / 32;
     const uint32_t lane = tid & 31u, warp = tid >> 5;
     uint32_t* my_hist = hist + warp * 256;
@@ -306,7 +308,7 @@ __device__ uint64_t reg_radix_threshold(const uint64_t (&keys)[PER], uint32_t cn
         prefix |= static_cast<uint64_t>(ctl->digit) << shift;
         const bool done = ctl->bucket == rem;
         named_bar_sync(bar_id, NT);
-        if (done) break;
+        if (done || --max_passes == 0) break;
     }
     return prefix;
 }
@@ -362,7 +364,7 @@ struct TopkGroup {
     // Collective: writes the min(count, K) largest keys of buf, in buffer (= position) order, to
     // dst (shared or global; may be buf itself) and returns how many. Each thread loads its
     // contiguous chunk into registers first, so writing over buf is safe.
-    __device__ uint32_t select_to(uint64_t* dst) {
+    __device__ uint32_t select_to(uint64_t* dst, int max_passes = 64) {
         sync();  // every push's writes to buf are visible
         const uint32_t n = count;
         const uint32_t per = (n + NT - 1) / NT;
@@ -372,7 +374,7 @@ struct TopkGroup {
 #pragma unroll
         for (int j = 0; j < PER; ++j) keys[j] = (static_cast<uint32_t>(j) < cnt) ? buf[c0 + j] : 0ull;
         uint64_t thr = 0ull;
-        if (n > K) thr = reg_radix_threshold<NT, PER>(keys, cnt, K, hist, ctl, tid, bar_id);
+        if (n > K) thr = reg_radix_threshold<NT, PER>(keys, cnt, K, hist, ctl, tid, bar_id, max_passes);
         uint32_t mine = 0;
 #pragma unroll
         for (int j = 0; j < PER; ++j) mine += (static_cast<uint32_t>(j) < cnt && keys[j] >= thr) ? 1u : 0u;
@@ -387,8 +389,9 @@ struct TopkGroup {
     }
 
     // Keeps the K largest keys of buf (in order) and raises the admission threshold.
+    // (mid-stream: two radix passes bound the threshold tightly enough; the flush is exact)
     __device__ void select() {
-        count = select_to(buf);
+        count = select_to(buf, 2);
         sync();
     }
 

@@ -30,13 +30,14 @@ constexpr int kQHalfBytes = kHeads * 128;     // [64 heads x 64 bf16] = 8 KB
 constexpr int kQBytes = 2 * kQHalfBytes;      // 16 KB
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr int kTmemCols = 128;
+constexpr int kAcc = 4;  // score accumulators in TMEM (64 columns each): the MMA runs ahead of a busy epilogue
+constexpr int kTmemCols = kAcc * 64;
 constexpr uint32_t kIdesc = idesc_f16(128, kHeads, 1u, 0u, 0u);
 
 struct Smem {
     uint64_t full[kStages], empty[kStages];
     uint64_t qfull, qempty;
-    uint64_t tfull[2], tempty[2];
+    uint64_t tfull[kAcc], tempty[kAcc];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_u32(&S.qfull), 1);
         mbar_init(smem_u32(&S.qempty), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kAcc; ++i) {
             mbar_init(smem_u32(&S.tfull[i]), 1);
             mbar_init(smem_u32(&S.tempty[i]), kEpiThreads / 32);  // one elected arrive per epilogue warp
         }
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
                     const uint32_t st = n_it % kStages, use = n_it / kStages;
-                    const uint32_t acc = n_it & 1u, ause = n_it >> 1;
+                    const uint32_t acc = n_it % kAcc, ause = n_it / kAcc;
                     ok = mbar_wait(smem_u32(&S.full[st]), use & 1u, abort_flag, a.err);
                     if (!ok) break;
                     ok = mbar_wait(smem_u32(&S.tempty[acc]), (ause & 1u) ^ 1u, abort_flag, a.err);
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             const int32_t* bt = a.block_table + static_cast<int64_t>(row_seq(a, t)) * a.max_blocks;
             for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
-                const uint32_t acc = n_it & 1u, ause = n_it >> 1;
+                const uint32_t acc = n_it % kAcc, ause = n_it / kAcc;
                 const int s = j * kTileKeys + static_cast<int>(row);
                 const int blk = (s < n) ? bt[s >> 6] : -1;  // issued before the wait: latency hidden
                 const bool got = mbar_wait(smem_u32(&S.tfull[acc]), ause & 1u, abort_flag, a.err);
