@@ -49,7 +49,8 @@ constexpr int kStageBytes = kMaxChunks * kChunkBytes;
 constexpr int kXBytes = kHeads * kRows * 2;   // one partial-logit tile (fp16, prescaled by 2^-8)
 constexpr float kXScale = 1.0f / 256.0f;      // partial logits travel as fp16(S_r * 2^-8)
 constexpr int kMaxRows = 2048;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
+constexpr int kWarpSoftB = 10;  // second softmax group: warps 10..13
 constexpr int kProducers = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // S/P buffers at 256 and 320; Q chunks 32 apart
@@ -71,7 +72,8 @@ constexpr size_t kOffKv = kOffQ + kQChunkBytes;
 constexpr size_t kOffX = kOffKv + static_cast<size_t>(kStages) * kStageBytes;  // received partials
 constexpr size_t kOffValid = kOffX + 2 * kXBytes;                                // 1 bit per selected row
 constexpr size_t kOffPhys = kOffValid + kMaxRows / 8;                             // physical row per selected row
-constexpr size_t kOffCtl = kOffPhys + kMaxRows * sizeof(int32_t);
+constexpr size_t kOffRed = kOffPhys + kMaxRows * sizeof(int32_t);  // softmax maxima / row sums
+constexpr size_t kOffCtl = kOffRed + 4 * kHeads * sizeof(float);
 constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(Smem);
 static_assert(kSmemBytes <= 232448, "attention shared memory over the limit");
 
@@ -129,10 +131,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&S.s_full[i]), 1);
-            mbar_init(smem_u32(&S.p_full[i]), 4);  // one elected arrive per softmax warp
+            mbar_init(smem_u32(&S.p_full[i]), 8);  // one elected arrive per softmax warp
             mbar_init(smem_u32(&S.s_free[i]), 1);
             mbar_init(smem_u32(&S.xfull[i]), 1);   // arrive.expect_tx here + the peer's st.async bytes
-            mbar_init(smem_u32(&S.xempty[i]), 4);  // the peer's four softmax warps
+            mbar_init(smem_u32(&S.xempty[i]), 8);  // the peer's eight softmax warps
             mbar_init(smem_u32(&S.s_sent[i]), 4);  // this CTA's four producer warps
         }
         mbar_init(smem_u32(&S.qfull), 1);
@@ -357,59 +359,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             tc_commit(smem_u32(&S.mma_done));
             mbar_wait_drain(smem_u32(&S.mma_done), 0, a.err);
         }
-    } else if (warp < 4) {
+    } else if (warp < 4 || warp >= kWarpSoftB) {
         // ------------------------------------------------------------- softmax + epilogue
-        const int h = threadIdx.x;  // head = TMEM lane
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        // Two warps per TMEM lane quarter: group 0 (warps 0-3) takes rows 0..31 of every tile and
+        // O columns 0..127 of the CTA, group 1 (warps 10-13) rows 32..63 and O columns 128..255.
+        // The two threads of a head agree on the running maximum through shared memory, so both
+        // scale by the same reference; each keeps its own part of the row sum l.
+        const int grp = warp < 4 ? 0 : 1;
+        const int quarter = warp & 3;                 // TMEM lanes this warp can access
+        const int h = quarter * 32 + lane;            // head = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const float scale2 = a.sm_scale * 1.4426950408889634f / kXScale;  // exchanged units -> log2 units
         const uint32_t peer_xempty = mapa_shared(smem_u32(&S.xempty[0]), peer);  // [1] at +8
+        float* red = reinterpret_cast<float*>(smem + kOffRed);  // [2 tiles][2 groups][128 heads]
         float m_ref = -INFINITY, l = 0.0f;
         bool dead = false;
         for (int i = 0; i < ntiles; ++i) {
             const int sb = i & 1;
-            const bool got = mbar_wait(smem_u32(&S.s_full[sb]), (i >> 1) & 1, abort_flag, a.err) &&
-                             mbar_wait_cluster(smem_u32(&S.xfull[sb]), (i >> 1) & 1, abort_flag, a.err);
-            if (__any_sync(0xFFFFFFFFu, !got)) {
+            const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&S.s_full[sb]), (i >> 1) & 1, abort_flag, a.err) &&
+                                                         mbar_wait_cluster(smem_u32(&S.xfull[sb]), (i >> 1) & 1, abort_flag, a.err));
+            float z[32];
+            float mloc = -INFINITY;
+            if (got) {
+                tc_fence_after();
+                // this CTA's partial, rounded exactly as the producers sent it, plus the peer's;
+                // both in units of 2^8 (the scale is folded into scale2)
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kColS + sb * kRows + grp * 32, v);
+                tmem_ld_wait();
+                const uint8_t* theirs = smem + kOffX + sb * kXBytes;
+                const uint32_t vm = valid_bits[2 * i + grp];  // rows without a position take no weight
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(theirs + xoff(h, 4 * grp + g));
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int r = 8 * g + 2 * q;  // rows grp*32 + r, + 1
+                        const float2 a2 = __half22float2(
+                            __floats2half2_rn(__uint_as_float(v[r]) * kXScale, __uint_as_float(v[r + 1]) * kXScale));
+                        const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&ws[q]));
+                        z[r] = ((vm >> r) & 1u) ? a2.x + b2.x : -INFINITY;
+                        z[r + 1] = ((vm >> (r + 1)) & 1u) ? a2.y + b2.y : -INFINITY;
+                    }
+                }
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], z[j]);
+                mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            }
+            red[(sb * 2 + grp) * kHeads + h] = mloc;
+            if (named_bar_or(3, 256, dead || !got)) {  // also publishes red (double-buffered by tile)
                 dead = true;
                 break;
             }
-            tc_fence_after();
-            // this CTA's partial, rounded exactly as the producers sent it, plus the peer's; both
-            // in units of 2^8 (the scale is folded into scale2)
-            uint32_t v0[32], v1[32];
-            tmem_ld32(tmem + lane_base + kColS + sb * kRows, v0);
-            tmem_ld32(tmem + lane_base + kColS + sb * kRows + 32, v1);
-            tmem_ld_wait();
-            float z[kRows];
-            const uint8_t* theirs = smem + kOffX + sb * kXBytes;
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                const uint4 w = *reinterpret_cast<const uint4*>(theirs + xoff(h, g));
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int r = 8 * g + 2 * q;  // rows r, r + 1
-                    const float o0 = __uint_as_float(r < 32 ? v0[r] : v1[r - 32]);
-                    const float o1 = __uint_as_float(r < 32 ? v0[r + 1] : v1[r - 31]);
-                    const float2 a2 = __half22float2(__floats2half2_rn(o0 * kXScale, o1 * kXScale));
-                    const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&ws[q]));
-                    z[r] = a2.x + b2.x;
-                    z[r + 1] = a2.y + b2.y;
-                }
-            }
-            // rows without a position (past the split's end, idx -1, bad entries) take no weight
-            const uint32_t vm0 = valid_bits[2 * i], vm1 = valid_bits[2 * i + 1];
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int j = 0; j < kRows; ++j) {
-                const uint32_t vm = j < 32 ? vm0 : vm1;
-                z[j] = ((vm >> (j & 31)) & 1u) ? z[j] : -INFINITY;
-                mx[j & 3] = fmaxf(mx[j & 3], z[j]);
-            }
             // scale2 > 0 and rounding is monotone, so max(z) * scale2 is the max of the scaled logits
-            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale2;
+            const float mt = fmaxf(red[(sb * 2) * kHeads + h], red[(sb * 2 + 1) * kHeads + h]) * scale2;
             const bool need = mt > m_ref + 8.0f;
-            if (__any_sync(0xFFFFFFFFu, need)) {
+            if (__any_sync(0xFFFFFFFFu, need)) {  // the partner warp sees the same heads: same decision
                 const float m_new = need ? mt : m_ref;
                 if (i > 0) {
                     const bool freed = mbar_wait(smem_u32(&S.s_free[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort_flag, a.err);
@@ -418,13 +425,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                         tc_fence_after();
                         const float alpha = (m_new == m_ref) ? 1.0f : exp2f(m_ref - m_new);
 #pragma unroll 1
-                        for (int cc = 0; cc < kDVH / 32; ++cc) {
+                        for (int cc = 0; cc < kDVH / 64; ++cc) {  // this group's half of O
+                            const uint32_t col = kColO + grp * (kDVH / 2) + cc * 32;
                             uint32_t v[32];
-                            tmem_ld32(tmem + lane_base + kColO + cc * 32, v);
+                            tmem_ld32(tmem + lane_base + col, v);
                             tmem_ld_wait();
 #pragma unroll
                             for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                            tmem_st32(tmem + lane_base + kColO + cc * 32, v);
+                            tmem_st32(tmem + lane_base + col, v);
                         }
                         tmem_st_wait();
                         l *= alpha;
@@ -434,11 +442,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             }
             // p = 2^(z * scale2 - m_ref), rounded to bf16 in pairs; l sums the rounded values that
             // the P.V product uses (masked rows: 2^-inf = 0)
-            uint32_t packed[kRows / 2];
+            uint32_t packed[16];
             float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;  // no valid row yet: all p = 0
 #pragma unroll
-            for (int j = 0; j < kRows; j += 2) {
+            for (int j = 0; j < 32; j += 2) {
                 const float p0 = ex2_approx(fmaf(z[j], scale2, neg_m));
                 const float p1 = ex2_approx(fmaf(z[j + 1], scale2, neg_m));
                 const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);  // .x (low half) = p0
@@ -447,11 +455,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                 ls[(j >> 1) & 3] += __uint_as_float(u << 16) + __uint_as_float(u & 0xFFFF0000u);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            // P (bf16) over the first 32 columns of this tile's S, once the producers have read S
+            // P (bf16 pairs) over S columns grp*16 .. +16, once the producers have read S
             const bool read_ok = mbar_wait(smem_u32(&S.s_sent[sb]), (i >> 1) & 1, abort_flag, a.err);
             if (__any_sync(0xFFFFFFFFu, !read_ok)) dead = true;
             if (!dead) {
-                tmem_st32(tmem + lane_base + kColS + sb * kRows, packed);
+                tmem_st16(tmem + lane_base + kColS + sb * kRows + grp * 16, packed);
                 tmem_st_wait();
                 tc_fence_before();
             }
@@ -466,20 +474,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         }
         if (ntiles > 0) {  // every softmax thread takes this barrier, dead or not
             const bool got = dead ? false : mbar_wait(smem_u32(&S.o_full), 0, abort_flag, a.err);
-            dead = named_bar_or(2, 128, dead || !got);
+            dead = named_bar_or(3, 256, dead || !got);
         }
+        // the full row sum: both groups' parts
+        red[grp * kHeads + h] = l;
+        named_bar_sync(3, 256);
+        l = red[h] + red[kHeads + h];
         const bool have_o = ntiles > 0 && !dead;
         if (have_o) tc_fence_after();
         // O rows leave through a per-warp 32 x 32 transpose in the (now idle) row stages, so that
         // every store of a warp covers whole 128-byte runs of head rows
-        float* tile = reinterpret_cast<float*>(smem + kOffKv) + warp * (32 * 33);
-        const int h0 = warp * 32;
+        float* tile = reinterpret_cast<float*>(smem + kOffKv) + (grp * 4 + quarter) * (32 * 33);
+        const int h0 = quarter * 32;
         const bool zero = !(have_o && l > 0.0f);  // the row is written as zeros
-        const int col0 = rank * kDVH;
-        auto stage_chunk = [&](int cc) {  // O[h0 + lane][cc*32 .. +32) -> tile[lane][.]
+        const int col0 = rank * kDVH + grp * (kDVH / 2);
+        auto stage_chunk = [&](int cc) {  // O[h0 + lane][col0 + cc*32 .. +32) -> tile[lane][.]
             uint32_t v[32];
             if (have_o) {
-                tmem_ld32(tmem + lane_base + kColO + cc * 32, v);
+                tmem_ld32(tmem + lane_base + kColO + grp * (kDVH / 2) + cc * 32, v);
                 tmem_ld_wait();
             }
             __syncwarp();
@@ -494,7 +506,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
 #pragma unroll
             for (int j = 0; j < 8; ++j) invk[j] = __shfl_sync(0xFFFFFFFFu, inv, (lane >> 3) + 4 * j);
 #pragma unroll 1
-            for (int cc = 0; cc < kDVH / 32; ++cc) {
+            for (int cc = 0; cc < kDVH / 64; ++cc) {
                 stage_chunk(cc);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -508,13 +520,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                         make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
                 }
             }
-            if (rank == 0 && a.lse)
+            if (rank == 0 && grp == 0 && a.lse)
                 a.lse[static_cast<int64_t>(t) * kHeads + h] =
                     (l > 0.0f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
         } else {
             // split-K: this CTA's partial (O half, m, l) to the workspace; attn_combine_kernel merges
 #pragma unroll 1
-            for (int cc = 0; cc < kDVH / 32; ++cc) {
+            for (int cc = 0; cc < kDVH / 64; ++cc) {
                 stage_chunk(cc);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -525,9 +537,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                     *reinterpret_cast<float4*>(po) = make_float4(tr[0], tr[1], tr[2], tr[3]);
                 }
             }
-            const int64_t mlrow = ((static_cast<int64_t>(t) * a.S + split) * 2 + rank) * kHeads + h;
-            a.part_ml[mlrow * 2] = (l > 0.0f && !zero) ? m_ref : -INFINITY;
-            a.part_ml[mlrow * 2 + 1] = zero ? 0.0f : l;
+            if (grp == 0) {
+                const int64_t mlrow = ((static_cast<int64_t>(t) * a.S + split) * 2 + rank) * kHeads + h;
+                a.part_ml[mlrow * 2] = (l > 0.0f && !zero) ? m_ref : -INFINITY;
+                a.part_ml[mlrow * 2 + 1] = zero ? 0.0f : l;
+            }
         }
     }
 
