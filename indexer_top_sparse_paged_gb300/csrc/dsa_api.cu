@@ -50,7 +50,9 @@ bool set_max_dynamic_smem(const void* func, size_t bytes) {
     return true;
 }
 
-bool indexer_uses_tc(const dsa_dims& d) { return d.mode == DSA_BF16 && d.H_I == 64 && d.d_I == 128; }
+bool indexer_uses_tc(const dsa_dims& d) {
+    return (d.mode == DSA_BF16 || d.mode == DSA_BF16_KFP8) && d.H_I == 64 && d.d_I == 128;
+}
 
 bool attn_uses_tc(const dsa_dims& d) {
     return (d.mode == DSA_BF16 || d.mode == DSA_BF16_KFP8) && d.H == 128 && d.d == 576 && d.d_v == 512;

@@ -1,5 +1,5 @@
 // Decode indexer + streaming Top-K on the 5th-generation tensor cores (tcgen05), for 64 indexer
-// heads of width 128 with bf16 keys.
+// heads of width 128 with bf16 keys, or FP8 e4m3 keys with one fp32 scale per 64-token block.
 //
 // Per 128-key tile (two 64-token cache blocks fetched by TMA through the block table) the tile
 // is one M=128 x N=64 x K=128 contraction: A = the tile's keys (one key per row, K-major, 128-byte
@@ -14,8 +14,19 @@
 //
 // Roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
 // warps 2..5 = epilogue (TMEM lane quarter = warp % 4). Pipelines: 5 smem stages of 32 KB (the
-// HBM round trip under full load is ~3.7 us: 160 KB in flight per SM keeps it busy), 2 TMEM
+// HBM round trip under full load is ~3.7 us: 160 KB in flight per SM keeps it busy), 4 TMEM
 // accumulators of 64 columns, one query buffer.
+//
+// FP8 keys (320 threads): the TMA lands the e4m3 codes of a tile (16 KB) in a staging ring of 6
+// stages, and four more warps (6..9, one key row per thread) widen them to bf16 in the swizzled
+// operand layout of a 2-stage ring that the MMA reads. Every e4m3 value is exactly a bf16 value,
+// so the product is still exact-input bf16 x bf16 -> fp32; the block's scale multiplies the
+// accumulator in the epilogue, before the ReLU:
+//     S[s] = sum_j w_j * max(0, scale_blk * D[s, j]).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "internal.h"
 
 namespace dsa {
@@ -23,19 +34,33 @@ namespace tcidx {
 
 constexpr int kHeads = 64;
 constexpr int kDim = 128;
-constexpr int kStages = 5;
 constexpr int kHalfBytes = kTileKeys * 128;   // [128 keys x 64 bf16] = 16 KB
 constexpr int kStageBytes = 2 * kHalfBytes;   // both K halves = 32 KB
 constexpr int kQHalfBytes = kHeads * 128;     // [64 heads x 64 bf16] = 8 KB
 constexpr int kQBytes = 2 * kQHalfBytes;      // 16 KB
-constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kAcc = 4;  // score accumulators in TMEM (64 columns each): the MMA runs ahead of a busy epilogue
 constexpr int kTmemCols = kAcc * 64;
 constexpr uint32_t kIdesc = idesc_f16(128, kHeads, 1u, 0u, 0u);
+constexpr int kF8TileBytes = kTileKeys * kDim;  // e4m3 codes of one tile: 16 KB
+constexpr int kF8BlockBytes = kBlock * kDim;    // one 64-token block: 8 KB
 
+// Shape of the pipelines per key storage.
+template <bool kFp8>
+struct Cfg {
+    static constexpr int kThreads = kFp8 ? 320 : 192;  // + 4 converter warps for FP8 keys
+    static constexpr int kStages = kFp8 ? 2 : 5;       // bf16 operand stages (32 KB) the MMA reads
+    static constexpr int kStages8 = kFp8 ? 6 : 1;      // e4m3 staging stages (16 KB) the TMA fills
+    static constexpr size_t kOffA = 0;
+    static constexpr size_t kOffQ = kOffA + static_cast<size_t>(kStages) * kStageBytes;
+    static constexpr size_t kOffF8 = kOffQ + kQBytes;
+    static constexpr size_t kOffBuf = kOffF8 + (kFp8 ? static_cast<size_t>(kStages8) * kF8TileBytes : 0);
+};
+
+template <bool kFp8>
 struct Smem {
-    uint64_t full[kStages], empty[kStages];
+    uint64_t full[Cfg<kFp8>::kStages], empty[Cfg<kFp8>::kStages];
+    uint64_t full8[Cfg<kFp8>::kStages8], empty8[Cfg<kFp8>::kStages8];
     uint64_t qfull, qempty;
     uint64_t tfull[kAcc], tempty[kAcc];
     uint64_t mma_done;
@@ -45,28 +70,53 @@ struct Smem {
     TopkCtl ctl;
 };
 
-constexpr size_t kOffA = 0;
-constexpr size_t kOffQ = kOffA + static_cast<size_t>(kStages) * kStageBytes;
-constexpr size_t kOffBuf = kOffQ + kQBytes;
-
 constexpr int kTopkPer = 33;  // candidate keys per epilogue thread held in registers while selecting
 constexpr size_t kSmemLimit = 232448;
 __host__ __device__ constexpr uint32_t topk_cap(int K) { return static_cast<uint32_t>(2 * K + kEpiThreads); }
 
+template <bool kFp8>
 __host__ __device__ constexpr size_t smem_bytes(int K) {
-    return 1024 /*alignment slack*/ + kOffBuf + static_cast<size_t>(topk_cap(K)) * 8 + sizeof(Smem) + 64;
+    return 1024 /*alignment slack*/ + Cfg<kFp8>::kOffBuf + static_cast<size_t>(topk_cap(K)) * 8 + sizeof(Smem<kFp8>) +
+           64;
 }
 static_assert(topk_cap(2048) <= static_cast<uint32_t>(kEpiThreads * kTopkPer), "candidate buffer exceeds registers");
-static_assert(smem_bytes(2048) <= kSmemLimit, "indexer shared memory over the limit");
+static_assert(smem_bytes<false>(2048) <= kSmemLimit, "indexer shared memory over the limit");
+static_assert(smem_bytes<true>(2048) <= kSmemLimit, "FP8 indexer shared memory over the limit");
 
-__global__ void __launch_bounds__(kThreads, 1)
+// 16 e4m3 codes -> 16 bf16 (two 16-byte groups), exactly: e4m3 -> f16 is exact (every e4m3 value,
+// subnormals included, is an f16 normal or zero), and so is f16 -> fp32 -> bf16 for values with
+// at most 4 significant bits inside bf16's exponent range.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+            const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * hlf)) & 0xFFFFu);
+            const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+            const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);  // .x = the lower code
+            o[2 * i + hlf] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     indexer_tc_kernel(IndexerArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
+    using C = Cfg<kFp8>;
+    constexpr int kStages = C::kStages;
+    constexpr int kStages8 = C::kStages8;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t sA = smem_u32(smem + kOffA);
-    const uint32_t sQ = smem_u32(smem + kOffQ);
-    uint64_t* buf = reinterpret_cast<uint64_t*>(smem + kOffBuf);
-    Smem& S = *reinterpret_cast<Smem*>(smem + kOffBuf + static_cast<size_t>(topk_cap(a.K)) * 8);
+    const uint32_t sA = smem_u32(smem + C::kOffA);
+    const uint32_t sQ = smem_u32(smem + C::kOffQ);
+    const uint32_t sF8 = smem_u32(smem + C::kOffF8);
+    uint64_t* buf = reinterpret_cast<uint64_t*>(smem + C::kOffBuf);
+    Smem<kFp8>& S = *reinterpret_cast<Smem<kFp8>*>(smem + C::kOffBuf + static_cast<size_t>(topk_cap(a.K)) * 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -75,8 +125,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(smem_u32(&S.full[i]), 1);
+            // FP8: filled by the four converter warps (one elected arrive each), else by the TMA
+            mbar_init(smem_u32(&S.full[i]), kFp8 ? 4 : 1);
             mbar_init(smem_u32(&S.empty[i]), 1);
+        }
+        if (kFp8) {
+            for (int i = 0; i < kStages8; ++i) {
+                mbar_init(smem_u32(&S.full8[i]), 1);
+                mbar_init(smem_u32(&S.empty8[i]), 4);  // the four converter warps
+            }
         }
         mbar_init(smem_u32(&S.qfull), 1);
         mbar_init(smem_u32(&S.qempty), 1);
@@ -138,8 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     cur = nxt;
                     nxt = load_window(w0 + 32);
                 }
-                const uint32_t st = n_it % kStages, use = n_it / kStages;
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&S.empty[st]), (use & 1u) ^ 1u, abort_flag, a.err));
+                const uint32_t st = n_it % (kFp8 ? kStages8 : kStages), use = n_it / (kFp8 ? kStages8 : kStages);
+                const uint32_t ebar = kFp8 ? smem_u32(&S.empty8[st]) : smem_u32(&S.empty[st]);
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(ebar, (use & 1u) ^ 1u, abort_flag, a.err));
                 if (!ok) break;
                 int blk[2];
                 uint32_t bytes = 0;
@@ -151,17 +209,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool good = v >= 0 && v < a.num_blocks;
                     if (inside && !good && lane == 0) atomicOr(a.err, DSA_FAULT_BLOCK_TABLE);
                     blk[p] = (inside && good) ? v : -1;
-                    if (blk[p] >= 0) bytes += 2 * (kBlock * 128);
+                    if (blk[p] >= 0) bytes += kFp8 ? kF8BlockBytes : 2 * (kBlock * 128);
                 }
                 if (lane == 0) {
-                    const uint32_t fb = smem_u32(&S.full[st]);
+                    const uint32_t fb = kFp8 ? smem_u32(&S.full8[st]) : smem_u32(&S.full[st]);
                     mbar_arrive_expect_tx(fb, bytes);
 #pragma unroll
                     for (int p = 0; p < 2; ++p) {
                         if (blk[p] < 0) continue;
-                        const uint32_t dst = sA + st * kStageBytes + p * (kBlock * 128);
-                        tma_load_2d(dst, &map_k, 0, blk[p] * kBlock, fb);
-                        tma_load_2d(dst + kHalfBytes, &map_k, 64, blk[p] * kBlock, fb);
+                        if (kFp8) {
+                            tma_load_2d(sF8 + st * kF8TileBytes + p * kF8BlockBytes, &map_k, 0, blk[p] * kBlock, fb);
+                        } else {
+                            const uint32_t dst = sA + st * kStageBytes + p * (kBlock * 128);
+                            tma_load_2d(dst, &map_k, 0, blk[p] * kBlock, fb);
+                            tma_load_2d(dst + kHalfBytes, &map_k, 64, blk[p] * kBlock, fb);
+                        }
                     }
                 }
                 __syncwarp();
@@ -204,6 +266,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_drain(smem_u32(&S.mma_done), 0, a.err);
         }
         __syncwarp();  // the whole warp reaches the final CTA barrier together
+    } else if (kFp8 && warp >= 6) {
+        // ------------------------------------------------------------- e4m3 -> bf16 converters
+        // Thread r widens key row r of the tile: 8 swizzled 16-byte groups of codes (block r / 64,
+        // row r % 64) become 16 swizzled 16-byte groups of bf16 in the two K halves of the operand
+        // stage. Rows whose block was not loaded hold stale codes; the epilogue masks their keys.
+        const int r = threadIdx.x - 192;
+        const int rr = r & 63, p = r >> 6, sw = r & 7;
+        uint32_t n_it = 0;
+        bool ok = true;
+        while (ok && it.next(seg)) {
+            for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
+                const uint32_t s8 = n_it % kStages8, u8 = n_it / kStages8;
+                const uint32_t st = n_it % kStages, use = n_it / kStages;
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&S.full8[s8]), u8 & 1u, abort_flag, a.err) &&
+                                                 mbar_wait(smem_u32(&S.empty[st]), (use & 1u) ^ 1u, abort_flag, a.err));
+                if (!ok) break;
+                const uint8_t* src = smem + C::kOffF8 + s8 * kF8TileBytes + p * kF8BlockBytes + rr * 128;
+                uint4 codes[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) codes[c] = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.empty8[s8]));  // codes are in registers
+                uint8_t* dst = smem + C::kOffA + st * kStageBytes + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    // codes 16c..16c+15 -> K half c / 4, bf16 groups 2(c % 4) and 2(c % 4) + 1
+                    uint4 lo, hi;
+                    e4m3x16_to_bf16(codes[c], lo, hi);
+                    uint8_t* row = dst + (c >> 2) * kHalfBytes;
+                    const int g = 2 * (c & 3);
+                    *reinterpret_cast<uint4*>(row + ((g ^ sw) << 4)) = lo;
+                    *reinterpret_cast<uint4*>(row + (((g + 1) ^ sw) << 4)) = hi;
+                }
+                fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.full[st]));
+            }
+        }
     } else {
         // ------------------------------------------------------------- epilogue + Top-K
         const uint32_t quarter = warp & 3;             // TMEM lane quarter of this warp
@@ -231,6 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t acc = n_it % kAcc, ause = n_it / kAcc;
                 const int s = j * kTileKeys + static_cast<int>(row);
                 const int blk = (s < n) ? bt[s >> 6] : -1;  // issued before the wait: latency hidden
+                const bool blk_ok = blk >= 0 && blk < a.num_blocks;
+                float sc = 1.0f;
+                if (kFp8) sc = blk_ok ? a.k_I_scale[blk] : 0.0f;
                 const bool got = mbar_wait(smem_u32(&S.tfull[acc]), ause & 1u, abort_flag, a.err);
                 if (named_bar_or(1, kEpiThreads, !got)) { ok = false; break; }
                 tc_fence_after();
@@ -243,12 +346,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.tempty[acc]));
                 float score = 0.0f;
+                if (!kFp8 || sc >= 0.0f) {
+                    // scale >= 0: max(0, scale * x) = scale * max(0, x), applied once to the sum
 #pragma unroll
-                for (int h = 0; h < 32; ++h) score = fmaf(wv[h], fmaxf(__uint_as_float(v0[h]), 0.0f), score);
+                    for (int h = 0; h < 32; ++h) score = fmaf(wv[h], fmaxf(__uint_as_float(v0[h]), 0.0f), score);
 #pragma unroll
-                for (int h = 0; h < 32; ++h) score = fmaf(wv[32 + h], fmaxf(__uint_as_float(v1[h]), 0.0f), score);
+                    for (int h = 0; h < 32; ++h) score = fmaf(wv[32 + h], fmaxf(__uint_as_float(v1[h]), 0.0f), score);
+                } else {
+                    // scale < 0: max(0, scale * x) = scale * min(0, x)
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) score = fmaf(wv[h], fminf(__uint_as_float(v0[h]), 0.0f), score);
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) score = fmaf(wv[32 + h], fminf(__uint_as_float(v1[h]), 0.0f), score);
+                }
+                if (kFp8) score *= sc;
                 // a block whose table entry is invalid was never loaded: its keys do not count
-                const bool valid = s < n && blk >= 0 && blk < a.num_blocks;
+                const bool valid = s < n && blk_ok;
                 topk.push(make_key(score, static_cast<uint32_t>(s)), valid);
             }
             if (!ok) break;
@@ -267,24 +380,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-}  // namespace tcidx
-
-bool launch_indexer_tc(const IndexerArgs& a, cudaStream_t s, int* launches) {
+template <bool kFp8>
+static bool launch(const IndexerArgs& a, cudaStream_t s, int* launches) {
     CUtensorMap map_q, map_k;
-    if (!make_tmap_2d(&map_q, a.q_I, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcidx::kDim,
-                      static_cast<uint64_t>(a.T) * tcidx::kHeads, tcidx::kDim * 2, 64, 64))
+    if (!make_tmap_2d(&map_q, a.q_I, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kDim, static_cast<uint64_t>(a.T) * kHeads,
+                      kDim * 2, 64, 64))
         return false;
-    if (!make_tmap_2d(&map_k, a.k_I, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcidx::kDim,
-                      static_cast<uint64_t>(a.num_blocks) * kBlock, tcidx::kDim * 2, 64, 64))
-        return false;
-    const size_t smem = tcidx::smem_bytes(a.K);
-    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(tcidx::indexer_tc_kernel), smem)) return false;
-    if (!launch_kernel(true, tcidx::indexer_tc_kernel, dim3(a.G), dim3(tcidx::kThreads), smem, s, a, map_q, map_k))
+    if (kFp8) {
+        if (!make_tmap_2d(&map_k, a.k_I, CU_TENSOR_MAP_DATA_TYPE_UINT8, kDim,
+                          static_cast<uint64_t>(a.num_blocks) * kBlock, kDim, kDim, kBlock))
+            return false;
+    } else {
+        if (!make_tmap_2d(&map_k, a.k_I, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kDim,
+                          static_cast<uint64_t>(a.num_blocks) * kBlock, kDim * 2, 64, 64))
+            return false;
+    }
+    const size_t smem = smem_bytes<kFp8>(a.K);
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(indexer_tc_kernel<kFp8>), smem)) return false;
+    if (!launch_kernel(true, indexer_tc_kernel<kFp8>, dim3(a.G), dim3(Cfg<kFp8>::kThreads), smem, s, a, map_q, map_k))
         return false;
     ++*launches;
     return true;
 }
 
-size_t indexer_tc_smem(int K) { return tcidx::smem_bytes(K); }
+}  // namespace tcidx
+
+bool launch_indexer_tc(const IndexerArgs& a, cudaStream_t s, int* launches) {
+    return a.mode == DSA_BF16_KFP8 ? tcidx::launch<true>(a, s, launches) : tcidx::launch<false>(a, s, launches);
+}
+
 
 }  // namespace dsa
