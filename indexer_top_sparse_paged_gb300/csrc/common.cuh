@@ -51,6 +51,11 @@ __host__ __device__ __forceinline__ int64_t tile_begin(int64_t c, int64_t total,
     return c * total / G;
 }
 
+// The CTA that owns global tile x (x < total): the largest c with tile_begin(c) <= x.
+__host__ __device__ __forceinline__ int64_t tile_owner(int64_t x, int64_t total, int64_t G) {
+    return ((x + 1) * G - 1) / total;
+}
+
 // First row t with tile_prefix[t] <= tile < tile_prefix[t + 1] (tile < total).
 __device__ __forceinline__ int row_of_tile(const int32_t* tile_prefix, int T, int64_t tile) {
     int lo = 0, hi = T - 1;
@@ -117,93 +122,6 @@ __device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool
     if (active) atomicAdd(&hist[bin], 1u);
 }
 
-// Collective over NT threads (named barrier bar_id): the threshold thr such that exactly K of the
-// keys in the spans are >= thr (keys are distinct; the total count must exceed K). MSB-first radix
-// select with 8-bit digits, starting below the bits all keys share, stopping as soon as the
-// boundary bucket is taken whole. `hist` holds NT/32 private 256-bin histograms (one per warp, so
-// warps never contend on a hot bin); they are summed into the first one after every pass.
-template <int NT>
-__device__ uint64_t radix_threshold(const uint64_t* const* span_ptr, const uint32_t* span_cnt, int ns, uint32_t K,
-                                    uint32_t* hist, TopkCtl* ctl, uint32_t tid, uint32_t bar_id) {
-    constexpr uint32_t NW = NT / 32;
-    const uint32_t lane = tid & 31u, warp = tid >> 5;
-    uint32_t* my_hist = hist + warp * 256;
-    // 1. bits shared by every key
-    if (tid == 0) ctl->diff = 0ull;
-    named_bar_sync(bar_id, NT);
-    const uint64_t k0 = span_ptr[0][0];
-    uint64_t d = 0;
-    for (int s = 0; s < ns; ++s) {
-        const uint64_t* sp = span_ptr[s];
-        for (uint32_t i = tid; i < span_cnt[s]; i += NT) d |= sp[i] ^ k0;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) d |= __shfl_xor_sync(0xFFFFFFFFu, d, o);
-    if (lane == 0 && d) atomicOr(&ctl->diff, static_cast<unsigned long long>(d));
-    named_bar_sync(bar_id, NT);
-    const uint64_t diff = ctl->diff;
-    const int hi = 63 - __clzll(static_cast<long long>(diff | 1ull));
-    int shift = (hi >> 3) << 3;
-    uint64_t prefix = (shift >= 56) ? 0ull : (k0 & (~0ull << (shift + 8)));
-    uint32_t rem = K;
-    // 2. radix passes
-    for (; shift >= 0; shift -= 8) {
-        for (uint32_t i = lane; i < 256; i += 32) my_hist[i] = 0;
-        __syncwarp();
-        for (int s = 0; s < ns; ++s) {
-            const uint64_t* sp = span_ptr[s];
-            const uint32_t cnt = span_cnt[s];
-            for (uint32_t base = 0; base < cnt; base += NT) {
-                const uint32_t i = base + tid;
-                const uint64_t k = (i < cnt) ? sp[i] : 0ull;
-                const bool match = (i < cnt) && ((shift == 56) || ((k >> (shift + 8)) == (prefix >> (shift + 8))));
-                hist_add_warp(my_hist, static_cast<uint32_t>(k >> shift) & 255u, match);
-            }
-        }
-        named_bar_sync(bar_id, NT);
-        for (uint32_t b = tid; b < 256; b += NT) {  // sum the private histograms into the first
-            uint32_t c = hist[b];
-#pragma unroll
-            for (uint32_t w = 1; w < NW; ++w) c += hist[w * 256 + b];
-            hist[b] = c;
-        }
-        named_bar_sync(bar_id, NT);
-        if (tid < 32) {
-            uint32_t c = 0;
-#pragma unroll
-            for (int b = 0; b < 8; ++b) c += hist[lane * 8 + b];
-            uint32_t S = c;  // inclusive suffix sum over lanes
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, S, o);
-                if (lane + o < 32) S += v;
-            }
-            const uint32_t mask = __ballot_sync(0xFFFFFFFFu, S >= rem);
-            const int L = 31 - __clz(mask);
-            if (static_cast<int>(lane) == L) {
-                uint32_t running = S - c;
-                for (int b = 7; b >= 0; --b) {
-                    const uint32_t h = hist[lane * 8 + b];
-                    if (running + h >= rem) {
-                        ctl->digit = lane * 8 + b;
-                        ctl->above = running;
-                        ctl->bucket = h;
-                        break;
-                    }
-                    running += h;
-                }
-            }
-        }
-        named_bar_sync(bar_id, NT);
-        rem -= ctl->above;
-        prefix |= static_cast<uint64_t>(ctl->digit) << shift;
-        const bool done = ctl->bucket == rem;
-        named_bar_sync(bar_id, NT);  // ctl and hist are rewritten by the next pass
-        if (done) break;
-    }
-    return prefix;
-}
-
 // Collective over NT threads (named barrier bar_id): exclusive prefix of v over the threads in
 // thread order, and the total. Two barriers; warp_tot is free again when it returns.
 template <int NT>
@@ -230,8 +148,12 @@ __device__ __forceinline__ uint32_t group_excl_scan(uint32_t v, uint32_t* warp_t
     return before + x - v;
 }
 
-// Collective over NT threads: radix threshold (as radix_threshold) over keys held in registers,
-// keys[j] valid for j < cnt; thread 0 must hold at least one key. hist: NT/32 x 256 words.
+// Collective over NT threads (named barrier bar_id): the threshold thr such that exactly K of the
+// keys are >= thr (keys are distinct; more than K in total), over keys held in registers, keys[j]
+// valid for j < cnt; thread 0 must hold at least one key. MSB-first radix select with 8-bit
+// digits, starting below the bits all keys share, stopping as soon as the boundary bucket is taken
+// whole. `hist` holds NT/32 private 256-bin histograms (one per warp, so warps never contend on a
+// hot bin); they are summed into the first one after every pass.
 // With max_passes, the select stops early and returns a threshold that keeps the whole boundary
 // bucket: at least K keys (fewer passes, a few keys more than K).
 template <int NT, int PER>
@@ -430,6 +352,8 @@ struct IndexerArgs {
     const int32_t* q_seq;  // may be null: row t is sequence t
     const int32_t* q_pos;  // may be null: decode, pos = seq_len - 1
     int32_t* tile_prefix;  // [T + 1] (workspace)
+    int32_t* group_prefix; // [T + 1] merge groups before row t (workspace)
+    int32_t* merge_count;  // [3][merge groups] finished children per merge-tree group (workspace)
     int32_t* slot_count;   // [G + T] (workspace)
     uint64_t* slots;       // [G + T][K] (workspace)
     int32_t* idx;          // [T][K] out

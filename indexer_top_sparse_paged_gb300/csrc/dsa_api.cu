@@ -85,6 +85,10 @@ WsLayout ws_layout(const dsa_dims& d, int T) {
     off += 256;
     w.tile_prefix = off;
     off = align256(off + sizeof(int32_t) * (static_cast<size_t>(T) + 1));
+    w.group_prefix = off;
+    off = align256(off + sizeof(int32_t) * (static_cast<size_t>(T) + 1));
+    w.merge_count = off;
+    off = align256(off + sizeof(int32_t) * (kMergeLevels - 1) * static_cast<size_t>(merge_group_bound(T, w.G)));
     w.slot_count = off;
     off = align256(off + sizeof(int32_t) * (static_cast<size_t>(w.G) + T));
     w.slots = off;
@@ -197,6 +201,8 @@ static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w
     a.q_seq = q_seq;
     a.q_pos = q_pos;
     a.tile_prefix = reinterpret_cast<int32_t*>(base + L.tile_prefix);
+    a.group_prefix = reinterpret_cast<int32_t*>(base + L.group_prefix);
+    a.merge_count = reinterpret_cast<int32_t*>(base + L.merge_count);
     a.slot_count = reinterpret_cast<int32_t*>(base + L.slot_count);
     a.slots = reinterpret_cast<uint64_t*>(base + L.slots);
     a.idx = idx;

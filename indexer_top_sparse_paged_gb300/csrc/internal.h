@@ -14,11 +14,19 @@ namespace dsa {
 
 constexpr int kMaxSplits = 32;   // split-K pieces per attention row
 constexpr int kMaxIndexerCtas = 1024;
+constexpr int kMergeFanIn = 8;   // candidate lists one merge CTA selects from (<= 8 x 2048 keys)
+constexpr int kMergeLevels = 4;  // 8^4 >= kMaxIndexerCtas lists per row
+
+// Upper bound on the merge groups of a call (one merge CTA each): sum over rows of
+// ceil(lists / 8) <= T + G / 8, since the rows' lists number at most G + T.
+__host__ __device__ inline int merge_group_bound(int T, int G) { return T + (G + kMergeFanIn - 1) / kMergeFanIn + 1; }
 
 // Byte offsets of the workspace regions for one call shape.
 struct WsLayout {
     size_t err;          // int32 error word (+ padding to 256 B)
     size_t tile_prefix;  // int32 [T + 1]
+    size_t group_prefix; // int32 [T + 1] merge groups before each row
+    size_t merge_count;  // int32 [3][T + G/8 + 1] finished children of the merge tree's groups (levels 2..4)
     size_t slot_count;   // int32 [G + T]
     size_t slots;        // uint64 [G + T][K]
     size_t idx;          // int32 [T][K] (dsa_decode without a caller idx)

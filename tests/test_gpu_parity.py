@@ -171,6 +171,20 @@ def test_split_count_does_not_change_results():
     assert_attn_parity(case1, idx1, out1, lse1)
 
 
+def test_long_rows_merge_through_the_group_tree():
+    """A row whose tiles span ~130 indexer CTAs (17 merge groups, merged by the row's last group),
+    one spanning ~18 (3 groups) and a short one (1 group)."""
+    spec = small_spec("bf16", [150000, 3000, 20000], 2048)
+    case = W.generate(spec, seed=116)
+    _full_check(case, attn_rows=np.arange(3))
+
+
+def test_long_row_fp8_keys_k512():
+    spec = small_spec("bf16_kfp8", [90000, 400], 512)
+    case = W.generate(spec, seed=117)
+    _full_check(case)
+
+
 # ------------------------------------------------------------------ the named workloads at full size
 
 def test_decode_bf16_b32_full_size():
