@@ -10,6 +10,9 @@
 // per-thread insertion), and only the per-CTA survivors leave shared memory.
 #pragma once
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "ptx.cuh"
@@ -335,6 +338,56 @@ struct TopkGroup {
 };
 
 // ------------------------------------------------------------------------------------------------
+// FP8 e4m3 key tiles -> bf16 tensor-core operands
+// ------------------------------------------------------------------------------------------------
+
+// 16 e4m3 codes -> 16 bf16 (two 16-byte groups), exactly: e4m3 -> f16 is exact (every e4m3 value,
+// subnormals included, is an f16 normal or zero), and so is f16 -> fp32 -> bf16 for values with
+// at most 4 significant bits inside bf16's exponent range.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+            const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * hlf)) & 0xFFFFu);
+            const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+            const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);  // .x = the lower code
+            o[2 * i + hlf] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Key row r (0..127) of a staged e4m3 tile: two 64-token blocks of 64 rows x 128 codes, each
+// row 128 bytes, 128-byte swizzled as the TMA wrote it (16-byte group c of row rr at c ^ (rr & 7)).
+__device__ __forceinline__ void load_e4m3_row(const uint8_t* tile, int r, uint4 (&codes)[8]) {
+    const uint8_t* src = tile + (r >> 6) * (64 * 128) + (r & 63) * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) codes[c] = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
+}
+
+// Writes key row r as bf16 into the tensor core's operand stage: two K halves of [128 rows x 64
+// bf16] (16 KB each), rows 128 bytes apart, 128-byte swizzled. Codes 16c..16c+15 go to K half
+// c / 4, 16-byte groups 2(c % 4) and 2(c % 4) + 1.
+__device__ __forceinline__ void store_bf16_row(uint8_t* stage, int r, const uint4 (&codes)[8]) {
+    uint8_t* dst = stage + r * 128;
+    const int sw = r & 7;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4 lo, hi;
+        e4m3x16_to_bf16(codes[c], lo, hi);
+        uint8_t* row = dst + (c >> 2) * (128 * 128);
+        const int g = 2 * (c & 3);
+        *reinterpret_cast<uint4*>(row + ((g ^ sw) << 4)) = lo;
+        *reinterpret_cast<uint4*>(row + (((g + 1) ^ sw) << 4)) = hi;
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
 // kernel parameter blocks
 // ------------------------------------------------------------------------------------------------
 
@@ -359,7 +412,18 @@ struct IndexerArgs {
     int32_t* idx;          // [T][K] out
     int* err;              // device error word (workspace)
     int G;                 // indexer CTAs
+    // prefill: groups of 4 consecutive query rows of one sequence are scored by a GEMM kernel
+    int NG;                     // candidate groups (T / 4), 0 when the call has no prefill path
+    int32_t* gemm_flag;         // [NG] 1: group g runs on the score GEMM (its rows skip the decode path)
+    int32_t* gemm_tile_prefix;  // [NG + 1] 128-key tiles of the GEMM groups before group g
+    float* scores;              // [T][max_blocks * 64] fp32 scores of the GEMM rows (NaN: excluded)
+    int G2;                     // score GEMM CTAs
 };
+
+// Is query row t scored by the prefill GEMM (written by the plan)?
+__device__ __forceinline__ bool gemm_row(const IndexerArgs& a, int t) {
+    return (t >> 2) < a.NG && a.gemm_flag[t >> 2] != 0;
+}
 
 __device__ __forceinline__ int row_seq(const IndexerArgs& a, int t) { return a.q_seq ? a.q_seq[t] : t; }
 

@@ -76,10 +76,13 @@ int attn_splits(const dsa_dims& d, int T) {
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-WsLayout ws_layout(const dsa_dims& d, int T) {
+bool prefill_path(const dsa_dims& d, int T) { return indexer_uses_tc(d) && T >= 4 && T > d.B; }
+
+WsLayout ws_layout(const dsa_dims& d, int T, bool allow_prefill) {
     WsLayout w{};
     w.G = indexer_ctas(d);
     w.S = attn_splits(d, T);
+    w.NG = (allow_prefill && prefill_path(d, T)) ? T / 4 : 0;
     size_t off = 0;
     w.err = off;
     off += 256;
@@ -99,7 +102,12 @@ WsLayout ws_layout(const dsa_dims& d, int T) {
     if (w.S > 1) off = align256(off + sizeof(float) * static_cast<size_t>(T) * w.S * d.H * d.d_v);
     w.part_ml = off;
     if (w.S > 1) off = align256(off + sizeof(float) * static_cast<size_t>(T) * w.S * 2 * d.H * 2);
+    w.gemm_flag = off;
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(w.NG));
+    w.gemm_tile_prefix = off;
+    off = align256(off + sizeof(int32_t) * (static_cast<size_t>(w.NG) + 1));
     w.scores = off;
+    if (w.NG > 0) off = align256(off + sizeof(float) * static_cast<size_t>(T) * d.max_blocks * kBlock);
     w.total = off;
     return w;
 }
@@ -180,8 +188,8 @@ static dsa_status check_ws(const dsa_dims* d, int T, void* ws, size_t ws_bytes) 
 static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w, const void* k_I_cache,
                               const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                               const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx, void* ws,
-                              cudaStream_t stream, int* launches) {
-    const WsLayout L = ws_layout(*d, T);
+                              cudaStream_t stream, int* launches, bool allow_prefill = true) {
+    const WsLayout L = ws_layout(*d, T, allow_prefill);
     uint8_t* base = static_cast<uint8_t*>(ws);
     IndexerArgs a{};
     a.mode = d->mode;
@@ -208,10 +216,17 @@ static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w
     a.idx = idx;
     a.err = reinterpret_cast<int*>(base + L.err);
     a.G = L.G;
+    a.NG = q_seq ? L.NG : 0;
+    a.gemm_flag = reinterpret_cast<int32_t*>(base + L.gemm_flag);
+    a.gemm_tile_prefix = reinterpret_cast<int32_t*>(base + L.gemm_tile_prefix);
+    a.scores = reinterpret_cast<float*>(base + L.scores);
+    a.G2 = device_sm_count();
     if (!launch_plan(a, stream, launches)) return DSA_ERR_LAUNCH;
+    if (a.NG > 0 && !launch_indexer_prefill(a, stream, launches)) return DSA_ERR_LAUNCH;
     const bool ok = indexer_uses_tc(*d) ? launch_indexer_tc(a, stream, launches) : launch_indexer_simt(a, stream, launches);
     if (!ok) return DSA_ERR_LAUNCH;
     if (!launch_merge(a, stream, launches)) return DSA_ERR_LAUNCH;
+    if (a.NG > 0 && !launch_prefill_topk(a, stream, launches)) return DSA_ERR_LAUNCH;
     return DSA_OK;
 }
 
@@ -373,7 +388,7 @@ dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const
     if (!aligned16(q_I) || !aligned16(w) || !aligned16(k_I_cache)) return DSA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(fault_word) & 3u) return DSA_ERR_INVALID_ARG;
     // the indexer uses the workspace regions up to the attention's (error word, plan, candidates)
-    if (ws_layout(*dims, T).idx > kNoAllocScratchBytes) return DSA_ERR_TOO_LARGE;
+    if (ws_layout(*dims, T, false).idx > kNoAllocScratchBytes) return DSA_ERR_TOO_LARGE;
     void* ws = noalloc_scratch();
     if (!ws) return DSA_ERR_LAUNCH;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -383,7 +398,7 @@ dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const
     if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return DSA_ERR_LAUNCH;
     if (T > 0)
         st = run_indexer(dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, q_seq, q_pos, T, idx, ws, s,
-                         &launches);
+                         &launches, /*allow_prefill=*/false);
     if (st == DSA_OK && fault_word &&
         cudaMemcpyAsync(fault_word, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
         st = DSA_ERR_LAUNCH;

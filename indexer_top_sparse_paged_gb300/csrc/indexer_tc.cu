@@ -23,10 +23,6 @@
 // so the product is still exact-input bf16 x bf16 -> fp32; the block's scale multiplies the
 // accumulator in the epilogue, before the ReLU:
 //     S[s] = sum_j w_j * max(0, scale_blk * D[s, j]).
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
-
 #include "internal.h"
 
 namespace dsa {
@@ -82,27 +78,6 @@ __host__ __device__ constexpr size_t smem_bytes(int K) {
 static_assert(topk_cap(2048) <= static_cast<uint32_t>(kEpiThreads * kTopkPer), "candidate buffer exceeds registers");
 static_assert(smem_bytes<false>(2048) <= kSmemLimit, "indexer shared memory over the limit");
 static_assert(smem_bytes<true>(2048) <= kSmemLimit, "FP8 indexer shared memory over the limit");
-
-// 16 e4m3 codes -> 16 bf16 (two 16-byte groups), exactly: e4m3 -> f16 is exact (every e4m3 value,
-// subnormals included, is an f16 normal or zero), and so is f16 -> fp32 -> bf16 for values with
-// at most 4 significant bits inside bf16's exponent range.
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint4& lo, uint4& hi) {
-    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-    uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-            const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * hlf)) & 0xFFFFu);
-            const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-            const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);  // .x = the lower code
-            o[2 * i + hlf] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-    }
-    lo = make_uint4(o[0], o[1], o[2], o[3]);
-    hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
 
 template <bool kFp8>
 __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
@@ -272,7 +247,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         // row r % 64) become 16 swizzled 16-byte groups of bf16 in the two K halves of the operand
         // stage. Rows whose block was not loaded hold stale codes; the epilogue masks their keys.
         const int r = threadIdx.x - 192;
-        const int rr = r & 63, p = r >> 6, sw = r & 7;
         uint32_t n_it = 0;
         bool ok = true;
         while (ok && it.next(seg)) {
@@ -282,23 +256,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&S.full8[s8]), u8 & 1u, abort_flag, a.err) &&
                                                  mbar_wait(smem_u32(&S.empty[st]), (use & 1u) ^ 1u, abort_flag, a.err));
                 if (!ok) break;
-                const uint8_t* src = smem + C::kOffF8 + s8 * kF8TileBytes + p * kF8BlockBytes + rr * 128;
                 uint4 codes[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) codes[c] = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+                load_e4m3_row(smem + C::kOffF8 + s8 * kF8TileBytes, r, codes);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.empty8[s8]));  // codes are in registers
-                uint8_t* dst = smem + C::kOffA + st * kStageBytes + r * 128;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    // codes 16c..16c+15 -> K half c / 4, bf16 groups 2(c % 4) and 2(c % 4) + 1
-                    uint4 lo, hi;
-                    e4m3x16_to_bf16(codes[c], lo, hi);
-                    uint8_t* row = dst + (c >> 2) * kHalfBytes;
-                    const int g = 2 * (c & 3);
-                    *reinterpret_cast<uint4*>(row + ((g ^ sw) << 4)) = lo;
-                    *reinterpret_cast<uint4*>(row + (((g + 1) ^ sw) << 4)) = hi;
-                }
+                store_bf16_row(smem + C::kOffA + st * kStageBytes, r, codes);
                 fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.full[st]));

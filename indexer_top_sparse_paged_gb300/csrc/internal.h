@@ -32,16 +32,22 @@ struct WsLayout {
     size_t idx;          // int32 [T][K] (dsa_decode without a caller idx)
     size_t part_o;       // fp32 [T][S][H][d_v]
     size_t part_ml;      // fp32 [T][S][2 CTAs][H][2] (m, l)
-    size_t scores;       // fp32 [T][max_blocks * 64] (prefill only)
+    size_t gemm_flag;    // int32 [NG] prefill groups on the score GEMM (prefill path only)
+    size_t gemm_tile_prefix;  // int32 [NG + 1]
+    size_t scores;       // fp32 [T][max_blocks * 64] (prefill path only)
     size_t total;
     int G;               // indexer CTAs
     int S;               // attention splits
+    int NG;              // candidate prefill groups (T / 4), 0 without the prefill path
 };
 
 int device_sm_count();
 int indexer_ctas(const dsa_dims& d);
 int attn_splits(const dsa_dims& d, int T);
-WsLayout ws_layout(const dsa_dims& d, int T);
+// The prefill path (score GEMM + per-row Top-K for groups of 4 rows of one sequence) is taken
+// by calls with more query rows than sequences, on the tensor-core indexer shapes.
+bool prefill_path(const dsa_dims& d, int T);
+WsLayout ws_layout(const dsa_dims& d, int T, bool allow_prefill = true);
 
 bool indexer_uses_tc(const dsa_dims& d);
 bool attn_uses_tc(const dsa_dims& d);
@@ -80,6 +86,8 @@ bool launch_plan(const IndexerArgs& a, cudaStream_t s, int* launches);
 bool launch_merge(const IndexerArgs& a, cudaStream_t s, int* launches);
 bool launch_indexer_simt(const IndexerArgs& a, cudaStream_t s, int* launches);
 bool launch_indexer_tc(const IndexerArgs& a, cudaStream_t s, int* launches);
+bool launch_indexer_prefill(const IndexerArgs& a, cudaStream_t s, int* launches);
+bool launch_prefill_topk(const IndexerArgs& a, cudaStream_t s, int* launches);
 
 struct AttnArgs {
     int mode;

@@ -1,7 +1,8 @@
 // Work plan and Top-K merge.
 //
-// plan:  tile_prefix[t] = number of 128-key tiles of all query rows before row t, and the merge
-//        groups of every row (one CTA).
+// plan:  which groups of 4 prefill rows run on the score GEMM, tile_prefix[t] = number of 128-key
+//        tiles of the decode-path rows before row t, the merge groups of every decode-path row,
+//        and the tile prefix of the GEMM groups (one CTA).
 // merge: the candidate lists that the indexer CTAs left for a row's segments (each already cut
 //        to at most K keys, in position order) are reduced by a tree with fan-in 8. A merge
 //        CTA selects the K largest keys of up to 8 lists with an MSB-first radix select over
@@ -52,21 +53,34 @@ __device__ __forceinline__ int plan_scan(int v, int* warp_sums, int& total) {
 // Merge groups of row t: lists come from the CTAs c_first..c_last that own the row's tiles
 // [p0, p1), kMergeFanIn consecutive CTA indices per group (a row without tiles has one group).
 __device__ __forceinline__ int merge_groups(int64_t p0, int64_t p1, int64_t total, int64_t G) {
-    if (p1 <= p0) return 1;
+    if (p1 <= p0) return 1;  // one group writes the row's -1s
     const int64_t n = tile_owner(p1 - 1, total, G) - tile_owner(p0, total, G) + 1;
     return static_cast<int>((n + kMergeFanIn - 1) / kMergeFanIn);
+}
+
+// Does group g (rows 4g..4g+3) run on the prefill score GEMM? All four rows belong to one
+// valid sequence.
+__device__ __forceinline__ bool group_on_gemm(const IndexerArgs& a, int g) {
+    if (g >= a.NG) return false;
+    const int b = a.q_seq[4 * g];
+    if (b < 0 || b >= a.B) return false;
+    return a.q_seq[4 * g + 1] == b && a.q_seq[4 * g + 2] == b && a.q_seq[4 * g + 3] == b;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(IndexerArgs a) {
     __shared__ int warp_sums[32];
     griddep_launch_dependents();  // the indexer may start its prologue
     const int tid = threadIdx.x;
-    // 1. tiles per row -> tile_prefix
+    // 1. GEMM groups; tiles per row of the decode path (GEMM rows have none) -> tile_prefix
     int carry = 0;
     for (int base = 0; base < a.T; base += kPlanThreads) {
         const int t = base + tid;
-        const int n = (t < a.T) ? row_len(a, t) : 0;
-        const int tiles = (n + kTileKeys - 1) / kTileKeys;
+        int tiles = 0;
+        if (t < a.T) {
+            const bool gemm = group_on_gemm(a, t >> 2);
+            if ((t & 3) == 0 && (t >> 2) < a.NG) a.gemm_flag[t >> 2] = gemm ? 1 : 0;
+            if (!gemm) tiles = (row_len(a, t) + kTileKeys - 1) / kTileKeys;
+        }
         int sum;
         const int excl = plan_scan(tiles, warp_sums, sum);
         if (t < a.T) a.tile_prefix[t] = carry + excl;
@@ -74,12 +88,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(IndexerArgs a) {
     }
     if (tid == 0) a.tile_prefix[a.T] = carry;
     block_sync();
-    // 2. merge groups per row -> group_prefix; the rows' group counters start at zero
+    // 2. merge groups per row (none for GEMM rows) -> group_prefix; their counters start at zero
     const int64_t total = carry;
     int gcarry = 0;
     for (int base = 0; base < a.T; base += kPlanThreads) {
         const int t = base + tid;
-        const int g = (t < a.T) ? merge_groups(a.tile_prefix[t], a.tile_prefix[t + 1], total, a.G) : 0;
+        const int g = (t < a.T && !gemm_row(a, t)) ? merge_groups(a.tile_prefix[t], a.tile_prefix[t + 1], total, a.G) : 0;
         int sum;
         const int excl = plan_scan(g, warp_sums, sum);
         if (t < a.T) {
@@ -91,6 +105,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(IndexerArgs a) {
         gcarry += sum;
     }
     if (tid == 0) a.group_prefix[a.T] = gcarry;
+    // 3. tiles of the GEMM groups (their longest causal prefix) -> gemm_tile_prefix
+    int tcarry = 0;
+    for (int base = 0; base < a.NG; base += kPlanThreads) {
+        const int g = base + tid;
+        int tiles = 0;
+        if (g < a.NG && a.gemm_flag[g]) {
+            int n = 0;
+            for (int q = 0; q < 4; ++q) n = max(n, row_len(a, 4 * g + q));
+            tiles = (n + kTileKeys - 1) / kTileKeys;
+        }
+        int sum;
+        const int excl = plan_scan(tiles, warp_sums, sum);
+        if (g < a.NG) a.gemm_tile_prefix[g] = tcarry + excl;
+        tcarry += sum;
+    }
+    if (tid == 0 && a.NG > 0) a.gemm_tile_prefix[a.NG] = tcarry;
 }
 
 constexpr int kPer = kMergeSmemKeys / kMergeThreads;  // candidates per thread held in registers

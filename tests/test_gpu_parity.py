@@ -185,6 +185,37 @@ def test_long_row_fp8_keys_k512():
     _full_check(case)
 
 
+def test_prefill_groups_on_the_score_gemm():
+    """Rows 0-7 and 8-11 form groups of four rows of one sequence (score GEMM + per-row Top-K,
+    rows longer than the 8192-key candidate buffer: sampled admission threshold); row 12 is left
+    over for the decode kernels."""
+    spec = small_spec("bf16", [12000, 9000], 2048, new_tokens=[8, 5])
+    case = W.generate(spec, seed=118)
+    _full_check(case, attn_rows=np.array([0, 7, 8, 12]))
+
+
+def test_prefill_gemm_fp8_keys_and_mixed_groups():
+    """FP8 keys; decode rows first, so the first groups mix sequences (decode path) and the
+    chunk's groups run on the score GEMM."""
+    spec = small_spec("bf16_kfp8", [700, 5000, 20000, 10000], 1024, new_tokens=[1, 1, 1, 14])
+    case = W.generate(spec, seed=119)
+    _full_check(case, attn_rows=np.array([0, 2, 3, 16]))
+
+
+def test_prefill_gemm_equal_scores_take_the_lowest_positions():
+    """Zero queries give every key the score 0: the admission threshold admits the whole row,
+    which overflows the candidate buffer, and the exact streaming selection must return the K
+    lowest positions (ties go to the lower position)."""
+    spec = small_spec("bf16", [20000], 2048, new_tokens=[4])
+    case = W.generate(spec, seed=120)
+    case.q_I[:] = W.to_bf16_bits(np.zeros(case.q_I.shape, np.float32))
+    dev = Dev(case)
+    idx = dev.indexer()
+    assert dev.faults() == 0
+    for t in range(spec.T):
+        assert idx[t].tolist() == list(range(2048))
+
+
 # ------------------------------------------------------------------ the named workloads at full size
 
 def test_decode_bf16_b32_full_size():
