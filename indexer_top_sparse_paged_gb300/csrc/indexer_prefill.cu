@@ -14,9 +14,10 @@
 // scoring reuses a matrix multiplication), so here it runs on the tensor cores at full width
 // while the selection streams the scores once.
 //
-// Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer, warps 2..5 = epilogue
-// (TMEM lane quarter = warp % 4); FP8 keys add warps 6..9, which widen the staged e4m3 codes to
-// bf16 operands exactly (as the decode indexer does), once per tile for all four rows.
+// Roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer, warps 2..9 = epilogue (two
+// warps per TMEM lane quarter = warp % 4, each taking two of the four rows, so the epilogue's
+// arithmetic keeps up with the tensor pipe); FP8 keys add warps 10..13, which widen the staged
+// e4m3 codes to bf16 operands exactly (as the decode indexer does), once per tile for all rows.
 #include "internal.h"
 
 namespace dsa {
@@ -30,7 +31,9 @@ constexpr int kHalfBytes = kTileKeys * 128;   // [128 keys x 64 bf16] = 16 KB
 constexpr int kStageBytes = 2 * kHalfBytes;   // 32 KB
 constexpr int kQHalfBytes = kN * 128;         // [256 rows x 64 bf16] = 32 KB
 constexpr int kQBytes = 2 * kQHalfBytes;      // 64 KB
-constexpr int kEpiThreads = 128;
+constexpr int kEpiThreads = 256;
+constexpr int kEpiWarps = kEpiThreads / 32;
+constexpr int kConvWarp0 = 2 + kEpiWarps;  // first converter warp (FP8 keys)
 constexpr int kAcc = 2;
 constexpr int kTmemCols = kAcc * kN;          // 512
 constexpr uint32_t kIdesc = idesc_f16(128, kN, 1u, 0u, 0u);
@@ -39,7 +42,7 @@ constexpr int kF8BlockBytes = kBlock * kDim;
 
 template <bool kFp8>
 struct Cfg {
-    static constexpr int kThreads = kFp8 ? 320 : 192;
+    static constexpr int kThreads = kFp8 ? 32 * (kConvWarp0 + 4) : 32 * kConvWarp0;
     static constexpr int kStages = kFp8 ? 2 : 4;
     static constexpr int kStages8 = kFp8 ? 5 : 1;
     static constexpr size_t kOffQ = 0;
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         mbar_init(smem_u32(&S.qempty), 1);
         for (int i = 0; i < kAcc; ++i) {
             mbar_init(smem_u32(&S.tfull[i]), 1);
-            mbar_init(smem_u32(&S.tempty[i]), kEpiThreads / 32);
+            mbar_init(smem_u32(&S.tempty[i]), kEpiWarps);
         }
         mbar_init(smem_u32(&S.mma_done), 1);
         S.abort_flag = 0;
@@ -230,9 +233,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             mbar_wait_drain(smem_u32(&S.mma_done), 0, a.err);
         }
         __syncwarp();
-    } else if (kFp8 && warp >= 6) {
+    } else if (kFp8 && warp >= kConvWarp0) {
         // ------------------------------------------------------------- e4m3 -> bf16 converters
-        const int r = threadIdx.x - 192;
+        const int r = threadIdx.x - 32 * kConvWarp0;
         uint32_t n_it = 0;
         bool ok = true;
         while (ok && it.next(seg)) {
@@ -256,7 +259,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         // ------------------------------------------------------------- epilogue: scores
         const uint32_t quarter = warp & 3;
         const uint32_t row = quarter * 32 + lane;  // key within the tile
-        const int etid = threadIdx.x - 64;         // 0..127 over the epilogue warps
+        const int etid = threadIdx.x - 64;         // 0..255 over the epilogue warps
+        const int q0 = (warp - 2) / 4 * 2;         // this warp's two rows of the group: q0, q0 + 1
         const int64_t lmax = static_cast<int64_t>(a.max_blocks) * kBlock;
         uint32_t n_it = 0;
         while (it.next(seg)) {
@@ -280,16 +284,16 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 float sc = 1.0f;
                 if (kFp8) sc = blk_ok ? a.k_I_scale[blk] : 0.0f;
                 const bool got = mbar_wait(smem_u32(&S.tfull[acc]), ause & 1u, abort_flag, a.err);
-                if (named_bar_or(1, kEpiThreads, !got)) { ok = false; break; }  // one decision for all four warps
+                if (named_bar_or(1, kEpiThreads, !got)) { ok = false; break; }  // one decision for all epilogue warps
                 tc_fence_after();
                 const uint32_t taddr = tmem + acc * kN + ((quarter * 32) << 16);
 #pragma unroll 1
-                for (int q = 0; q < kRowsPerGroup; ++q) {
+                for (int q = q0; q < q0 + 2; ++q) {
                     uint32_t v0[32], v1[32];
                     tmem_ld32(taddr + q * kHeads, v0);
                     tmem_ld32(taddr + q * kHeads + 32, v1);
                     tmem_ld_wait();
-                    if (q == kRowsPerGroup - 1) {  // every column of this accumulator has been read
+                    if (q == q0 + 1) {  // this warp has read all of its columns of the accumulator
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(smem_u32(&S.tempty[acc]));

@@ -150,7 +150,7 @@ __device__ uint64_t row_radix_threshold(const float* srow, int n, uint32_t K, Pt
     return prefix;
 }
 
-__global__ void __launch_bounds__(kPtThreads) prefill_topk_kernel(IndexerArgs a) {
+__global__ void __launch_bounds__(kPtThreads, 2) prefill_topk_kernel(IndexerArgs a) {
     extern __shared__ __align__(16) uint8_t pt_smem[];
     __shared__ TopkCtl ctl;
     __shared__ uint32_t warp_tot[32];

@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a
     griddep_wait();  // the indexer's candidate lists and the plan are complete
     const uint32_t tid = threadIdx.x, lane = tid & 31u;
     const int b = blockIdx.x;
+    if (b >= a.group_prefix[a.T]) return;  // the grid is an upper bound on the groups
     // row t with group_prefix[t] <= b < group_prefix[t + 1], one row per thread (one round trip
     // to memory for up to kMergeThreads rows, where a binary search would chain several)
     if (tid == 0) row_found = -1;
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a
         if (row_found >= 0) break;
     }
     const int t = row_found;
-    if (t < 0) return;  // the grid is an upper bound on the groups
+    if (t < 0) return;
     const uint32_t K = static_cast<uint32_t>(a.K);
     int32_t* out = a.idx + static_cast<int64_t>(t) * a.K;
     const int64_t p0 = a.tile_prefix[t], p1 = a.tile_prefix[t + 1], total = a.tile_prefix[a.T];
