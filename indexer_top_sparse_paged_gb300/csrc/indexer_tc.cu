@@ -307,20 +307,42 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.tempty[acc]));
-                float score = 0.0f;
+                // four independent partial sums (heads j mod 4) keep the FMA pipe busy
+                float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
                 if (!kFp8 || sc >= 0.0f) {
                     // scale >= 0: max(0, scale * x) = scale * max(0, x), applied once to the sum
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) score = fmaf(wv[h], fmaxf(__uint_as_float(v0[h]), 0.0f), score);
+                    for (int h = 0; h < 32; h += 4) {
+                        p0 = fmaf(wv[h], fmaxf(__uint_as_float(v0[h]), 0.0f), p0);
+                        p1 = fmaf(wv[h + 1], fmaxf(__uint_as_float(v0[h + 1]), 0.0f), p1);
+                        p2 = fmaf(wv[h + 2], fmaxf(__uint_as_float(v0[h + 2]), 0.0f), p2);
+                        p3 = fmaf(wv[h + 3], fmaxf(__uint_as_float(v0[h + 3]), 0.0f), p3);
+                    }
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) score = fmaf(wv[32 + h], fmaxf(__uint_as_float(v1[h]), 0.0f), score);
+                    for (int h = 0; h < 32; h += 4) {
+                        p0 = fmaf(wv[32 + h], fmaxf(__uint_as_float(v1[h]), 0.0f), p0);
+                        p1 = fmaf(wv[33 + h], fmaxf(__uint_as_float(v1[h + 1]), 0.0f), p1);
+                        p2 = fmaf(wv[34 + h], fmaxf(__uint_as_float(v1[h + 2]), 0.0f), p2);
+                        p3 = fmaf(wv[35 + h], fmaxf(__uint_as_float(v1[h + 3]), 0.0f), p3);
+                    }
                 } else {
                     // scale < 0: max(0, scale * x) = scale * min(0, x)
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) score = fmaf(wv[h], fminf(__uint_as_float(v0[h]), 0.0f), score);
+                    for (int h = 0; h < 32; h += 4) {
+                        p0 = fmaf(wv[h], fminf(__uint_as_float(v0[h]), 0.0f), p0);
+                        p1 = fmaf(wv[h + 1], fminf(__uint_as_float(v0[h + 1]), 0.0f), p1);
+                        p2 = fmaf(wv[h + 2], fminf(__uint_as_float(v0[h + 2]), 0.0f), p2);
+                        p3 = fmaf(wv[h + 3], fminf(__uint_as_float(v0[h + 3]), 0.0f), p3);
+                    }
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) score = fmaf(wv[32 + h], fminf(__uint_as_float(v1[h]), 0.0f), score);
+                    for (int h = 0; h < 32; h += 4) {
+                        p0 = fmaf(wv[32 + h], fminf(__uint_as_float(v1[h]), 0.0f), p0);
+                        p1 = fmaf(wv[33 + h], fminf(__uint_as_float(v1[h + 1]), 0.0f), p1);
+                        p2 = fmaf(wv[34 + h], fminf(__uint_as_float(v1[h + 2]), 0.0f), p2);
+                        p3 = fmaf(wv[35 + h], fminf(__uint_as_float(v1[h + 3]), 0.0f), p3);
+                    }
                 }
+                float score = (p0 + p1) + (p2 + p3);
                 if (kFp8) score *= sc;
                 // a block whose table entry is invalid was never loaded: its keys do not count
                 const bool valid = s < n && blk_ok;

@@ -3,9 +3,9 @@
 //
 //  1. A sample of the row (16 evenly spaced runs of 256 consecutive scores) gives an admission
 //     threshold: the score ranked about 1.5 K / n of the way down the sample.
-//  2. One pass over the row stages 8192 scores at a time in shared memory, and every thread
-//     keeps the admitted keys of its 16 consecutive positions; a block scan places them, so the
-//     candidate buffer stays in position order.
+//  2. One pass over the row stages 8192 scores at a time in shared memory; every warp keeps the
+//     admitted keys of its 512 consecutive positions (ballots within the warp, a scan of the warp
+//     counts across warps), so the candidate buffer stays in position order.
 //  3. If at least K and at most the buffer's 8192 keys were admitted, the K-th key is found
 //     among them by a radix select in registers, and the kept positions are written in
 //     ascending order; every key of the true Top-K was admitted, since at least K keys score at
@@ -42,39 +42,56 @@ struct PtShared {
 };
 
 // One pass over the row: keeps, in position order, the keys >= thr of valid scores in sh.cand
-// (the first kPtCap of them) and returns how many there were.
+// (the first kPtCap of them) and returns how many there were. Per round, warp w owns 512
+// consecutive staged positions and walks them 32 at a time (lane = position, conflict-free
+// shared loads); warp ballots order the keys within a warp and a scan of the warp counts places
+// the warps.
 __device__ uint32_t compact_row(const float* srow, int n, uint64_t thr, PtShared& sh, uint32_t tid) {
+    constexpr int kWarpSpan = kPtRound / (kPtThreads / 32);  // 512
+    const uint32_t lane = tid & 31u, warp = tid >> 5;
     uint32_t total = 0;
     for (int base = 0; base < n; base += kPtRound) {
         const int m = min(kPtRound, n - base);
-        // coalesced staging (16-byte loads where the row allows; rows start 16-byte aligned)
         const uint32_t* src = reinterpret_cast<const uint32_t*>(srow + base);
 #pragma unroll
         for (int k = 0; k < kPtPer; ++k) {
             const int i = k * kPtThreads + static_cast<int>(tid);
-            sh.stage[i] = (i < m) ? __ldcs(src + i) : 0x7FC00000u;
+            sh.stage[i] = (i < m) ? __ldcs(src + i) : 0x7FC00000u;  // past the row: invalid
         }
         block_sync();
-        uint64_t keys[kPtPer];
-        uint32_t mine = 0;
-#pragma unroll
-        for (int k = 0; k < kPtPer; ++k) {
-            const int i = static_cast<int>(tid) * kPtPer + k;
+        auto key_at = [&](int k, uint64_t& key) -> bool {
+            const int i = static_cast<int>(warp) * kWarpSpan + k * 32 + static_cast<int>(lane);
             const uint32_t bits = sh.stage[i];
-            keys[k] = score_valid(bits) ? score_key(bits, static_cast<uint32_t>(base + i)) : 0ull;
-            mine += (keys[k] != 0ull && keys[k] >= thr) ? 1u : 0u;
-        }
-        uint32_t round_total;
-        uint32_t o = total + group_excl_scan<kPtThreads>(mine, sh.warp_tot, tid, 2, round_total);
+            key = score_valid(bits) ? score_key(bits, static_cast<uint32_t>(base + i)) : 0ull;
+            return key != 0ull && key >= thr;
+        };
+        uint32_t cnt = 0;
 #pragma unroll
-        for (int k = 0; k < kPtPer; ++k) {
-            if (keys[k] != 0ull && keys[k] >= thr) {
-                if (o < static_cast<uint32_t>(kPtCap)) sh.cand[o] = keys[k];
-                ++o;
-            }
+        for (int k = 0; k < kWarpSpan / 32; ++k) {
+            uint64_t key;
+            cnt += __popc(__ballot_sync(0xFFFFFFFFu, key_at(k, key)));
+        }
+        if (lane == 0) sh.warp_tot[warp] = cnt;
+        block_sync();
+        uint32_t off = total, round_total = 0;
+#pragma unroll
+        for (uint32_t w = 0; w < kPtThreads / 32; ++w) {
+            const uint32_t c = sh.warp_tot[w];
+            off += (w < warp) ? c : 0u;
+            round_total += c;
+        }
+        const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+        for (int k = 0; k < kWarpSpan / 32; ++k) {
+            uint64_t key;
+            const bool pass = key_at(k, key);
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
+            const uint32_t o = off + __popc(bal & below);
+            if (pass && o < static_cast<uint32_t>(kPtCap)) sh.cand[o] = key;
+            off += __popc(bal);
         }
         total += round_total;
-        block_sync();  // the stage is rewritten by the next round
+        block_sync();  // the stage and the warp counts are rewritten by the next round
     }
     return total;
 }
