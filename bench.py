@@ -4,6 +4,8 @@ attention over a paged KV cache) on GB300, through the library's C ABI.
 Default workload: decode, bf16, batch 32, context lengths uniform in [16384, 32768], 64 indexer
 heads of 128, Top-K 2048, 128 query heads over a 576-wide latent cache (V = first 512 columns),
 64-token blocks, shuffled block table. One step = one dsa_decode call on a batch resident in HBM.
+The same JSON line carries the chunked-prefill throughput (2 x 4096 new tokens on a 61,440-token
+prefix: indexer + sparse attention calls) under "prefill".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -70,12 +72,33 @@ def attn_bytes(case) -> int:
     return b
 
 
+def indexer_flops(case) -> int:
+    """Tensor flops of the indexer scores: every causal (row, key) pair, H_I x d_I MACs."""
+    s = case.spec
+    n = (case.q_pos.astype(np.int64) + 1).clip(min=0)
+    return int(n.sum()) * s.H_I * s.d_I * 2
+
+
+def attn_flops(case) -> int:
+    """Tensor flops of sparse attention: QK^T over d and PV over d_v for every selected row."""
+    s = case.spec
+    n = np.minimum((case.q_pos.astype(np.int64) + 1).clip(min=0), s.K)
+    return int(n.sum()) * s.H * (s.d + s.d_v) * 2
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def measured_tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
 
 
 def kernel_digest() -> str:
@@ -188,6 +211,90 @@ def to_dev(a, dev):
     if a.dtype == np.uint16:
         return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
     return torch.from_numpy(a).to(dev)
+
+
+class Resident:
+    """One workload's inputs in device memory and a workspace (inputs copied once, untimed)."""
+
+    def __init__(self, case, dev):
+        import indexer_top_sparse_paged_gb300 as dsa
+        s = case.spec
+        self.case, self.dev = case, dev
+        self.dims = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K)
+        self.q_I, self.w, self.k_I = to_dev(case.q_I, dev), to_dev(case.w, dev), to_dev(case.k_I, dev)
+        self.ksc = to_dev(case.k_I_scale, dev) if case.k_I_scale is not None else None
+        self.q, self.kv = to_dev(case.q, dev), to_dev(case.kv, dev)
+        self.bt, self.sl = to_dev(case.block_table, dev), to_dev(case.seq_lens, dev)
+        self.qs, self.qp = to_dev(case.q_seq, dev), to_dev(case.q_pos, dev)
+        self.ws = dsa.workspace(self.dims, s.T, dev)
+        self.idx = torch.empty((s.T, s.K), dtype=torch.int32, device=dev)
+        self.out = torch.empty((s.T, s.H, s.d_v), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((s.T, s.H), dtype=torch.float32, device=dev)
+
+    def indexer(self):
+        import indexer_top_sparse_paged_gb300 as dsa
+        dsa.indexer_topk(self.dims, self.q_I, self.w, self.k_I, self.ksc, self.bt, self.sl, self.qs, self.qp,
+                         ws=self.ws, idx=self.idx)
+
+    def attn(self):
+        import indexer_top_sparse_paged_gb300 as dsa
+        dsa.sparse_attn(self.dims, self.q, self.kv, self.bt, self.sl, self.idx, self.case.spec.sm_scale, q_seq=self.qs,
+                        ws=self.ws, out=self.out, lse=self.lse)
+
+
+def run_prefill(steps: int, warmup: int, dev, flush):
+    """Chunked prefill (2 x 4096 new tokens on 61,440 cached, Top-K 2048): indexer and sparse
+    attention calls timed with CUDA events on the current stream, L2 flushed before each."""
+    import indexer_top_sparse_paged_gb300 as dsa
+    spec, seed = W.named(4)
+    case = W.generate(spec, seed)
+    r = Resident(case, dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, warmup)):
+        r.indexer()
+        r.attn()
+    torch.cuda.synchronize(dev)
+    if dsa.read_error(r.ws) != 0:
+        raise RuntimeError("device fault bits set during the prefill warm-up")
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        r.indexer()
+        ev[i][1].record(stream)
+        r.attn()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    if dsa.read_error(r.ws) != 0:
+        raise RuntimeError("device fault bits set during the prefill timing")
+    idx_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
+    att_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev)
+    peak, kind = measured_tensor_peak()
+    fi, fa = indexer_flops(case), attn_flops(case)
+    res = {
+        "workload": "prefill_2x4096_64k: 2 sequences x 4096 new tokens at positions 61440..65535, indexer 64x128 bf16, "
+                    "Top-K 2048 per row, 128 heads x 576 latent",
+        "tokens_per_s": round(spec.T / ((idx_ms + att_ms) * 1e-3), 1),
+        "indexer_ms": round(idx_ms, 3),
+        "attn_ms": round(att_ms, 3),
+        "indexer_tflops": round(fi / (idx_ms * 1e-3) / 1e12, 1),
+        "attn_tflops": round(fa / (att_ms * 1e-3) / 1e12, 1),
+        "tensor_peak_tflops": peak,
+        "indexer_tensor_frac_of_" + kind: round(fi / (idx_ms * 1e-3) / 1e12 / peak, 4),
+        "attn_tensor_frac_of_" + kind: round(fa / (att_ms * 1e-3) / 1e12 / peak, 4),
+        "indexer_flops": fi,
+        "attn_flops": fa,
+        "steps": steps,
+        "l2": "flushed (256 MiB write) before every timed step",
+        "gpu_launches_per_step": None,
+    }
+    r.indexer()
+    n_idx = dsa.last_launch_count()
+    r.attn()
+    res["gpu_launches_per_step"] = n_idx + dsa.last_launch_count()
+    del r
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args, rank, world):
@@ -323,6 +430,8 @@ def run_ours(args, rank, world):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if not args.no_prefill:
+        res["prefill"] = run_prefill(max(3, min(args.steps, 10)), args.warmup, dev, flush)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(case)
     return res
@@ -393,10 +502,24 @@ def run_reference(args, rank, world):
 
 
 def run_profile(args):
-    """warmup + 1 decode steps of the default workload and nothing else (for ncu)."""
+    """warmup + 1 steps of one case and nothing else (for ncu):
+      decode         the default workload (fused decode steps),
+      prefill        the chunked prefill workload at full size (indexer + attention calls),
+      prefill-small  2 x 2048 new tokens on 16,384 (a small case of the prefill kernels)."""
     import indexer_top_sparse_paged_gb300 as dsa
 
     dev = torch.device("cuda", 0)
+    if args.profile in ("prefill", "prefill-small"):
+        spec, seed = W.named(4)
+        if args.profile == "prefill-small":
+            spec = W.prefill_chunk(B=2, new=2048, total=16384)
+        r = Resident(W.generate(spec, seed), dev)
+        for _ in range(args.warmup + 1):
+            r.indexer()
+            r.attn()
+        torch.cuda.synchronize(dev)
+        assert dsa.read_error(r.ws) == 0
+        return
     spec, seed = W.named(2)
     case = W.generate(spec, seed)
     s = case.spec
@@ -422,8 +545,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", action="store_true",
-                    help="only run --warmup + 1 decode steps (a short command for ncu captures)")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill measurement")
+    ap.add_argument("--profile", nargs="?", const="decode", choices=["decode", "prefill", "prefill-small"],
+                    help="only run --warmup + 1 steps of one case (a short command for ncu captures)")
     args = ap.parse_args()
     if args.profile:
         run_profile(args)

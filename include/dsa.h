@@ -94,8 +94,9 @@ typedef struct {
 dsa_status dsa_workspace_init(void* ws, size_t ws_bytes, dsa_stream_t stream);
 
 /* Bytes of workspace needed by any of the calls below for T query rows with these dims on the
- * current device. T > B means some sequence has several query rows (prefill) and includes the
- * prefill score buffer. Returns 0 for invalid dims. */
+ * current device. T > B means some sequence has several query rows (prefill): on the tensor-core
+ * indexer shapes this includes the prefill score matrix, T * max_blocks * 64 fp32 values.
+ * Returns 0 for invalid dims. */
 size_t dsa_workspace_size(const dsa_dims* dims, int32_t T);
 
 /*
@@ -112,8 +113,14 @@ size_t dsa_workspace_size(const dsa_dims* dims, int32_t T);
  *   idx        [T][K]               int32 out: the selected logical positions of each row in
  *                                   ascending order, then -1 for the slots past min(K, pos + 1)
  * Decode-shaped calls (each sequence has at most one query row) stream the keys once with the
- * Top-K fused (no score tensor leaves the chip); calls with several rows per sequence (prefill)
- * score each tile of queries x keys on tensor cores into the workspace, then select per row.
+ * Top-K fused (no score tensor leaves the chip). In calls with more rows than sequences on the
+ * tensor-core indexer shapes (H_I, d_I) == (64, 128), every group of four consecutive rows
+ * (4g..4g+3) of one sequence is scored on the tensor cores as one contraction over the group's
+ * causal prefix into an fp32 score matrix in the workspace, then each row's Top-K is selected from
+ * its scores; the other rows take the decode kernels. The result is the same either way.
+ * ("Day0 Inference Support ... on Huawei Ascend CANN Architecture" §2.1: the lightning indexer
+ * maps the quantised query, head weights and paged key cache to Top-K indices; "Engineering Path
+ * for Day-0 Adaptation ..." §3.1: index selection is scoring followed by Top-K filtering.)
  */
 dsa_status dsa_indexer_topk(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
                             const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
@@ -145,9 +152,9 @@ dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, con
                       size_t ws_bytes, dsa_stream_t stream);
 
 /*
- * Indexer + Top-K that allocates nothing and takes no workspace: the same computation and kernels
- * as dsa_indexer_topk (arguments as there), with the scratch in one statically sized device
- * buffer inside libdsa.so (DSA_NOALLOC_SCRATCH_BYTES per device).
+ * Indexer + Top-K that allocates nothing and takes no workspace: the same computation as
+ * dsa_indexer_topk (arguments as there) on its decode-path kernels for every row, with the scratch
+ * in one statically sized device buffer inside libdsa.so (DSA_NOALLOC_SCRATCH_BYTES per device).
  *
  * The method's pages have no counterpart of this call: it serves callers that cannot allocate
  * device memory or hand over a workspace -- code running inside another framework's caching
