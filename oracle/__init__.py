@@ -17,6 +17,9 @@ return NumPy arrays:
 * :func:`sparse_attn` -- fp64 ``out[t, h, :d_v]``, ``lse[t, h]`` and the sum of
   the softmax weights, over the rows ``idx`` selects (lightweight indexer page
   §1, "sparse flash attention").
+* :func:`cache_append` -- the caches after writing new tokens' indexer keys and
+  latent rows into their paged slots (FP8 keys: block requantisation), the step
+  before the path (Ascend adaptation page §2.2, cache-update flow).
 
 Parity pins for every function live in ``tests/test_oracle_pins.py``.
 """
@@ -66,6 +69,10 @@ def _bind(lib):
     lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
     lib.oracle_e4m3_to_f64.restype = ctypes.c_double
     lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+    lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+    lib.oracle_cache_append.restype = ctypes.c_int
+    lib.oracle_cache_append.argtypes = [ctypes.POINTER(ODims), P, P, P, P, P, P, ctypes.c_int, P, P, P]
     lib.oracle_index_scores.restype = ctypes.c_int
     lib.oracle_index_scores.argtypes = [ctypes.POINTER(ODims), P, P, P, P, P, P, P, P, ctypes.c_int,
                                         ctypes.c_int64, P, ctypes.c_int]
@@ -172,3 +179,31 @@ def sparse_attn(case, idx, rows=None, sm_scale=None, threads=None):
     if rc:
         raise RuntimeError(f"oracle_sparse_attn failed: {rc}")
     return out, lse, psum
+
+
+def f32_to_e4m3(x: float) -> int:
+    """OCP e4m3 code of an fp32 value (round to nearest even, saturating at +-448)."""
+    return int(_load().oracle_f32_to_e4m3(float(x)))
+
+
+def cache_append(case, k_new, kv_new, rows=None):
+    """(k_I, k_I_scale, kv) after appending new tokens: row r of k_new / kv_new is the token at
+    position case.q_pos[r] of sequence case.q_seq[r] (all rows, or the rows ``rows``). The
+    case's arrays are not modified; updated copies are returned."""
+    lib = _load()
+    s = case.spec
+    q_seq = case.q_seq if rows is None else case.q_seq[np.asarray(rows)]
+    q_pos = case.q_pos if rows is None else case.q_pos[np.asarray(rows)]
+    T = len(q_seq)
+    k_I = np.ascontiguousarray(case.k_I).copy()
+    kv = np.ascontiguousarray(case.kv).copy()
+    scale = None if case.k_I_scale is None else np.ascontiguousarray(case.k_I_scale, dtype=np.float32).copy()
+    kdt = np.float32 if s.mode == "f32" else np.uint16
+    adt = np.float32 if s.mode == "f32" else np.uint16
+    keep = [_c(k_new, kdt), _c(kv_new, adt), _c(case.block_table, np.int32), _c(case.seq_lens, np.int32),
+            _c(q_seq, np.int32), _c(q_pos, np.int32)]
+    rc = lib.oracle_cache_append(ctypes.byref(dims_of(case)), *[_ptr(a) for a in keep], T, _ptr(k_I), _ptr(scale),
+                                 _ptr(kv))
+    if rc:
+        raise RuntimeError(f"oracle_cache_append failed: {rc}")
+    return k_I, scale, kv

@@ -28,6 +28,16 @@
  *     over the valid (!= -1) entries of idx[t]; V is the first d_v columns of
  *     the same shared latent row.  No valid entry -> out = 0, lse = -inf.
  *
+ *  0. Cache append (the step before the path: "Residual and normalization ...
+ *     fused with the cache-update flow", Ascend adaptation page §2.2 table; the
+ *     indexer prolog quantises keys, Ascend CANN page §2.2/§3): each new token t
+ *     of sequence b sits at position pos(t) of the sequence's tail; its latent
+ *     row and (fp32 / bf16 modes) its indexer key are copied to the paged slot.
+ *     With FP8 indexer keys every touched 64-token block is requantised: with
+ *     x = code * scale_old (fp32) for the block's earlier tokens and the new keys'
+ *     values, scale = amax / 448 (fp32; 1 when amax is 0) and every code of the
+ *     block becomes RNE_e4m3(x / scale), saturating at +-448.
+ *
  * Input decoding:
  *  - bf16: the 16 bits are the top half of an IEEE binary32 (exact widening).
  *  - e4m3 (OCP 8-bit floating point spec, E4M3): sign, 4 exponent bits with
@@ -71,6 +81,30 @@ double oracle_e4m3_to_f64(uint8_t code) {
     if (e == 0) v = ldexp((double)m, -9);            /* (m/8) * 2^(1-7) */
     else v = ldexp(1.0 + (double)m / 8.0, e - 7);
     return sign ? -v : v;
+}
+
+/* e4m3 encoder (same spec): round to nearest, ties to even, values beyond the
+ * largest finite (448) saturate to it; NaN -> S.1111.111. */
+uint8_t oracle_f32_to_e4m3(float f) {
+    if (isnan(f)) return 0x7F;
+    const uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    const double a = fabs((double)f);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {                    /* subnormal: multiples of 2^-9 */
+        const double m = rint(ldexp(a, 9));      /* 0..8; 8 is the smallest normal, 0x08 */
+        return sign | (uint8_t)m;
+    }
+    int e;
+    frexp(a, &e);                                /* a = f * 2^e, f in [0.5, 1) */
+    int E = e - 1;                               /* a = 1.m * 2^E, E >= -6 */
+    double m = rint((ldexp(a, -E) - 1.0) * 8.0); /* 0..8 */
+    if (m == 8.0) {
+        m = 0.0;
+        E += 1;
+    }
+    int code = ((E + 7) << 3) | (int)m;
+    if (code > 0x7E) code = 0x7E;
+    return sign | (uint8_t)code;
 }
 
 static double f32_at(const void* p, size_t i) { return (double)((const float*)p)[i]; }
@@ -393,4 +427,101 @@ int oracle_sparse_attn(const odims* D, const void* q, const void* kv, const int3
     int rc = run_items(attn_row, &C, T, scratch, threads);
     if (rc) return rc;
     return C.bad ? O_BAD_IDX : O_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* step 0: cache append                                                      */
+/* ------------------------------------------------------------------------- */
+
+/* position of new token t (the sequence's tail when q_pos is NULL: one row per sequence) */
+static int append_pos(const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int t, int* b_out) {
+    const int b = q_seq ? q_seq[t] : t;
+    *b_out = b;
+    return q_pos ? q_pos[t] : seq_lens[b] - 1;
+}
+
+/* k_new[T][d_I] (fp32 in mode 0, bf16 otherwise), kv_new[T][d] (act type); the caches are updated
+ * in place. Rows must name valid sequences, positions inside their block-table rows, and every
+ * block's table entry must be valid (returns O_BAD_ARG otherwise, before writing anything). */
+int oracle_cache_append(const odims* D, const void* k_new, const void* kv_new, const int32_t* block_table,
+                        const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T, void* k_cache,
+                        float* k_scale, void* kv_cache) {
+    if (!check_dims(D) || T < 0 || D->block_size > 1024) return O_BAD_ARG;
+    const int bs = D->block_size;
+    const size_t act = D->mode == 0 ? 4 : 2;
+    const size_t kb = D->mode == 0 ? 4 : (D->mode == 1 ? 2 : 1);
+    for (int t = 0; t < T; ++t) {  /* validate first */
+        int b;
+        const int pos = append_pos(seq_lens, q_seq, q_pos, t, &b);
+        if (b < 0 || b >= D->B || pos < 0 || pos >= seq_lens[b] || pos / bs >= D->max_blocks) return O_BAD_ARG;
+        const int blk = block_table[(int64_t)b * D->max_blocks + pos / bs];
+        if (blk < 0 || blk >= D->num_blocks) return O_BAD_ARG;
+    }
+    /* latent rows, and indexer keys in the fp32 / bf16 modes: copies */
+    for (int t = 0; t < T; ++t) {
+        int b;
+        const int pos = append_pos(seq_lens, q_seq, q_pos, t, &b);
+        const int64_t row = (int64_t)block_table[(int64_t)b * D->max_blocks + pos / bs] * bs + pos % bs;
+        memcpy((char*)kv_cache + row * D->d * act, (const char*)kv_new + (int64_t)t * D->d * act, D->d * act);
+        if (D->mode != 2)
+            memcpy((char*)k_cache + row * D->d_I * kb, (const char*)k_new + (int64_t)t * D->d_I * kb, D->d_I * kb);
+    }
+    if (D->mode != 2) return O_OK;
+    /* FP8 keys: every block that receives new tokens, once (at its first new token) */
+    uint8_t* codes = (uint8_t*)k_cache;
+    const uint16_t* knew = (const uint16_t*)k_new;
+    for (int t = 0; t < T; ++t) {
+        int b;
+        const int pos = append_pos(seq_lens, q_seq, q_pos, t, &b);
+        const int lb = pos / bs;
+        int seen = 0;
+        for (int u = 0; u < t && !seen; ++u) {
+            int b2;
+            const int p2 = append_pos(seq_lens, q_seq, q_pos, u, &b2);
+            seen = (b2 == b && p2 / bs == lb);
+        }
+        if (seen) continue;
+        /* the block's new tokens (slot -> row) and its first new position */
+        int row_of_slot[1024];
+        int first_new = pos;
+        for (int i = 0; i < bs; ++i) row_of_slot[i] = -1;
+        for (int u = 0; u < T; ++u) {
+            int b2;
+            const int p2 = append_pos(seq_lens, q_seq, q_pos, u, &b2);
+            if (b2 == b && p2 / bs == lb) {
+                row_of_slot[p2 % bs] = u;
+                if (p2 < first_new) first_new = p2;
+            }
+        }
+        const int blk = block_table[(int64_t)b * D->max_blocks + lb];
+        const float old_scale = k_scale[blk];
+        const int n_old = first_new - lb * bs; /* earlier tokens of the block: slots [0, n_old) */
+        /* values of the block's tokens (fp32), then amax */
+        float amax = 0.0f;
+        for (int i = 0; i < bs; ++i) {
+            const int u = row_of_slot[i];
+            if (u < 0 && i >= n_old) continue;
+            for (int d = 0; d < D->d_I; ++d) {
+                float x;
+                if (u >= 0) x = (float)oracle_bf16_to_f64(knew[(int64_t)u * D->d_I + d]);
+                else x = (float)oracle_e4m3_to_f64(codes[((int64_t)blk * bs + i) * D->d_I + d]) * old_scale;
+                const float ax = fabsf(x);
+                if (ax > amax) amax = ax;
+            }
+        }
+        const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        for (int i = 0; i < bs; ++i) {
+            const int u = row_of_slot[i];
+            if (u < 0 && i >= n_old) continue;
+            for (int d = 0; d < D->d_I; ++d) {
+                uint8_t* c = &codes[((int64_t)blk * bs + i) * D->d_I + d];
+                float x;
+                if (u >= 0) x = (float)oracle_bf16_to_f64(knew[(int64_t)u * D->d_I + d]);
+                else x = (float)oracle_e4m3_to_f64(*c) * old_scale;
+                *c = oracle_f32_to_e4m3(x / scale);
+            }
+        }
+        k_scale[blk] = scale;
+    }
+    return O_OK;
 }

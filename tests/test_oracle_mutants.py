@@ -8,6 +8,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_append as app
 import test_oracle_pins as pins
 
 SRC = open(oracle._SRC).read()
@@ -29,6 +30,14 @@ MUTANTS = {
     "no_max_shift": ("for (int i = 0; i < n; ++i) { z[i] = exp(z[i] - m); l += z[i]; }",
                      "for (int i = 0; i < n; ++i) { z[i] = exp(z[i]); l += z[i]; }"),
     "kth_off_by_one": ("C->kth[2 * t + 0] = (K - 1 < n) ? a[K - 1].s : NAN;", "C->kth[2 * t + 0] = (K < n) ? a[K].s : NAN;"),
+    "e4m3_encode_truncates": ("double m = rint((ldexp(a, -E) - 1.0) * 8.0); /* 0..8 */",
+                              "double m = floor((ldexp(a, -E) - 1.0) * 8.0); /* 0..8 */"),
+    "e4m3_encode_no_subnormal": ("const double m = rint(ldexp(a, 9));", "const double m = 0.0;"),
+    "append_ignores_earlier_tokens": ("if (u < 0 && i >= n_old) continue;\n            for (int d = 0; d < D->d_I; ++d) {\n                float x;\n                if (u >= 0) x = (float)oracle_bf16_to_f64(knew[(int64_t)u * D->d_I + d]);\n                else x = (float)oracle_e4m3_to_f64(codes[((int64_t)blk * bs + i) * D->d_I + d]) * old_scale;\n                const float ax",
+                                      "if (u < 0) continue;\n            for (int d = 0; d < D->d_I; ++d) {\n                float x;\n                if (u >= 0) x = (float)oracle_bf16_to_f64(knew[(int64_t)u * D->d_I + d]);\n                else x = (float)oracle_e4m3_to_f64(codes[((int64_t)blk * bs + i) * D->d_I + d]) * old_scale;\n                const float ax"),
+    "append_keeps_old_scale": ("const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;", "const float scale = old_scale;"),
+    "append_wrong_slot": ("const int64_t row = (int64_t)block_table[(int64_t)b * D->max_blocks + pos / bs] * bs + pos % bs;",
+                          "const int64_t row = (int64_t)block_table[(int64_t)b * D->max_blocks + pos / bs] * bs + (pos + 1) % bs;"),
 }
 
 PIN_TESTS = [
@@ -40,6 +49,11 @@ PIN_TESTS = [
     pins.test_exact_ties_go_to_lower_position,
     lambda: [pins.test_attention_full_selection_equals_dense_sdpa(m) for m in ("f32", "bf16")],
     pins.test_attention_zero_query_is_mean_of_values,
+    app.test_e4m3_encoder_matches_torch_cast,
+    app.test_append_copies_rows_in_f32_and_bf16,
+    app.test_append_whole_new_block_matches_the_generators_quantisation,
+    app.test_append_requantises_the_earlier_tokens_of_the_block,
+    app.test_append_keeps_codes_when_the_block_scale_does_not_grow,
 ]
 
 
