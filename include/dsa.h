@@ -152,6 +152,33 @@ dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, con
                       size_t ws_bytes, dsa_stream_t stream);
 
 /*
+ * Cache append: writes new tokens' indexer keys and latent rows into their paged slots (the step
+ * before dsa_indexer_topk / dsa_sparse_attn; "How the Ascend Computing Platform Achieves Same-Day
+ * Inference Adaptation ..." §2.2: the cache update is fused with the flow producing the entries;
+ * "Day0 Inference Support ... on Huawei Ascend CANN Architecture" §3: the indexer's keys are
+ * quantised on the way in).
+ *   k_I_new    [T][d_I]   fp32 (DSA_F32) or bf16 (DSA_BF16 and DSA_BF16_KFP8: the values to quantise)
+ *   kv_new     [T][d]     fp32 or bf16 latent rows
+ *   seq_lens   [B]        cached positions per sequence AFTER the append (new tokens included)
+ *   q_seq, q_pos [T]      sequence and position of each new token, as in dsa_indexer_topk (NULL: one
+ *                         token per sequence at position seq_lens - 1)
+ *   k_I_cache, k_I_scale, kv_cache   updated in place (k_I_scale only for DSA_BF16_KFP8)
+ *   ws         any workspace of this library (only its error word is used), ws_bytes >= 256
+ * The new tokens of a sequence are its tail (positions seq_len - n .. seq_len - 1), given as
+ * consecutive rows in ascending position. fp32 / bf16 keys and all latent rows are copied. FP8
+ * keys: every block that receives new tokens is requantised as a whole: with x = code * scale
+ * (fp32) for its earlier tokens and the new keys' values, the block's scale becomes amax / 448
+ * (1 when amax is 0) and each code RNE_e4m3(x / scale), saturating at +-448, all in fp32. Rows
+ * with an invalid sequence, position or block-table entry are skipped and reported through the
+ * error word (DSA_FAULT_INDEX / DSA_FAULT_BLOCK_TABLE). Requires (d * elem) and (d_I * elem) to be
+ * multiples of 16 bytes.
+ */
+dsa_status dsa_cache_append(const dsa_dims* dims, const void* k_I_new, const void* kv_new,
+                            const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
+                            const int32_t* q_pos, int32_t T, void* k_I_cache, float* k_I_scale, void* kv_cache,
+                            void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/*
  * Indexer + Top-K that allocates nothing and takes no workspace: the same computation as
  * dsa_indexer_topk (arguments as there) on its decode-path kernels for every row, with the scratch
  * in one statically sized device buffer inside libdsa.so (DSA_NOALLOC_SCRATCH_BYTES per device).

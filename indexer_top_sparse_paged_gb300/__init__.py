@@ -10,6 +10,8 @@ Entry points (same names as the C ABI):
 * :func:`indexer_topk` -- lightning indexer + Top-K: ``idx[T][K]`` of the selected positions.
 * :func:`sparse_attn` -- sparse attention over the rows ``idx`` selects.
 * :func:`decode` -- both, fused on one stream, for one query row per sequence.
+* :func:`cache_append` -- new tokens' indexer keys and latent rows into the paged caches (FP8 keys:
+  block requantisation).
 * :func:`indexer_topk_noalloc` -- :func:`indexer_topk` with the library's static scratch instead of
   a workspace, for callers that cannot allocate device memory.
 """
@@ -59,6 +61,8 @@ def lib():
         L.dsa_sparse_attn.argtypes = [D, P, P, P, P, P, P, I32, ctypes.c_float, P, P, P, SZ, P]
         L.dsa_decode.restype = ctypes.c_int
         L.dsa_decode.argtypes = [D, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, SZ, P]
+        L.dsa_cache_append.restype = ctypes.c_int
+        L.dsa_cache_append.argtypes = [D, P, P, P, P, P, P, I32, P, P, P, P, SZ, P]
         L.dsa_indexer_topk_noalloc.restype = ctypes.c_int
         L.dsa_indexer_topk_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, I32, P, P, P]
         L.dsa_read_error.restype = ctypes.c_int
@@ -169,6 +173,16 @@ def decode(dims: Dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, q, k
                           ws.numel(), _stream(stream))
     _check("dsa_decode", st)
     return idx, out, lse
+
+
+def cache_append(dims: Dims, k_I_new, kv_new, block_table, seq_lens, k_I_cache, k_I_scale, kv_cache, q_seq=None,
+                 q_pos=None, *, ws, stream=None) -> None:
+    """Writes new tokens (rows of k_I_new / kv_new) into the paged caches in place."""
+    T = kv_new.shape[0]
+    st = lib().dsa_cache_append(ctypes.byref(dims), _p(k_I_new), _p(kv_new), _p(block_table), _p(seq_lens), _p(q_seq),
+                                _p(q_pos), T, _p(k_I_cache), _p(k_I_scale), _p(kv_cache), _p(ws), ws.numel(),
+                                _stream(stream))
+    _check("dsa_cache_append", st)
 
 
 def read_error(ws, stream=None) -> int:

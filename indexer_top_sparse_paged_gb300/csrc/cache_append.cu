@@ -1,0 +1,140 @@
+// Cache append: new tokens' latent rows and indexer keys into their paged slots, the step before
+// the indexer and the sparse attention ("How the Ascend Computing Platform Achieves Same-Day
+// Inference Adaptation ..." §2.2 table: the cache update is fused with the flow that produces the
+// new entries; "Day0 Inference Support ... on Huawei Ascend CANN Architecture" §2.2/§3: the
+// indexer's keys are quantised on the way in).
+//
+// One CTA per new token t (sequence b, position pos in the sequence's tail) copies its latent
+// row, and in the fp32 / bf16 modes its indexer key, into physical row
+// block_table[b][pos / 64] * 64 + pos % 64. With FP8 e4m3 keys (one fp32 scale per 64-token
+// block) the first new token of every touched block requantises the whole block: with
+// x = code * scale_old (fp32) for the block's earlier tokens and the new keys' values,
+// scale = amax / 448 (1 when amax is 0) and every code becomes RNE_e4m3(x / scale), saturating
+// at +-448. The new tokens of one block must be consecutive rows (ascending positions).
+#include "internal.h"
+
+namespace dsa {
+
+constexpr int kAppendThreads = 256;
+
+struct AppendArgs {
+    int mode;
+    int B, max_blocks, num_blocks;
+    int d_I, d;
+    int T;
+    const void* k_new;
+    const void* kv_new;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const int32_t* q_seq;
+    const int32_t* q_pos;
+    void* k_cache;
+    float* k_scale;
+    void* kv_cache;
+    int* err;
+};
+
+// Sequence, position and physical cache block of new token t (-1 when invalid).
+__device__ __forceinline__ int append_block(const AppendArgs& a, int t, int& b, int& pos) {
+    b = a.q_seq ? a.q_seq[t] : t;
+    if (b < 0 || b >= a.B) return -1;
+    const int L = a.seq_lens[b];
+    pos = a.q_pos ? a.q_pos[t] : L - 1;
+    if (pos < 0 || pos >= L || pos / kBlock >= a.max_blocks) return -1;
+    const int blk = a.block_table[static_cast<int64_t>(b) * a.max_blocks + pos / kBlock];
+    return (blk >= 0 && blk < a.num_blocks) ? blk : -1;
+}
+
+__device__ __forceinline__ void copy_row(void* dst, const void* src, int bytes) {
+    const uint4* s = static_cast<const uint4*>(src);
+    uint4* d = static_cast<uint4*>(dst);
+    for (int i = threadIdx.x; i < bytes / 16; i += kAppendThreads) d[i] = s[i];
+}
+
+__device__ __forceinline__ float e4m3_value(uint8_t code) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(code, __NV_E4M3);  // exact
+    return __half2float(*reinterpret_cast<const __half*>(&h));
+}
+
+__global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(AppendArgs a) {
+    __shared__ float red[kAppendThreads / 32];
+    __shared__ int run_end;
+    const int t = blockIdx.x;
+    int b, pos;
+    const int blk = append_block(a, t, b, pos);
+    if (blk < 0) {
+        if (threadIdx.x == 0) atomicOr(a.err, (b < 0 || b >= a.B) ? DSA_FAULT_INDEX : DSA_FAULT_BLOCK_TABLE);
+        return;
+    }
+    const int64_t row = static_cast<int64_t>(blk) * kBlock + pos % kBlock;
+    const int act = a.mode == DSA_F32 ? 4 : 2;
+    copy_row(static_cast<uint8_t*>(a.kv_cache) + row * a.d * act, static_cast<const uint8_t*>(a.kv_new) + static_cast<int64_t>(t) * a.d * act,
+             a.d * act);
+    if (a.mode != DSA_BF16_KFP8) {
+        copy_row(static_cast<uint8_t*>(a.k_cache) + row * a.d_I * act,
+                 static_cast<const uint8_t*>(a.k_new) + static_cast<int64_t>(t) * a.d_I * act, a.d_I * act);
+        return;
+    }
+    // FP8 keys: the first new token of the block requantises it
+    const int lb = pos / kBlock;
+    if (t > 0) {
+        int b0, p0;
+        const int prev = append_block(a, t - 1, b0, p0);
+        if (prev >= 0 && b0 == b && p0 / kBlock == lb) return;
+    }
+    // the block's run of new tokens: rows t .. run_end - 1
+    if (threadIdx.x == 0) run_end = min(a.T, t + kBlock);  // a block holds at most 64 new tokens
+    __syncthreads();
+    if (threadIdx.x < kBlock && threadIdx.x > 0) {
+        const int u = t + static_cast<int>(threadIdx.x);
+        int b2, p2;
+        const bool same = u < a.T && append_block(a, u, b2, p2) >= 0 && b2 == b && p2 / kBlock == lb;
+        if (!same) atomicMin(&run_end, u);
+    }
+    __syncthreads();
+    const int m = run_end - t;
+    const int n_old = pos - lb * kBlock;  // the block's earlier tokens: slots [0, n_old)
+    const float old_scale = a.k_scale[blk];
+    uint8_t* codes = static_cast<uint8_t*>(a.k_cache) + static_cast<int64_t>(blk) * kBlock * a.d_I;
+    const uint16_t* knew = static_cast<const uint16_t*>(a.k_new) + static_cast<int64_t>(t) * a.d_I;
+    const int n_elem_old = n_old * a.d_I, n_elem_new = m * a.d_I;
+    // amax over the earlier tokens (code * old scale) and the new keys
+    float amax = 0.0f;
+    for (int i = threadIdx.x; i < n_elem_old; i += kAppendThreads) amax = fmaxf(amax, fabsf(e4m3_value(codes[i]) * old_scale));
+    for (int i = threadIdx.x; i < n_elem_new; i += kAppendThreads)
+        amax = fmaxf(amax, fabsf(__uint_as_float(static_cast<uint32_t>(knew[i]) << 16)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < kAppendThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    // every code of the block's tokens, re-rounded against the new scale
+    for (int i = threadIdx.x; i < n_elem_old; i += kAppendThreads) {
+        const float x = e4m3_value(codes[i]) * old_scale;
+        codes[i] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(x / scale, __NV_SATFINITE, __NV_E4M3));
+    }
+    for (int i = threadIdx.x; i < n_elem_new; i += kAppendThreads) {
+        const int u = t + i / a.d_I;  // each new row into its own slot
+        const int pu = a.q_pos ? a.q_pos[u] : pos;
+        const float x = __uint_as_float(static_cast<uint32_t>(knew[i]) << 16);
+        codes[(pu % kBlock) * a.d_I + i % a.d_I] =
+            static_cast<uint8_t>(__nv_cvt_float_to_fp8(x / scale, __NV_SATFINITE, __NV_E4M3));
+    }
+    if (threadIdx.x == 0) a.k_scale[blk] = scale;
+}
+
+bool launch_cache_append(const dsa_dims& d, const void* k_new, const void* kv_new, const int32_t* block_table,
+                         const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T, void* k_cache,
+                         float* k_scale, void* kv_cache, int* err, cudaStream_t s, int* launches) {
+    if (T == 0) return true;
+    AppendArgs a{d.mode, d.B, d.max_blocks, d.num_blocks, d.d_I, d.d, T, k_new, kv_new, block_table, seq_lens,
+                 q_seq, q_pos, k_cache, k_scale, kv_cache, err};
+    if (!launch_kernel(false, cache_append_kernel, dim3(T), dim3(kAppendThreads), 0, s, a)) return false;
+    ++*launches;
+    return true;
+}
+
+}  // namespace dsa

@@ -406,6 +406,29 @@ dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const
     return st;
 }
 
+dsa_status dsa_cache_append(const dsa_dims* dims, const void* k_I_new, const void* kv_new,
+                            const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
+                            const int32_t* q_pos, int32_t T, void* k_I_cache, float* k_I_scale, void* kv_cache,
+                            void* ws, size_t ws_bytes, dsa_stream_t stream) {
+    dsa_status st = check_common(dims);
+    if (st != DSA_OK) return st;
+    if (T < 0 || dims->d_I <= 0 || dims->d <= 0) return DSA_ERR_INVALID_ARG;
+    if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
+    if (T > 0 && (!k_I_new || !kv_new || !block_table || !seq_lens || !k_I_cache || !kv_cache)) return DSA_ERR_INVALID_ARG;
+    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    const int act = dims->mode == DSA_F32 ? 4 : 2;
+    if ((dims->d * act) % 16 || (dims->d_I * act) % 16) return DSA_ERR_UNSUPPORTED;
+    if (!aligned16(k_I_new) || !aligned16(kv_new) || !aligned16(k_I_cache) || !aligned16(kv_cache))
+        return DSA_ERR_INVALID_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return DSA_ERR_WORKSPACE;
+    int launches = 0;
+    if (!launch_cache_append(*dims, k_I_new, kv_new, block_table, seq_lens, q_seq, q_pos, T, k_I_cache, k_I_scale,
+                             kv_cache, static_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream), &launches))
+        st = DSA_ERR_LAUNCH;
+    g_last_launches = launches;
+    return st;
+}
+
 dsa_status dsa_read_error(void* ws, int32_t* fault_bits, dsa_stream_t stream) {
     if (!ws) return DSA_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

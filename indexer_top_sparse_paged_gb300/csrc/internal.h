@@ -111,6 +111,9 @@ struct AttnArgs {
 };
 
 bool launch_attn_simt(const AttnArgs& a, cudaStream_t s, int* launches);
+bool launch_cache_append(const dsa_dims& d, const void* k_new, const void* kv_new, const int32_t* block_table,
+                         const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T, void* k_cache,
+                         float* k_scale, void* kv_cache, int* err, cudaStream_t s, int* launches);
 bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches);
 
 }  // namespace dsa
