@@ -392,6 +392,23 @@ def run_ours(args, rank, world):
     if dsa.read_error(ws) != 0:
         raise RuntimeError("device fault bits set during the timed region")
 
+    # --- cache append of the step's new tokens (the step before the path; runs after the decode
+    #     timing because it rewrites the caches in place)
+    rng = np.random.default_rng(77)
+    k_new = to_dev(W.to_bf16_bits(rng.standard_normal((s.T, s.d_I), dtype=np.float32)), dev)
+    kv_new = to_dev(W.to_bf16_bits(rng.standard_normal((s.T, s.d), dtype=np.float32)), dev)
+    app_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        app_ev[i][0].record(stream)
+        dsa.cache_append(dims, k_new, kv_new, bt, sl, k_I, None, kv, ws=ws)
+        app_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if dsa.read_error(ws) != 0:
+        raise RuntimeError("device fault bits set during the cache append")
+    app_us = statistics.mean(a.elapsed_time(b) for a, b in app_ev) * 1e3
+    app_bytes = 2 * s.T * (s.d_I + s.d) * 2  # new rows read + cache rows written (bf16)
+
     ib, ab = indexer_bytes(case), attn_bytes(case)
     step_bytes = ib + ab
     total_ms, e2e_total = reduce_across_ranks([sum(step_ms), sum(e2e_ms)], "max", world, dev)
@@ -429,6 +446,8 @@ def run_ours(args, rank, world):
                 "ms_per_step": round(e2e_total / args.steps, 5)},
         "gpu_launches": launches,
         "clocks": clocks,
+        "cache_append": {"us": round(app_us, 2), "rows": s.T, "bytes": app_bytes,
+                         "note": "dsa_cache_append of the batch's new keys and latent rows (launch-bound at 32 rows)"},
     }
     if not args.no_prefill:
         res["prefill"] = run_prefill(max(3, min(args.steps, 10)), args.warmup, dev, flush)
