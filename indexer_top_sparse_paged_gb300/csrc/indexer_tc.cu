@@ -41,10 +41,13 @@ constexpr uint32_t kIdesc = idesc_f16(128, kHeads, 1u, 0u, 0u);
 constexpr int kF8TileBytes = kTileKeys * kDim;  // e4m3 codes of one tile: 16 KB
 constexpr int kF8BlockBytes = kBlock * kDim;    // one 64-token block: 8 KB
 
-// Shape of the pipelines per key storage.
+constexpr int kRing = 16;  // score tiles between the scoring warps and the Top-K warps (bf16 keys)
+
+// Shape of the pipelines per key storage. bf16 keys: warps 2-5 score, warps 6-9 select (a ring
+// of score tiles between them); FP8 keys: warps 6-9 convert, warps 2-5 score and select.
 template <bool kFp8>
 struct Cfg {
-    static constexpr int kThreads = kFp8 ? 320 : 192;  // + 4 converter warps for FP8 keys
+    static constexpr int kThreads = 320;
     static constexpr int kStages = kFp8 ? 2 : 5;       // bf16 operand stages (32 KB) the MMA reads
     static constexpr int kStages8 = kFp8 ? 6 : 1;      // e4m3 staging stages (16 KB) the TMA fills
     static constexpr size_t kOffA = 0;
@@ -59,11 +62,13 @@ struct Smem {
     uint64_t full8[Cfg<kFp8>::kStages8], empty8[Cfg<kFp8>::kStages8];
     uint64_t qfull, qempty;
     uint64_t tfull[kAcc], tempty[kAcc];
+    uint64_t ring_full[kRing], ring_empty[kRing];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
     uint32_t hist[kEpiThreads / 32 * 256];
     TopkCtl ctl;
+    uint32_t ring_valid[kRing][kEpiThreads / 32];  // validity bits of a ring tile's keys, per warp
 };
 
 constexpr int kTopkPer = 33;  // candidate keys per epilogue thread held in registers while selecting
@@ -72,8 +77,8 @@ __host__ __device__ constexpr uint32_t topk_cap(int K) { return static_cast<uint
 
 template <bool kFp8>
 __host__ __device__ constexpr size_t smem_bytes(int K) {
-    return 1024 /*alignment slack*/ + Cfg<kFp8>::kOffBuf + static_cast<size_t>(topk_cap(K)) * 8 + sizeof(Smem<kFp8>) +
-           64;
+    return 1024 /*alignment slack*/ + Cfg<kFp8>::kOffBuf + static_cast<size_t>(topk_cap(K)) * 8 +
+           (kFp8 ? 0 : static_cast<size_t>(kRing) * kTileKeys * 4) + sizeof(Smem<kFp8>) + 64;
 }
 static_assert(topk_cap(2048) <= static_cast<uint32_t>(kEpiThreads * kTopkPer), "candidate buffer exceeds registers");
 static_assert(smem_bytes<false>(2048) <= kSmemLimit, "indexer shared memory over the limit");
@@ -91,7 +96,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     const uint32_t sQ = smem_u32(smem + C::kOffQ);
     const uint32_t sF8 = smem_u32(smem + C::kOffF8);
     uint64_t* buf = reinterpret_cast<uint64_t*>(smem + C::kOffBuf);
-    Smem<kFp8>& S = *reinterpret_cast<Smem<kFp8>*>(smem + C::kOffBuf + static_cast<size_t>(topk_cap(a.K)) * 8);
+    float* ring = reinterpret_cast<float*>(smem + C::kOffBuf + static_cast<size_t>(topk_cap(a.K)) * 8);  // [kRing][128]
+    Smem<kFp8>& S = *reinterpret_cast<Smem<kFp8>*>(reinterpret_cast<uint8_t*>(ring) +
+                                                   (kFp8 ? 0 : static_cast<size_t>(kRing) * kTileKeys * 4));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -115,6 +122,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         for (int i = 0; i < kAcc; ++i) {
             mbar_init(smem_u32(&S.tfull[i]), 1);
             mbar_init(smem_u32(&S.tempty[i]), kEpiThreads / 32);  // one elected arrive per epilogue warp
+        }
+        if (!kFp8) {
+            for (int i = 0; i < kRing; ++i) {
+                mbar_init(smem_u32(&S.ring_full[i]), kEpiThreads / 32);   // the four scoring warps
+                mbar_init(smem_u32(&S.ring_empty[i]), kEpiThreads / 32);  // the four Top-K warps
+            }
         }
         mbar_init(smem_u32(&S.mma_done), 1);
         S.abort_flag = 0;
@@ -154,14 +167,30 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 const int v = bt[pg];
                 return v;
             };
-            // one query buffer: reload it once the previous segment's MMAs are done with it
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&S.qempty), (sg & 1u) ^ 1u, abort_flag, a.err));
-            if (!ok) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(smem_u32(&S.qfull), kQBytes);
-                tma_load_2d(sQ, &map_q, 0, t * kHeads, smem_u32(&S.qfull));
-                tma_load_2d(sQ + kQHalfBytes, &map_q, 64, t * kHeads, smem_u32(&S.qfull));
-            }
+            // one query buffer, reloaded once the previous segment's MMAs are done with it. The
+            // segment's key tiles do not wait for that: they keep filling the ring while the
+            // previous segment drains, and the query is loaded as soon as its buffer is free
+            // (probed after every tile, waited for at the end of the segment's tiles).
+            bool q_loaded = false;
+            auto load_q = [&](bool block) -> bool {  // warp-uniform; false only on a failed wait
+                if (q_loaded) return true;
+                const uint32_t qe = smem_u32(&S.qempty), par = (sg & 1u) ^ 1u;
+                bool ready = __shfl_sync(0xFFFFFFFFu, mbar_test(qe, par) ? 1 : 0, 0) != 0;
+                if (!ready && block) {
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(qe, par, abort_flag, a.err))) return false;
+                    ready = true;
+                }
+                if (ready) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(smem_u32(&S.qfull), kQBytes);
+                        tma_load_2d(sQ, &map_q, 0, t * kHeads, smem_u32(&S.qfull));
+                        tma_load_2d(sQ + kQHalfBytes, &map_q, 64, t * kHeads, smem_u32(&S.qfull));
+                    }
+                    q_loaded = true;
+                }
+                return true;
+            };
+            load_q(false);
             int w0 = (2 * seg.tile0) & ~31;
             int cur = load_window(w0), nxt = load_window(w0 + 32);
             for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
@@ -172,6 +201,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 }
                 const uint32_t st = n_it % (kFp8 ? kStages8 : kStages), use = n_it / (kFp8 ? kStages8 : kStages);
                 const uint32_t ebar = kFp8 ? smem_u32(&S.empty8[st]) : smem_u32(&S.empty[st]);
+                // a full ring can only drain once the MMA has this segment's query: load it first
+                if (!q_loaded && __shfl_sync(0xFFFFFFFFu, mbar_test(ebar, (use & 1u) ^ 1u) ? 1 : 0, 0) == 0) {
+                    ok = load_q(true);
+                    if (!ok) break;
+                }
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(ebar, (use & 1u) ^ 1u, abort_flag, a.err));
                 if (!ok) break;
                 int blk[2];
@@ -202,7 +236,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                     }
                 }
                 __syncwarp();
+                load_q(false);
             }
+            if (ok) ok = load_q(true);
             ++sg;
         }
     } else if (warp == 1) {
@@ -241,6 +277,98 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             mbar_wait_drain(smem_u32(&S.mma_done), 0, a.err);
         }
         __syncwarp();  // the whole warp reaches the final CTA barrier together
+    } else if (!kFp8 && warp >= 2 && warp < 6) {
+        // ------------------------------------------------------------- scoring (bf16 keys)
+        // Thread = TMEM lane = key row of the tile: S[s] = sum_j w_j max(0, D[s, j]) into ring
+        // slot n_it % kRing with the warp's validity bits; no group barrier, so the tensor
+        // memory is drained at the pace of the stream while the Top-K warps select.
+        const uint32_t quarter = warp & 3;
+        const uint32_t row = quarter * 32 + lane;
+        uint32_t n_it = 0;
+        bool ok = true;
+        while (ok && it.next(seg)) {
+            const int t = seg.row;
+            const int n = row_len(a, t);
+            float wv[kHeads];
+            const float4* w4 = reinterpret_cast<const float4*>(a.w + static_cast<int64_t>(t) * kHeads);
+#pragma unroll
+            for (int i = 0; i < kHeads / 4; ++i) {
+                const float4 v = w4[i];
+                wv[4 * i] = v.x;
+                wv[4 * i + 1] = v.y;
+                wv[4 * i + 2] = v.z;
+                wv[4 * i + 3] = v.w;
+            }
+            const int32_t* bt = a.block_table + static_cast<int64_t>(row_seq(a, t)) * a.max_blocks;
+            for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
+                const uint32_t acc = n_it % kAcc, ause = n_it / kAcc;
+                const uint32_t slot = n_it % kRing, ruse = n_it / kRing;
+                const int s = j * kTileKeys + static_cast<int>(row);
+                const int blk = (s < n) ? bt[s >> 6] : -1;  // issued before the wait: latency hidden
+                const bool valid = s < n && blk >= 0 && blk < a.num_blocks;
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&S.tfull[acc]), ause & 1u, abort_flag, a.err));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t v0[32], v1[32];
+                const uint32_t taddr = tmem + acc * kHeads + ((quarter * 32) << 16);
+                tmem_ld32(taddr, v0);
+                tmem_ld32(taddr + 32, v1);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.tempty[acc]));
+                // four independent partial sums (heads j mod 4) keep the FMA pipe busy
+                float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
+#pragma unroll
+                for (int h = 0; h < 32; h += 4) {
+                    p0 = fmaf(wv[h], fmaxf(__uint_as_float(v0[h]), 0.0f), p0);
+                    p1 = fmaf(wv[h + 1], fmaxf(__uint_as_float(v0[h + 1]), 0.0f), p1);
+                    p2 = fmaf(wv[h + 2], fmaxf(__uint_as_float(v0[h + 2]), 0.0f), p2);
+                    p3 = fmaf(wv[h + 3], fmaxf(__uint_as_float(v0[h + 3]), 0.0f), p3);
+                }
+#pragma unroll
+                for (int h = 0; h < 32; h += 4) {
+                    p0 = fmaf(wv[32 + h], fmaxf(__uint_as_float(v1[h]), 0.0f), p0);
+                    p1 = fmaf(wv[33 + h], fmaxf(__uint_as_float(v1[h + 1]), 0.0f), p1);
+                    p2 = fmaf(wv[34 + h], fmaxf(__uint_as_float(v1[h + 2]), 0.0f), p2);
+                    p3 = fmaf(wv[35 + h], fmaxf(__uint_as_float(v1[h + 3]), 0.0f), p3);
+                }
+                const float score = (p0 + p1) + (p2 + p3);
+                const uint32_t vbits = __ballot_sync(0xFFFFFFFFu, valid);
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&S.ring_empty[slot]), (ruse & 1u) ^ 1u, abort_flag, a.err));
+                if (!ok) break;
+                ring[slot * kTileKeys + row] = score;
+                if (lane == 0) S.ring_valid[slot][quarter] = vbits;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.ring_full[slot]));
+            }
+        }
+    } else if (!kFp8 && warp >= 6) {
+        // ------------------------------------------------------------- Top-K (bf16 keys)
+        // Thread = key row of the tile (TopkGroup index, so stable compaction keeps position
+        // order); consumes the ring's score tiles in the plan's order.
+        const uint32_t row = static_cast<uint32_t>(warp - 6) * 32 + lane;
+        TopkGroup<kEpiThreads, kTopkPer> topk{buf, S.hist, &S.ctl, topk_cap(a.K), static_cast<uint32_t>(a.K), row, 1};
+        uint32_t n_it = 0;
+        while (it.next(seg)) {
+            topk.reset();
+            bool ok = true;
+            for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
+                const uint32_t slot = n_it % kRing, ruse = n_it / kRing;
+                const bool got = mbar_wait(smem_u32(&S.ring_full[slot]), ruse & 1u, abort_flag, a.err);
+                if (named_bar_or(1, kEpiThreads, !got)) { ok = false; break; }
+                const float score = ring[slot * kTileKeys + row];
+                const bool valid = (S.ring_valid[slot][row >> 5] >> (row & 31)) & 1u;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.ring_empty[slot]));
+                const int s = j * kTileKeys + static_cast<int>(row);
+                topk.push(make_key(score, static_cast<uint32_t>(s)), valid);
+            }
+            if (!ok) break;
+            const int64_t slot = static_cast<int64_t>(blockIdx.x) + seg.row;
+            topk.flush(a.slots + slot * a.K, a.slot_count + slot);
+            topk.sync();
+        }
     } else if (kFp8 && warp >= 6) {
         // ------------------------------------------------------------- e4m3 -> bf16 converters
         // Thread r widens key row r of the tile: 8 swizzled 16-byte groups of codes (block r / 64,
@@ -266,8 +394,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 if (lane == 0) mbar_arrive(smem_u32(&S.full[st]));
             }
         }
-    } else {
-        // ------------------------------------------------------------- epilogue + Top-K
+    } else if (kFp8) {
+        // ------------------------------------------------------------- epilogue + Top-K (FP8 keys)
         const uint32_t quarter = warp & 3;             // TMEM lane quarter of this warp
         const uint32_t row = quarter * 32 + lane;      // key within the tile
         // the group's thread index is the key row, so stable compaction keeps position order
