@@ -298,31 +298,31 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(smem_u32(&S.tempty[acc]));
                     }
-                    // four independent partial sums (heads j mod 4) keep the FMA pipe busy
+                    // two packed fp32x2 accumulators (heads j mod 4): one paired FMA per two heads
                     const float4* w4 = reinterpret_cast<const float4*>(sW + q * kHeads);
-                    float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
+                    float2 pa = make_float2(0.0f, 0.0f), pb = make_float2(0.0f, 0.0f);
                     if (!kFp8 || sc >= 0.0f) {
 #pragma unroll
                         for (int h = 0; h < 16; ++h) {
                             const float4 wv = w4[h];
                             const uint32_t* v = h < 8 ? v0 + 4 * h : v1 + 4 * (h - 8);
-                            p0 = fmaf(wv.x, fmaxf(__uint_as_float(v[0]), 0.0f), p0);
-                            p1 = fmaf(wv.y, fmaxf(__uint_as_float(v[1]), 0.0f), p1);
-                            p2 = fmaf(wv.z, fmaxf(__uint_as_float(v[2]), 0.0f), p2);
-                            p3 = fmaf(wv.w, fmaxf(__uint_as_float(v[3]), 0.0f), p3);
+                            pa = __ffma2_rn(make_float2(wv.x, wv.y),
+                                            make_float2(fmaxf(__uint_as_float(v[0]), 0.0f), fmaxf(__uint_as_float(v[1]), 0.0f)), pa);
+                            pb = __ffma2_rn(make_float2(wv.z, wv.w),
+                                            make_float2(fmaxf(__uint_as_float(v[2]), 0.0f), fmaxf(__uint_as_float(v[3]), 0.0f)), pb);
                         }
                     } else {  // scale < 0: max(0, scale * x) = scale * min(0, x)
 #pragma unroll
                         for (int h = 0; h < 16; ++h) {
                             const float4 wv = w4[h];
                             const uint32_t* v = h < 8 ? v0 + 4 * h : v1 + 4 * (h - 8);
-                            p0 = fmaf(wv.x, fminf(__uint_as_float(v[0]), 0.0f), p0);
-                            p1 = fmaf(wv.y, fminf(__uint_as_float(v[1]), 0.0f), p1);
-                            p2 = fmaf(wv.z, fminf(__uint_as_float(v[2]), 0.0f), p2);
-                            p3 = fmaf(wv.w, fminf(__uint_as_float(v[3]), 0.0f), p3);
+                            pa = __ffma2_rn(make_float2(wv.x, wv.y),
+                                            make_float2(fminf(__uint_as_float(v[0]), 0.0f), fminf(__uint_as_float(v[1]), 0.0f)), pa);
+                            pb = __ffma2_rn(make_float2(wv.z, wv.w),
+                                            make_float2(fminf(__uint_as_float(v[2]), 0.0f), fminf(__uint_as_float(v[3]), 0.0f)), pb);
                         }
                     }
-                    float score = (p0 + p1) + (p2 + p3);
+                    float score = (pa.x + pb.x) + (pa.y + pb.y);
                     if (kFp8) score *= sc;
                     if (s < nq[q]) srow[q * lmax + s] = blk_ok ? score : __uint_as_float(0x7FC00000u);
                 }
