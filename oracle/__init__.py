@@ -17,6 +17,10 @@ return NumPy arrays:
 * :func:`sparse_attn` -- fp64 ``out[t, h, :d_v]``, ``lse[t, h]`` and the sum of
   the softmax weights, over the rows ``idx`` selects (lightweight indexer page
   §1, "sparse flash attention").
+* :func:`block_summaries`, :func:`summary_case`, :func:`hierarchical_topk` --
+  hierarchical (coarse -> fine) selection: blocks shortlisted by the indexer
+  score of their mean key, then the indexer's Top-K over the tokens of the
+  shortlisted blocks (Day-0 accelerator page §3.1; adaptation page §3.1).
 * :func:`cache_append` -- the caches after writing new tokens' indexer keys and
   latent rows into their paged slots (FP8 keys: block requantisation), the step
   before the path (Ascend adaptation page §2.2, cache-update flow).
@@ -71,6 +75,8 @@ def _bind(lib):
     lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
     lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
     lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+    lib.oracle_block_summaries.restype = ctypes.c_int
+    lib.oracle_block_summaries.argtypes = [ctypes.POINTER(ODims), P, P, P, P, P]
     lib.oracle_cache_append.restype = ctypes.c_int
     lib.oracle_cache_append.argtypes = [ctypes.POINTER(ODims), P, P, P, P, P, P, ctypes.c_int, P, P, P]
     lib.oracle_index_scores.restype = ctypes.c_int
@@ -207,3 +213,63 @@ def cache_append(case, k_new, kv_new, rows=None):
     if rc:
         raise RuntimeError(f"oracle_cache_append failed: {rc}")
     return k_I, scale, kv
+
+
+def block_summaries(case) -> np.ndarray:
+    """bf16 bits [B][max_blocks][d_I]: the mean key of every valid 64-token block (zeros elsewhere)."""
+    lib = _load()
+    s = case.spec
+    out = np.zeros((s.B, case.max_blocks, s.d_I), dtype=np.uint16)
+    kdt = {"f32": np.float32, "bf16": np.uint16, "bf16_kfp8": np.uint8}[s.mode]
+    keep = [_c(case.k_I, kdt), _c(case.k_I_scale, np.float32), _c(case.block_table, np.int32),
+            _c(case.seq_lens, np.int32)]
+    rc = lib.oracle_block_summaries(ctypes.byref(dims_of(case)), *[_ptr(a) for a in keep], _ptr(out))
+    if rc:
+        raise RuntimeError(f"oracle_block_summaries failed: {rc}")
+    return out
+
+
+def summary_case(case, summaries, n_sel: int):
+    """The coarse stage as an indexer problem: sequence b's block summaries are its "keys" at
+    logical positions 0..ceil(L_b/64)-1, stored densely (64 summaries per summary block), with a
+    query row at position pos(t) // 64 and Top-K = n_sel."""
+    import types
+    s = case.spec
+    bs = s.block_size
+    mb2 = (case.max_blocks + bs - 1) // bs
+    lens = ((case.seq_lens.astype(np.int64) + bs - 1) // bs).astype(np.int32)
+    keys = np.zeros((s.B * mb2 * bs, s.d_I), dtype=np.uint16)
+    keys.reshape(s.B, mb2 * bs, s.d_I)[:, : case.max_blocks] = summaries
+    table = (np.arange(s.B)[:, None] * mb2 + np.arange(mb2)[None, :]).astype(np.int32)
+    spec2 = types.SimpleNamespace(mode="bf16", B=s.B, T=s.T, H_I=s.H_I, d_I=s.d_I, H=s.H, d=s.d, d_v=s.d_v, K=n_sel,
+                                  block_size=bs, sm_scale=s.sm_scale, new_tokens=s.new_tokens)
+    return types.SimpleNamespace(spec=spec2, block_table=table, seq_lens=lens, q_seq=case.q_seq,
+                                 q_pos=(case.q_pos // bs).astype(np.int32), q_I=case.q_I, w=case.w,
+                                 k_I=keys.reshape(s.B * mb2, bs, s.d_I), k_I_scale=None, max_blocks=mb2,
+                                 num_blocks=s.B * mb2, q=case.q, kv=case.kv)
+
+
+def hierarchical_topk(case, n_sel: int, rows=None, threads=None):
+    """(idx[r, K] ascending positions -1 padded, blocks[r, n_sel] ascending logical blocks -1 padded)
+    of hierarchical selection: the n_sel blocks with the largest summary scores (ties to the lower
+    block), then the K largest token scores (ties to the lower position) among the tokens of those
+    blocks inside the causal prefix."""
+    s = case.spec
+    bs = s.block_size
+    sel = np.arange(s.T) if rows is None else np.asarray(rows)
+    summ = block_summaries(case)
+    c2 = summary_case(case, summ, n_sel)
+    bidx, _ = indexer_topk(c2, rows=sel, threads=threads)
+    S = index_scores(case, rows=sel, threads=threads)
+    idx = np.full((len(sel), s.K), -1, np.int32)
+    blocks = np.full((len(sel), n_sel), -1, np.int32)
+    for r, t in enumerate(sel):
+        n = int(case.q_pos[t]) + 1
+        bl = np.sort(bidx[r][bidx[r] >= 0])
+        blocks[r, : len(bl)] = bl
+        pos = np.concatenate([np.arange(b * bs, min((b + 1) * bs, n)) for b in bl]) if len(bl) else np.zeros(0, np.int64)
+        sc = S[r, pos]
+        order = np.lexsort((pos, -sc))[: s.K]
+        chosen = np.sort(pos[order])
+        idx[r, : len(chosen)] = chosen
+    return idx, blocks

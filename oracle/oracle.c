@@ -28,6 +28,13 @@
  *     over the valid (!= -1) entries of idx[t]; V is the first d_v columns of
  *     the same shared latent row.  No valid entry -> out = 0, lse = -inf.
  *
+ *  H. Hierarchical selection (coarse -> fine, Day-0 accelerator page §3.1 and the
+ *     adaptation page §3.1: blocks shortlisted by summary scores, then fine
+ *     filtering inside them): a block's summary key is the mean of its valid
+ *     keys (fp32 sum in token order, fp32 division by the count, bf16 round to
+ *     nearest even); the coarse stage is the indexer over the summaries, the
+ *     fine stage the indexer over the tokens of the chosen blocks.  This file
+ *     holds the summary; the two stages reuse steps 1-3 (oracle/__init__.py).
  *  0. Cache append (the step before the path: "Residual and normalization ...
  *     fused with the cache-update flow", Ascend adaptation page §2.2 table; the
  *     indexer prolog quantises keys, Ascend CANN page §2.2/§3): each new token t
@@ -522,6 +529,49 @@ int oracle_cache_append(const odims* D, const void* k_new, const void* kv_new, c
             }
         }
         k_scale[blk] = scale;
+    }
+    return O_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* hierarchical selection: block summaries                                   */
+/* ------------------------------------------------------------------------- */
+
+/* fp32 -> bf16 bits, round to nearest even (finite inputs) */
+static uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    const uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* summaries[b][lb][d] (bf16 bits) for every logical block lb < ceil(seq_lens[b] / bs): the mean
+ * over the block's valid tokens (fp32 sum in token order, fp32 division, bf16 RNE). Blocks past a
+ * sequence's end are left untouched. */
+int oracle_block_summaries(const odims* D, const void* k_I, const float* k_I_scale, const int32_t* block_table,
+                           const int32_t* seq_lens, uint16_t* summaries) {
+    if (!check_dims(D)) return O_BAD_ARG;
+    const int bs = D->block_size;
+    for (int b = 0; b < D->B; ++b) {
+        const int L = seq_lens[b];
+        for (int lb = 0; lb * bs < L && lb < D->max_blocks; ++lb) {
+            const int blk = block_table[(int64_t)b * D->max_blocks + lb];
+            if (blk < 0 || blk >= D->num_blocks) return O_BAD_ARG;
+            const int cnt = (L - lb * bs) < bs ? (L - lb * bs) : bs;
+            for (int d = 0; d < D->d_I; ++d) {
+                float acc = 0.0f;
+                for (int i = 0; i < cnt; ++i) {
+                    const size_t e = ((size_t)blk * bs + i) * D->d_I + d;
+                    float x;
+                    if (D->mode == 0) x = ((const float*)k_I)[e];
+                    else if (D->mode == 1) x = (float)oracle_bf16_to_f64(((const uint16_t*)k_I)[e]);
+                    else x = (float)oracle_e4m3_to_f64(((const uint8_t*)k_I)[e]) * k_I_scale[blk];
+                    acc = acc + x;
+                }
+                summaries[((size_t)b * D->max_blocks + lb) * D->d_I + d] = f32_to_bf16_rne(acc / (float)cnt);
+            }
+        }
     }
     return O_OK;
 }

@@ -9,6 +9,7 @@ import pytest
 
 import oracle
 import test_oracle_append as app
+import test_oracle_hier as hier
 import test_oracle_pins as pins
 
 SRC = open(oracle._SRC).read()
@@ -35,6 +36,9 @@ MUTANTS = {
     "e4m3_encode_no_subnormal": ("const double m = rint(ldexp(a, 9));", "const double m = 0.0;"),
     "append_ignores_earlier_tokens": ("if (u < 0 && i >= n_old) continue;\n            for (int d = 0; d < D->d_I; ++d) {\n                float x;\n                if (u >= 0) x = (float)oracle_bf16_to_f64(knew[(int64_t)u * D->d_I + d]);\n                else x = (float)oracle_e4m3_to_f64(codes[((int64_t)blk * bs + i) * D->d_I + d]) * old_scale;\n                const float ax",
                                       "if (u < 0) continue;\n            for (int d = 0; d < D->d_I; ++d) {\n                float x;\n                if (u >= 0) x = (float)oracle_bf16_to_f64(knew[(int64_t)u * D->d_I + d]);\n                else x = (float)oracle_e4m3_to_f64(codes[((int64_t)blk * bs + i) * D->d_I + d]) * old_scale;\n                const float ax"),
+    "summary_divides_by_block_size": ("f32_to_bf16_rne(acc / (float)cnt);", "f32_to_bf16_rne(acc / (float)bs);"),
+    "summary_skips_last_token": ("for (int i = 0; i < cnt; ++i) {\n                    const size_t e = ((size_t)blk * bs + i) * D->d_I + d;",
+                                 "for (int i = 0; i + 1 < cnt; ++i) {\n                    const size_t e = ((size_t)blk * bs + i) * D->d_I + d;"),
     "append_keeps_old_scale": ("const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;", "const float scale = old_scale;"),
     "append_wrong_slot": ("const int64_t row = (int64_t)block_table[(int64_t)b * D->max_blocks + pos / bs] * bs + pos % bs;",
                           "const int64_t row = (int64_t)block_table[(int64_t)b * D->max_blocks + pos / bs] * bs + (pos + 1) % bs;"),
@@ -54,6 +58,8 @@ PIN_TESTS = [
     app.test_append_whole_new_block_matches_the_generators_quantisation,
     app.test_append_requantises_the_earlier_tokens_of_the_block,
     app.test_append_keeps_codes_when_the_block_scale_does_not_grow,
+    lambda: [hier.test_summaries_match_sequential_numpy_mean(m) for m in ("f32", "bf16", "bf16_kfp8")],
+    hier.test_planted_block_is_chosen,
 ]
 
 
