@@ -179,6 +179,41 @@ dsa_status dsa_cache_append(const dsa_dims* dims, const void* k_I_new, const voi
                             void* ws, size_t ws_bytes, dsa_stream_t stream);
 
 /*
+ * Hierarchical (coarse -> fine) index selection ("Engineering Path for Day-0 Adaptation ..." §3.1:
+ * coarse filtering at block granularity followed by refinement; "How the Ascend Computing
+ * Platform Achieves Same-Day Inference Adaptation ..." §3.1: the coarse filter reuses summary
+ * information held in the cache, the fine filter computes only within the candidate blocks).
+ * A variant of dsa_indexer_topk that reads one summary key per 64-token block plus the keys of
+ * n_sel chosen blocks per row instead of every key; its result is the method's own, not the
+ * exact Top-K (they agree when n_sel covers every block).
+ *
+ * dsa_block_summaries: summaries [B][pages * 64][d_I] bf16, pages = ceil(max_blocks / 64): row
+ *   b * pages * 64 + lb of every valid logical block lb of sequence b (lb < ceil(seq_len / 64))
+ *   receives the mean of the block's valid keys -- fp32 sum in token order of the keys' values
+ *   (FP8: code * block scale in fp32), fp32 division by the count, bf16 round to nearest even.
+ *   Other rows are not written. Any workspace with ws_bytes >= 256 (only its error word is used).
+ * dsa_indexer_topk_hier: arguments as dsa_indexer_topk (bf16 modes only; DSA_F32 gives
+ *   DSA_ERR_UNSUPPORTED), plus the summaries and n_sel (1..2048):
+ *   1. coarse: the n_sel blocks with the largest indexer score of their summary (the indexer
+ *      formula with the summary as the key; ties to the lower block) among the blocks
+ *      0 .. pos(t) / 64 of the row's sequence;
+ *   2. fine: the K largest indexer scores (ties to the lower position) among the tokens of the
+ *      chosen blocks with s <= pos(t).
+ *   idx [T][K] ascending positions then -1; blocks_out [T][n_sel] (optional) the chosen logical
+ *   blocks ascending then -1. ws of at least dsa_hier_workspace_size(dims, T, n_sel) bytes,
+ *   initialised with dsa_workspace_init.
+ */
+size_t dsa_hier_workspace_size(const dsa_dims* dims, int32_t T, int32_t n_sel);
+dsa_status dsa_block_summaries(const dsa_dims* dims, const void* k_I_cache, const float* k_I_scale,
+                               const int32_t* block_table, const int32_t* seq_lens, uint16_t* summaries, void* ws,
+                               size_t ws_bytes, dsa_stream_t stream);
+dsa_status dsa_indexer_topk_hier(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+                                 const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                                 const int32_t* q_seq, const int32_t* q_pos, int32_t T, const uint16_t* summaries,
+                                 int32_t n_sel, int32_t* idx, int32_t* blocks_out, void* ws, size_t ws_bytes,
+                                 dsa_stream_t stream);
+
+/*
  * Indexer + Top-K that allocates nothing and takes no workspace: the same computation as
  * dsa_indexer_topk (arguments as there) on its decode-path kernels for every row, with the scratch
  * in one statically sized device buffer inside libdsa.so (DSA_NOALLOC_SCRATCH_BYTES per device).

@@ -12,6 +12,8 @@ Entry points (same names as the C ABI):
 * :func:`decode` -- both, fused on one stream, for one query row per sequence.
 * :func:`cache_append` -- new tokens' indexer keys and latent rows into the paged caches (FP8 keys:
   block requantisation).
+* :func:`block_summaries`, :func:`indexer_topk_hier` -- hierarchical (coarse -> fine) selection over
+  per-block summary keys.
 * :func:`indexer_topk_noalloc` -- :func:`indexer_topk` with the library's static scratch instead of
   a workspace, for callers that cannot allocate device memory.
 """
@@ -61,6 +63,12 @@ def lib():
         L.dsa_sparse_attn.argtypes = [D, P, P, P, P, P, P, I32, ctypes.c_float, P, P, P, SZ, P]
         L.dsa_decode.restype = ctypes.c_int
         L.dsa_decode.argtypes = [D, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, SZ, P]
+        L.dsa_hier_workspace_size.restype = SZ
+        L.dsa_hier_workspace_size.argtypes = [D, I32, I32]
+        L.dsa_block_summaries.restype = ctypes.c_int
+        L.dsa_block_summaries.argtypes = [D, P, P, P, P, P, P, SZ, P]
+        L.dsa_indexer_topk_hier.restype = ctypes.c_int
+        L.dsa_indexer_topk_hier.argtypes = [D, P, P, P, P, P, P, P, P, I32, P, I32, P, P, P, SZ, P]
         L.dsa_cache_append.restype = ctypes.c_int
         L.dsa_cache_append.argtypes = [D, P, P, P, P, P, P, I32, P, P, P, P, SZ, P]
         L.dsa_indexer_topk_noalloc.restype = ctypes.c_int
@@ -183,6 +191,45 @@ def cache_append(dims: Dims, k_I_new, kv_new, block_table, seq_lens, k_I_cache, 
                                 _p(q_pos), T, _p(k_I_cache), _p(k_I_scale), _p(kv_cache), _p(ws), ws.numel(),
                                 _stream(stream))
     _check("dsa_cache_append", st)
+
+
+def summaries_buffer(dims: Dims, device="cuda") -> torch.Tensor:
+    """A bf16 [B][pages * 64][d_I] tensor for dsa_block_summaries (pages = ceil(max_blocks / 64))."""
+    pages = (dims.max_blocks + 63) // 64
+    return torch.zeros((dims.B, pages * 64, dims.d_I), dtype=torch.bfloat16, device=device)
+
+
+def block_summaries(dims: Dims, k_I_cache, k_I_scale, block_table, seq_lens, summaries, *, ws, stream=None) -> None:
+    """Writes the mean key of every valid 64-token block into ``summaries``."""
+    st = lib().dsa_block_summaries(ctypes.byref(dims), _p(k_I_cache), _p(k_I_scale), _p(block_table), _p(seq_lens),
+                                   _p(summaries), _p(ws), ws.numel(), _stream(stream))
+    _check("dsa_block_summaries", st)
+
+
+def hier_workspace(dims: Dims, T: int, n_sel: int, device="cuda", stream=None) -> torch.Tensor:
+    n = int(lib().dsa_hier_workspace_size(ctypes.byref(dims), T, n_sel))
+    if n == 0:
+        raise ValueError("invalid dims")
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off: off + n]
+    _check("dsa_workspace_init", lib().dsa_workspace_init(_p(ws), n, _stream(stream)))
+    return ws
+
+
+def indexer_topk_hier(dims: Dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, summaries, n_sel: int,
+                      q_seq=None, q_pos=None, *, ws, idx=None, blocks=None, stream=None):
+    """(idx[T][K], blocks[T][n_sel]) of hierarchical selection (coarse blocks, then fine tokens)."""
+    T = q_I.shape[0]
+    if idx is None:
+        idx = torch.empty((T, dims.K), dtype=torch.int32, device=q_I.device)
+    if blocks is None:
+        blocks = torch.empty((T, n_sel), dtype=torch.int32, device=q_I.device)
+    st = lib().dsa_indexer_topk_hier(ctypes.byref(dims), _p(q_I), _p(w), _p(k_I_cache), _p(k_I_scale), _p(block_table),
+                                     _p(seq_lens), _p(q_seq), _p(q_pos), T, _p(summaries), n_sel, _p(idx), _p(blocks),
+                                     _p(ws), ws.numel(), _stream(stream))
+    _check("dsa_indexer_topk_hier", st)
+    return idx, blocks
 
 
 def read_error(ws, stream=None) -> int:

@@ -289,6 +289,59 @@ static void* noalloc_scratch() {
     return g_noalloc_base[dev];
 }
 
+// ------------------------------------------------------------------------------------------------
+// hierarchical selection: the coarse and fine problems and the workspace that holds both
+// ------------------------------------------------------------------------------------------------
+
+struct HierLayout {
+    dsa_dims coarse, fine;
+    int pages;            // summary pages per sequence: ceil(max_blocks / 64)
+    size_t coarse_ws;     // at offset 0: its error word is the call's
+    size_t coarse_table;  // int32 [B][pages]
+    size_t coarse_lens;   // int32 [B]
+    size_t coarse_pos;    // int32 [T]
+    size_t bidx;          // int32 [T][n_sel] chosen blocks
+    size_t vtable;        // int32 [T][n_sel] virtual block tables
+    size_t vlen;          // int32 [T]
+    size_t vidx;          // int32 [T][K] fine Top-K in virtual positions
+    size_t fine_ws;
+    size_t total;
+};
+
+static HierLayout hier_layout(const dsa_dims& d, int T, int n_sel) {
+    HierLayout h{};
+    h.pages = (d.max_blocks + kBlock - 1) / kBlock;
+    h.coarse = d;
+    h.coarse.mode = DSA_BF16;
+    h.coarse.max_blocks = h.pages;
+    h.coarse.num_blocks = d.B * h.pages;
+    h.coarse.K = n_sel;
+    h.fine = d;
+    h.fine.B = T;
+    h.fine.max_blocks = n_sel;
+    size_t off = 0;
+    h.coarse_ws = off;
+    off = align256(off + ws_layout(h.coarse, T).total);
+    h.coarse_table = off;
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(d.B) * h.pages);
+    h.coarse_lens = off;
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(d.B));
+    h.coarse_pos = off;
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(T));
+    h.bidx = off;
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(T) * n_sel);
+    h.vtable = off;
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(T) * n_sel);
+    h.vlen = off;
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(T));
+    h.vidx = off;
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(T) * d.K);
+    h.fine_ws = off;
+    off = align256(off + (T > 0 ? ws_layout(h.fine, T).total : 256));
+    h.total = off;
+    return h;
+}
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -427,6 +480,71 @@ dsa_status dsa_cache_append(const dsa_dims* dims, const void* k_I_new, const voi
         st = DSA_ERR_LAUNCH;
     g_last_launches = launches;
     return st;
+}
+
+size_t dsa_hier_workspace_size(const dsa_dims* dims, int32_t T, int32_t n_sel) {
+    if (!dims || T <= 0 || n_sel <= 0 || n_sel > 2048 || check_common(dims) != DSA_OK) return 0;
+    return hier_layout(*dims, T, n_sel).total;
+}
+
+dsa_status dsa_block_summaries(const dsa_dims* dims, const void* k_I_cache, const float* k_I_scale,
+                               const int32_t* block_table, const int32_t* seq_lens, uint16_t* summaries, void* ws,
+                               size_t ws_bytes, dsa_stream_t stream) {
+    dsa_status st = check_common(dims);
+    if (st != DSA_OK) return st;
+    if (dims->d_I <= 0) return DSA_ERR_INVALID_ARG;
+    if (!k_I_cache || !block_table || !seq_lens || !summaries) return DSA_ERR_INVALID_ARG;
+    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return DSA_ERR_WORKSPACE;
+    int launches = 0;
+    if (!launch_block_summaries(*dims, k_I_cache, k_I_scale, block_table, seq_lens, summaries, static_cast<int*>(ws),
+                                reinterpret_cast<cudaStream_t>(stream), &launches))
+        st = DSA_ERR_LAUNCH;
+    g_last_launches = launches;
+    return st;
+}
+
+dsa_status dsa_indexer_topk_hier(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+                                 const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                                 const int32_t* q_seq, const int32_t* q_pos, int32_t T, const uint16_t* summaries,
+                                 int32_t n_sel, int32_t* idx, int32_t* blocks_out, void* ws, size_t ws_bytes,
+                                 dsa_stream_t stream) {
+    dsa_status st = check_indexer_dims(dims);
+    if (st != DSA_OK) return st;
+    if (dims->mode == DSA_F32) return DSA_ERR_UNSUPPORTED;  // the coarse stage scores bf16 summaries with bf16 q_I
+    if (T < 0 || n_sel <= 0 || n_sel > 2048) return DSA_ERR_INVALID_ARG;
+    if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
+    if (T == 0) return DSA_OK;
+    if (!q_I || !w || !k_I_cache || !block_table || !seq_lens || !summaries || !idx) return DSA_ERR_INVALID_ARG;
+    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_I) || !aligned16(w) || !aligned16(k_I_cache) || !aligned16(summaries)) return DSA_ERR_INVALID_ARG;
+    const HierLayout H = hier_layout(*dims, T, n_sel);
+    if (check_indexer_dims(&H.coarse) != DSA_OK) return DSA_ERR_UNSUPPORTED;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < H.total) return DSA_ERR_WORKSPACE;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    auto at = [&](size_t off) { return reinterpret_cast<int32_t*>(base + off); };
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int launches = 0;
+    int* fine_err = reinterpret_cast<int*>(base + H.fine_ws);
+    if (!launch_hier_setup(dims->B, H.pages, T, seq_lens, q_seq, q_pos, at(H.coarse_table), at(H.coarse_lens),
+                           at(H.coarse_pos), fine_err, s, &launches))
+        return DSA_ERR_LAUNCH;
+    // coarse: the indexer over the summaries, Top-n_sel blocks per row
+    st = run_indexer(&H.coarse, q_I, w, summaries, nullptr, at(H.coarse_table), at(H.coarse_lens), q_seq,
+                     at(H.coarse_pos), T, at(H.bidx), base + H.coarse_ws, s, &launches);
+    if (st != DSA_OK) return st;
+    if (!launch_hier_virtualize(dims->B, dims->max_blocks, n_sel, T, block_table, seq_lens, q_seq, q_pos, at(H.bidx),
+                                at(H.vtable), at(H.vlen), blocks_out, s, &launches))
+        return DSA_ERR_LAUNCH;
+    // fine: the indexer over the tokens of the chosen blocks (one virtual sequence per row)
+    st = run_indexer(&H.fine, q_I, w, k_I_cache, k_I_scale, at(H.vtable), at(H.vlen), nullptr, nullptr, T, at(H.vidx),
+                     base + H.fine_ws, s, &launches);
+    if (st != DSA_OK) return st;
+    if (!launch_hier_remap(T, n_sel, dims->K, at(H.bidx), at(H.vidx), idx, fine_err, reinterpret_cast<int*>(base), s,
+                           &launches))
+        return DSA_ERR_LAUNCH;
+    g_last_launches = launches;
+    return DSA_OK;
 }
 
 dsa_status dsa_read_error(void* ws, int32_t* fault_bits, dsa_stream_t stream) {

@@ -111,6 +111,16 @@ struct AttnArgs {
 };
 
 bool launch_attn_simt(const AttnArgs& a, cudaStream_t s, int* launches);
+bool launch_block_summaries(const dsa_dims& d, const void* k_I, const float* k_scale, const int32_t* block_table,
+                            const int32_t* seq_lens, uint16_t* summaries, int* err, cudaStream_t s, int* launches);
+bool launch_hier_setup(int B, int pages, int T, const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos,
+                       int32_t* coarse_table, int32_t* coarse_lens, int32_t* coarse_pos, int* fine_err, cudaStream_t s,
+                       int* launches);
+bool launch_hier_virtualize(int B, int max_blocks, int n_sel, int T, const int32_t* block_table,
+                            const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, const int32_t* bidx,
+                            int32_t* vtable, int32_t* vlen, int32_t* blocks_out, cudaStream_t s, int* launches);
+bool launch_hier_remap(int T, int n_sel, int K, const int32_t* bidx, const int32_t* vidx, int32_t* idx, int* fine_err,
+                       int* err, cudaStream_t s, int* launches);
 bool launch_cache_append(const dsa_dims& d, const void* k_new, const void* kv_new, const int32_t* block_table,
                          const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T, void* k_cache,
                          float* k_scale, void* kv_cache, int* err, cudaStream_t s, int* launches);
