@@ -418,6 +418,7 @@ struct IndexerArgs {
     int32_t* gemm_tile_prefix;  // [NG + 1] 128-key tiles of the GEMM groups before group g
     float* scores;              // [T][max_blocks * 64] fp32 scores of the GEMM rows (NaN: excluded)
     int G2;                     // score GEMM CTAs
+    int self_plan;              // 1: the decode indexer computes the work plan itself (no plan kernel)
 };
 
 // Is query row t scored by the prefill GEMM (written by the plan)?

@@ -221,7 +221,9 @@ static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w
     a.gemm_tile_prefix = reinterpret_cast<int32_t*>(base + L.gemm_tile_prefix);
     a.scores = reinterpret_cast<float*>(base + L.scores);
     a.G2 = device_sm_count();
-    if (!launch_plan(a, stream, launches)) return DSA_ERR_LAUNCH;
+    // decode calls on the tensor-core indexer plan inside its kernel (no plan kernel, no gap)
+    a.self_plan = (a.NG == 0 && indexer_uses_tc(*d) && T <= kSelfPlanRows) ? 1 : 0;
+    if (!a.self_plan && !launch_plan(a, stream, launches)) return DSA_ERR_LAUNCH;
     if (a.NG > 0 && !launch_indexer_prefill(a, stream, launches)) return DSA_ERR_LAUNCH;
     const bool ok = indexer_uses_tc(*d) ? launch_indexer_tc(a, stream, launches) : launch_indexer_simt(a, stream, launches);
     if (!ok) return DSA_ERR_LAUNCH;

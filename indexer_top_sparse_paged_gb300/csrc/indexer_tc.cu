@@ -75,10 +75,80 @@ constexpr int kTopkPer = 33;  // candidate keys per epilogue thread held in regi
 constexpr size_t kSmemLimit = 232448;
 __host__ __device__ constexpr uint32_t topk_cap(int K) { return static_cast<uint32_t>(2 * K + kEpiThreads); }
 
+constexpr size_t kPlanBytes = (kSelfPlanRows + 1) * sizeof(int32_t);  // the work plan, when computed in the kernel
+
 template <bool kFp8>
 __host__ __device__ constexpr size_t smem_bytes(int K) {
     return 1024 /*alignment slack*/ + Cfg<kFp8>::kOffBuf + static_cast<size_t>(topk_cap(K)) * 8 +
-           (kFp8 ? 0 : static_cast<size_t>(kRing) * kTileKeys * 4) + sizeof(Smem<kFp8>) + 64;
+           (kFp8 ? 0 : static_cast<size_t>(kRing) * kTileKeys * 4) + sizeof(Smem<kFp8>) + kPlanBytes + 64;
+}
+
+// Exclusive scan of v over the CTA (in thread order) and the total; `sums` holds one int per warp.
+template <int NT>
+__device__ __forceinline__ int cta_scan(int v, int* sums, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sums[warp] = x;
+    block_sync();
+    int before = 0;
+    total = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        const int c = sums[w];
+        before += (w < warp) ? c : 0;
+        total += c;
+    }
+    block_sync();
+    return before + x - v;
+}
+
+// The decode work plan computed by every CTA into shared memory (plan[t] = tiles of the rows
+// before t); CTA 0 also publishes it with the rows' merge groups and clears the merge counters,
+// as the plan kernel would.
+template <int NT>
+__device__ void self_plan(const IndexerArgs& a, int32_t* plan, int* sums) {
+    int carry = 0;
+    for (int base = 0; base < a.T; base += NT) {
+        const int t = base + static_cast<int>(threadIdx.x);
+        const int tiles = t < a.T ? (row_len(a, t) + kTileKeys - 1) / kTileKeys : 0;
+        int tot;
+        const int excl = cta_scan<NT>(tiles, sums, tot);
+        if (t < a.T) plan[t] = carry + excl;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) plan[a.T] = carry;
+    block_sync();
+    if (blockIdx.x != 0) return;
+    const int64_t total = carry, G = a.G;
+    const int GB = merge_group_bound(a.T, a.G);
+    int gcarry = 0;
+    for (int base = 0; base < a.T; base += NT) {
+        const int t = base + static_cast<int>(threadIdx.x);
+        int g = 0;
+        if (t < a.T) {
+            const int64_t p0 = plan[t], p1 = plan[t + 1];
+            if (p1 <= p0) g = 1;
+            else g = static_cast<int>((tile_owner(p1 - 1, total, G) - tile_owner(p0, total, G) + kMergeFanIn) / kMergeFanIn);
+        }
+        int tot;
+        const int excl = cta_scan<NT>(g, sums, tot);
+        if (t < a.T) {
+            a.tile_prefix[t] = plan[t];
+            a.group_prefix[t] = gcarry + excl;
+            for (int l = 0; l < kMergeLevels - 1; ++l)
+                for (int i = 0; i < g; ++i) a.merge_count[l * GB + gcarry + excl + i] = 0;
+        }
+        gcarry += tot;
+    }
+    if (threadIdx.x == 0) {
+        a.tile_prefix[a.T] = carry;
+        a.group_prefix[a.T] = gcarry;
+    }
 }
 static_assert(topk_cap(2048) <= static_cast<uint32_t>(kEpiThreads * kTopkPer), "candidate buffer exceeds registers");
 static_assert(smem_bytes<false>(2048) <= kSmemLimit, "indexer shared memory over the limit");
@@ -99,6 +169,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     float* ring = reinterpret_cast<float*>(smem + C::kOffBuf + static_cast<size_t>(topk_cap(a.K)) * 8);  // [kRing][128]
     Smem<kFp8>& S = *reinterpret_cast<Smem<kFp8>*>(reinterpret_cast<uint8_t*>(ring) +
                                                    (kFp8 ? 0 : static_cast<size_t>(kRing) * kTileKeys * 4));
+    int32_t* plan_s = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(&S) + sizeof(Smem<kFp8>));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -143,10 +214,16 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     block_sync();
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
-    griddep_wait();  // the work plan (tile prefix) is written
+    griddep_wait();  // the work plan (tile prefix) is written (or the inputs, when planned here)
+    const int32_t* plan = a.tile_prefix;
+    if (a.self_plan) {
+        __shared__ int scan_sums[C::kThreads / 32];
+        self_plan<C::kThreads>(a, plan_s, scan_sums);
+        plan = plan_s;
+    }
 
     SegmentIter it;
-    it.init(a.tile_prefix, a.T, blockIdx.x, a.G);
+    it.init(plan, a.T, blockIdx.x, a.G);
     Segment seg;
 
     if (warp == 0) {
@@ -509,7 +586,8 @@ static bool launch(const IndexerArgs& a, cudaStream_t s, int* launches) {
     }
     const size_t smem = smem_bytes<kFp8>(a.K);
     if (!set_max_dynamic_smem(reinterpret_cast<const void*>(indexer_tc_kernel<kFp8>), smem)) return false;
-    if (!launch_kernel(true, indexer_tc_kernel<kFp8>, dim3(a.G), dim3(Cfg<kFp8>::kThreads), smem, s, a, map_q, map_k))
+    // the first kernel of the call when it plans itself: it waits for all earlier work on the stream
+    if (!launch_kernel(!a.self_plan, indexer_tc_kernel<kFp8>, dim3(a.G), dim3(Cfg<kFp8>::kThreads), smem, s, a, map_q, map_k))
         return false;
     ++*launches;
     return true;

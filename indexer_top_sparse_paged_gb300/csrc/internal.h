@@ -16,6 +16,7 @@ constexpr int kMaxSplits = 32;   // split-K pieces per attention row
 constexpr int kMaxIndexerCtas = 1024;
 constexpr int kMergeFanIn = 8;   // candidate lists one merge CTA selects from (<= 8 x 2048 keys)
 constexpr int kMergeLevels = 4;  // 8^4 >= kMaxIndexerCtas lists per row
+constexpr int kSelfPlanRows = 512;  // decode calls up to this many rows plan inside the indexer kernel
 
 // Upper bound on the merge groups of a call (one merge CTA each): sum over rows of
 // ceil(lists / 8) <= T + G / 8, since the rows' lists number at most G + T.
