@@ -204,6 +204,13 @@ dsa_status dsa_cache_append(const dsa_dims* dims, const void* k_I_new, const voi
  *   initialised with dsa_workspace_init.
  */
 size_t dsa_hier_workspace_size(const dsa_dims* dims, int32_t T, int32_t n_sel);
+/* After dsa_cache_append of the same T new tokens (same q_seq / q_pos convention, seq_lens after
+ * the append): recomputes the summaries of the blocks those tokens touched, exactly as
+ * dsa_block_summaries would (the other blocks' summaries are unchanged by an append). */
+dsa_status dsa_block_summaries_append(const dsa_dims* dims, const void* k_I_cache, const float* k_I_scale,
+                                      const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
+                                      const int32_t* q_pos, int32_t T, uint16_t* summaries, void* ws, size_t ws_bytes,
+                                      dsa_stream_t stream);
 dsa_status dsa_block_summaries(const dsa_dims* dims, const void* k_I_cache, const float* k_I_scale,
                                const int32_t* block_table, const int32_t* seq_lens, uint16_t* summaries, void* ws,
                                size_t ws_bytes, dsa_stream_t stream);

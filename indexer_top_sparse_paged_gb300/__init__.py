@@ -67,6 +67,8 @@ def lib():
         L.dsa_hier_workspace_size.argtypes = [D, I32, I32]
         L.dsa_block_summaries.restype = ctypes.c_int
         L.dsa_block_summaries.argtypes = [D, P, P, P, P, P, P, SZ, P]
+        L.dsa_block_summaries_append.restype = ctypes.c_int
+        L.dsa_block_summaries_append.argtypes = [D, P, P, P, P, P, P, I32, P, P, SZ, P]
         L.dsa_indexer_topk_hier.restype = ctypes.c_int
         L.dsa_indexer_topk_hier.argtypes = [D, P, P, P, P, P, P, P, P, I32, P, I32, P, P, P, SZ, P]
         L.dsa_cache_append.restype = ctypes.c_int
@@ -204,6 +206,15 @@ def block_summaries(dims: Dims, k_I_cache, k_I_scale, block_table, seq_lens, sum
     st = lib().dsa_block_summaries(ctypes.byref(dims), _p(k_I_cache), _p(k_I_scale), _p(block_table), _p(seq_lens),
                                    _p(summaries), _p(ws), ws.numel(), _stream(stream))
     _check("dsa_block_summaries", st)
+
+
+def block_summaries_append(dims: Dims, k_I_cache, k_I_scale, block_table, seq_lens, T: int, summaries, q_seq=None,
+                           q_pos=None, *, ws, stream=None) -> None:
+    """Recomputes the summaries of the blocks that T appended tokens touched."""
+    st = lib().dsa_block_summaries_append(ctypes.byref(dims), _p(k_I_cache), _p(k_I_scale), _p(block_table),
+                                          _p(seq_lens), _p(q_seq), _p(q_pos), T, _p(summaries), _p(ws), ws.numel(),
+                                          _stream(stream))
+    _check("dsa_block_summaries_append", st)
 
 
 def hier_workspace(dims: Dims, T: int, n_sel: int, device="cuda", stream=None) -> torch.Tensor:

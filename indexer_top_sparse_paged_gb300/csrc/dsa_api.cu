@@ -506,6 +506,25 @@ dsa_status dsa_block_summaries(const dsa_dims* dims, const void* k_I_cache, cons
     return st;
 }
 
+dsa_status dsa_block_summaries_append(const dsa_dims* dims, const void* k_I_cache, const float* k_I_scale,
+                                      const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
+                                      const int32_t* q_pos, int32_t T, uint16_t* summaries, void* ws, size_t ws_bytes,
+                                      dsa_stream_t stream) {
+    dsa_status st = check_common(dims);
+    if (st != DSA_OK) return st;
+    if (T < 0 || dims->d_I <= 0) return DSA_ERR_INVALID_ARG;
+    if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
+    if (T > 0 && (!k_I_cache || !block_table || !seq_lens || !summaries)) return DSA_ERR_INVALID_ARG;
+    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return DSA_ERR_WORKSPACE;
+    int launches = 0;
+    if (!launch_summaries_append(*dims, k_I_cache, k_I_scale, block_table, seq_lens, q_seq, q_pos, T, summaries,
+                                 static_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream), &launches))
+        st = DSA_ERR_LAUNCH;
+    g_last_launches = launches;
+    return st;
+}
+
 dsa_status dsa_indexer_topk_hier(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
                                  const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                                  const int32_t* q_seq, const int32_t* q_pos, int32_t T, const uint16_t* summaries,

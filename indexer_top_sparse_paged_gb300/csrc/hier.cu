@@ -18,15 +18,13 @@ namespace dsa {
 
 constexpr int kSumThreads = 128;
 
-// summaries[b][lb][:] for one logical block per CTA (blockIdx.x = lb, blockIdx.y = b).
-__global__ void __launch_bounds__(kSumThreads) block_summaries_kernel(int mode, int max_blocks, int num_blocks,
-                                                                      int d_I, int sum_rows, const void* k_I,
-                                                                      const float* k_scale, const int32_t* block_table,
-                                                                      const int32_t* seq_lens, uint16_t* summaries,
-                                                                      int* err) {
-    const int lb = blockIdx.x, b = blockIdx.y;
+// The summary of logical block lb of sequence b (one CTA): the mean of the block's valid keys,
+// fp32 sum in token order (never contracted), fp32 division, bf16 round to nearest even.
+__device__ void block_summary(int mode, int max_blocks, int num_blocks, int d_I, int sum_rows, const void* k_I,
+                              const float* k_scale, const int32_t* block_table, const int32_t* seq_lens, int b, int lb,
+                              uint16_t* summaries, int* err) {
     const int L = seq_lens[b];
-    if (lb * kBlock >= L) return;
+    if (lb < 0 || lb * kBlock >= L || lb >= max_blocks) return;
     const int blk = block_table[static_cast<int64_t>(b) * max_blocks + lb];
     if (blk < 0 || blk >= num_blocks) {
         if (threadIdx.x == 0) atomicOr(err, DSA_FAULT_BLOCK_TABLE);
@@ -50,6 +48,41 @@ __global__ void __launch_bounds__(kSumThreads) block_summaries_kernel(int mode, 
         }
         dst[d] = __bfloat16_as_ushort(__float2bfloat16_rn(__fdiv_rn(acc, static_cast<float>(cnt))));
     }
+}
+
+// Every valid block: one per CTA (blockIdx.x = lb, blockIdx.y = b).
+__global__ void __launch_bounds__(kSumThreads) block_summaries_kernel(int mode, int max_blocks, int num_blocks,
+                                                                      int d_I, int sum_rows, const void* k_I,
+                                                                      const float* k_scale, const int32_t* block_table,
+                                                                      const int32_t* seq_lens, uint16_t* summaries,
+                                                                      int* err) {
+    block_summary(mode, max_blocks, num_blocks, d_I, sum_rows, k_I, k_scale, block_table, seq_lens, blockIdx.y,
+                  blockIdx.x, summaries, err);
+}
+
+// The blocks that new tokens touched: the CTA of a block's first new token (rows of one block are
+// consecutive) recomputes that block's summary from the updated cache.
+__global__ void __launch_bounds__(kSumThreads) summaries_append_kernel(int mode, int B, int max_blocks, int num_blocks,
+                                                                       int d_I, int sum_rows, int T, const void* k_I,
+                                                                       const float* k_scale, const int32_t* block_table,
+                                                                       const int32_t* seq_lens, const int32_t* q_seq,
+                                                                       const int32_t* q_pos, uint16_t* summaries, int* err) {
+    const int t = blockIdx.x;
+    auto where = [&](int r, int& b, int& lb) -> bool {
+        b = q_seq ? q_seq[r] : r;
+        if (b < 0 || b >= B) return false;
+        const int pos = q_pos ? q_pos[r] : seq_lens[b] - 1;
+        if (pos < 0) return false;
+        lb = pos / kBlock;
+        return true;
+    };
+    int b, lb;
+    if (!where(t, b, lb)) return;
+    if (t > 0) {
+        int b0, lb0;
+        if (where(t - 1, b0, lb0) && b0 == b && lb0 == lb) return;
+    }
+    block_summary(mode, max_blocks, num_blocks, d_I, sum_rows, k_I, k_scale, block_table, seq_lens, b, lb, summaries, err);
 }
 
 // coarse paging: page i of sequence b is summary page b * pages + i; block counts and block
@@ -114,6 +147,17 @@ bool launch_block_summaries(const dsa_dims& d, const void* k_I, const float* k_s
     block_summaries_kernel<<<dim3(d.max_blocks, d.B), kSumThreads, 0, s>>>(d.mode, d.max_blocks, d.num_blocks, d.d_I,
                                                                            sum_rows, k_I, k_scale, block_table,
                                                                            seq_lens, summaries, err);
+    ++*launches;
+    return cudaGetLastError() == cudaSuccess;
+}
+
+bool launch_summaries_append(const dsa_dims& d, const void* k_I, const float* k_scale, const int32_t* block_table,
+                             const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T,
+                             uint16_t* summaries, int* err, cudaStream_t s, int* launches) {
+    if (T == 0) return true;
+    const int sum_rows = (d.max_blocks + kBlock - 1) / kBlock * kBlock;
+    summaries_append_kernel<<<T, kSumThreads, 0, s>>>(d.mode, d.B, d.max_blocks, d.num_blocks, d.d_I, sum_rows, T, k_I,
+                                                      k_scale, block_table, seq_lens, q_seq, q_pos, summaries, err);
     ++*launches;
     return cudaGetLastError() == cudaSuccess;
 }

@@ -114,6 +114,9 @@ struct AttnArgs {
 bool launch_attn_simt(const AttnArgs& a, cudaStream_t s, int* launches);
 bool launch_block_summaries(const dsa_dims& d, const void* k_I, const float* k_scale, const int32_t* block_table,
                             const int32_t* seq_lens, uint16_t* summaries, int* err, cudaStream_t s, int* launches);
+bool launch_summaries_append(const dsa_dims& d, const void* k_I, const float* k_scale, const int32_t* block_table,
+                             const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T,
+                             uint16_t* summaries, int* err, cudaStream_t s, int* launches);
 bool launch_hier_setup(int B, int pages, int T, const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos,
                        int32_t* coarse_table, int32_t* coarse_lens, int32_t* coarse_pos, int* fine_err, cudaStream_t s,
                        int* launches);

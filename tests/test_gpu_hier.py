@@ -114,3 +114,28 @@ def test_planted_block_is_found():
     idx, blocks = _gpu_hier(dev, case, summ, n_sel=1, explicit_rows=False)
     assert blocks[0].tolist() == [40]
     assert idx[0][:64].tolist() == list(range(40 * 64, 41 * 64)) and np.all(idx[0][64:] == -1)
+
+
+@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8"])
+def test_summaries_follow_the_cache_append(mode):
+    """Append new tokens (a decode token, a chunk crossing blocks), update only the touched
+    blocks' summaries, and compare with the oracle's summaries of the oracle's appended cache."""
+    spec = small_spec(mode, [700, 3000, 129], 256, new_tokens=[1, 150, 2])
+    case = W.generate(spec, seed=506)
+    dev = Dev(case)
+    summ = _gpu_summaries(dev, case)
+    rng = np.random.default_rng(507)
+    k_new = W.to_bf16_bits(rng.standard_normal((spec.T, spec.d_I), dtype=np.float32) * 2.0)
+    kv_new = W.to_bf16_bits(rng.standard_normal((spec.T, spec.d), dtype=np.float32))
+    t_k = torch.from_numpy(k_new.view(np.int16)).cuda()
+    t_kv = torch.from_numpy(kv_new.view(np.int16)).cuda()
+    dsa.cache_append(dev.dims, t_k, t_kv, dev.block_table, dev.seq_lens, dev.k_I, dev.k_I_scale, dev.kv,
+                     q_seq=dev.q_seq, q_pos=dev.q_pos, ws=dev.ws)
+    dsa.block_summaries_append(dev.dims, dev.k_I, dev.k_I_scale, dev.block_table, dev.seq_lens, spec.T, summ,
+                               q_seq=dev.q_seq, q_pos=dev.q_pos, ws=dev.ws)
+    torch.cuda.synchronize()
+    assert dsa.read_error(dev.ws) == 0
+    k2, s2, kv2 = oracle.cache_append(case, k_new, kv_new)
+    case.k_I, case.k_I_scale, case.kv = k2, s2, kv2
+    got = summ.view(torch.int16).cpu().numpy().view(np.uint16)[:, : case.max_blocks]
+    assert np.array_equal(got, oracle.block_summaries(case))
