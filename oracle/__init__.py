@@ -40,7 +40,7 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-MODES = {"f32": 0, "bf16": 1, "bf16_kfp8": 2}
+MODES = {"f32": 0, "bf16": 1, "bf16_kfp8": 2, "mxfp8": 3}
 
 
 class ODims(ctypes.Structure):
@@ -73,6 +73,8 @@ def _bind(lib):
     lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
     lib.oracle_e4m3_to_f64.restype = ctypes.c_double
     lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_mx_quantize32.restype = ctypes.c_int
+    lib.oracle_mx_quantize32.argtypes = [P, P]
     lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
     lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
     lib.oracle_block_summaries.restype = ctypes.c_int
@@ -101,6 +103,23 @@ def _ptr(a):
 
 def _c(a, dtype):
     return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def _scale(case):
+    """The key-scale array in its storage type: fp32 per block (FP8 keys) or E8M0 bytes (MXFP8)."""
+    if case.k_I_scale is None:
+        return None
+    if case.spec.mode == "mxfp8":
+        return np.ascontiguousarray(case.k_I_scale, dtype=np.uint8)
+    return np.ascontiguousarray(case.k_I_scale, dtype=np.float32)
+
+
+def mx_quantize32(v) -> tuple:
+    """(shared exponent X, 32 e4m3 codes) of 32 fp32 values (OCP MX, E4M3 elements)."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    codes = np.zeros(32, np.uint8)
+    X = _load().oracle_mx_quantize32(_ptr(v), _ptr(codes))
+    return int(X), codes
 
 
 def dims_of(case, K=None) -> ODims:
@@ -133,10 +152,10 @@ def index_scores(case, rows=None, threads=None) -> np.ndarray:
     stride = int(q_pos.max()) + 1 if T else 1
     S = np.full((T, stride), np.nan, dtype=np.float64)
     D = dims_of(case)
-    kdt = {"f32": np.float32, "bf16": np.uint16, "bf16_kfp8": np.uint8}[case.spec.mode]
+    kdt = {"f32": np.float32, "bf16": np.uint16, "bf16_kfp8": np.uint8, "mxfp8": np.uint8}[case.spec.mode]
     adt = np.float32 if case.spec.mode == "f32" else np.uint16
     rc = lib.oracle_index_scores(ctypes.byref(D), _ptr(_c(q_I, adt)), _ptr(_c(w, np.float32)),
-                                 _ptr(_c(case.k_I, kdt)), _ptr(_c(case.k_I_scale, np.float32)),
+                                 _ptr(_c(case.k_I, kdt)), _ptr(_scale(case)),
                                  _ptr(_c(case.block_table, np.int32)), _ptr(_c(case.seq_lens, np.int32)),
                                  _ptr(_c(q_seq, np.int32)), _ptr(_c(q_pos, np.int32)), T, stride, _ptr(S),
                                  threads or default_threads())
@@ -153,9 +172,9 @@ def indexer_topk(case, rows=None, K=None, threads=None):
     D = dims_of(case, K)
     idx = np.full((T, D.K), -1, dtype=np.int32)
     kth = np.full((T, 2), np.nan, dtype=np.float64)
-    kdt = {"f32": np.float32, "bf16": np.uint16, "bf16_kfp8": np.uint8}[case.spec.mode]
+    kdt = {"f32": np.float32, "bf16": np.uint16, "bf16_kfp8": np.uint8, "mxfp8": np.uint8}[case.spec.mode]
     adt = np.float32 if case.spec.mode == "f32" else np.uint16
-    keep = [_c(q_I, adt), _c(w, np.float32), _c(case.k_I, kdt), _c(case.k_I_scale, np.float32),
+    keep = [_c(q_I, adt), _c(w, np.float32), _c(case.k_I, kdt), _scale(case),
             _c(case.block_table, np.int32), _c(case.seq_lens, np.int32), _c(q_seq, np.int32), _c(q_pos, np.int32)]
     rc = lib.oracle_indexer_topk(ctypes.byref(D), *[_ptr(a) for a in keep], T, _ptr(idx), _ptr(kth),
                                  threads or default_threads())
@@ -203,7 +222,7 @@ def cache_append(case, k_new, kv_new, rows=None):
     T = len(q_seq)
     k_I = np.ascontiguousarray(case.k_I).copy()
     kv = np.ascontiguousarray(case.kv).copy()
-    scale = None if case.k_I_scale is None else np.ascontiguousarray(case.k_I_scale, dtype=np.float32).copy()
+    scale = None if case.k_I_scale is None else _scale(case).copy()
     kdt = np.float32 if s.mode == "f32" else np.uint16
     adt = np.float32 if s.mode == "f32" else np.uint16
     keep = [_c(k_new, kdt), _c(kv_new, adt), _c(case.block_table, np.int32), _c(case.seq_lens, np.int32),
@@ -220,8 +239,8 @@ def block_summaries(case) -> np.ndarray:
     lib = _load()
     s = case.spec
     out = np.zeros((s.B, case.max_blocks, s.d_I), dtype=np.uint16)
-    kdt = {"f32": np.float32, "bf16": np.uint16, "bf16_kfp8": np.uint8}[s.mode]
-    keep = [_c(case.k_I, kdt), _c(case.k_I_scale, np.float32), _c(case.block_table, np.int32),
+    kdt = {"f32": np.float32, "bf16": np.uint16, "bf16_kfp8": np.uint8, "mxfp8": np.uint8}[s.mode]
+    keep = [_c(case.k_I, kdt), _scale(case), _c(case.block_table, np.int32),
             _c(case.seq_lens, np.int32)]
     rc = lib.oracle_block_summaries(ctypes.byref(dims_of(case)), *[_ptr(a) for a in keep], _ptr(out))
     if rc:

@@ -45,6 +45,15 @@
  *     values, scale = amax / 448 (fp32; 1 when amax is 0) and every code of the
  *     block becomes RNE_e4m3(x / scale), saturating at +-448.
  *
+ * MXFP8 indexer (mode 3; "MXFP8 dynamic quantization in the indexing stage",
+ * Ascend CANN page §3: groups of 32 adjacent elements share one scale): the
+ * indexer keys are OCP MX E4M3 codes with one E8M0 scale byte (2^(byte-127))
+ * per 32 elements of a key, and the bf16 query q_I is quantised the same way
+ * before scoring (OCP Microscaling Formats: shared exponent
+ * X = floor(log2(amax)) - 8 for E4M3, clamped to [-127, 127], -127 for an
+ * all-zero group; element = RNE_e4m3(v * 2^-X), saturating at +-448; value =
+ * element * 2^X).  Attention stays bf16.
+ *
  * Input decoding:
  *  - bf16: the 16 bits are the top half of an IEEE binary32 (exact widening).
  *  - e4m3 (OCP 8-bit floating point spec, E4M3): sign, 4 exponent bits with
@@ -61,7 +70,7 @@
 #include <string.h>
 
 typedef struct {
-    int32_t mode; /* 0: fp32 everything; 1: bf16 (w fp32); 2: bf16 with e4m3 indexer keys */
+    int32_t mode; /* 0: fp32 everything; 1: bf16 (w fp32); 2: bf16 with e4m3 indexer keys; 3: MXFP8 indexer */
     int32_t B, max_blocks, num_blocks, block_size;
     int32_t H_I, d_I, H, d, d_v, K;
 } odims;
@@ -113,6 +122,35 @@ uint8_t oracle_f32_to_e4m3(float f) {
     if (code > 0x7E) code = 0x7E;
     return sign | (uint8_t)code;
 }
+
+/* OCP MX (E4M3 elements, E8M0 scale) quantisation of 32 fp32 values: returns the shared
+ * exponent X and writes the element codes. */
+static int mx_quantize32(const float* v, uint8_t* codes) {
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i)
+        if (fabsf(v[i]) > amax) amax = fabsf(v[i]);
+    int X = -127;
+    if (amax > 0.0f) {
+        int e;
+        frexpf(amax, &e);  /* amax = f * 2^e, f in [0.5, 1): floor(log2(amax)) = e - 1 */
+        X = (e - 1) - 8;
+        if (X < -127) X = -127;
+        if (X > 127) X = 127;
+    }
+    for (int i = 0; i < 32; ++i) codes[i] = oracle_f32_to_e4m3(ldexpf(v[i], -X));
+    return X;
+}
+
+/* the MXFP8 value of 32 bf16 values (quantise, then decode exactly) */
+static void mx_roundtrip32(const uint16_t* bits, double* out) {
+    float v[32];
+    uint8_t c[32];
+    for (int i = 0; i < 32; ++i) v[i] = (float)oracle_bf16_to_f64(bits[i]);
+    const int X = mx_quantize32(v, c);
+    for (int i = 0; i < 32; ++i) out[i] = ldexp(oracle_e4m3_to_f64(c[i]), X);
+}
+
+int oracle_mx_quantize32(const float* v, uint8_t* codes) { return mx_quantize32(v, codes); }
 
 static double f32_at(const void* p, size_t i) { return (double)((const float*)p)[i]; }
 static double bf16_at(const void* p, size_t i) { return oracle_bf16_to_f64(((const uint16_t*)p)[i]); }
@@ -223,6 +261,11 @@ static void score_item(void* vctx, int64_t item, void* scratch) {
             size_t i = ((size_t)t * D->H_I + j) * D->d_I + e;
             q[(size_t)j * D->d_I + e] = act_at(D, C->q_I, i);
         }
+    if (D->mode == 3)  /* the MXFP8 query: every group of 32 quantised and decoded */
+        for (int j = 0; j < D->H_I; ++j)
+            for (int g = 0; g < D->d_I / 32; ++g)
+                mx_roundtrip32((const uint16_t*)C->q_I + ((size_t)t * D->H_I + j) * D->d_I + 32 * g,
+                               q + (size_t)j * D->d_I + 32 * g);
     for (int64_t s = s0; s < s1; ++s) {
         int32_t blk;
         int64_t row = phys_row(D, C->block_table, b, s, &blk);
@@ -234,6 +277,8 @@ static void score_item(void* vctx, int64_t item, void* scratch) {
             if (D->mode == 0) v = f32_at(C->k_I, i);
             else if (D->mode == 1) v = bf16_at(C->k_I, i);
             else v = oracle_e4m3_to_f64(((const uint8_t*)C->k_I)[i]);
+            if (D->mode == 3)  /* E8M0 byte of the key's group of 32 */
+                v = ldexp(v, (int)((const uint8_t*)C->k_I_scale)[(size_t)row * (D->d_I / 32) + e / 32] - 127);
             k[e] = v * scale;
         }
         double total = 0.0;
@@ -249,7 +294,8 @@ static void score_item(void* vctx, int64_t item, void* scratch) {
 
 static int check_dims(const odims* D) {
     if (!D || D->block_size <= 0 || D->H_I <= 0 || D->d_I <= 0 || D->K <= 0) return 0;
-    if (D->mode < 0 || D->mode > 2) return 0;
+    if (D->mode < 0 || D->mode > 3) return 0;
+    if (D->mode == 3 && D->d_I % 32) return 0;
     return 1;
 }
 
@@ -289,7 +335,7 @@ int oracle_index_scores(const odims* D, const void* q_I, const float* w, const v
                         const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
                         const int32_t* q_pos, int T, int64_t row_stride, double* S, int threads) {
     if (!check_dims(D) || T < 0 || !check_rows(D, seq_lens, q_seq, q_pos, T)) return O_BAD_ARG;
-    if (D->mode == 2 && !k_I_scale) return O_BAD_ARG;
+    if ((D->mode == 2 || D->mode == 3) && !k_I_scale) return O_BAD_ARG;
     int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T > 0 ? T : 1));
     if (!off) return O_NOMEM;
     for (int t = 0; t < T; ++t) {
@@ -345,7 +391,7 @@ int oracle_indexer_topk(const odims* D, const void* q_I, const float* w, const v
                         const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
                         const int32_t* q_pos, int T, int32_t* idx, double* kth, int threads) {
     if (!check_dims(D) || T < 0 || !check_rows(D, seq_lens, q_seq, q_pos, T)) return O_BAD_ARG;
-    if (D->mode == 2 && !k_I_scale) return O_BAD_ARG;
+    if ((D->mode == 2 || D->mode == 3) && !k_I_scale) return O_BAD_ARG;
     int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T + 1));
     if (!off) return O_NOMEM;
     off[0] = 0;
@@ -426,7 +472,7 @@ int oracle_sparse_attn(const odims* D, const void* q, const void* kv, const int3
                        const int32_t* seq_lens, const int32_t* q_seq, const int32_t* idx, int idx_stride, int T,
                        double sm_scale, double* out, double* lse, double* psum, int threads) {
     if (!D || D->H <= 0 || D->d <= 0 || D->d_v <= 0 || D->d_v > D->d || idx_stride <= 0 || T < 0) return O_BAD_ARG;
-    if (D->mode < 0 || D->mode > 2 || D->block_size <= 0) return O_BAD_ARG;
+    if (D->mode < 0 || D->mode > 3 || D->block_size <= 0) return O_BAD_ARG;
     for (int t = 0; t < T; ++t)
         if (q_seq[t] < 0 || q_seq[t] >= D->B) return O_BAD_ARG;
     attn_ctx C = {D, q, kv, block_table, seq_lens, q_seq, idx, idx_stride, sm_scale, out, lse, psum, 0};
@@ -457,6 +503,7 @@ int oracle_cache_append(const odims* D, const void* k_new, const void* kv_new, c
     const int bs = D->block_size;
     const size_t act = D->mode == 0 ? 4 : 2;
     const size_t kb = D->mode == 0 ? 4 : (D->mode == 1 ? 2 : 1);
+    if (D->mode == 3 && D->d_I % 32) return O_BAD_ARG;
     for (int t = 0; t < T; ++t) {  /* validate first */
         int b;
         const int pos = append_pos(seq_lens, q_seq, q_pos, t, &b);
@@ -470,8 +517,17 @@ int oracle_cache_append(const odims* D, const void* k_new, const void* kv_new, c
         const int pos = append_pos(seq_lens, q_seq, q_pos, t, &b);
         const int64_t row = (int64_t)block_table[(int64_t)b * D->max_blocks + pos / bs] * bs + pos % bs;
         memcpy((char*)kv_cache + row * D->d * act, (const char*)kv_new + (int64_t)t * D->d * act, D->d * act);
-        if (D->mode != 2)
+        if (D->mode <= 1)
             memcpy((char*)k_cache + row * D->d_I * kb, (const char*)k_new + (int64_t)t * D->d_I * kb, D->d_I * kb);
+        if (D->mode == 3) {  /* MXFP8 keys: each group of 32 quantised on its own (no block state) */
+            for (int g = 0; g < D->d_I / 32; ++g) {
+                float v[32];
+                for (int i = 0; i < 32; ++i)
+                    v[i] = (float)oracle_bf16_to_f64(((const uint16_t*)k_new)[(int64_t)t * D->d_I + 32 * g + i]);
+                const int X = mx_quantize32(v, (uint8_t*)k_cache + row * D->d_I + 32 * g);
+                ((uint8_t*)k_scale)[row * (D->d_I / 32) + g] = (uint8_t)(X + 127);
+            }
+        }
     }
     if (D->mode != 2) return O_OK;
     /* FP8 keys: every block that receives new tokens, once (at its first new token) */
@@ -566,7 +622,9 @@ int oracle_block_summaries(const odims* D, const void* k_I, const float* k_I_sca
                     float x;
                     if (D->mode == 0) x = ((const float*)k_I)[e];
                     else if (D->mode == 1) x = (float)oracle_bf16_to_f64(((const uint16_t*)k_I)[e]);
-                    else x = (float)oracle_e4m3_to_f64(((const uint8_t*)k_I)[e]) * k_I_scale[blk];
+                    else if (D->mode == 2) x = (float)oracle_e4m3_to_f64(((const uint8_t*)k_I)[e]) * k_I_scale[blk];
+                    else x = ldexpf((float)oracle_e4m3_to_f64(((const uint8_t*)k_I)[e]),
+                                    (int)((const uint8_t*)k_I_scale)[((size_t)blk * bs + i) * (D->d_I / 32) + d / 32] - 127);
                     acc = acc + x;
                 }
                 summaries[((size_t)b * D->max_blocks + lb) * D->d_I + d] = f32_to_bf16_rne(acc / (float)cnt);

@@ -57,10 +57,27 @@ def logical_rows(case, b: int, cache: np.ndarray, scale=None, n=None) -> np.ndar
     return rows
 
 
+def np_mx(codes, scale_bytes) -> np.ndarray:
+    """MXFP8 values: e4m3 code times 2^(byte - 127), one byte per 32 elements of the last axis."""
+    x = np_e4m3(codes)
+    return x * np.exp2(np.repeat(np.asarray(scale_bytes, np.float64) - 127.0, 32, axis=-1))
+
+
+def mx_roundtrip(x) -> np.ndarray:
+    """fp32 values -> their MXFP8 quantisation (the generator's NumPy/torch recipe), decoded."""
+    return np_mx(*W.to_mx_e4m3(np.asarray(x, np.float32)))
+
+
 def logical_keys(case, b: int, n=None) -> np.ndarray:
     if case.spec.mode == "bf16_kfp8":
         codes, sc = logical_rows(case, b, case.k_I, case.k_I_scale, n)
         return np_e4m3(codes) * sc.astype(np.float64)[:, None]
+    if case.spec.mode == "mxfp8":
+        bs = case.spec.block_size
+        L = int(case.seq_lens[b]) if n is None else int(n)
+        s = np.arange(L)
+        blk = case.block_table[b, s // bs]
+        return np_mx(case.k_I[blk, s % bs], case.k_I_scale[blk, s % bs])
     return act(case, logical_rows(case, b, case.k_I, None, n))
 
 
@@ -79,6 +96,8 @@ def brute_scores_row(case, t: int) -> np.ndarray:
         return np.zeros(0)
     K = logical_keys(case, b, n)                      # [n, d_I]
     q = act(case, case.q_I[t])                        # [H_I, d_I]
+    if case.spec.mode == "mxfp8":                     # the query is MX-quantised too
+        q = mx_roundtrip(q)
     w = case.w[t].astype(np.float64)                  # [H_I]
     return w @ np.maximum(q @ K.T, 0.0)               # [n]
 

@@ -118,3 +118,25 @@ def test_append_keeps_codes_when_the_block_scale_does_not_grow():
     assert np.array_equal(k_I[blk, :25], old_codes)
     x = np_bf16(k_new[0]).astype(np.float32)
     assert np.array_equal(k_I[blk, 25], torch_e4m3(x / case.k_I_scale[blk]))
+
+
+def test_append_mx_quantises_each_new_key_on_its_own():
+    """MXFP8 keys: every new token's key gets its own codes and E8M0 bytes (the generator's
+    NumPy/torch recipe applied to the bf16 key); no other key row and no other scale changes."""
+    spec = small_spec("mxfp8", [130, 64, 7], 64, new_tokens=[70, 1, 7], H_I=4, d_I=64)
+    case = W.generate(spec, seed=35)
+    k_new, kv_new = _new_tokens(case, 36)
+    k_I, scale, kv = oracle.cache_append(case, k_new, kv_new)
+    codes, byts = W.to_mx_e4m3(np_bf16(k_new).astype(np.float32))
+    touched = set()
+    for t in range(spec.T):
+        blk, off = _slot(case, t)
+        assert np.array_equal(k_I[blk, off], codes[t])
+        assert np.array_equal(scale[blk, off], byts[t])
+        assert np.array_equal(kv[blk, off], kv_new[t])
+        touched.add((blk, off))
+    for blk in range(case.num_blocks):
+        for off in range(64):
+            if (blk, off) not in touched:
+                assert np.array_equal(k_I[blk, off], case.k_I[blk, off])
+                assert np.array_equal(scale[blk, off], case.k_I_scale[blk, off])

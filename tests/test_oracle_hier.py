@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import workloads as W
-from cases import brute_scores_row, logical_rows, np_bf16, np_e4m3, small_spec
+from cases import brute_scores_row, logical_rows, np_bf16, np_e4m3, np_mx, small_spec
 
 
 def np_summaries(case):
@@ -22,6 +22,8 @@ def np_summaries(case):
                 x = case.k_I[blk, :cnt].astype(np.float32)
             elif s.mode == "bf16":
                 x = np_bf16(case.k_I[blk, :cnt]).astype(np.float32)
+            elif s.mode == "mxfp8":
+                x = np_mx(case.k_I[blk, :cnt], case.k_I_scale[blk, :cnt]).astype(np.float32)
             else:
                 x = (np_e4m3(case.k_I[blk, :cnt]).astype(np.float32) * np.float32(case.k_I_scale[blk])).astype(np.float32)
             acc = np.zeros(s.d_I, np.float32)
@@ -32,7 +34,7 @@ def np_summaries(case):
     return out
 
 
-@pytest.mark.parametrize("mode", ["f32", "bf16", "bf16_kfp8"])
+@pytest.mark.parametrize("mode", ["f32", "bf16", "bf16_kfp8", "mxfp8"])
 def test_summaries_match_sequential_numpy_mean(mode):
     spec = small_spec(mode, [1, 63, 64, 65, 300], 64, H_I=4, d_I=64) if mode != "f32" else small_spec(mode, [1, 63, 64, 65, 300], 64)
     case = W.generate(spec, seed=401)

@@ -42,6 +42,12 @@ MUTANTS = {
     "append_keeps_old_scale": ("const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;", "const float scale = old_scale;"),
     "append_wrong_slot": ("const int64_t row = (int64_t)block_table[(int64_t)b * D->max_blocks + pos / bs] * bs + pos % bs;",
                           "const int64_t row = (int64_t)block_table[(int64_t)b * D->max_blocks + pos / bs] * bs + (pos + 1) % bs;"),
+    "mx_query_not_quantised": ("    if (D->mode == 3)  /* the MXFP8 query", "    if (0)  /* the MXFP8 query"),
+    "mx_scale_bias_126": ("e / 32] - 127);\n            k[e]", "e / 32] - 126);\n            k[e]"),
+    "mx_first_group_scale_only": ("[(size_t)row * (D->d_I / 32) + e / 32] - 127);", "[(size_t)row * (D->d_I / 32)] - 127);"),
+    "mx_exponent_is_ceil": ("X = (e - 1) - 8;", "X = e - 8;"),
+    "mx_append_wrong_scale_row": ("((uint8_t*)k_scale)[row * (D->d_I / 32) + g] = (uint8_t)(X + 127);",
+                                  "((uint8_t*)k_scale)[(row ^ 1) * (D->d_I / 32) + g] = (uint8_t)(X + 127);"),
 }
 
 PIN_TESTS = [
@@ -58,7 +64,11 @@ PIN_TESTS = [
     app.test_append_whole_new_block_matches_the_generators_quantisation,
     app.test_append_requantises_the_earlier_tokens_of_the_block,
     app.test_append_keeps_codes_when_the_block_scale_does_not_grow,
-    lambda: [hier.test_summaries_match_sequential_numpy_mean(m) for m in ("f32", "bf16", "bf16_kfp8")],
+    lambda: [hier.test_summaries_match_sequential_numpy_mean(m) for m in ("f32", "bf16", "bf16_kfp8", "mxfp8")],
+    lambda: pins.test_topk_matches_brute_force(*pins.TINY[-1]),
+    pins.test_mx_quantiser_matches_numpy_torch_recipe,
+    pins.test_mx_scores_equal_bf16_scores_of_the_decoded_values,
+    app.test_append_mx_quantises_each_new_key_on_its_own,
     hier.test_planted_block_is_chosen,
 ]
 

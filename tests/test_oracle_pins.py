@@ -4,14 +4,17 @@
   against torch's float8_e4m3fn cast and the OCP spec values in
   tests/golden/e4m3_spec_values.json;
 * indexer + Top-K: a hand-worked example (tests/golden/indexer_hand.json),
-  NumPy brute force (full score matrix + lexsort) on tiny inputs in all three
+  NumPy brute force (full score matrix + lexsort) on tiny inputs in all four
   storage modes, exact ties on integer data, the single-column special case
   (a plain sort), power-of-two FP8 scale changes and planted index sets;
 * attention: the hand-worked example, K >= L equals dense attention (torch
   CPU float64 SDPA), softmax weights sum to one, q = 0 gives the mean of the
   selected value rows, a dominant logit gives that row, one row gives that
   row, no row gives zeros and lse = -inf;
-* paging: a different physical block permutation changes nothing.
+* paging: a different physical block permutation changes nothing;
+* MXFP8: the oracle's group quantiser against the generator's NumPy/torch
+  recipe and closed forms, and MXFP8 scores equal to bf16 scores of the
+  decoded values (the bf16 path being pinned above).
 """
 import json
 import math
@@ -23,8 +26,8 @@ import torch
 
 import oracle
 import workloads as W
-from cases import (act, brute_attn_row, brute_scores_row, brute_topk_row, logical_keys, logical_kv, np_bf16,
-                   np_e4m3, sdpa_f64, small_spec)
+from cases import (act, brute_attn_row, brute_scores_row, brute_topk_row, logical_keys, logical_kv, mx_roundtrip,
+                   np_bf16, np_e4m3, np_mx, sdpa_f64, small_spec)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -114,12 +117,13 @@ TINY = [
     ("f32", [130, 7], 256),          # K > L
     ("bf16", [1, 64, 65, 129], 16),
     ("bf16_kfp8", [63, 64, 65, 300], 32),
+    ("mxfp8", [63, 64, 65, 300], 32),
 ]
 
 
 @pytest.mark.parametrize("mode,lens,K", TINY)
 def test_topk_matches_brute_force(mode, lens, K):
-    kw = {} if mode == "f32" else dict(H_I=8, d_I=32, H=4, d=64, d_v=48)
+    kw = {} if mode == "f32" else dict(H_I=8, d_I=64 if mode == "mxfp8" else 32, H=4, d=64, d_v=48)
     spec = small_spec(mode, lens, K, **kw)
     case = W.generate(spec, seed=11 + len(lens))
     S_or = oracle.index_scores(case)
@@ -330,3 +334,74 @@ def test_poisoned_slots_are_never_read():
     assert np.nanmax(np.abs(S)) < 1e3
     tail = case.k_I[case.block_table[0, 1], 70 % 64:]
     assert np.all(tail == W.POISON)
+
+
+# ----------------------------------------------------------------------------
+# MXFP8 (OCP Microscaling, E4M3 elements, one E8M0 scale per 32)
+# ----------------------------------------------------------------------------
+
+def _mx_groups():
+    rng = np.random.default_rng(77)
+    out = []
+    for e in (-140, -126, -100, -20, -8, -1, 0, 1, 7, 8, 9, 60, 120, 126):  # scales across the range
+        out.append(rng.standard_normal(32).astype(np.float32) * np.float32(2.0 ** e))
+    out.append(np.zeros(32, np.float32))
+    p = np.zeros(32, np.float32)
+    p[3] = 2.0 ** 5                                                # amax exactly a power of two
+    p[4] = -(2.0 ** -20)                                           # underflows to a zero code
+    out.append(p)
+    for m in (1.75, 1.8125, 1.875, 1.9375, 1.96875, 1.99):         # scaled amax near / above 448
+        g = rng.uniform(-1, 1, 32).astype(np.float32)
+        g[0] = np.float32(m * 4.0)
+        out.append(g)
+    reps = np.array([oracle.e4m3_to_f64(c) for c in range(0x7F)], np.float64)
+    mids = ((reps[1:] + reps[:-1]) / 2)                            # ties at the element rounding
+    for k in range(0, len(mids), 31):
+        g = np.zeros(32, np.float32)
+        g[:len(mids[k:k + 31])] = mids[k:k + 31] / 256.0
+        g[31] = 1.0                                                # X = -8: element = x * 256
+        out.append(g)
+    return out
+
+
+def test_mx_quantiser_matches_numpy_torch_recipe():
+    for g in _mx_groups():
+        X, codes = oracle.mx_quantize32(g)
+        ref_codes, ref_byte = W.to_mx_e4m3(g)
+        assert X == int(ref_byte[0]) - 127, g
+        same = (codes == ref_codes) | (((codes & 0x7F) == 0) & ((ref_codes & 0x7F) == 0))
+        assert same.all(), (g, codes, ref_codes)
+
+
+def test_mx_closed_forms():
+    X, c = oracle.mx_quantize32(np.full(32, 3.0, np.float32))      # floor(log2 3) = 1 -> X = -7, 3*2^7 = 384
+    assert X == -7 and (c == 0x7C).all()
+    X, c = oracle.mx_quantize32(np.zeros(32, np.float32))
+    assert X == -127 and (c == 0).all()
+    g = np.zeros(32, np.float32)
+    g[0], g[1], g[2] = 1.0, -0.5, 2.0 ** -20                       # X = -8: 256, -128, below the smallest code
+    X, c = oracle.mx_quantize32(g)
+    assert X == -8 and c[0] == 0x78 and c[1] == 0xF0 and (c[2] & 0x7F) == 0
+    g = np.full(32, 1.99, np.float32)                              # 1.99 * 256 = 509 saturates to 448
+    X, c = oracle.mx_quantize32(g)
+    assert X == -8 and (c == 0x7E).all()
+
+
+def test_mx_scores_equal_bf16_scores_of_the_decoded_values():
+    spec = small_spec("mxfp8", [200, 64, 1], 24, H_I=8, d_I=64)
+    mx = W.generate(spec, seed=61)
+    bf = W.generate(small_spec("bf16", [200, 64, 1], 24, H_I=8, d_I=64), seed=61)
+    bf.block_table = mx.block_table.copy()
+    keys = np_mx(mx.k_I, mx.k_I_scale).astype(np.float32)
+    bf.k_I = W.to_bf16_bits(keys)
+    assert np.array_equal(np_bf16(bf.k_I), keys.astype(np.float64))   # exactly representable
+    qd = mx_roundtrip(np_bf16(mx.q_I)).astype(np.float32)
+    bf.q_I = W.to_bf16_bits(qd)
+    assert np.array_equal(np_bf16(bf.q_I), qd.astype(np.float64))
+    bf.w = mx.w.copy()
+    S_mx, S_bf = oracle.index_scores(mx), oracle.index_scores(bf)
+    assert np.array_equal(S_mx, S_bf, equal_nan=True)
+    assert np.array_equal(oracle.indexer_topk(mx)[0], oracle.indexer_topk(bf)[0])
+    # and the query really was quantised: scores with the unquantised query differ
+    bf.q_I = mx.q_I.copy()
+    assert not np.array_equal(oracle.index_scores(bf), S_mx, equal_nan=True)

@@ -8,7 +8,9 @@ out in a paged cache.
 * Values: ``q, kv, q_I, k_I ~ N(0,1)``; head weights ``w ~ U(0,1)`` (fp32).
 * Storage: fp32, bf16 (round to nearest even) or OCP FP8 e4m3 indexer keys with
   one fp32 scale per 64-token physical block (``scale = amax/448``, codes
-  rounded to nearest even, saturating at 448).
+  rounded to nearest even, saturating at 448), or MXFP8 indexer keys (OCP
+  Microscaling: e4m3 codes with one E8M0 scale byte per 32 elements of a key,
+  quantised from the bf16-rounded draw).
 * Paging: every sequence's logical 64-token blocks are placed in a pool of
   physical blocks by a seeded random permutation (plus a few spare blocks),
   recorded in ``block_table[B][max_blocks]``; unused table entries are -1.
@@ -48,7 +50,7 @@ class Spec:
     """
 
     name: str
-    mode: str  # "f32" | "bf16" | "bf16_kfp8"
+    mode: str  # "f32" | "bf16" | "bf16_kfp8" | "mxfp8"
     seq_lens: list
     new_tokens: list
     H_I: int
@@ -136,6 +138,23 @@ def to_e4m3_codes(x: np.ndarray) -> np.ndarray:
     return t.view(torch.uint8).numpy()
 
 
+def to_mx_e4m3(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """fp32 ``[..., n]`` (n a multiple of 32) -> (e4m3 codes ``[..., n]``, E8M0 bytes ``[..., n/32]``).
+
+    OCP Microscaling with E4M3 elements: each group of 32 shares the exponent
+    ``X = floor(log2(amax)) - 8`` (clamped to [-127, 127]; -127 for an all-zero
+    group), stored as the byte ``X + 127``; the elements are ``x * 2^-X``
+    rounded to e4m3 (nearest even, saturating at 448).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    g = x.reshape(x.shape[:-1] + (-1, 32))
+    amax = np.abs(g).max(axis=-1)
+    _, e = np.frexp(amax)  # amax = f * 2^e with f in [0.5, 1)
+    X = np.clip(np.where(amax > 0, e.astype(np.int64) - 9, -127), -127, 127)
+    scaled = np.ldexp(g, (-X)[..., None]).astype(np.float32)
+    return to_e4m3_codes(scaled).reshape(x.shape), (X + 127).astype(np.uint8)
+
+
 # ----------------------------------------------------------------------------
 # case generation
 # ----------------------------------------------------------------------------
@@ -151,7 +170,7 @@ class Case:
     q_I: np.ndarray          # f32 [T,H_I,d_I] or u16 bf16 bits
     w: np.ndarray            # f32 [T,H_I]
     k_I: np.ndarray          # f32/u16/u8 [NB,64,d_I]
-    k_I_scale: np.ndarray | None  # f32 [NB] (FP8 keys only)
+    k_I_scale: np.ndarray | None  # f32 [NB] (FP8 keys) | u8 [NB,64,d_I/32] E8M0 (MXFP8 keys)
     q: np.ndarray            # f32 [T,H,d] or u16
     kv: np.ndarray           # f32 [NB,64,d] or u16
 
@@ -205,11 +224,14 @@ def generate(spec: Spec, seed: int, chunk_blocks: int = 1024) -> Case:
     q = _store(_normal(rng, (T, spec.H, spec.d)), spec.mode)
 
     fp8 = spec.mode == "bf16_kfp8"
-    kdt = np.float32 if spec.mode == "f32" else (np.uint8 if fp8 else np.uint16)
+    mx = spec.mode == "mxfp8"
+    kdt = np.float32 if spec.mode == "f32" else (np.uint8 if fp8 or mx else np.uint16)
     vdt = np.float32 if spec.mode == "f32" else np.uint16
     k_I = np.empty((NB, bs, spec.d_I), dtype=kdt)
     kv = np.empty((NB, bs, spec.d), dtype=vdt)
     scale = np.ones(NB, dtype=np.float32) if fp8 else None
+    if mx:
+        scale = np.full((NB, bs, spec.d_I // 32), 127, dtype=np.uint8)
 
     # logical block list in (sequence, block) order -> physical slot
     phys_of_logical = perm[:n_logical]
@@ -223,22 +245,28 @@ def generate(spec: Spec, seed: int, chunk_blocks: int = 1024) -> Case:
             s[s == 0] = 1.0
             k_I[dst] = to_e4m3_codes(kx / s[:, None, None])
             scale[dst] = s
+        elif mx:
+            k_I[dst], scale[dst] = to_mx_e4m3(bf16_bits_to_f32(to_bf16_bits(kx)))
         else:
             k_I[dst] = _store(kx, spec.mode)
         kv[dst] = _store(_normal(rng, (c1 - c0, bs, spec.d)), spec.mode)
 
     # poison: spare blocks and the tail slots of each sequence's last block
-    kpois = np.uint8(POISON_E4M3) if fp8 else _poison_value(spec.mode)
+    kpois = np.uint8(POISON_E4M3) if fp8 or mx else _poison_value(spec.mode)
     vpois = _poison_value(spec.mode)
     spare = perm[n_logical:]
     k_I[spare] = kpois
     kv[spare] = vpois
+    if mx:
+        scale[spare] = 127
     for b in range(spec.B):
         L = int(lens[b])
         if L % bs:
             pb = table[b, L // bs]
             k_I[pb, L % bs :] = kpois
             kv[pb, L % bs :] = vpois
+            if mx:
+                scale[pb, L % bs :] = 127
 
     return Case(spec, seed, table, lens.astype(np.int32), q_seq, q_pos, q_I, w, k_I, scale, q, kv)
 
