@@ -66,14 +66,20 @@ typedef enum {
 typedef enum {
     DSA_F32 = 0,       /* q_I, k_I, q, kv, out: fp32 */
     DSA_BF16 = 1,      /* q_I, k_I, q, kv, out: bf16 */
-    DSA_BF16_KFP8 = 2  /* as DSA_BF16, but k_I is OCP e4m3 with one fp32 scale per 64-token block */
+    DSA_BF16_KFP8 = 2, /* as DSA_BF16, but k_I is OCP e4m3 with one fp32 scale per 64-token block */
+    DSA_MXFP8 = 3      /* as DSA_BF16, but the indexer runs in MXFP8 (OCP Microscaling, E4M3 elements):
+                        * k_I is e4m3 codes with one E8M0 scale byte per 32 elements of a key, and
+                        * q_I (bf16) is quantised the same way inside the call ("Day0 Inference
+                        * Support ... on Huawei Ascend CANN Architecture" §3: MXFP8 dynamic
+                        * quantisation in the indexing stage) */
 } dsa_mode;
 
 /*
  * Problem dimensions.
  *   block_size must be 64 (tokens per physical cache block).
  *   DSA_F32:              H_I <= 64, d_I <= 256, d_I % 4 == 0, H <= 128, d <= 1024, d % 4 == 0, d_v <= d
- *   DSA_BF16 / _KFP8:     indexer (H_I, d_I) == (64, 128) [tensor cores] or H_I <= 64, d_I <= 256, d_I % 8 == 0;
+ *   DSA_BF16 / _KFP8 / DSA_MXFP8: indexer (H_I, d_I) == (64, 128) [tensor cores] or H_I <= 64, d_I <= 256,
+ *                         d_I % 8 == 0 (DSA_MXFP8: d_I % 32 == 0);
  *                         attention (H, d, d_v) == (128, 576, 512) [tensor cores] or H <= 128, d <= 1024,
  *                         d % 8 == 0, d_v <= d, d_v % 8 == 0
  *   1 <= K <= 2048.
@@ -104,7 +110,12 @@ size_t dsa_workspace_size(const dsa_dims* dims, int32_t T);
  *   q_I        [T][H_I][d_I]        fp32 or bf16 (per mode)
  *   w          [T][H_I]             fp32 head weights (any sign)
  *   k_I_cache  [num_blocks][64][d_I] fp32 / bf16 / e4m3 codes (per mode)
- *   k_I_scale  [num_blocks]         fp32 per-block scale; required for DSA_BF16_KFP8, else ignored
+ *   k_I_scale  DSA_BF16_KFP8: [num_blocks] fp32 per-block scale; DSA_MXFP8: [num_blocks][64][d_I / 32]
+ *              uint8 E8M0 scales (value 2^(byte - 127); byte 255, NaN in the MX format, is not a
+ *              supported input), 16-byte aligned; ignored in the other modes
+ *   (DSA_MXFP8: each group of 32 elements of every q_I head row is quantised to E4M3 with shared
+ *   exponent X = floor(log2(amax)) - 8, at least -127, codes RNE(x * 2^-X) saturating at +-448,
+ *   and scored with the values code * 2^X; keys score with code * 2^(byte - 127).)
  *   block_table[B][max_blocks]      int32 physical block ids (entries past a sequence's end unread)
  *   seq_lens   [B]                  int32 cached positions per sequence, new tokens included
  *   q_seq      [T]                  int32 sequence of each query row; NULL means row t is sequence t (T == B)
@@ -123,7 +134,7 @@ size_t dsa_workspace_size(const dsa_dims* dims, int32_t T);
  * for Day-0 Adaptation ..." §3.1: index selection is scoring followed by Top-K filtering.)
  */
 dsa_status dsa_indexer_topk(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
-                            const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                            const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                             const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx, void* ws,
                             size_t ws_bytes, dsa_stream_t stream);
 
@@ -147,7 +158,7 @@ dsa_status dsa_sparse_attn(const dsa_dims* dims, const void* q, const void* kv_c
  * workspace only). Arguments as in dsa_indexer_topk / dsa_sparse_attn.
  */
 dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
-                      const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens, const void* q,
+                      const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens, const void* q,
                       const void* kv_cache, float sm_scale, int32_t* idx, void* out, float* lse, void* ws,
                       size_t ws_bytes, dsa_stream_t stream);
 
@@ -157,25 +168,28 @@ dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, con
  * Inference Adaptation ..." §2.2: the cache update is fused with the flow producing the entries;
  * "Day0 Inference Support ... on Huawei Ascend CANN Architecture" §3: the indexer's keys are
  * quantised on the way in).
- *   k_I_new    [T][d_I]   fp32 (DSA_F32) or bf16 (DSA_BF16 and DSA_BF16_KFP8: the values to quantise)
+ *   k_I_new    [T][d_I]   fp32 (DSA_F32) or bf16 (the other modes; DSA_BF16_KFP8 and DSA_MXFP8: the
+ *                         values to quantise)
  *   kv_new     [T][d]     fp32 or bf16 latent rows
  *   seq_lens   [B]        cached positions per sequence AFTER the append (new tokens included)
  *   q_seq, q_pos [T]      sequence and position of each new token, as in dsa_indexer_topk (NULL: one
  *                         token per sequence at position seq_lens - 1)
- *   k_I_cache, k_I_scale, kv_cache   updated in place (k_I_scale only for DSA_BF16_KFP8)
+ *   k_I_cache, k_I_scale, kv_cache   updated in place (k_I_scale only for DSA_BF16_KFP8 / DSA_MXFP8)
  *   ws         any workspace of this library (only its error word is used), ws_bytes >= 256
  * The new tokens of a sequence are its tail (positions seq_len - n .. seq_len - 1), given as
  * consecutive rows in ascending position. fp32 / bf16 keys and all latent rows are copied. FP8
  * keys: every block that receives new tokens is requantised as a whole: with x = code * scale
  * (fp32) for its earlier tokens and the new keys' values, the block's scale becomes amax / 448
  * (1 when amax is 0) and each code RNE_e4m3(x / scale), saturating at +-448, all in fp32. Rows
+ * MXFP8 keys: each new key's groups of 32 are quantised on their own (as q_I is in the indexer),
+ * writing its codes and its d_I / 32 scale bytes; no other row changes. Rows
  * with an invalid sequence, position or block-table entry are skipped and reported through the
  * error word (DSA_FAULT_INDEX / DSA_FAULT_BLOCK_TABLE). Requires (d * elem) and (d_I * elem) to be
  * multiples of 16 bytes.
  */
 dsa_status dsa_cache_append(const dsa_dims* dims, const void* k_I_new, const void* kv_new,
                             const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
-                            const int32_t* q_pos, int32_t T, void* k_I_cache, float* k_I_scale, void* kv_cache,
+                            const int32_t* q_pos, int32_t T, void* k_I_cache, void* k_I_scale, void* kv_cache,
                             void* ws, size_t ws_bytes, dsa_stream_t stream);
 
 /*
@@ -190,12 +204,14 @@ dsa_status dsa_cache_append(const dsa_dims* dims, const void* k_I_new, const voi
  * dsa_block_summaries: summaries [B][pages * 64][d_I] bf16, pages = ceil(max_blocks / 64): row
  *   b * pages * 64 + lb of every valid logical block lb of sequence b (lb < ceil(seq_len / 64))
  *   receives the mean of the block's valid keys -- fp32 sum in token order of the keys' values
- *   (FP8: code * block scale in fp32), fp32 division by the count, bf16 round to nearest even.
+ *   (FP8: code * block scale in fp32; MXFP8: code * 2^(byte - 127)), fp32 division by the count,
+ *   bf16 round to nearest even.
  *   Other rows are not written. Any workspace with ws_bytes >= 256 (only its error word is used).
  * dsa_indexer_topk_hier: arguments as dsa_indexer_topk (bf16 modes only; DSA_F32 gives
  *   DSA_ERR_UNSUPPORTED), plus the summaries and n_sel (1..2048):
  *   1. coarse: the n_sel blocks with the largest indexer score of their summary (the indexer
- *      formula with the summary as the key; ties to the lower block) among the blocks
+ *      formula with the summary as the key and the bf16 q_I as given, also in DSA_MXFP8; ties to
+ *      the lower block) among the blocks
  *      0 .. pos(t) / 64 of the row's sequence;
  *   2. fine: the K largest indexer scores (ties to the lower position) among the tokens of the
  *      chosen blocks with s <= pos(t).
@@ -207,15 +223,15 @@ size_t dsa_hier_workspace_size(const dsa_dims* dims, int32_t T, int32_t n_sel);
 /* After dsa_cache_append of the same T new tokens (same q_seq / q_pos convention, seq_lens after
  * the append): recomputes the summaries of the blocks those tokens touched, exactly as
  * dsa_block_summaries would (the other blocks' summaries are unchanged by an append). */
-dsa_status dsa_block_summaries_append(const dsa_dims* dims, const void* k_I_cache, const float* k_I_scale,
+dsa_status dsa_block_summaries_append(const dsa_dims* dims, const void* k_I_cache, const void* k_I_scale,
                                       const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
                                       const int32_t* q_pos, int32_t T, uint16_t* summaries, void* ws, size_t ws_bytes,
                                       dsa_stream_t stream);
-dsa_status dsa_block_summaries(const dsa_dims* dims, const void* k_I_cache, const float* k_I_scale,
+dsa_status dsa_block_summaries(const dsa_dims* dims, const void* k_I_cache, const void* k_I_scale,
                                const int32_t* block_table, const int32_t* seq_lens, uint16_t* summaries, void* ws,
                                size_t ws_bytes, dsa_stream_t stream);
 dsa_status dsa_indexer_topk_hier(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
-                                 const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                                 const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                                  const int32_t* q_seq, const int32_t* q_pos, int32_t T, const uint16_t* summaries,
                                  int32_t n_sel, int32_t* idx, int32_t* blocks_out, void* ws, size_t ws_bytes,
                                  dsa_stream_t stream);
@@ -246,7 +262,7 @@ dsa_status dsa_indexer_topk_hier(const dsa_dims* dims, const void* q_I, const fl
  */
 #define DSA_NOALLOC_SCRATCH_BYTES (16u << 20)
 dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
-                                    const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                                    const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                                     const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx,
                                     int32_t* fault_word, dsa_stream_t stream);
 

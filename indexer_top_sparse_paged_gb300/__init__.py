@@ -28,7 +28,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdsa.so")
 _lib = None
 
-MODES = {"f32": 0, "bf16": 1, "bf16_kfp8": 2}
+MODES = {"f32": 0, "bf16": 1, "bf16_kfp8": 2, "mxfp8": 3}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "launch", 5: "device fault",
           6: "timeout", 7: "too large for the static scratch"}
 

@@ -10,7 +10,8 @@
 // block) the first new token of every touched block requantises the whole block: with
 // x = code * scale_old (fp32) for the block's earlier tokens and the new keys' values,
 // scale = amax / 448 (1 when amax is 0) and every code becomes RNE_e4m3(x / scale), saturating
-// at +-448. The new tokens of one block must be consecutive rows (ascending positions).
+// at +-448. The new tokens of one block must be consecutive rows (ascending positions). MXFP8
+// keys have no block state: each new key's groups of 32 get their own E8M0 scale and codes.
 #include "internal.h"
 
 namespace dsa {
@@ -29,7 +30,7 @@ struct AppendArgs {
     const int32_t* q_seq;
     const int32_t* q_pos;
     void* k_cache;
-    float* k_scale;
+    void* k_scale;
     void* kv_cache;
     int* err;
 };
@@ -70,6 +71,26 @@ __global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(AppendArgs
     const int act = a.mode == DSA_F32 ? 4 : 2;
     copy_row(static_cast<uint8_t*>(a.kv_cache) + row * a.d * act, static_cast<const uint8_t*>(a.kv_new) + static_cast<int64_t>(t) * a.d * act,
              a.d * act);
+    if (a.mode == DSA_MXFP8) {  // every group of 32 of the new key is quantised on its own
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.k_new) + static_cast<int64_t>(t) * a.d_I);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.k_cache) + row * a.d_I);
+        for (int g = threadIdx.x; g < a.d_I / 32; g += kAppendThreads) {
+            uint32_t w[16], codes[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = src[4 * g + i];
+                w[4 * i] = v.x;
+                w[4 * i + 1] = v.y;
+                w[4 * i + 2] = v.z;
+                w[4 * i + 3] = v.w;
+            }
+            const int X = mx_encode32(w, codes);
+            dst[2 * g] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            dst[2 * g + 1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+            static_cast<uint8_t*>(a.k_scale)[row * (a.d_I / 32) + g] = static_cast<uint8_t>(X + 127);
+        }
+        return;
+    }
     if (a.mode != DSA_BF16_KFP8) {
         copy_row(static_cast<uint8_t*>(a.k_cache) + row * a.d_I * act,
                  static_cast<const uint8_t*>(a.k_new) + static_cast<int64_t>(t) * a.d_I * act, a.d_I * act);
@@ -94,7 +115,7 @@ __global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(AppendArgs
     __syncthreads();
     const int m = run_end - t;
     const int n_old = pos - lb * kBlock;  // the block's earlier tokens: slots [0, n_old)
-    const float old_scale = a.k_scale[blk];
+    const float old_scale = static_cast<const float*>(a.k_scale)[blk];
     uint8_t* codes = static_cast<uint8_t*>(a.k_cache) + static_cast<int64_t>(blk) * kBlock * a.d_I;
     const uint16_t* knew = static_cast<const uint16_t*>(a.k_new) + static_cast<int64_t>(t) * a.d_I;
     const int n_elem_old = n_old * a.d_I, n_elem_new = m * a.d_I;
@@ -123,12 +144,12 @@ __global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(AppendArgs
         codes[(pu % kBlock) * a.d_I + i % a.d_I] =
             static_cast<uint8_t>(__nv_cvt_float_to_fp8(x / scale, __NV_SATFINITE, __NV_E4M3));
     }
-    if (threadIdx.x == 0) a.k_scale[blk] = scale;
+    if (threadIdx.x == 0) static_cast<float*>(a.k_scale)[blk] = scale;
 }
 
 bool launch_cache_append(const dsa_dims& d, const void* k_new, const void* kv_new, const int32_t* block_table,
                          const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T, void* k_cache,
-                         float* k_scale, void* kv_cache, int* err, cudaStream_t s, int* launches) {
+                         void* k_scale, void* kv_cache, int* err, cudaStream_t s, int* launches) {
     if (T == 0) return true;
     AppendArgs a{d.mode, d.B, d.max_blocks, d.num_blocks, d.d_I, d.d, T, k_new, kv_new, block_table, seq_lens,
                  q_seq, q_pos, k_cache, k_scale, kv_cache, err};

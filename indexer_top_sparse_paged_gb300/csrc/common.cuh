@@ -388,6 +388,86 @@ __device__ __forceinline__ void store_bf16_row(uint8_t* stage, int r, const uint
 }
 
 // ------------------------------------------------------------------------------------------------
+// MXFP8 (OCP Microscaling Formats: E4M3 elements sharing one E8M0 scale 2^(byte - 127) per 32)
+// ------------------------------------------------------------------------------------------------
+
+// 2^(byte - 127) as fp32; byte 0 is the subnormal 2^-127. Byte 255 (NaN in the MX format) is not
+// a supported input (it reads as +inf).
+__device__ __forceinline__ float e8m0_value(uint32_t byte) { return __uint_as_float(byte ? (byte << 23) : 0x00400000u); }
+
+// Shared exponent of a group whose largest magnitude is amax (finite): X = floor(log2(amax)) - 8,
+// at least -127 (so -127 for amax = 0). amax's fp32 exponent field is floor(log2(amax)) + 127
+// for normal values; subnormal amax (field 0) lies below 2^-126 and clamps to -127.
+__device__ __forceinline__ int mx_exponent(float amax) {
+    const int E = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+    return max(E - 135, -127);
+}
+
+// OCP MX quantisation of 32 bf16 values (16 words of two, the lower element in the low half):
+// returns the shared exponent X and writes the codes RNE_e4m3(x * 2^-X), saturating at +-448,
+// four per word (element 4i + k in byte k of word i). x * 2^-X is exact in fp32 whenever the
+// code can be non-zero.
+__device__ __forceinline__ int mx_encode32(const uint32_t (&w)[16], uint32_t (&codes)[8]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+    }
+    const int X = mx_exponent(amax);                                          // -127 .. 119
+    const float down = __uint_as_float(static_cast<uint32_t>(127 - X) << 23);  // 2^-X, a normal float
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t word = w[2 * i + (k >> 1)];
+            const float x = __uint_as_float((k & 1) ? (word & 0xFFFF0000u) : (word << 16));
+            c |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(x * down, __NV_SATFINITE, __NV_E4M3)) << (8 * k);
+        }
+        codes[i] = c;
+    }
+    return X;
+}
+
+// 16 e4m3 codes times the power of two f -> 16 bf16. The fp32 products are exact (at most 4
+// significant bits, magnitudes >= 2^-136); so is their bf16 rounding unless a value lies below
+// bf16's normal range (an MX exponent under -117).
+__device__ __forceinline__ void e4m3x16_to_bf16_scaled(const uint4& in, float f, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+            const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * hlf)) & 0xFFFFu);
+            const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+            const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+            const __nv_bfloat162 b = __floats2bfloat162_rn(v.x * f, v.y * f);
+            o[2 * i + hlf] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// As store_bf16_row for MXFP8 keys of width 128: byte g of `scales` is the E8M0 scale of
+// elements 32g..32g+31 (codes group c holds elements 16c..16c+15, so it takes byte c / 2).
+__device__ __forceinline__ void store_bf16_row_mx(uint8_t* stage, int r, const uint4 (&codes)[8], uint32_t scales) {
+    uint8_t* dst = stage + r * 128;
+    const int sw = r & 7;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4 lo, hi;
+        e4m3x16_to_bf16_scaled(codes[c], e8m0_value((scales >> (8 * (c >> 1))) & 0xFFu), lo, hi);
+        uint8_t* row = dst + (c >> 2) * (128 * 128);
+        const int g = 2 * (c & 3);
+        *reinterpret_cast<uint4*>(row + ((g ^ sw) << 4)) = lo;
+        *reinterpret_cast<uint4*>(row + (((g + 1) ^ sw) << 4)) = hi;
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
 // kernel parameter blocks
 // ------------------------------------------------------------------------------------------------
 
@@ -399,7 +479,7 @@ struct IndexerArgs {
     const void* q_I;
     const float* w;
     const void* k_I;
-    const float* k_I_scale;
+    const void* k_I_scale;
     const int32_t* block_table;
     const int32_t* seq_lens;
     const int32_t* q_seq;  // may be null: row t is sequence t
@@ -419,6 +499,7 @@ struct IndexerArgs {
     float* scores;              // [T][max_blocks * 64] fp32 scores of the GEMM rows (NaN: excluded)
     int G2;                     // score GEMM CTAs
     int self_plan;              // 1: the decode indexer computes the work plan itself (no plan kernel)
+    int after_quant;            // 1: q_I is the MX-quantised copy written by this call's first kernel
 };
 
 // Is query row t scored by the prefill GEMM (written by the plan)?

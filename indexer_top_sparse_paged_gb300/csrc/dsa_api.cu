@@ -51,11 +51,12 @@ bool set_max_dynamic_smem(const void* func, size_t bytes) {
 }
 
 bool indexer_uses_tc(const dsa_dims& d) {
-    return (d.mode == DSA_BF16 || d.mode == DSA_BF16_KFP8) && d.H_I == 64 && d.d_I == 128;
+    return (d.mode == DSA_BF16 || d.mode == DSA_BF16_KFP8 || d.mode == DSA_MXFP8) && d.H_I == 64 && d.d_I == 128;
 }
 
 bool attn_uses_tc(const dsa_dims& d) {
-    return (d.mode == DSA_BF16 || d.mode == DSA_BF16_KFP8) && d.H == 128 && d.d == 576 && d.d_v == 512;
+    return (d.mode == DSA_BF16 || d.mode == DSA_BF16_KFP8 || d.mode == DSA_MXFP8) && d.H == 128 && d.d == 576 &&
+           d.d_v == 512;
 }
 
 int indexer_ctas(const dsa_dims& d) {
@@ -96,6 +97,8 @@ WsLayout ws_layout(const dsa_dims& d, int T, bool allow_prefill) {
     off = align256(off + sizeof(int32_t) * (static_cast<size_t>(w.G) + T));
     w.slots = off;
     off = align256(off + sizeof(uint64_t) * (static_cast<size_t>(w.G) + T) * d.K);
+    w.q_mx = off;
+    if (d.mode == DSA_MXFP8) off = align256(off + sizeof(uint16_t) * static_cast<size_t>(T) * d.H_I * d.d_I);
     w.idx = off;
     off = align256(off + sizeof(int32_t) * static_cast<size_t>(T) * d.K);
     w.part_o = off;
@@ -149,7 +152,7 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static dsa_status check_common(const dsa_dims* d) {
     if (!d) return DSA_ERR_INVALID_ARG;
-    if (d->mode < DSA_F32 || d->mode > DSA_BF16_KFP8) return DSA_ERR_UNSUPPORTED;
+    if (d->mode < DSA_F32 || d->mode > DSA_MXFP8) return DSA_ERR_UNSUPPORTED;
     if (d->block_size != kBlock) return DSA_ERR_UNSUPPORTED;
     if (d->B <= 0 || d->max_blocks <= 0 || d->num_blocks <= 0) return DSA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(d->num_blocks) * kBlock >= (1ll << 31)) return DSA_ERR_UNSUPPORTED;
@@ -164,9 +167,17 @@ static dsa_status check_indexer_dims(const dsa_dims* d) {
     if (d->H_I <= 0 || d->d_I <= 0) return DSA_ERR_INVALID_ARG;
     if (indexer_uses_tc(*d)) return DSA_OK;
     if (d->H_I > 64 || d->d_I > 256) return DSA_ERR_UNSUPPORTED;
-    const int unit = d->mode == DSA_F32 ? 4 : (d->mode == DSA_BF16 ? 8 : 16);
+    const int unit = d->mode == DSA_F32 ? 4 : (d->mode == DSA_BF16 ? 8 : (d->mode == DSA_MXFP8 ? 32 : 16));
     if (d->d_I % unit) return DSA_ERR_UNSUPPORTED;
     return DSA_OK;
+}
+
+// The key scales a mode needs: fp32 per block (FP8 keys) or E8M0 bytes, 16-byte aligned (MXFP8,
+// fetched with bulk copies).
+static bool scale_ok(const dsa_dims* d, const void* k_I_scale) {
+    if (d->mode == DSA_BF16_KFP8) return k_I_scale != nullptr;
+    if (d->mode == DSA_MXFP8) return k_I_scale != nullptr && aligned16(k_I_scale);
+    return true;
 }
 
 static dsa_status check_attn_dims(const dsa_dims* d) {
@@ -186,7 +197,7 @@ static dsa_status check_ws(const dsa_dims* d, int T, void* ws, size_t ws_bytes) 
 }
 
 static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w, const void* k_I_cache,
-                              const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                              const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                               const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx, void* ws,
                               cudaStream_t stream, int* launches, bool allow_prefill = true) {
     const WsLayout L = ws_layout(*d, T, allow_prefill);
@@ -221,6 +232,13 @@ static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w
     a.gemm_tile_prefix = reinterpret_cast<int32_t*>(base + L.gemm_tile_prefix);
     a.scores = reinterpret_cast<float*>(base + L.scores);
     a.G2 = device_sm_count();
+    if (d->mode == DSA_MXFP8) {  // the quantised query first; the indexer kernels read it as bf16
+        void* q_mx = base + L.q_mx;
+        if (!launch_mx_quantize_q(q_I, q_mx, static_cast<int64_t>(T) * d->H_I * d->d_I, stream, launches))
+            return DSA_ERR_LAUNCH;
+        a.q_I = q_mx;
+        a.after_quant = 1;
+    }
     // decode calls on the tensor-core indexer plan inside its kernel (no plan kernel, no gap)
     a.self_plan = (a.NG == 0 && indexer_uses_tc(*d) && T <= kSelfPlanRows) ? 1 : 0;
     if (!a.self_plan && !launch_plan(a, stream, launches)) return DSA_ERR_LAUNCH;
@@ -362,7 +380,7 @@ dsa_status dsa_workspace_init(void* ws, size_t ws_bytes, dsa_stream_t stream) {
 }
 
 dsa_status dsa_indexer_topk(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
-                            const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                            const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                             const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx, void* ws,
                             size_t ws_bytes, dsa_stream_t stream) {
     dsa_status st = check_indexer_dims(dims);
@@ -370,7 +388,7 @@ dsa_status dsa_indexer_topk(const dsa_dims* dims, const void* q_I, const float* 
     if (T < 0) return DSA_ERR_INVALID_ARG;
     if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
     if (T > 0 && (!q_I || !w || !k_I_cache || !block_table || !seq_lens || !idx)) return DSA_ERR_INVALID_ARG;
-    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!scale_ok(dims, k_I_scale)) return DSA_ERR_INVALID_ARG;
     if (!aligned16(q_I) || !aligned16(w) || !aligned16(k_I_cache)) return DSA_ERR_INVALID_ARG;
     st = check_ws(dims, T, ws, ws_bytes);
     if (st != DSA_OK) return st;
@@ -402,7 +420,7 @@ dsa_status dsa_sparse_attn(const dsa_dims* dims, const void* q, const void* kv_c
 }
 
 dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
-                      const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens, const void* q,
+                      const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens, const void* q,
                       const void* kv_cache, float sm_scale, int32_t* idx, void* out, float* lse, void* ws,
                       size_t ws_bytes, dsa_stream_t stream) {
     dsa_status st = check_indexer_dims(dims);
@@ -411,7 +429,7 @@ dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, con
     if (st != DSA_OK) return st;
     const int T = dims->B;
     if (!q_I || !w || !k_I_cache || !block_table || !seq_lens || !q || !kv_cache || !out) return DSA_ERR_INVALID_ARG;
-    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!scale_ok(dims, k_I_scale)) return DSA_ERR_INVALID_ARG;
     if (!aligned16(q_I) || !aligned16(w) || !aligned16(k_I_cache) || !aligned16(q) || !aligned16(kv_cache) ||
         !aligned16(out))
         return DSA_ERR_INVALID_ARG;
@@ -431,7 +449,7 @@ dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, con
 }
 
 dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
-                                    const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                                    const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                                     const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx,
                                     int32_t* fault_word, dsa_stream_t stream) {
     dsa_status st = check_indexer_dims(dims);
@@ -439,7 +457,7 @@ dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const
     if (T < 0) return DSA_ERR_INVALID_ARG;
     if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
     if (T > 0 && (!q_I || !w || !k_I_cache || !block_table || !seq_lens || !idx)) return DSA_ERR_INVALID_ARG;
-    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!scale_ok(dims, k_I_scale)) return DSA_ERR_INVALID_ARG;
     if (!aligned16(q_I) || !aligned16(w) || !aligned16(k_I_cache)) return DSA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(fault_word) & 3u) return DSA_ERR_INVALID_ARG;
     // the indexer uses the workspace regions up to the attention's (error word, plan, candidates)
@@ -463,16 +481,17 @@ dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const
 
 dsa_status dsa_cache_append(const dsa_dims* dims, const void* k_I_new, const void* kv_new,
                             const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
-                            const int32_t* q_pos, int32_t T, void* k_I_cache, float* k_I_scale, void* kv_cache,
+                            const int32_t* q_pos, int32_t T, void* k_I_cache, void* k_I_scale, void* kv_cache,
                             void* ws, size_t ws_bytes, dsa_stream_t stream) {
     dsa_status st = check_common(dims);
     if (st != DSA_OK) return st;
     if (T < 0 || dims->d_I <= 0 || dims->d <= 0) return DSA_ERR_INVALID_ARG;
     if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
     if (T > 0 && (!k_I_new || !kv_new || !block_table || !seq_lens || !k_I_cache || !kv_cache)) return DSA_ERR_INVALID_ARG;
-    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!scale_ok(dims, k_I_scale)) return DSA_ERR_INVALID_ARG;
     const int act = dims->mode == DSA_F32 ? 4 : 2;
     if ((dims->d * act) % 16 || (dims->d_I * act) % 16) return DSA_ERR_UNSUPPORTED;
+    if (dims->mode == DSA_MXFP8 && dims->d_I % 32) return DSA_ERR_UNSUPPORTED;
     if (!aligned16(k_I_new) || !aligned16(kv_new) || !aligned16(k_I_cache) || !aligned16(kv_cache))
         return DSA_ERR_INVALID_ARG;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return DSA_ERR_WORKSPACE;
@@ -489,14 +508,15 @@ size_t dsa_hier_workspace_size(const dsa_dims* dims, int32_t T, int32_t n_sel) {
     return hier_layout(*dims, T, n_sel).total;
 }
 
-dsa_status dsa_block_summaries(const dsa_dims* dims, const void* k_I_cache, const float* k_I_scale,
+dsa_status dsa_block_summaries(const dsa_dims* dims, const void* k_I_cache, const void* k_I_scale,
                                const int32_t* block_table, const int32_t* seq_lens, uint16_t* summaries, void* ws,
                                size_t ws_bytes, dsa_stream_t stream) {
     dsa_status st = check_common(dims);
     if (st != DSA_OK) return st;
     if (dims->d_I <= 0) return DSA_ERR_INVALID_ARG;
+    if (dims->mode == DSA_MXFP8 && dims->d_I % 32) return DSA_ERR_UNSUPPORTED;
     if (!k_I_cache || !block_table || !seq_lens || !summaries) return DSA_ERR_INVALID_ARG;
-    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!scale_ok(dims, k_I_scale)) return DSA_ERR_INVALID_ARG;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return DSA_ERR_WORKSPACE;
     int launches = 0;
     if (!launch_block_summaries(*dims, k_I_cache, k_I_scale, block_table, seq_lens, summaries, static_cast<int*>(ws),
@@ -506,16 +526,17 @@ dsa_status dsa_block_summaries(const dsa_dims* dims, const void* k_I_cache, cons
     return st;
 }
 
-dsa_status dsa_block_summaries_append(const dsa_dims* dims, const void* k_I_cache, const float* k_I_scale,
+dsa_status dsa_block_summaries_append(const dsa_dims* dims, const void* k_I_cache, const void* k_I_scale,
                                       const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
                                       const int32_t* q_pos, int32_t T, uint16_t* summaries, void* ws, size_t ws_bytes,
                                       dsa_stream_t stream) {
     dsa_status st = check_common(dims);
     if (st != DSA_OK) return st;
     if (T < 0 || dims->d_I <= 0) return DSA_ERR_INVALID_ARG;
+    if (dims->mode == DSA_MXFP8 && dims->d_I % 32) return DSA_ERR_UNSUPPORTED;
     if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
     if (T > 0 && (!k_I_cache || !block_table || !seq_lens || !summaries)) return DSA_ERR_INVALID_ARG;
-    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!scale_ok(dims, k_I_scale)) return DSA_ERR_INVALID_ARG;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return DSA_ERR_WORKSPACE;
     int launches = 0;
     if (!launch_summaries_append(*dims, k_I_cache, k_I_scale, block_table, seq_lens, q_seq, q_pos, T, summaries,
@@ -526,7 +547,7 @@ dsa_status dsa_block_summaries_append(const dsa_dims* dims, const void* k_I_cach
 }
 
 dsa_status dsa_indexer_topk_hier(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
-                                 const float* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
+                                 const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                                  const int32_t* q_seq, const int32_t* q_pos, int32_t T, const uint16_t* summaries,
                                  int32_t n_sel, int32_t* idx, int32_t* blocks_out, void* ws, size_t ws_bytes,
                                  dsa_stream_t stream) {
@@ -537,7 +558,7 @@ dsa_status dsa_indexer_topk_hier(const dsa_dims* dims, const void* q_I, const fl
     if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
     if (T == 0) return DSA_OK;
     if (!q_I || !w || !k_I_cache || !block_table || !seq_lens || !summaries || !idx) return DSA_ERR_INVALID_ARG;
-    if (dims->mode == DSA_BF16_KFP8 && !k_I_scale) return DSA_ERR_INVALID_ARG;
+    if (!scale_ok(dims, k_I_scale)) return DSA_ERR_INVALID_ARG;
     if (!aligned16(q_I) || !aligned16(w) || !aligned16(k_I_cache) || !aligned16(summaries)) return DSA_ERR_INVALID_ARG;
     const HierLayout H = hier_layout(*dims, T, n_sel);
     if (check_indexer_dims(&H.coarse) != DSA_OK) return DSA_ERR_UNSUPPORTED;

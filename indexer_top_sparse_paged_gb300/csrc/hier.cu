@@ -21,7 +21,7 @@ constexpr int kSumThreads = 128;
 // The summary of logical block lb of sequence b (one CTA): the mean of the block's valid keys,
 // fp32 sum in token order (never contracted), fp32 division, bf16 round to nearest even.
 __device__ void block_summary(int mode, int max_blocks, int num_blocks, int d_I, int sum_rows, const void* k_I,
-                              const float* k_scale, const int32_t* block_table, const int32_t* seq_lens, int b, int lb,
+                              const void* k_scale, const int32_t* block_table, const int32_t* seq_lens, int b, int lb,
                               uint16_t* summaries, int* err) {
     const int L = seq_lens[b];
     if (lb < 0 || lb * kBlock >= L || lb >= max_blocks) return;
@@ -31,7 +31,7 @@ __device__ void block_summary(int mode, int max_blocks, int num_blocks, int d_I,
         return;
     }
     const int cnt = min(kBlock, L - lb * kBlock);
-    const float sc = mode == DSA_BF16_KFP8 ? k_scale[blk] : 1.0f;
+    const float sc = mode == DSA_BF16_KFP8 ? static_cast<const float*>(k_scale)[blk] : 1.0f;
     uint16_t* dst = summaries + (static_cast<int64_t>(b) * sum_rows + lb) * d_I;
     for (int d = threadIdx.x; d < d_I; d += kSumThreads) {
         float acc = 0.0f;
@@ -42,7 +42,10 @@ __device__ void block_summary(int mode, int max_blocks, int num_blocks, int d_I,
             else if (mode == DSA_BF16) x = __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(k_I)[e]) << 16);
             else {
                 const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<const uint8_t*>(k_I)[e], __NV_E4M3);
-                x = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(&h)), sc);
+                const float f = mode == DSA_MXFP8
+                                    ? e8m0_value(static_cast<const uint8_t*>(k_scale)[(e / d_I) * (d_I / 32) + d / 32])
+                                    : sc;
+                x = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(&h)), f);
             }
             acc = __fadd_rn(acc, x);  // in token order, never contracted
         }
@@ -53,7 +56,7 @@ __device__ void block_summary(int mode, int max_blocks, int num_blocks, int d_I,
 // Every valid block: one per CTA (blockIdx.x = lb, blockIdx.y = b).
 __global__ void __launch_bounds__(kSumThreads) block_summaries_kernel(int mode, int max_blocks, int num_blocks,
                                                                       int d_I, int sum_rows, const void* k_I,
-                                                                      const float* k_scale, const int32_t* block_table,
+                                                                      const void* k_scale, const int32_t* block_table,
                                                                       const int32_t* seq_lens, uint16_t* summaries,
                                                                       int* err) {
     block_summary(mode, max_blocks, num_blocks, d_I, sum_rows, k_I, k_scale, block_table, seq_lens, blockIdx.y,
@@ -64,7 +67,7 @@ __global__ void __launch_bounds__(kSumThreads) block_summaries_kernel(int mode, 
 // consecutive) recomputes that block's summary from the updated cache.
 __global__ void __launch_bounds__(kSumThreads) summaries_append_kernel(int mode, int B, int max_blocks, int num_blocks,
                                                                        int d_I, int sum_rows, int T, const void* k_I,
-                                                                       const float* k_scale, const int32_t* block_table,
+                                                                       const void* k_scale, const int32_t* block_table,
                                                                        const int32_t* seq_lens, const int32_t* q_seq,
                                                                        const int32_t* q_pos, uint16_t* summaries, int* err) {
     const int t = blockIdx.x;
@@ -141,7 +144,7 @@ __global__ void hier_remap_kernel(int T, int n_sel, int K, const int32_t* bidx, 
         v < 0 ? -1 : bidx[static_cast<int64_t>(t) * n_sel + v / kBlock] * kBlock + v % kBlock;
 }
 
-bool launch_block_summaries(const dsa_dims& d, const void* k_I, const float* k_scale, const int32_t* block_table,
+bool launch_block_summaries(const dsa_dims& d, const void* k_I, const void* k_scale, const int32_t* block_table,
                             const int32_t* seq_lens, uint16_t* summaries, int* err, cudaStream_t s, int* launches) {
     const int sum_rows = (d.max_blocks + kBlock - 1) / kBlock * kBlock;
     block_summaries_kernel<<<dim3(d.max_blocks, d.B), kSumThreads, 0, s>>>(d.mode, d.max_blocks, d.num_blocks, d.d_I,
@@ -151,7 +154,7 @@ bool launch_block_summaries(const dsa_dims& d, const void* k_I, const float* k_s
     return cudaGetLastError() == cudaSuccess;
 }
 
-bool launch_summaries_append(const dsa_dims& d, const void* k_I, const float* k_scale, const int32_t* block_table,
+bool launch_summaries_append(const dsa_dims& d, const void* k_I, const void* k_scale, const int32_t* block_table,
                              const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T,
                              uint16_t* summaries, int* err, cudaStream_t s, int* launches) {
     if (T == 0) return true;

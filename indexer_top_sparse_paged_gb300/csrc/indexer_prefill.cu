@@ -18,6 +18,8 @@
 // warps per TMEM lane quarter = warp % 4, each taking two of the four rows, so the epilogue's
 // arithmetic keeps up with the tensor pipe); FP8 keys add warps 10..13, which widen the staged
 // e4m3 codes to bf16 operands exactly (as the decode indexer does), once per tile for all rows.
+// MXFP8 keys take the FP8 pipeline with each block's E8M0 scale bytes fetched beside its codes and
+// applied by the converters (see the decode indexer); q_I arrives MX-quantised.
 #include "internal.h"
 
 namespace dsa {
@@ -39,6 +41,8 @@ constexpr int kTmemCols = kAcc * kN;          // 512
 constexpr uint32_t kIdesc = idesc_f16(128, kN, 1u, 0u, 0u);
 constexpr int kF8TileBytes = kTileKeys * kDim;
 constexpr int kF8BlockBytes = kBlock * kDim;
+constexpr int kMxBlockBytes = kBlock * kDim / 32;  // MXFP8 scale bytes of one block: 256
+constexpr int kMxTileBytes = 2 * kMxBlockBytes;
 
 template <bool kFp8>
 struct Cfg {
@@ -48,7 +52,8 @@ struct Cfg {
     static constexpr size_t kOffQ = 0;
     static constexpr size_t kOffA = kOffQ + kQBytes;
     static constexpr size_t kOffF8 = kOffA + static_cast<size_t>(kStages) * kStageBytes;
-    static constexpr size_t kOffW = kOffF8 + (kFp8 ? static_cast<size_t>(kStages8) * kF8TileBytes : 0);
+    static constexpr size_t kOffF8S = kOffF8 + (kFp8 ? static_cast<size_t>(kStages8) * kF8TileBytes : 0);  // MX scales
+    static constexpr size_t kOffW = kOffF8S + (kFp8 ? static_cast<size_t>(kStages8) * kMxTileBytes : 0);
     static constexpr size_t kOffCtl = kOffW + kN * sizeof(float);
 };
 
@@ -78,9 +83,10 @@ __device__ __forceinline__ void group_shape(const IndexerArgs& a, int g, int& b,
     for (int q = 0; q < kRowsPerGroup; ++q) n = max(n, row_len(a, kRowsPerGroup * g + q));
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kMx>
 __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     indexer_prefill_kernel(IndexerArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
+    static_assert(kFp8 || !kMx, "MXFP8 keys take the FP8 pipeline");
     using C = Cfg<kFp8>;
     constexpr int kStages = C::kStages;
     constexpr int kStages8 = C::kStages8;
@@ -89,6 +95,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     const uint32_t sA = smem_u32(smem + C::kOffA);
     const uint32_t sQ = smem_u32(smem + C::kOffQ);
     const uint32_t sF8 = smem_u32(smem + C::kOffF8);
+    const uint32_t sF8S = smem_u32(smem + C::kOffF8S);
     float* sW = reinterpret_cast<float*>(smem + C::kOffW);
     Smem<kFp8>& S = *reinterpret_cast<Smem<kFp8>*>(smem + C::kOffCtl);
 
@@ -177,7 +184,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                     const bool good = v >= 0 && v < a.num_blocks;
                     if (inside && !good && lane == 0) atomicOr(a.err, DSA_FAULT_BLOCK_TABLE);
                     blk[p] = (inside && good) ? v : -1;
-                    if (blk[p] >= 0) bytes += kFp8 ? kF8BlockBytes : 2 * (kBlock * 128);
+                    if (blk[p] >= 0) bytes += kFp8 ? kF8BlockBytes + (kMx ? kMxBlockBytes : 0) : 2 * (kBlock * 128);
                 }
                 if (lane == 0) {
                     const uint32_t fb = kFp8 ? smem_u32(&S.full8[st]) : smem_u32(&S.full[st]);
@@ -187,6 +194,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                         if (blk[p] < 0) continue;
                         if (kFp8) {
                             tma_load_2d(sF8 + st * kF8TileBytes + p * kF8BlockBytes, &map_k, 0, blk[p] * kBlock, fb);
+                            if (kMx)
+                                bulk_load_g2s(sF8S + st * kMxTileBytes + p * kMxBlockBytes,
+                                              static_cast<const uint8_t*>(a.k_I_scale) +
+                                                  static_cast<int64_t>(blk[p]) * kMxBlockBytes,
+                                              kMxBlockBytes, fb);
                         } else {
                             const uint32_t dst = sA + st * kStageBytes + p * (kBlock * 128);
                             tma_load_2d(dst, &map_k, 0, blk[p] * kBlock, fb);
@@ -247,9 +259,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 if (!ok) break;
                 uint4 codes[8];
                 load_e4m3_row(smem + C::kOffF8 + s8 * kF8TileBytes, r, codes);
+                uint32_t mx = 0;  // the row's four E8M0 bytes
+                if (kMx) mx = *reinterpret_cast<const uint32_t*>(smem + C::kOffF8S + s8 * kMxTileBytes + r * 4);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.empty8[s8]));
-                store_bf16_row(smem + C::kOffA + st * kStageBytes, r, codes);
+                if (kMx) store_bf16_row_mx(smem + C::kOffA + st * kStageBytes, r, codes, mx);
+                else store_bf16_row(smem + C::kOffA + st * kStageBytes, r, codes);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.full[st]));
@@ -282,7 +297,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 const int blk = (s < n) ? bt[s >> 6] : -1;
                 const bool blk_ok = blk >= 0 && blk < a.num_blocks;
                 float sc = 1.0f;
-                if (kFp8) sc = blk_ok ? a.k_I_scale[blk] : 0.0f;
+                if (kFp8 && !kMx) sc = blk_ok ? static_cast<const float*>(a.k_I_scale)[blk] : 0.0f;
                 const bool got = mbar_wait(smem_u32(&S.tfull[acc]), ause & 1u, abort_flag, a.err);
                 if (named_bar_or(1, kEpiThreads, !got)) { ok = false; break; }  // one decision for all epilogue warps
                 tc_fence_after();
@@ -323,7 +338,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                         }
                     }
                     float score = (pa.x + pb.x) + (pa.y + pb.y);
-                    if (kFp8) score *= sc;
+                    if (kFp8 && !kMx) score *= sc;
                     if (s < nq[q]) srow[q * lmax + s] = blk_ok ? score : __uint_as_float(0x7FC00000u);
                 }
             }
@@ -340,7 +355,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     }
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kMx>
 static bool launch(const IndexerArgs& a, cudaStream_t s, int* launches) {
     CUtensorMap map_q, map_k;
     if (!make_tmap_2d(&map_q, a.q_I, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kDim, static_cast<uint64_t>(a.T) * kHeads,
@@ -356,8 +371,8 @@ static bool launch(const IndexerArgs& a, cudaStream_t s, int* launches) {
             return false;
     }
     const size_t smem = smem_bytes<kFp8>();
-    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(indexer_prefill_kernel<kFp8>), smem)) return false;
-    if (!launch_kernel(true, indexer_prefill_kernel<kFp8>, dim3(a.G2), dim3(Cfg<kFp8>::kThreads), smem, s, a, map_q,
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(indexer_prefill_kernel<kFp8, kMx>), smem)) return false;
+    if (!launch_kernel(true, indexer_prefill_kernel<kFp8, kMx>, dim3(a.G2), dim3(Cfg<kFp8>::kThreads), smem, s, a, map_q,
                        map_k))
         return false;
     ++*launches;
@@ -367,7 +382,8 @@ static bool launch(const IndexerArgs& a, cudaStream_t s, int* launches) {
 }  // namespace tcpre
 
 bool launch_indexer_prefill(const IndexerArgs& a, cudaStream_t s, int* launches) {
-    return a.mode == DSA_BF16_KFP8 ? tcpre::launch<true>(a, s, launches) : tcpre::launch<false>(a, s, launches);
+    if (a.mode == DSA_MXFP8) return tcpre::launch<true, true>(a, s, launches);
+    return a.mode == DSA_BF16_KFP8 ? tcpre::launch<true, false>(a, s, launches) : tcpre::launch<false, false>(a, s, launches);
 }
 
 }  // namespace dsa

@@ -5,8 +5,11 @@
 //     S = sum_j w_j * max(0, scale_blk * (q_I[j] . k))
 // and offered to the CTA's Top-K buffer; no score leaves the chip. ("Day0 Inference Support ...
 // on Huawei Ascend CANN Architecture" §2.1: scoring, head-weight weighting and Top-K fused in one
-// operator that reads the paged cache directly.)
+// operator that reads the paged cache directly.) MXFP8 keys: every 16 codes are widened and
+// multiplied by their 32-element group's E8M0 scale (exact in fp32); q_I arrives MX-quantised.
 #include "internal.h"
+
+#include <type_traits>
 
 namespace dsa {
 
@@ -59,6 +62,10 @@ struct Widen<E4m3Tag> {
             for (int b = 0; b < 4; ++b) out[4 * i + b] = e4m3_to_float((w[i] >> (8 * b)) & 0xFFu);
     }
 };
+
+struct MxTag {};  // e4m3 codes with one E8M0 scale byte per 32 elements of a key
+template <>
+struct Widen<MxTag> : Widen<E4m3Tag> {};
 
 template <typename QT>
 __device__ __forceinline__ float load_act(const void* p, int64_t i);
@@ -113,7 +120,8 @@ __global__ void __launch_bounds__(kSimtThreads) indexer_simt_kernel(IndexerArgs 
                 int blk = -1;
                 if (lb * kBlock < n) blk = phys_block(a, b, lb);
                 blk_s[tid] = blk;
-                scale_s[tid] = (a.k_I_scale && blk >= 0) ? a.k_I_scale[blk] : 1.0f;
+                scale_s[tid] = (std::is_same<KT, E4m3Tag>::value && blk >= 0) ? static_cast<const float*>(a.k_I_scale)[blk]
+                                                                                : 1.0f;
             }
             topk.sync();
             for (int u = tid; u < kTileKeys * units_per_row; u += kSimtThreads) {
@@ -126,6 +134,12 @@ __global__ void __launch_bounds__(kSimtThreads) indexer_simt_kernel(IndexerArgs 
                                          ((static_cast<int64_t>(blk) * kBlock + (r & 63)) * d_I) * key_bytes +
                                          static_cast<int64_t>(c) * 16;
                     Widen<KT>::unpack(*reinterpret_cast<const uint4*>(src), vals);
+                    if constexpr (std::is_same<KT, MxTag>::value) {  // 16 codes lie in group c / 2 of the key
+                        const float f = e8m0_value(static_cast<const uint8_t*>(a.k_I_scale)
+                                                       [(static_cast<int64_t>(blk) * kBlock + (r & 63)) * (d_I / 32) + (c >> 1)]);
+#pragma unroll
+                        for (int e = 0; e < per; ++e) vals[e] *= f;
+                    }
                 } else {
 #pragma unroll
                     for (int e = 0; e < per; ++e) vals[e] = 0.0f;
@@ -175,6 +189,7 @@ bool launch_indexer_simt(const IndexerArgs& a, cudaStream_t s, int* launches) {
         case DSA_F32: return launch_typed<float, float>(a, s, launches);
         case DSA_BF16: return launch_typed<Bf16Tag, Bf16Tag>(a, s, launches);
         case DSA_BF16_KFP8: return launch_typed<E4m3Tag, Bf16Tag>(a, s, launches);
+        case DSA_MXFP8: return launch_typed<MxTag, Bf16Tag>(a, s, launches);
         default: return false;
     }
 }

@@ -23,6 +23,13 @@
 // so the product is still exact-input bf16 x bf16 -> fp32; the block's scale multiplies the
 // accumulator in the epilogue, before the ReLU:
 //     S[s] = sum_j w_j * max(0, scale_blk * D[s, j]).
+//
+// MXFP8 keys (OCP Microscaling: one E8M0 scale per 32 elements of a key) take the FP8 pipeline;
+// the TMA producer also fetches each block's 256 scale bytes (64 keys x 4) with an untiled bulk
+// copy into the same stage, and the converters multiply every code by its group's power of two
+// while widening (exact), so no scale is left for the epilogue. q_I arrives already MX-quantised
+// (and decoded to bf16, exactly) by this call's first kernel ("Day0 Inference Support ... on
+// Huawei Ascend CANN Architecture" §3: MXFP8 dynamic quantisation in the indexing stage).
 #include "internal.h"
 
 namespace dsa {
@@ -40,6 +47,8 @@ constexpr int kTmemCols = kAcc * 64;
 constexpr uint32_t kIdesc = idesc_f16(128, kHeads, 1u, 0u, 0u);
 constexpr int kF8TileBytes = kTileKeys * kDim;  // e4m3 codes of one tile: 16 KB
 constexpr int kF8BlockBytes = kBlock * kDim;    // one 64-token block: 8 KB
+constexpr int kMxBlockBytes = kBlock * kDim / 32;  // MXFP8 scale bytes of one block: 256
+constexpr int kMxTileBytes = 2 * kMxBlockBytes;
 
 constexpr int kRing = 16;  // score tiles between the scoring warps and the Top-K warps (bf16 keys)
 
@@ -53,7 +62,8 @@ struct Cfg {
     static constexpr size_t kOffA = 0;
     static constexpr size_t kOffQ = kOffA + static_cast<size_t>(kStages) * kStageBytes;
     static constexpr size_t kOffF8 = kOffQ + kQBytes;
-    static constexpr size_t kOffBuf = kOffF8 + (kFp8 ? static_cast<size_t>(kStages8) * kF8TileBytes : 0);
+    static constexpr size_t kOffF8S = kOffF8 + (kFp8 ? static_cast<size_t>(kStages8) * kF8TileBytes : 0);  // MX scales
+    static constexpr size_t kOffBuf = kOffF8S + (kFp8 ? static_cast<size_t>(kStages8) * kMxTileBytes : 0);
 };
 
 template <bool kFp8>
@@ -154,9 +164,10 @@ static_assert(topk_cap(2048) <= static_cast<uint32_t>(kEpiThreads * kTopkPer), "
 static_assert(smem_bytes<false>(2048) <= kSmemLimit, "indexer shared memory over the limit");
 static_assert(smem_bytes<true>(2048) <= kSmemLimit, "FP8 indexer shared memory over the limit");
 
-template <bool kFp8>
+template <bool kFp8, bool kMx>
 __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     indexer_tc_kernel(IndexerArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
+    static_assert(kFp8 || !kMx, "MXFP8 keys take the FP8 pipeline");
     using C = Cfg<kFp8>;
     constexpr int kStages = C::kStages;
     constexpr int kStages8 = C::kStages8;
@@ -165,6 +176,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     const uint32_t sA = smem_u32(smem + C::kOffA);
     const uint32_t sQ = smem_u32(smem + C::kOffQ);
     const uint32_t sF8 = smem_u32(smem + C::kOffF8);
+    const uint32_t sF8S = smem_u32(smem + C::kOffF8S);
     uint64_t* buf = reinterpret_cast<uint64_t*>(smem + C::kOffBuf);
     float* ring = reinterpret_cast<float*>(smem + C::kOffBuf + static_cast<size_t>(topk_cap(a.K)) * 8);  // [kRing][128]
     Smem<kFp8>& S = *reinterpret_cast<Smem<kFp8>*>(reinterpret_cast<uint8_t*>(ring) +
@@ -295,7 +307,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                     const bool good = v >= 0 && v < a.num_blocks;
                     if (inside && !good && lane == 0) atomicOr(a.err, DSA_FAULT_BLOCK_TABLE);
                     blk[p] = (inside && good) ? v : -1;
-                    if (blk[p] >= 0) bytes += kFp8 ? kF8BlockBytes : 2 * (kBlock * 128);
+                    if (blk[p] >= 0) bytes += kFp8 ? kF8BlockBytes + (kMx ? kMxBlockBytes : 0) : 2 * (kBlock * 128);
                 }
                 if (lane == 0) {
                     const uint32_t fb = kFp8 ? smem_u32(&S.full8[st]) : smem_u32(&S.full[st]);
@@ -305,6 +317,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                         if (blk[p] < 0) continue;
                         if (kFp8) {
                             tma_load_2d(sF8 + st * kF8TileBytes + p * kF8BlockBytes, &map_k, 0, blk[p] * kBlock, fb);
+                            if (kMx)
+                                bulk_load_g2s(sF8S + st * kMxTileBytes + p * kMxBlockBytes,
+                                              static_cast<const uint8_t*>(a.k_I_scale) +
+                                                  static_cast<int64_t>(blk[p]) * kMxBlockBytes,
+                                              kMxBlockBytes, fb);
                         } else {
                             const uint32_t dst = sA + st * kStageBytes + p * (kBlock * 128);
                             tma_load_2d(dst, &map_k, 0, blk[p] * kBlock, fb);
@@ -463,9 +480,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 if (!ok) break;
                 uint4 codes[8];
                 load_e4m3_row(smem + C::kOffF8 + s8 * kF8TileBytes, r, codes);
+                uint32_t mx = 0;  // the row's four E8M0 bytes
+                if (kMx) mx = *reinterpret_cast<const uint32_t*>(smem + C::kOffF8S + s8 * kMxTileBytes + r * 4);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.empty8[s8]));  // codes are in registers
-                store_bf16_row(smem + C::kOffA + st * kStageBytes, r, codes);
+                if (kMx) store_bf16_row_mx(smem + C::kOffA + st * kStageBytes, r, codes, mx);
+                else store_bf16_row(smem + C::kOffA + st * kStageBytes, r, codes);
                 fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.full[st]));
@@ -500,7 +520,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 const int blk = (s < n) ? bt[s >> 6] : -1;  // issued before the wait: latency hidden
                 const bool blk_ok = blk >= 0 && blk < a.num_blocks;
                 float sc = 1.0f;
-                if (kFp8) sc = blk_ok ? a.k_I_scale[blk] : 0.0f;
+                if (kFp8 && !kMx) sc = blk_ok ? static_cast<const float*>(a.k_I_scale)[blk] : 0.0f;
                 const bool got = mbar_wait(smem_u32(&S.tfull[acc]), ause & 1u, abort_flag, a.err);
                 if (named_bar_or(1, kEpiThreads, !got)) { ok = false; break; }
                 tc_fence_after();
@@ -548,7 +568,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                     }
                 }
                 float score = (p0 + p1) + (p2 + p3);
-                if (kFp8) score *= sc;
+                if (kFp8 && !kMx) score *= sc;
                 // a block whose table entry is invalid was never loaded: its keys do not count
                 const bool valid = s < n && blk_ok;
                 topk.push(make_key(score, static_cast<uint32_t>(s)), valid);
@@ -569,7 +589,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     }
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kMx>
 static bool launch(const IndexerArgs& a, cudaStream_t s, int* launches) {
     CUtensorMap map_q, map_k;
     if (!make_tmap_2d(&map_q, a.q_I, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kDim, static_cast<uint64_t>(a.T) * kHeads,
@@ -585,9 +605,11 @@ static bool launch(const IndexerArgs& a, cudaStream_t s, int* launches) {
             return false;
     }
     const size_t smem = smem_bytes<kFp8>(a.K);
-    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(indexer_tc_kernel<kFp8>), smem)) return false;
-    // the first kernel of the call when it plans itself: it waits for all earlier work on the stream
-    if (!launch_kernel(!a.self_plan, indexer_tc_kernel<kFp8>, dim3(a.G), dim3(Cfg<kFp8>::kThreads), smem, s, a, map_q, map_k))
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(indexer_tc_kernel<kFp8, kMx>), smem)) return false;
+    // the first kernel of the call when it plans itself (and q_I needs no quantisation): it waits
+    // for all earlier work on the stream
+    if (!launch_kernel(!a.self_plan || a.after_quant, indexer_tc_kernel<kFp8, kMx>, dim3(a.G),
+                       dim3(Cfg<kFp8>::kThreads), smem, s, a, map_q, map_k))
         return false;
     ++*launches;
     return true;
@@ -596,7 +618,8 @@ static bool launch(const IndexerArgs& a, cudaStream_t s, int* launches) {
 }  // namespace tcidx
 
 bool launch_indexer_tc(const IndexerArgs& a, cudaStream_t s, int* launches) {
-    return a.mode == DSA_BF16_KFP8 ? tcidx::launch<true>(a, s, launches) : tcidx::launch<false>(a, s, launches);
+    if (a.mode == DSA_MXFP8) return tcidx::launch<true, true>(a, s, launches);
+    return a.mode == DSA_BF16_KFP8 ? tcidx::launch<true, false>(a, s, launches) : tcidx::launch<false, false>(a, s, launches);
 }
 
 

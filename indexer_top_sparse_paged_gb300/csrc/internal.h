@@ -30,6 +30,7 @@ struct WsLayout {
     size_t merge_count;  // int32 [3][T + G/8 + 1] finished children of the merge tree's groups (levels 2..4)
     size_t slot_count;   // int32 [G + T]
     size_t slots;        // uint64 [G + T][K]
+    size_t q_mx;         // bf16 [T][H_I][d_I] the MX-quantised q_I (DSA_MXFP8 only)
     size_t idx;          // int32 [T][K] (dsa_decode without a caller idx)
     size_t part_o;       // fp32 [T][S][H][d_v]
     size_t part_ml;      // fp32 [T][S][2 CTAs][H][2] (m, l)
@@ -89,6 +90,8 @@ bool launch_indexer_simt(const IndexerArgs& a, cudaStream_t s, int* launches);
 bool launch_indexer_tc(const IndexerArgs& a, cudaStream_t s, int* launches);
 bool launch_indexer_prefill(const IndexerArgs& a, cudaStream_t s, int* launches);
 bool launch_prefill_topk(const IndexerArgs& a, cudaStream_t s, int* launches);
+// MXFP8 q_I: `elements` bf16 values (a multiple of 32) -> their MXFP8 values as bf16, into `out`
+bool launch_mx_quantize_q(const void* q_I, void* out, int64_t elements, cudaStream_t s, int* launches);
 
 struct AttnArgs {
     int mode;
@@ -112,9 +115,9 @@ struct AttnArgs {
 };
 
 bool launch_attn_simt(const AttnArgs& a, cudaStream_t s, int* launches);
-bool launch_block_summaries(const dsa_dims& d, const void* k_I, const float* k_scale, const int32_t* block_table,
+bool launch_block_summaries(const dsa_dims& d, const void* k_I, const void* k_scale, const int32_t* block_table,
                             const int32_t* seq_lens, uint16_t* summaries, int* err, cudaStream_t s, int* launches);
-bool launch_summaries_append(const dsa_dims& d, const void* k_I, const float* k_scale, const int32_t* block_table,
+bool launch_summaries_append(const dsa_dims& d, const void* k_I, const void* k_scale, const int32_t* block_table,
                              const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T,
                              uint16_t* summaries, int* err, cudaStream_t s, int* launches);
 bool launch_hier_setup(int B, int pages, int T, const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos,
@@ -127,7 +130,7 @@ bool launch_hier_remap(int T, int n_sel, int K, const int32_t* bidx, const int32
                        int* err, cudaStream_t s, int* launches);
 bool launch_cache_append(const dsa_dims& d, const void* k_new, const void* kv_new, const int32_t* block_table,
                          const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T, void* k_cache,
-                         float* k_scale, void* kv_cache, int* err, cudaStream_t s, int* launches);
+                         void* k_scale, void* kv_cache, int* err, cudaStream_t s, int* launches);
 bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches);
 
 }  // namespace dsa

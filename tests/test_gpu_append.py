@@ -60,7 +60,7 @@ def _check(case, seed, explicit_rows=True):
     assert len(diff) == 0, f"indexer-key blocks differ: {diff[:5]}"
 
 
-@pytest.mark.parametrize("mode", ["f32", "bf16", "bf16_kfp8"])
+@pytest.mark.parametrize("mode", ["f32", "bf16", "bf16_kfp8", "mxfp8"])
 def test_decode_append_one_token_per_sequence(mode):
     kw = dict(H_I=8, d_I=32, H=4, d=64, d_v=48) if mode == "f32" else {}
     spec = small_spec(mode, [1, 63, 64, 65, 128, 500, 2049], 64, **kw)
@@ -68,7 +68,7 @@ def test_decode_append_one_token_per_sequence(mode):
     _check(case, 202, explicit_rows=False)
 
 
-@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8"])
+@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8", "mxfp8"])
 def test_prefill_append_crosses_blocks(mode):
     spec = small_spec(mode, [300, 1000, 77, 4096], 64, new_tokens=[150, 1, 13, 200])
     case = W.generate(spec, seed=203)

@@ -34,7 +34,7 @@ def _gpu_hier(dev, case, summ, n_sel, explicit_rows=True):
     return idx.cpu().numpy(), blocks.cpu().numpy()
 
 
-@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8"])
+@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8", "mxfp8"])
 def test_block_summaries_bit_exact(mode):
     spec = small_spec(mode, [1, 63, 64, 65, 700, 5000], 64)
     case = W.generate(spec, seed=501)
@@ -65,7 +65,7 @@ def _check_fine(case, t, gpu_row, oracle_blocks, S_row, K):
     return (sk - sk1) / (abs(sk) if sk else 1.0) > REL_GAP
 
 
-@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8"])
+@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8", "mxfp8"])
 def test_hierarchical_decode_and_prefill_rows(mode):
     spec = small_spec(mode, [20000, 9000, 3000, 700, 16384], 512, new_tokens=[1, 1, 6, 1, 9])
     case = W.generate(spec, seed=502 if mode == "bf16" else 503)
@@ -116,7 +116,7 @@ def test_planted_block_is_found():
     assert idx[0][:64].tolist() == list(range(40 * 64, 41 * 64)) and np.all(idx[0][64:] == -1)
 
 
-@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8"])
+@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8", "mxfp8"])
 def test_summaries_follow_the_cache_append(mode):
     """Append new tokens (a decode token, a chunk crossing blocks), update only the touched
     blocks' summaries, and compare with the oracle's summaries of the oracle's appended cache."""

@@ -20,10 +20,12 @@ def _noalloc(dev: Dev, fault_word=None):
     return idx.cpu().numpy()
 
 
-@pytest.mark.parametrize("which", ["tc_ragged", "simt_fp8", "decode_b32"])
+@pytest.mark.parametrize("which", ["tc_ragged", "simt_fp8", "decode_b32", "tc_mxfp8"])
 def test_noalloc_matches_workspace_call_twice(which):
     if which == "tc_ragged":
         case = W.generate(small_spec("bf16", [3000, 130, 2049, 64], 2048), seed=301)
+    elif which == "tc_mxfp8":
+        case = W.generate(small_spec("mxfp8", [1500, 700, 64], 512), seed=305)
     elif which == "simt_fp8":
         case = W.generate(small_spec("bf16_kfp8", [1500, 700], 512, H_I=64, d_I=128), seed=302)
     else:
