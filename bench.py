@@ -48,12 +48,14 @@ PROFILE = os.path.join(ROOT, "profiles", "indexer_tc_decode_bf16_b32.md")
 
 def indexer_bytes(case) -> int:
     s = case.spec
-    key_b = {"f32": 4, "bf16": 2, "bf16_kfp8": 1}[s.mode] * s.d_I
+    key_b = {"f32": 4, "bf16": 2, "bf16_kfp8": 1, "mxfp8": 1}[s.mode] * s.d_I
     L = case.seq_lens.astype(np.int64)
     blocks = (L + 63) // 64
     b = int(L.sum()) * key_b
     if s.mode == "bf16_kfp8":
-        b += int(blocks.sum()) * 4
+        b += int(blocks.sum()) * 4                              # fp32 scale per block
+    if s.mode == "mxfp8":
+        b += int(L.sum()) * (s.d_I // 32)                       # E8M0 byte per 32 elements
     act = 4 if s.mode == "f32" else 2
     b += s.T * s.H_I * s.d_I * act + s.T * s.H_I * 4           # q_I, w
     b += int(blocks.sum()) * 4 + s.B * 4                        # block-table entries, seq_lens
@@ -297,6 +299,43 @@ def run_prefill(steps: int, warmup: int, dev, flush):
     return res
 
 
+def run_key_formats(case, steps: int, dev, flush):
+    """The decode indexer over the same keys re-stored in the two 8-bit formats (FP8 e4m3 with a
+    per-block scale, MXFP8): CUDA-event time per call with L2 flushed, algorithmic bytes, HBM
+    fraction. The attention half of the step does not read the indexer keys."""
+    import indexer_top_sparse_paged_gb300 as dsa
+    peak, kind = measured_peaks()
+    res = {}
+    stream = torch.cuda.current_stream(dev)
+    for mode in ("bf16_kfp8", "mxfp8"):
+        c = W.with_key_format(case, mode)
+        s = c.spec
+        dims = dsa.make_dims(mode, s.B, c.max_blocks, c.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K)
+        q_I, w, k_I, ksc = to_dev(c.q_I, dev), to_dev(c.w, dev), to_dev(c.k_I, dev), to_dev(c.k_I_scale, dev)
+        bt, sl = to_dev(c.block_table, dev), to_dev(c.seq_lens, dev)
+        ws = dsa.workspace(dims, s.T, dev)
+        idx = torch.empty((s.T, s.K), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            dsa.indexer_topk(dims, q_I, w, k_I, ksc, bt, sl, ws=ws, idx=idx)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            dsa.indexer_topk(dims, q_I, w, k_I, ksc, bt, sl, ws=ws, idx=idx)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        if dsa.read_error(ws) != 0:
+            raise RuntimeError(f"device fault bits set while timing the {mode} indexer")
+        us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+        ib = indexer_bytes(c)
+        res[mode] = {"indexer_us": round(us, 2), "indexer_bytes": ib, "gbs": round(ib / (us * 1e-6) / 1e9, 1),
+                     "hbm_frac_of_" + kind: round(ib / (us * 1e-6) / 1e9 / peak, 4),
+                     "gpu_launches": dsa.last_launch_count()}
+        del q_I, w, k_I, ksc, bt, sl, ws, idx
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, world):
     import indexer_top_sparse_paged_gb300 as dsa
 
@@ -438,7 +477,7 @@ def run_ours(args, rank, world):
                    "parallelism": f"replicas x{world}", "l2": "flushed (256 MiB write) before every timed step",
                    "step_bytes": step_bytes, "indexer_bytes": ib, "attention_bytes": ab},
         "breakdown_us": {"indexer_topk": round(idx_avg * 1e3, 2), "sparse_attn": round(statistics.mean(att_ms) * 1e3, 2)},
-        "roofline": {"kernel": "dsa_indexer_topk (plan + indexer_tc_kernel + topk_merge)", "bound": "hbm",
+        "roofline": {"kernel": "dsa_indexer_topk (indexer_tc_kernel + topk_merge)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                      "algorithmic_bytes_per_launch": ib},
@@ -449,6 +488,7 @@ def run_ours(args, rank, world):
         "cache_append": {"us": round(app_us, 2), "rows": s.T, "bytes": app_bytes,
                          "note": "dsa_cache_append of the batch's new keys and latent rows (launch-bound at 32 rows)"},
     }
+    res["indexer_key_formats"] = run_key_formats(case, max(3, min(args.steps, 20)), dev, flush)
     if not args.no_prefill:
         res["prefill"] = run_prefill(max(3, min(args.steps, 10)), args.warmup, dev, flush)
     if rank == 0 and not args.no_cpu_baseline:

@@ -6,12 +6,15 @@ The GPU computes every row; the fp64 oracle checks a sample of rows (it scores o
 * 1M-token decode with FP8 e4m3 indexer keys (one fp32 scale per 64-token block);
 * chunked prefill, 2 x 4096 new tokens on a 61,440-token cached prefix (64K in total);
 * a mixed serving batch: 64 decode rows (contexts log-uniform in [1K, 256K]) plus one
-  2048-token prefill chunk at 128K, FP8 keys.
+  2048-token prefill chunk at 128K, FP8 keys;
+* the chunked prefill with an MXFP8 indexer (MX keys, MX-quantised queries).
 
 Index sets follow the same rule as the other parity tests (exact where the oracle's K-th gap
 exceeds 1e-3 relative, else the 1e-3 band); attention is compared with the oracle evaluated on
 the GPU's own index sets, max-abs 2e-2 (bf16 outputs).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -57,4 +60,12 @@ def test_mixed_serving_batch_full_size():
     case = W.generate(spec, seed)
     n_dec = 64
     rows = np.concatenate([np.arange(n_dec), n_dec + np.linspace(0, spec.T - n_dec - 1, 8).astype(np.int64)])
+    _check_rows(case, rows)
+
+
+def test_chunked_prefill_2x4096_mxfp8_full_size():
+    spec, seed = W.named(4)
+    case = W.generate(dataclasses.replace(spec, mode="mxfp8"), seed)
+    T = spec.T
+    rows = np.array([0, 1, 2047, T // 2 - 1, T // 2, T // 2 + 3001, T - 1])
     _check_rows(case, rows)

@@ -271,6 +271,35 @@ def generate(spec: Spec, seed: int, chunk_blocks: int = 1024) -> Case:
     return Case(spec, seed, table, lens.astype(np.int32), q_seq, q_pos, q_I, w, k_I, scale, q, kv)
 
 
+def with_key_format(case: Case, mode: str) -> Case:
+    """The same case with its bf16 indexer keys re-stored as ``"bf16_kfp8"`` (e4m3 codes with one
+    fp32 scale per physical block, amax / 448 over the block's tokens) or ``"mxfp8"`` (OCP MX codes
+    and E8M0 bytes per 32 elements). Slots that hold no token get the poison code; every other
+    input (queries, weights, latent cache, block table) is shared with ``case``."""
+    import dataclasses
+    assert case.spec.mode == "bf16" and mode in ("bf16_kfp8", "mxfp8")
+    bs = case.spec.block_size
+    x = bf16_bits_to_f32(case.k_I)
+    valid = np.zeros(x.shape[:2], dtype=bool)
+    for b, L in enumerate(case.seq_lens.tolist()):
+        nblk = (L + bs - 1) // bs
+        blks = case.block_table[b, :nblk]
+        valid[blks] = True
+        if L % bs:
+            valid[blks[-1], L % bs:] = False
+    x[~valid] = 0.0
+    if mode == "mxfp8":
+        codes, scale = to_mx_e4m3(x)
+        scale[~valid] = 127
+    else:
+        amax = np.abs(x).reshape(x.shape[0], -1).max(axis=1)
+        scale = (amax / np.float32(448.0)).astype(np.float32)
+        scale[scale == 0] = 1.0
+        codes = to_e4m3_codes(x / scale[:, None, None])
+    codes[~valid] = POISON_E4M3
+    return dataclasses.replace(case, spec=dataclasses.replace(case.spec, mode=mode), k_I=codes, k_I_scale=scale)
+
+
 def repage(case: Case, seed: int) -> Case:
     """Same logical content under another physical block permutation."""
     rng = np.random.default_rng(seed)
