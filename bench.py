@@ -296,6 +296,26 @@ def run_prefill(steps: int, warmup: int, dev, flush):
     res["gpu_launches_per_step"] = n_idx + dsa.last_launch_count()
     del r
     torch.cuda.empty_cache()
+    # the indexer over the same keys stored in the two 8-bit formats (scores on the same GEMM)
+    res["indexer_key_formats"] = {}
+    for mode in ("bf16_kfp8", "mxfp8"):
+        r = Resident(W.with_key_format(case, mode), dev)
+        for _ in range(3):
+            r.indexer()
+        evk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            evk[i][0].record(stream)
+            r.indexer()
+            evk[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        if dsa.read_error(r.ws) != 0:
+            raise RuntimeError(f"device fault bits set while timing the {mode} prefill indexer")
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evk)
+        res["indexer_key_formats"][mode] = {"indexer_ms": round(ms, 3),
+                                            "indexer_tflops": round(fi / (ms * 1e-3) / 1e12, 1)}
+        del r
+        torch.cuda.empty_cache()
     return res
 
 
@@ -564,7 +584,9 @@ def run_profile(args):
     """warmup + 1 steps of one case and nothing else (for ncu):
       decode         the default workload (fused decode steps),
       prefill        the chunked prefill workload at full size (indexer + attention calls),
-      prefill-small  2 x 2048 new tokens on 16,384 (a small case of the prefill kernels)."""
+      prefill-small  2 x 2048 new tokens on 16,384 (a small case of the prefill kernels),
+      decode-fp8     the default workload's keys stored as FP8 e4m3 with a per-block scale,
+      decode-mx      the default workload's keys stored as MXFP8."""
     import indexer_top_sparse_paged_gb300 as dsa
 
     dev = torch.device("cuda", 0)
@@ -581,14 +603,17 @@ def run_profile(args):
         return
     spec, seed = W.named(2)
     case = W.generate(spec, seed)
+    if args.profile in ("decode-fp8", "decode-mx"):
+        case = W.with_key_format(case, "bf16_kfp8" if args.profile == "decode-fp8" else "mxfp8")
     s = case.spec
     dims = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K)
     q_I, w, k_I = to_dev(case.q_I, dev), to_dev(case.w, dev), to_dev(case.k_I, dev)
+    ksc = to_dev(case.k_I_scale, dev) if case.k_I_scale is not None else None
     q, kv = to_dev(case.q, dev), to_dev(case.kv, dev)
     bt, sl = to_dev(case.block_table, dev), to_dev(case.seq_lens, dev)
     ws = dsa.workspace(dims, s.T, dev)
     for _ in range(args.warmup + 1):
-        dsa.decode(dims, q_I, w, k_I, None, bt, sl, q, kv, s.sm_scale, ws=ws)
+        dsa.decode(dims, q_I, w, k_I, ksc, bt, sl, q, kv, s.sm_scale, ws=ws)
     torch.cuda.synchronize(dev)
     assert dsa.read_error(ws) == 0
 
@@ -605,7 +630,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill measurement")
-    ap.add_argument("--profile", nargs="?", const="decode", choices=["decode", "prefill", "prefill-small"],
+    ap.add_argument("--profile", nargs="?", const="decode", choices=["decode", "prefill", "prefill-small", "decode-fp8", "decode-mx"],
                     help="only run --warmup + 1 steps of one case (a short command for ncu captures)")
     args = ap.parse_args()
     if args.profile:

@@ -79,6 +79,7 @@ struct Smem {
     uint32_t hist[kEpiThreads / 32 * 256];
     TopkCtl ctl;
     uint32_t ring_valid[kRing][kEpiThreads / 32];  // validity bits of a ring tile's keys, per warp
+    alignas(16) float w_s[kHeads];                  // FP8 keys: the current row's head weights
 };
 
 constexpr int kTopkPer = 33;  // candidate keys per epilogue thread held in registers while selecting
@@ -501,17 +502,13 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         while (it.next(seg)) {
             const int t = seg.row;
             const int n = row_len(a, t);
-            float wv[kHeads];
-            const float4* w4 = reinterpret_cast<const float4*>(a.w + static_cast<int64_t>(t) * kHeads);
-#pragma unroll
-            for (int i = 0; i < kHeads / 4; ++i) {
-                const float4 v = w4[i];
-                wv[4 * i] = v.x;
-                wv[4 * i + 1] = v.y;
-                wv[4 * i + 2] = v.z;
-                wv[4 * i + 3] = v.w;
-            }
-            topk.reset();
+            // the row's head weights live in shared memory and are read back as broadcasts, so the
+            // registers hold the TMEM values and the Top-K candidates without spilling (the end of
+            // the previous segment was a group barrier: nobody still reads the old weights)
+            if (row < kHeads / 4)
+                reinterpret_cast<float4*>(S.w_s)[row] = reinterpret_cast<const float4*>(a.w + static_cast<int64_t>(t) * kHeads)[row];
+            topk.reset();  // a group barrier: the weights are visible
+            const float4* wv4 = reinterpret_cast<const float4*>(S.w_s);
             bool ok = true;
             const int32_t* bt = a.block_table + static_cast<int64_t>(row_seq(a, t)) * a.max_blocks;
             for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
@@ -538,33 +535,29 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                     // scale >= 0: max(0, scale * x) = scale * max(0, x), applied once to the sum
 #pragma unroll
                     for (int h = 0; h < 32; h += 4) {
-                        p0 = fmaf(wv[h], fmaxf(__uint_as_float(v0[h]), 0.0f), p0);
-                        p1 = fmaf(wv[h + 1], fmaxf(__uint_as_float(v0[h + 1]), 0.0f), p1);
-                        p2 = fmaf(wv[h + 2], fmaxf(__uint_as_float(v0[h + 2]), 0.0f), p2);
-                        p3 = fmaf(wv[h + 3], fmaxf(__uint_as_float(v0[h + 3]), 0.0f), p3);
-                    }
-#pragma unroll
-                    for (int h = 0; h < 32; h += 4) {
-                        p0 = fmaf(wv[32 + h], fmaxf(__uint_as_float(v1[h]), 0.0f), p0);
-                        p1 = fmaf(wv[33 + h], fmaxf(__uint_as_float(v1[h + 1]), 0.0f), p1);
-                        p2 = fmaf(wv[34 + h], fmaxf(__uint_as_float(v1[h + 2]), 0.0f), p2);
-                        p3 = fmaf(wv[35 + h], fmaxf(__uint_as_float(v1[h + 3]), 0.0f), p3);
+                        const float4 wa = wv4[h / 4], wb = wv4[8 + h / 4];
+                        p0 = fmaf(wa.x, fmaxf(__uint_as_float(v0[h]), 0.0f), p0);
+                        p1 = fmaf(wa.y, fmaxf(__uint_as_float(v0[h + 1]), 0.0f), p1);
+                        p2 = fmaf(wa.z, fmaxf(__uint_as_float(v0[h + 2]), 0.0f), p2);
+                        p3 = fmaf(wa.w, fmaxf(__uint_as_float(v0[h + 3]), 0.0f), p3);
+                        p0 = fmaf(wb.x, fmaxf(__uint_as_float(v1[h]), 0.0f), p0);
+                        p1 = fmaf(wb.y, fmaxf(__uint_as_float(v1[h + 1]), 0.0f), p1);
+                        p2 = fmaf(wb.z, fmaxf(__uint_as_float(v1[h + 2]), 0.0f), p2);
+                        p3 = fmaf(wb.w, fmaxf(__uint_as_float(v1[h + 3]), 0.0f), p3);
                     }
                 } else {
                     // scale < 0: max(0, scale * x) = scale * min(0, x)
 #pragma unroll
                     for (int h = 0; h < 32; h += 4) {
-                        p0 = fmaf(wv[h], fminf(__uint_as_float(v0[h]), 0.0f), p0);
-                        p1 = fmaf(wv[h + 1], fminf(__uint_as_float(v0[h + 1]), 0.0f), p1);
-                        p2 = fmaf(wv[h + 2], fminf(__uint_as_float(v0[h + 2]), 0.0f), p2);
-                        p3 = fmaf(wv[h + 3], fminf(__uint_as_float(v0[h + 3]), 0.0f), p3);
-                    }
-#pragma unroll
-                    for (int h = 0; h < 32; h += 4) {
-                        p0 = fmaf(wv[32 + h], fminf(__uint_as_float(v1[h]), 0.0f), p0);
-                        p1 = fmaf(wv[33 + h], fminf(__uint_as_float(v1[h + 1]), 0.0f), p1);
-                        p2 = fmaf(wv[34 + h], fminf(__uint_as_float(v1[h + 2]), 0.0f), p2);
-                        p3 = fmaf(wv[35 + h], fminf(__uint_as_float(v1[h + 3]), 0.0f), p3);
+                        const float4 wa = wv4[h / 4], wb = wv4[8 + h / 4];
+                        p0 = fmaf(wa.x, fminf(__uint_as_float(v0[h]), 0.0f), p0);
+                        p1 = fmaf(wa.y, fminf(__uint_as_float(v0[h + 1]), 0.0f), p1);
+                        p2 = fmaf(wa.z, fminf(__uint_as_float(v0[h + 2]), 0.0f), p2);
+                        p3 = fmaf(wa.w, fminf(__uint_as_float(v0[h + 3]), 0.0f), p3);
+                        p0 = fmaf(wb.x, fminf(__uint_as_float(v1[h]), 0.0f), p0);
+                        p1 = fmaf(wb.y, fminf(__uint_as_float(v1[h + 1]), 0.0f), p1);
+                        p2 = fmaf(wb.z, fminf(__uint_as_float(v1[h + 2]), 0.0f), p2);
+                        p3 = fmaf(wb.w, fminf(__uint_as_float(v1[h + 3]), 0.0f), p3);
                     }
                 }
                 float score = (p0 + p1) + (p2 + p3);
