@@ -425,28 +425,62 @@ def run_ours(args, rank, world):
     idx_ms = [a.elapsed_time(b) for a, b, _ in ev3]
     att_ms = [b.elapsed_time(c) for _, b, c in ev3]
 
-    # --- end to end through the public API with host buffers (pinned), copies inside the region
-    h_in = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v)).pin_memory()
-            for k, v in (("q_I", case.q_I), ("w", case.w), ("q", case.q), ("bt", case.block_table),
-                         ("sl", case.seq_lens))}
-    h_out = torch.empty((s.T, s.H, s.d_v), dtype=torch.bfloat16).pin_memory()
-    h_idx = torch.empty((s.T, s.K), dtype=torch.int32).pin_memory()
-    d_in = {"q_I": q_I.view(torch.int16), "w": w, "q": q.view(torch.int16), "bt": bt, "sl": sl}
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = h_out.numel() * 2 + h_idx.numel() * 4
+    # --- end to end through the public API with host buffers (pinned), copies inside the region:
+    #     the step's inputs travel in one staging buffer (one host->device copy), and out and idx
+    #     come back in one (one device->host copy)
+    def packed(arrays):
+        offs, off = [], 0
+        for a in arrays:
+            offs.append(off)
+            off = (off + a.nbytes + 255) // 256 * 256
+        return offs, off
+
+    host_in = [np.ascontiguousarray(a) for a in (case.q_I, case.w, case.q, case.block_table, case.seq_lens)]
+    in_offs, in_bytes = packed(host_in)
+    h_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
+    for a, o in zip(host_in, in_offs):
+        h_in[o:o + a.nbytes].copy_(torch.from_numpy(a.view(np.uint8).reshape(-1)))
+    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+
+    def view(buf, o, dtype, shape):
+        n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        return buf[o:o + n].view(dtype).view(shape)
+
+    e_qI = view(d_in, in_offs[0], torch.bfloat16, case.q_I.shape)
+    e_w = view(d_in, in_offs[1], torch.float32, case.w.shape)
+    e_q = view(d_in, in_offs[2], torch.bfloat16, case.q.shape)
+    e_bt = view(d_in, in_offs[3], torch.int32, case.block_table.shape)
+    e_sl = view(d_in, in_offs[4], torch.int32, case.seq_lens.shape)
+    o_off1 = (s.T * s.H * s.d_v * 2 + 255) // 256 * 256
+    o_bytes = o_off1 + s.T * s.K * 4
+    d_out = torch.empty(o_bytes, dtype=torch.uint8, device=dev)
+    e_out = view(d_out, 0, torch.bfloat16, (s.T, s.H, s.d_v))
+    e_idx = view(d_out, o_off1, torch.int32, (s.T, s.K))
+    h_out = torch.empty(o_bytes, dtype=torch.uint8).pin_memory()
+    h2d = sum(a.nbytes for a in host_in)
+    d2h = s.T * s.H * s.d_v * 2 + s.T * s.K * 4
+
+    def e2e_step():
+        d_in.copy_(h_in, non_blocking=True)
+        dsa.decode(dims, e_qI, e_w, k_I, None, e_bt, e_sl, e_q, kv, s.sm_scale, ws=ws, idx=e_idx, out=e_out, lse=lse)
+        h_out.copy_(d_out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     for i in range(args.steps):
         flush.zero_()
         e2e_ev[i][0].record(stream)
-        for k in h_in:
-            d_in[k].copy_(h_in[k], non_blocking=True)
-        step()
-        h_out.copy_(out, non_blocking=True)
-        h_idx.copy_(idx, non_blocking=True)
+        e2e_step()
         e2e_ev[i][1].record(stream)
     barrier()
     e2e_ms = [a.elapsed_time(b) for a, b in e2e_ev]
+    # the host copy of the last step's result is the device result
+    got_idx = h_out[o_off1:o_off1 + s.T * s.K * 4].view(torch.int32).view(s.T, s.K)
+    if not torch.equal(got_idx, idx.cpu()):
+        raise RuntimeError("end-to-end indices differ from the device-resident step's")
 
     if dsa.read_error(ws) != 0:
         raise RuntimeError("device fault bits set during the timed region")

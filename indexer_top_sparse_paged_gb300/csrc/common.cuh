@@ -153,8 +153,9 @@ __device__ __forceinline__ uint32_t group_excl_scan(uint32_t v, uint32_t* warp_t
 
 // Collective over NT threads (named barrier bar_id): the threshold thr such that exactly K of the
 // keys are >= thr (keys are distinct; more than K in total), over keys held in registers, keys[j]
-// valid for j < cnt; thread 0 must hold at least one key. MSB-first radix select with 8-bit
-// digits, starting below the bits all keys share, stopping as soon as the boundary bucket is taken
+// valid for j < cnt; thread 0 must hold at least one key. MSB-first radix select with digits of
+// up to 8 bits, the first one starting at the highest bit in which two keys differ (bit-aligned,
+// so no pass is spent on bits all keys share), stopping as soon as the boundary bucket is taken
 // whole. `hist` holds NT/32 private 256-bin histograms (one per warp, so warps never contend on a
 // hot bin); they are summed into the first one after every pass.
 // With max_passes, the select stops early and returns a threshold that keeps the whole boundary
@@ -181,18 +182,20 @@ __device__ uint64_t reg_radix_threshold(const uint64_t (&keys)[PER], uint32_t cn
     if (lane == 0 && d) atomicOr(&ctl->diff, static_cast<unsigned long long>(d));
     named_bar_sync(bar_id, NT);
     const int hi = 63 - __clzll(static_cast<long long>(ctl->diff | 1ull));
-    int shift = (hi >> 3) << 3;
-    uint64_t prefix = (shift >= 56) ? 0ull : (ref & (~0ull << (shift + 8)));
+    // digit window [shift, top): bits >= top are fixed (shared by every key, or chosen by earlier passes)
+    int top = hi + 1;
+    int shift = top > 8 ? top - 8 : 0;
+    uint64_t prefix = (top >= 64) ? 0ull : (ref & (~0ull << top));
     uint32_t rem = K;
-    for (; shift >= 0; shift -= 8) {
+    for (;;) {
+        const uint32_t dmask = (1u << (top - shift)) - 1u;
         for (uint32_t i = lane; i < 256; i += 32) my_hist[i] = 0;
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             const uint64_t k = keys[j];
-            const bool match =
-                static_cast<uint32_t>(j) < cnt && ((shift == 56) || ((k >> (shift + 8)) == (prefix >> (shift + 8))));
-            if (match) atomicAdd(&my_hist[static_cast<uint32_t>(k >> shift) & 255u], 1u);
+            const bool match = static_cast<uint32_t>(j) < cnt && ((top >= 64) || ((k >> top) == (prefix >> top)));
+            if (match) atomicAdd(&my_hist[static_cast<uint32_t>(k >> shift) & dmask], 1u);
         }
         named_bar_sync(bar_id, NT);
         for (uint32_t b = tid; b < 256; b += NT) {
@@ -233,7 +236,9 @@ __device__ uint64_t reg_radix_threshold(const uint64_t (&keys)[PER], uint32_t cn
         prefix |= static_cast<uint64_t>(ctl->digit) << shift;
         const bool done = ctl->bucket == rem;
         named_bar_sync(bar_id, NT);
-        if (done || --max_passes == 0) break;
+        if (done || shift == 0 || --max_passes == 0) break;
+        top = shift;
+        shift = top > 8 ? top - 8 : 0;
     }
     return prefix;
 }
