@@ -42,34 +42,47 @@ struct PtShared {
 };
 
 // One pass over the row: keeps, in position order, the keys >= thr of valid scores in sh.cand
-// (the first kPtCap of them) and returns how many there were. Per round, warp w owns 512
-// consecutive staged positions and walks them 32 at a time (lane = position, conflict-free
-// shared loads); warp ballots order the keys within a warp and a scan of the warp counts places
-// the warps.
+// (the first kPtCap of them) and returns how many there were. Per round, 16-byte loads stage
+// 8192 scores; warp w owns 512 consecutive staged positions and walks them 32 at a time (lane =
+// position, conflict-free shared loads); warp ballots order the keys within a warp and a scan of
+// the warp counts places the warps. The admission test works on the 32-bit ordered score bits
+// (the position half of the key only decides at the threshold's own score), and a 64-bit key is
+// built only for the keys that are kept.
 __device__ uint32_t compact_row(const float* srow, int n, uint64_t thr, PtShared& sh, uint32_t tid) {
     constexpr int kWarpSpan = kPtRound / (kPtThreads / 32);  // 512
     const uint32_t lane = tid & 31u, warp = tid >> 5;
+    const uint32_t thr_hi = static_cast<uint32_t>(thr >> 32), thr_lo = static_cast<uint32_t>(thr);
     uint32_t total = 0;
     for (int base = 0; base < n; base += kPtRound) {
         const int m = min(kPtRound, n - base);
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(srow + base);
+        // the row holds max_blocks * 64 scores (a multiple of 4), so a 16-byte load that starts
+        // before m stays inside it; its entries at or past m are masked
+        const uint4* src = reinterpret_cast<const uint4*>(srow + base);
 #pragma unroll
-        for (int k = 0; k < kPtPer; ++k) {
-            const int i = k * kPtThreads + static_cast<int>(tid);
-            sh.stage[i] = (i < m) ? __ldcs(src + i) : 0x7FC00000u;  // past the row: invalid
+        for (int k = 0; k < kPtPer / 4; ++k) {
+            const int q = k * kPtThreads + static_cast<int>(tid);
+            uint4 v = make_uint4(0x7FC00000u, 0x7FC00000u, 0x7FC00000u, 0x7FC00000u);  // past the row: invalid
+            if (4 * q < m) {
+                v = __ldcs(src + q);
+                if (4 * q + 1 >= m) v.y = 0x7FC00000u;
+                if (4 * q + 2 >= m) v.z = 0x7FC00000u;
+                if (4 * q + 3 >= m) v.w = 0x7FC00000u;
+            }
+            reinterpret_cast<uint4*>(sh.stage)[q] = v;
         }
         block_sync();
-        auto key_at = [&](int k, uint64_t& key) -> bool {
+        auto pass_at = [&](int k, uint32_t& hi, uint32_t& lo) -> bool {
             const int i = static_cast<int>(warp) * kWarpSpan + k * 32 + static_cast<int>(lane);
             const uint32_t bits = sh.stage[i];
-            key = score_valid(bits) ? score_key(bits, static_cast<uint32_t>(base + i)) : 0ull;
-            return key != 0ull && key >= thr;
+            hi = ordered_bits(__uint_as_float(bits));
+            lo = 0xFFFFFFFFu - static_cast<uint32_t>(base + i);
+            return score_valid(bits) && (hi > thr_hi || (hi == thr_hi && lo >= thr_lo));
         };
         uint32_t cnt = 0;
 #pragma unroll
         for (int k = 0; k < kWarpSpan / 32; ++k) {
-            uint64_t key;
-            cnt += __popc(__ballot_sync(0xFFFFFFFFu, key_at(k, key)));
+            uint32_t hi, lo;
+            cnt += __popc(__ballot_sync(0xFFFFFFFFu, pass_at(k, hi, lo)));
         }
         if (lane == 0) sh.warp_tot[warp] = cnt;
         block_sync();
@@ -83,11 +96,11 @@ __device__ uint32_t compact_row(const float* srow, int n, uint64_t thr, PtShared
         const uint32_t below = (1u << lane) - 1u;
 #pragma unroll
         for (int k = 0; k < kWarpSpan / 32; ++k) {
-            uint64_t key;
-            const bool pass = key_at(k, key);
+            uint32_t hi, lo;
+            const bool pass = pass_at(k, hi, lo);
             const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
             const uint32_t o = off + __popc(bal & below);
-            if (pass && o < static_cast<uint32_t>(kPtCap)) sh.cand[o] = key;
+            if (pass && o < static_cast<uint32_t>(kPtCap)) sh.cand[o] = (static_cast<uint64_t>(hi) << 32) | lo;
             off += __popc(bal);
         }
         total += round_total;
