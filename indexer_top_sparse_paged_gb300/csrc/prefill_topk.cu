@@ -45,13 +45,17 @@ struct PtShared {
 // (the first kPtCap of them) and returns how many there were. Per round, 16-byte loads stage
 // 8192 scores; warp w owns 512 consecutive staged positions and walks them 32 at a time (lane =
 // position, conflict-free shared loads); warp ballots order the keys within a warp and a scan of
-// the warp counts places the warps. The admission test works on the 32-bit ordered score bits
-// (the position half of the key only decides at the threshold's own score), and a 64-bit key is
-// built only for the keys that are kept.
+// the warp counts places the warps. The admission test is one fp32 comparison against the
+// threshold's score (the ordered score bits are monotonic in the score, with -0 = +0, and NaN
+// fails every comparison); the position half of the key only decides at the threshold's own
+// score, and a 64-bit key is built only for the keys that are kept.
 __device__ uint32_t compact_row(const float* srow, int n, uint64_t thr, PtShared& sh, uint32_t tid) {
     constexpr int kWarpSpan = kPtRound / (kPtThreads / 32);  // 512
     const uint32_t lane = tid & 31u, warp = tid >> 5;
     const uint32_t thr_hi = static_cast<uint32_t>(thr >> 32), thr_lo = static_cast<uint32_t>(thr);
+    // the score whose ordered bits are thr_hi (thr_hi = 0, below every valid score: -inf)
+    const float thr_f = thr_hi == 0u ? __uint_as_float(0xFF800000u)
+                                     : __uint_as_float((thr_hi & 0x80000000u) ? (thr_hi & 0x7FFFFFFFu) : ~thr_hi);
     uint32_t total = 0;
     for (int base = 0; base < n; base += kPtRound) {
         const int m = min(kPtRound, n - base);
@@ -71,18 +75,18 @@ __device__ uint32_t compact_row(const float* srow, int n, uint64_t thr, PtShared
             reinterpret_cast<uint4*>(sh.stage)[q] = v;
         }
         block_sync();
-        auto pass_at = [&](int k, uint32_t& hi, uint32_t& lo) -> bool {
+        auto pass_at = [&](int k, float& x, uint32_t& lo) -> bool {
             const int i = static_cast<int>(warp) * kWarpSpan + k * 32 + static_cast<int>(lane);
-            const uint32_t bits = sh.stage[i];
-            hi = ordered_bits(__uint_as_float(bits));
+            x = __uint_as_float(sh.stage[i]);
             lo = 0xFFFFFFFFu - static_cast<uint32_t>(base + i);
-            return score_valid(bits) && (hi > thr_hi || (hi == thr_hi && lo >= thr_lo));
+            return x > thr_f || (x == thr_f && lo >= thr_lo);
         };
         uint32_t cnt = 0;
 #pragma unroll
         for (int k = 0; k < kWarpSpan / 32; ++k) {
-            uint32_t hi, lo;
-            cnt += __popc(__ballot_sync(0xFFFFFFFFu, pass_at(k, hi, lo)));
+            float x;
+            uint32_t lo;
+            cnt += __popc(__ballot_sync(0xFFFFFFFFu, pass_at(k, x, lo)));
         }
         if (lane == 0) sh.warp_tot[warp] = cnt;
         block_sync();
@@ -96,11 +100,12 @@ __device__ uint32_t compact_row(const float* srow, int n, uint64_t thr, PtShared
         const uint32_t below = (1u << lane) - 1u;
 #pragma unroll
         for (int k = 0; k < kWarpSpan / 32; ++k) {
-            uint32_t hi, lo;
-            const bool pass = pass_at(k, hi, lo);
+            float x;
+            uint32_t lo;
+            const bool pass = pass_at(k, x, lo);
             const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
             const uint32_t o = off + __popc(bal & below);
-            if (pass && o < static_cast<uint32_t>(kPtCap)) sh.cand[o] = (static_cast<uint64_t>(hi) << 32) | lo;
+            if (pass && o < static_cast<uint32_t>(kPtCap)) sh.cand[o] = (static_cast<uint64_t>(ordered_bits(x)) << 32) | lo;
             off += __popc(bal);
         }
         total += round_total;
