@@ -3,9 +3,9 @@
 //
 //  1. A sample of the row (16 evenly spaced runs of 256 consecutive scores) gives an admission
 //     threshold: the score ranked about 1.5 K / n of the way down the sample.
-//  2. One pass over the row stages 8192 scores at a time in shared memory; every warp keeps the
-//     admitted keys of its 512 consecutive positions (ballots within the warp, a scan of the warp
-//     counts across warps), so the candidate buffer stays in position order.
+//  2. One pass over the row, 8192 scores per round read straight into registers (16 consecutive
+//     positions per lane); lane and warp count scans place the admitted keys, so the candidate
+//     buffer stays in position order.
 //  3. If at least K and at most the buffer's 8192 keys were admitted, the K-th key is found
 //     among them by a radix select in registers, and the kept positions are written in
 //     ascending order; every key of the true Top-K was admitted, since at least K keys score at
@@ -24,8 +24,7 @@ constexpr int kPtKeysPer = kPtCap / kPtThreads;     // 16 keys per thread in the
 constexpr int kPtSampleRuns = 16, kPtSampleRun = 256;
 constexpr int kPtSample = kPtSampleRuns * kPtSampleRun;  // 4096
 constexpr int kPtSamplePer = kPtSample / kPtThreads;     // 8
-constexpr size_t kPtSmem = static_cast<size_t>(kPtCap) * 8 + static_cast<size_t>(kPtRound) * 4 +
-                           kPtThreads / 32 * 256 * 4;
+constexpr size_t kPtSmem = static_cast<size_t>(kPtCap) * 8 + kPtThreads / 32 * 256 * 4;
 
 __device__ __forceinline__ bool score_valid(uint32_t bits) { return (bits & 0x7FFFFFFFu) <= 0x7F800000u; }
 
@@ -35,82 +34,83 @@ __device__ __forceinline__ uint64_t score_key(uint32_t bits, uint32_t pos) {
 
 struct PtShared {
     uint64_t* cand;   // [kPtCap]
-    uint32_t* stage;  // [kPtRound] raw score bits
     uint32_t* hist;   // [16][256]
     TopkCtl* ctl;
     uint32_t* warp_tot;
 };
 
 // One pass over the row: keeps, in position order, the keys >= thr of valid scores in sh.cand
-// (the first kPtCap of them) and returns how many there were. Per round, 16-byte loads stage
-// 8192 scores; warp w owns 512 consecutive staged positions and walks them 32 at a time (lane =
-// position, conflict-free shared loads); warp ballots order the keys within a warp and a scan of
-// the warp counts places the warps. The admission test is one fp32 comparison against the
-// threshold's score (the ordered score bits are monotonic in the score, with -0 = +0, and NaN
-// fails every comparison); the position half of the key only decides at the threshold's own
-// score, and a 64-bit key is built only for the keys that are kept.
+// (the first kPtCap of them) and returns how many there were. Per round of 8192 positions, warp w
+// owns 512 consecutive positions and lane l of it the 16 consecutive positions from 16 l, read
+// straight from global memory with 16-byte loads: a lane marks its admitted scores in a bit mask,
+// a scan of the lanes' counts and of the warps' counts places every lane's keys, so the candidate
+// buffer stays in position order with one barrier per round. The admission test is one fp32
+// comparison against the threshold's score (the ordered score bits are monotonic in the score,
+// with -0 = +0, and NaN fails every comparison); the position half of the key only decides at
+// the threshold's own score, and a 64-bit key is built only for the keys that are kept.
 __device__ uint32_t compact_row(const float* srow, int n, uint64_t thr, PtShared& sh, uint32_t tid) {
     constexpr int kWarpSpan = kPtRound / (kPtThreads / 32);  // 512
+    constexpr int kLanePer = kWarpSpan / 32;                 // 16
     const uint32_t lane = tid & 31u, warp = tid >> 5;
     const uint32_t thr_hi = static_cast<uint32_t>(thr >> 32), thr_lo = static_cast<uint32_t>(thr);
     // the score whose ordered bits are thr_hi (thr_hi = 0, below every valid score: -inf)
     const float thr_f = thr_hi == 0u ? __uint_as_float(0xFF800000u)
                                      : __uint_as_float((thr_hi & 0x80000000u) ? (thr_hi & 0x7FFFFFFFu) : ~thr_hi);
-    uint32_t total = 0;
-    for (int base = 0; base < n; base += kPtRound) {
-        const int m = min(kPtRound, n - base);
-        // the row holds max_blocks * 64 scores (a multiple of 4), so a 16-byte load that starts
-        // before m stays inside it; its entries at or past m are masked
-        const uint4* src = reinterpret_cast<const uint4*>(srow + base);
+    const bool score_only = thr_lo <= 1u;  // 1: every valid key (positions never reach 0xFFFFFFFF)
+    uint32_t total = 0, parity = 0;
+    for (int base = 0; base < n; base += kPtRound, parity ^= 1u) {
+        const int p0 = base + static_cast<int>(warp) * kWarpSpan + static_cast<int>(lane) * kLanePer;
+        float x[kLanePer];
 #pragma unroll
-        for (int k = 0; k < kPtPer / 4; ++k) {
-            const int q = k * kPtThreads + static_cast<int>(tid);
-            uint4 v = make_uint4(0x7FC00000u, 0x7FC00000u, 0x7FC00000u, 0x7FC00000u);  // past the row: invalid
-            if (4 * q < m) {
-                v = __ldcs(src + q);
-                if (4 * q + 1 >= m) v.y = 0x7FC00000u;
-                if (4 * q + 2 >= m) v.z = 0x7FC00000u;
-                if (4 * q + 3 >= m) v.w = 0x7FC00000u;
-            }
-            reinterpret_cast<uint4*>(sh.stage)[q] = v;
+        for (int k = 0; k < kLanePer / 4; ++k) {
+            // the row holds max_blocks * 64 scores (a multiple of 4): a 16-byte load that starts
+            // before n stays inside it; positions at or past n are masked below
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (p0 + 4 * k < n) v = __ldcs(reinterpret_cast<const float4*>(srow + p0 + 4 * k));
+            x[4 * k] = v.x;
+            x[4 * k + 1] = v.y;
+            x[4 * k + 2] = v.z;
+            x[4 * k + 3] = v.w;
         }
-        block_sync();
-        auto pass_at = [&](int k, float& x, uint32_t& lo) -> bool {
-            const int i = static_cast<int>(warp) * kWarpSpan + k * 32 + static_cast<int>(lane);
-            x = __uint_as_float(sh.stage[i]);
-            lo = 0xFFFFFFFFu - static_cast<uint32_t>(base + i);
-            return x > thr_f || (x == thr_f && lo >= thr_lo);
-        };
-        uint32_t cnt = 0;
+        uint32_t mask = 0;
 #pragma unroll
-        for (int k = 0; k < kWarpSpan / 32; ++k) {
-            float x;
-            uint32_t lo;
-            cnt += __popc(__ballot_sync(0xFFFFFFFFu, pass_at(k, x, lo)));
+        for (int j = 0; j < kLanePer; ++j) {
+            const int p = p0 + j;
+            const uint32_t lo = 0xFFFFFFFFu - static_cast<uint32_t>(p);
+            const bool pass = p < n && (score_only ? (x[j] >= thr_f) : (x[j] > thr_f || (x[j] == thr_f && lo >= thr_lo)));
+            mask |= (pass ? 1u : 0u) << j;
         }
-        if (lane == 0) sh.warp_tot[warp] = cnt;
+        const uint32_t c = static_cast<uint32_t>(__popc(mask));
+        uint32_t incl = c;  // inclusive scan of the lanes' counts
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= static_cast<uint32_t>(o)) incl += y;
+        }
+        // warp totals alternate between two halves of warp_tot: the next round may write its
+        // totals while a slower warp still reads this round's
+        uint32_t* wt = sh.warp_tot + parity * (kPtThreads / 32);
+        if (lane == 31) wt[warp] = incl;
         block_sync();
-        uint32_t off = total, round_total = 0;
+        uint32_t off = total + incl - c, round_total = 0;
 #pragma unroll
         for (uint32_t w = 0; w < kPtThreads / 32; ++w) {
-            const uint32_t c = sh.warp_tot[w];
-            off += (w < warp) ? c : 0u;
-            round_total += c;
+            const uint32_t cw = wt[w];
+            off += (w < warp) ? cw : 0u;
+            round_total += cw;
         }
-        const uint32_t below = (1u << lane) - 1u;
 #pragma unroll
-        for (int k = 0; k < kWarpSpan / 32; ++k) {
-            float x;
-            uint32_t lo;
-            const bool pass = pass_at(k, x, lo);
-            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
-            const uint32_t o = off + __popc(bal & below);
-            if (pass && o < static_cast<uint32_t>(kPtCap)) sh.cand[o] = (static_cast<uint64_t>(ordered_bits(x)) << 32) | lo;
-            off += __popc(bal);
+        for (int j = 0; j < kLanePer; ++j) {
+            if ((mask >> j) & 1u) {
+                if (off < static_cast<uint32_t>(kPtCap))
+                    sh.cand[off] = (static_cast<uint64_t>(ordered_bits(x[j])) << 32) |
+                                   (0xFFFFFFFFu - static_cast<uint32_t>(p0 + j));
+                ++off;
+            }
         }
         total += round_total;
-        block_sync();  // the stage and the warp counts are rewritten by the next round
     }
+    block_sync();  // the candidates are complete
     return total;
 }
 
@@ -194,9 +194,8 @@ __global__ void __launch_bounds__(kPtThreads, 2) prefill_topk_kernel(IndexerArgs
     const int t = blockIdx.x;
     if (!gemm_row(a, t)) return;
     const uint32_t tid = threadIdx.x;
-    PtShared sh{reinterpret_cast<uint64_t*>(pt_smem),
-                reinterpret_cast<uint32_t*>(pt_smem + static_cast<size_t>(kPtCap) * 8),
-                reinterpret_cast<uint32_t*>(pt_smem + static_cast<size_t>(kPtCap) * 8 + kPtRound * 4), &ctl, warp_tot};
+    PtShared sh{reinterpret_cast<uint64_t*>(pt_smem), reinterpret_cast<uint32_t*>(pt_smem + static_cast<size_t>(kPtCap) * 8),
+                &ctl, warp_tot};
     const uint32_t K = static_cast<uint32_t>(a.K);
     const int n = row_len(a, t);
     const float* srow = a.scores + static_cast<int64_t>(t) * a.max_blocks * kBlock;
