@@ -319,9 +319,13 @@ struct TopkGroup {
     }
 
     // Keeps the K largest keys of buf (in order) and raises the admission threshold.
-    // (mid-stream: two radix passes bound the threshold tightly enough; the flush is exact)
+    // (mid-stream: two radix passes bound the threshold tightly enough; the flush is exact). Two
+    // passes keep the whole boundary bucket, which can be most of the buffer when many keys share
+    // one score (e.g. scores that the ReLU made exactly 0): then the exact selection runs, so the
+    // next push always has room.
     __device__ void select() {
         count = select_to(buf, 2);
+        if (count + NT > cap) count = select_to(buf);
         sync();
     }
 
