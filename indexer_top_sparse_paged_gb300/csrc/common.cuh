@@ -324,8 +324,10 @@ struct TopkGroup {
     // one score (e.g. scores that the ReLU made exactly 0): then the exact selection runs, so the
     // next push always has room.
     __device__ void select() {
-        count = select_to(buf, 2);
-        if (count + NT > cap) count = select_to(buf);
+        for (int passes = 2;; passes = 64) {  // one call site: the exact retry is rare
+            count = select_to(buf, passes);
+            if (count + NT <= cap || passes > 2) break;
+        }
         sync();
     }
 

@@ -67,3 +67,20 @@ def test_long_row_k2048_merge_tree():
 def test_prefill_gemm_and_mixed_groups():
     spec = small_spec("mxfp8", [700, 5000, 20000, 10000], 1024, new_tokens=[1, 1, 1, 14])
     _full_check(_spread_scales(W.generate(spec, seed=508), 509), attn_rows=np.array([0, 2, 3, 16]))
+
+
+def test_misaligned_or_missing_scales_are_rejected():
+    """The E8M0 scales are fetched with 16-byte bulk copies: a misaligned or missing scale pointer
+    is an argument error (nothing is launched), not a fault."""
+    import torch
+
+    import indexer_top_sparse_paged_gb300 as dsa
+    spec = small_spec("mxfp8", [300, 900], 256)
+    dev = Dev(W.generate(spec, seed=510))
+    shifted = torch.empty(dev.k_I_scale.numel() + 16, dtype=torch.uint8, device="cuda")[1:1 + dev.k_I_scale.numel()]
+    shifted.copy_(dev.k_I_scale.reshape(-1))
+    for bad in (shifted, None):
+        with pytest.raises(dsa.DsaError) as e:
+            dsa.indexer_topk(dev.dims, dev.q_I, dev.w, dev.k_I, bad, dev.block_table, dev.seq_lens, ws=dev.ws)
+        assert e.value.status == 1
+    assert dev.faults() == 0
