@@ -114,3 +114,23 @@ def test_noalloc_rejects_before_any_device_work(L):
     assert L.dsa_workspace_size(ctypes.byref(big), 4096) > 16 << 20
     assert L.dsa_indexer_topk_noalloc(ctypes.byref(big), FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None, 4096, FAKE,
                                       None, None) == 7
+
+
+def test_mxfp8_argument_checks(L):
+    args = [FAKE] * 8
+    mx = _dims(mode="mxfp8")
+    # MXFP8 keys need their E8M0 scales, 16-byte aligned (they are fetched with bulk copies)
+    for bad_scale in (None, ctypes.c_void_p((1 << 20) + 4)):
+        st = L.dsa_indexer_topk(ctypes.byref(mx), FAKE, FAKE, FAKE, bad_scale, FAKE, FAKE, FAKE, FAKE, 2, FAKE, FAKE,
+                                1 << 30, None)
+        assert st == 1
+    # groups of 32: d_I must be a multiple of 32 (CUDA-core shapes)
+    small = _dims(mode="mxfp8", H_I=8, d_I=48)
+    assert L.dsa_indexer_topk(ctypes.byref(small), *args, 2, FAKE, FAKE, 1 << 30, None) == 2
+    st = L.dsa_cache_append(ctypes.byref(small), FAKE, FAKE, FAKE, FAKE, None, None, 2, FAKE, FAKE, FAKE, FAKE, 1 << 30,
+                            None)
+    assert st == 2
+    # the workspace holds the quantised query: T x H_I x d_I bf16 more than for bf16 keys
+    T = 2
+    extra = L.dsa_workspace_size(ctypes.byref(mx), T) - L.dsa_workspace_size(ctypes.byref(_dims()), T)
+    assert extra >= T * 64 * 128 * 2
