@@ -271,6 +271,12 @@ dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const
  * DSA_ERR_DEVICE for any other bit, DSA_ERR_LAUNCH if the copy failed. */
 dsa_status dsa_read_error(void* ws, int32_t* fault_bits, dsa_stream_t stream);
 
+/* Self-test of the failure path every pipeline wait of this library takes: launches one CTA whose
+ * bounded wait on an mbarrier that nothing completes gives up after its limit (about one second),
+ * sets DSA_FAULT_TIMEOUT in the error word of `ws` (any workspace, ws_bytes >= 256) and returns;
+ * dsa_read_error then reports DSA_ERR_TIMEOUT and the context stays usable. */
+dsa_status dsa_selftest_wait_timeout(void* ws, size_t ws_bytes, dsa_stream_t stream);
+
 /* Number of kernels the last successful call on this thread launched (0 before any call). */
 int32_t dsa_last_launch_count(void);
 

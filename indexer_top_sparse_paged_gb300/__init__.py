@@ -77,6 +77,8 @@ def lib():
         L.dsa_indexer_topk_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, I32, P, P, P]
         L.dsa_read_error.restype = ctypes.c_int
         L.dsa_read_error.argtypes = [P, ctypes.POINTER(I32), P]
+        L.dsa_selftest_wait_timeout.restype = ctypes.c_int
+        L.dsa_selftest_wait_timeout.argtypes = [P, SZ, P]
         L.dsa_last_launch_count.restype = I32
         L.dsa_last_launch_count.argtypes = []
         L.dsa_status_string.restype = ctypes.c_char_p
@@ -250,6 +252,12 @@ def read_error(ws, stream=None) -> int:
     if st not in (0, 5, 6):
         raise DsaError("dsa_read_error", st)
     return int(bits.value)
+
+
+def selftest_wait_timeout(ws, stream=None) -> None:
+    """Runs the bounded-wait self-test (its wait runs out after about a second and sets the
+    timeout bit of ``ws``; read it with :func:`read_error`)."""
+    _check("dsa_selftest_wait_timeout", lib().dsa_selftest_wait_timeout(_p(ws), ws.numel(), _stream(stream)))
 
 
 def last_launch_count() -> int:

@@ -601,6 +601,14 @@ dsa_status dsa_read_error(void* ws, int32_t* fault_bits, dsa_stream_t stream) {
     return v ? DSA_ERR_DEVICE : DSA_OK;
 }
 
+dsa_status dsa_selftest_wait_timeout(void* ws, size_t ws_bytes, dsa_stream_t stream) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return DSA_ERR_WORKSPACE;
+    int launches = 0;
+    const bool ok = launch_wait_timeout(static_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream), &launches);
+    g_last_launches = launches;
+    return ok ? DSA_OK : DSA_ERR_LAUNCH;
+}
+
 int32_t dsa_last_launch_count(void) { return g_last_launches; }
 
 const char* dsa_status_string(dsa_status status) {

@@ -132,5 +132,6 @@ bool launch_cache_append(const dsa_dims& d, const void* k_new, const void* kv_ne
                          const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T, void* k_cache,
                          void* k_scale, void* kv_cache, int* err, cudaStream_t s, int* launches);
 bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches);
+bool launch_wait_timeout(int* err, cudaStream_t s, int* launches);
 
 }  // namespace dsa
