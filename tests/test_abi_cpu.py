@@ -134,3 +134,17 @@ def test_mxfp8_argument_checks(L):
     T = 2
     extra = L.dsa_workspace_size(ctypes.byref(mx), T) - L.dsa_workspace_size(ctypes.byref(_dims()), T)
     assert extra >= T * 64 * 128 * 2
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/dsa.h is a C header (no C++ or CUDA types in the signatures): a C11 translation unit
+    that includes it and takes every entry point's address compiles."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_dsa.c"
+    names = declared_symbols()
+    src.write_text('#include "dsa.h"\nvoid* entry_points[] = {' + ", ".join(f"(void*)&{n}" for n in names) + "};\n")
+    subprocess.check_call([cc, "-std=c11", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.dirname(HEADER), str(src)])
