@@ -1,8 +1,10 @@
 // Sparse attention on CUDA cores for small head shapes (the fp32 workload: 8 heads of 128). One
 // CTA per (query row, head): the selected positions are mapped through the block table once, the
-// logits z_i = sm_scale * q . row_i are reduced per warp (each warp reads whole 16-byte-coalesced
-// rows), then p = softmax(z) and out = sum_i p_i * row_i[0:d_v] with one thread per output column
-// ("Day0 Inference Support ... on Huawei Ascend CANN Architecture" §1 and §2.1: the sparse
+// logits z_i = sm_scale * q . row_i are reduced per warp (each warp reads four whole rows at a time,
+// coalesced, so their loads are in flight together), then p = softmax(z) and
+// out = sum_i p_i * row_i[0:d_v]: each warp accumulates every 8th row over 4 consecutive columns
+// per lane (128 columns per pass, vector loads), and the 8 warps' partial sums are added in shared
+// memory ("Day0 Inference Support ... on Huawei Ascend CANN Architecture" §1 and §2.1: the sparse
 // attention reads the main KV exactly at the selected indices).
 #include <cuda_bf16.h>
 
@@ -27,6 +29,7 @@ __global__ void __launch_bounds__(kAttnSimtThreads) attn_simt_kernel(AttnArgs a)
     float* z_s = q_s + d;                          // [K]
     int64_t* row_s = reinterpret_cast<int64_t*>(
         (reinterpret_cast<uintptr_t>(z_s + K) + 7) & ~static_cast<uintptr_t>(7));  // [K] physical rows
+    float* part = reinterpret_cast<float*>(row_s + K);                            // [8 warps][128]
     __shared__ float red[kAttnSimtThreads / 32];
     __shared__ float m_s, l_s;
 
@@ -55,16 +58,28 @@ __global__ void __launch_bounds__(kAttnSimtThreads) attn_simt_kernel(AttnArgs a)
     }
     block_sync();
 
-    // logits: one warp per selected row
-    for (int i = warp; i < K; i += kAttnSimtThreads / 32) {
-        const int64_t r = row_s[i];
-        float dot = 0.0f;
-        if (r >= 0) {
-            for (int e = lane; e < d; e += 32) dot = fmaf(q_s[e], act_f(a.kv, r * d + e, BF16), dot);
+    // logits: each warp takes four selected rows at a time (rows 4w .. 4w+3 of every 32)
+    constexpr int kNW = kAttnSimtThreads / 32;
+    for (int i0 = warp * 4; i0 < K; i0 += kNW * 4) {
+        int64_t rr[4];
+        float dot[4];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
+        for (int u = 0; u < 4; ++u) {
+            rr[u] = (i0 + u < K) ? row_s[i0 + u] : -1;
+            dot[u] = 0.0f;
         }
-        if (lane == 0) z_s[i] = (r >= 0) ? dot * a.sm_scale : -INFINITY;
+        for (int e = lane; e < d; e += 32) {
+            const float qe = q_s[e];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (rr[u] >= 0) dot[u] = fmaf(qe, act_f(a.kv, rr[u] * d + e, BF16), dot[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dot[u] += __shfl_xor_sync(0xFFFFFFFFu, dot[u], o);
+            if (lane == 0 && i0 + u < K) z_s[i0 + u] = (rr[u] >= 0) ? dot[u] * a.sm_scale : -INFINITY;
+        }
     }
     block_sync();
 
@@ -102,22 +117,57 @@ __global__ void __launch_bounds__(kAttnSimtThreads) attn_simt_kernel(AttnArgs a)
     const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
 
     const int64_t obase = (static_cast<int64_t>(t) * a.H + h) * a.d_v;
-    for (int c = tid; c < a.d_v; c += kAttnSimtThreads) {
-        float acc = 0.0f;
-        for (int i = 0; i < K; ++i) {
+    for (int c0 = 0; c0 < a.d_v; c0 += 128) {
+        const int c = c0 + lane * 4;  // this lane's 4 columns
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int i = warp; i < K; i += kNW) {
             const int64_t r = row_s[i];
-            if (r >= 0) acc = fmaf(z_s[i], act_f(a.kv, r * d + c, BF16), acc);
+            if (r < 0) continue;  // the same row for the whole warp
+            const float p = z_s[i];
+            const int64_t e = r * d + c;
+            if (c + 3 < a.d_v) {  // d % 4 == 0 (fp32) / d % 8 == 0 (bf16): 16- / 8-byte aligned
+                float v[4];
+                if (BF16) {
+                    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.kv) + e);
+                    v[0] = __uint_as_float(u.x << 16);
+                    v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+                    v[2] = __uint_as_float(u.y << 16);
+                    v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+                } else {
+                    const float4 f4 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.kv) + e);
+                    v[0] = f4.x;
+                    v[1] = f4.y;
+                    v[2] = f4.z;
+                    v[3] = f4.w;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[k] = fmaf(p, v[k], acc[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (c + k < a.d_v) acc[k] = fmaf(p, act_f(a.kv, e + k, BF16), acc[k]);
+            }
         }
-        const float o = acc * inv;
-        if (BF16) static_cast<uint16_t*>(a.out)[obase + c] = to_bf16_rn(o);
-        else static_cast<float*>(a.out)[obase + c] = o;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) part[warp * 128 + lane * 4 + k] = acc[k];
+        block_sync();
+        if (tid < 128 && c0 + tid < a.d_v) {
+            float o = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kNW; ++w) o += part[w * 128 + tid];
+            o *= inv;
+            if (BF16) static_cast<uint16_t*>(a.out)[obase + c0 + tid] = to_bf16_rn(o);
+            else static_cast<float*>(a.out)[obase + c0 + tid] = o;
+        }
+        block_sync();  // part is rewritten by the next pass
     }
     if (tid == 0 && a.lse) a.lse[static_cast<int64_t>(t) * a.H + h] = (l > 0.0f) ? m + logf(l) : -INFINITY;
 }
 
 bool launch_attn_simt(const AttnArgs& a, cudaStream_t s, int* launches) {
     if (a.T == 0) return true;
-    const size_t smem = static_cast<size_t>(a.d + a.K) * 4 + 8 + static_cast<size_t>(a.K) * 8;
+    const size_t smem = static_cast<size_t>(a.d + a.K) * 4 + 8 + static_cast<size_t>(a.K) * 8 +
+                        static_cast<size_t>(kAttnSimtThreads / 32) * 128 * 4;
     dim3 grid(a.H, a.T);
     const bool pdl = a.after_own_kernel != 0;
     if (a.mode == DSA_F32) {
