@@ -46,6 +46,8 @@ MUTANTS = {
     "mx_scale_bias_126": ("e / 32] - 127);\n            k[e]", "e / 32] - 126);\n            k[e]"),
     "mx_first_group_scale_only": ("[(size_t)row * (D->d_I / 32) + e / 32] - 127);", "[(size_t)row * (D->d_I / 32)] - 127);"),
     "mx_exponent_is_ceil": ("X = (e - 1) - 8;", "X = e - 8;"),
+    "mx_summary_first_group_scale": ("* (D->d_I / 32) + d / 32] - 127);", "* (D->d_I / 32)] - 127);"),
+    "mx_append_quantises_group_0_everywhere": ("[(int64_t)t * D->d_I + 32 * g + i]);", "[(int64_t)t * D->d_I + i]);"),
     "mx_append_wrong_scale_row": ("((uint8_t*)k_scale)[row * (D->d_I / 32) + g] = (uint8_t)(X + 127);",
                                   "((uint8_t*)k_scale)[(row ^ 1) * (D->d_I / 32) + g] = (uint8_t)(X + 127);"),
 }
