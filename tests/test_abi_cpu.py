@@ -148,3 +148,14 @@ def test_header_is_plain_c(tmp_path):
     names = declared_symbols()
     src.write_text('#include "dsa.h"\nvoid* entry_points[] = {' + ", ".join(f"(void*)&{n}" for n in names) + "};\n")
     subprocess.check_call([cc, "-std=c11", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.dirname(HEADER), str(src)])
+
+
+def test_calls_with_no_rows_launch_nothing(L):
+    """T = 0 is a valid call: arguments are checked, nothing is launched (no device needed)."""
+    d = _dims()
+    st = L.dsa_indexer_topk(ctypes.byref(d), FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, 1 << 30,
+                            None)
+    assert st == 0 and L.dsa_last_launch_count() == 0
+    st = L.dsa_sparse_attn(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, ctypes.c_float(0.04), FAKE, None,
+                           FAKE, 1 << 30, None)
+    assert st == 0 and L.dsa_last_launch_count() == 0
