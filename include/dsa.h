@@ -256,8 +256,9 @@ dsa_status dsa_indexer_topk_hier(const dsa_dims* dims, const void* q_I, const fl
  * (different streams or threads without ordering between them) race and give wrong indices;
  * order them on one stream.
  * Returns DSA_ERR_TOO_LARGE, launching nothing, when the indexer's scratch (error word, work plan
- * and candidate lists: about (indexer CTAs + T) * K * 8 bytes) exceeds DSA_NOALLOC_SCRATCH_BYTES
- * (for K = 2048: T <= 871 rows with the 64 x 128 bf16 indexer on 152 SMs);
+ * and candidate lists: about (indexer CTAs + T) * K * 8 bytes, plus T * H_I * d_I * 2 bytes for
+ * the quantised query in DSA_MXFP8) exceeds DSA_NOALLOC_SCRATCH_BYTES (for K = 2048: T <= 871
+ * rows with the 64 x 128 bf16 indexer on 152 SMs);
  * DSA_ERR_LAUNCH when the set-up or a launch fails.
  */
 #define DSA_NOALLOC_SCRATCH_BYTES (16u << 20)
