@@ -46,45 +46,60 @@ PROFILE = os.path.join(ROOT, "profiles", "indexer_tc_decode_bf16_b32.md")
 # selected rows once, queries, weights, block-table entries, indices and outputs)
 # ------------------------------------------------------------------------------------------------
 
-def indexer_bytes(case) -> int:
+def _decode_rows(case, rows):
+    return np.arange(case.spec.T) if rows is None else np.asarray(rows, dtype=np.int64)
+
+
+def indexer_bytes(case, rows=None) -> int:
+    """Algorithmic bytes of the indexer over decode rows (one query row per sequence): every causal
+    key once (with its scales), the row's query and head weights, its block-table entries and
+    sequence length, and the K indices written."""
     s = case.spec
+    rows = _decode_rows(case, rows)
     key_b = {"f32": 4, "bf16": 2, "bf16_kfp8": 1, "mxfp8": 1}[s.mode] * s.d_I
-    L = case.seq_lens.astype(np.int64)
-    blocks = (L + 63) // 64
-    b = int(L.sum()) * key_b
+    n = (case.q_pos[rows].astype(np.int64) + 1).clip(min=0)
+    blocks = (n + 63) // 64
+    b = int(n.sum()) * key_b
     if s.mode == "bf16_kfp8":
         b += int(blocks.sum()) * 4                              # fp32 scale per block
     if s.mode == "mxfp8":
-        b += int(L.sum()) * (s.d_I // 32)                       # E8M0 byte per 32 elements
+        b += int(n.sum()) * (s.d_I // 32)                       # E8M0 byte per 32 elements
     act = 4 if s.mode == "f32" else 2
-    b += s.T * s.H_I * s.d_I * act + s.T * s.H_I * 4           # q_I, w
-    b += int(blocks.sum()) * 4 + s.B * 4                        # block-table entries, seq_lens
-    b += s.T * s.K * 4                                          # idx written
+    T = len(rows)
+    b += T * s.H_I * s.d_I * act + T * s.H_I * 4               # q_I, w
+    b += int(blocks.sum()) * 4 + T * 4                          # block-table entries, seq_lens
+    b += T * s.K * 4                                            # idx written
     return b
 
 
-def attn_bytes(case) -> int:
+def attn_bytes(case, rows=None) -> int:
+    """Algorithmic bytes of sparse attention: the selected latent rows once, their indices and
+    block-table entries, the queries, outputs and log-sum-exps."""
     s = case.spec
+    rows = _decode_rows(case, rows)
     act = 4 if s.mode == "f32" else 2
-    n_sel = int(np.minimum(case.seq_lens.astype(np.int64), s.K).sum())
+    n_sel = int(np.minimum((case.q_pos[rows].astype(np.int64) + 1).clip(min=0), s.K).sum())
+    T = len(rows)
     b = n_sel * s.d * act                                       # gathered rows
-    b += s.T * s.K * 4 + n_sel * 4                              # idx read + table entries
-    b += s.T * s.H * s.d * act + s.T * s.H * s.d_v * act        # q, out
-    b += s.T * s.H * 4                                          # lse
+    b += T * s.K * 4 + n_sel * 4                                # idx read + table entries
+    b += T * s.H * s.d * act + T * s.H * s.d_v * act            # q, out
+    b += T * s.H * 4                                            # lse
     return b
 
 
-def indexer_flops(case) -> int:
+def indexer_flops(case, rows=None) -> int:
     """Tensor flops of the indexer scores: every causal (row, key) pair, H_I x d_I MACs."""
     s = case.spec
-    n = (case.q_pos.astype(np.int64) + 1).clip(min=0)
+    rows = _decode_rows(case, rows)
+    n = (case.q_pos[rows].astype(np.int64) + 1).clip(min=0)
     return int(n.sum()) * s.H_I * s.d_I * 2
 
 
-def attn_flops(case) -> int:
+def attn_flops(case, rows=None) -> int:
     """Tensor flops of sparse attention: QK^T over d and PV over d_v for every selected row."""
     s = case.spec
-    n = np.minimum((case.q_pos.astype(np.int64) + 1).clip(min=0), s.K)
+    rows = _decode_rows(case, rows)
+    n = np.minimum((case.q_pos[rows].astype(np.int64) + 1).clip(min=0), s.K)
     return int(n.sum()) * s.H * (s.d + s.d_v) * 2
 
 
@@ -103,9 +118,14 @@ def measured_tensor_peak():
     return 1900.0, "fallback"
 
 
+# every source file the measured indexer call (decode, bf16 keys) is built from: host-side launch
+# configuration and workspace layout, the indexer kernel, the merge and their shared headers
+TRAFFIC_SOURCES = ("dsa_api.cu", "internal.h", "common.cuh", "ptx.cuh", "indexer_tc.cu", "topk_merge.cu")
+
+
 def kernel_digest() -> str:
     h = hashlib.sha256()
-    for f in ("indexer_tc.cu", "common.cuh", "ptx.cuh"):
+    for f in TRAFFIC_SOURCES:
         h.update(open(os.path.join(ROOT, "indexer_top_sparse_paged_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -230,7 +250,8 @@ class Resident:
         self.qs, self.qp = to_dev(case.q_seq, dev), to_dev(case.q_pos, dev)
         self.ws = dsa.workspace(self.dims, s.T, dev)
         self.idx = torch.empty((s.T, s.K), dtype=torch.int32, device=dev)
-        self.out = torch.empty((s.T, s.H, s.d_v), dtype=torch.bfloat16, device=dev)
+        odt = torch.float32 if s.mode == "f32" else torch.bfloat16
+        self.out = torch.empty((s.T, s.H, s.d_v), dtype=odt, device=dev)
         self.lse = torch.empty((s.T, s.H), dtype=torch.float32, device=dev)
 
     def indexer(self):
@@ -269,8 +290,8 @@ def run_prefill(steps: int, warmup: int, dev, flush):
     torch.cuda.synchronize(dev)
     if dsa.read_error(r.ws) != 0:
         raise RuntimeError("device fault bits set during the prefill timing")
-    idx_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
-    att_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev)
+    idx_ms = statistics.median(a.elapsed_time(b) for a, b, _ in ev)
+    att_ms = statistics.median(b.elapsed_time(c) for _, b, c in ev)
     peak, kind = measured_tensor_peak()
     fi, fa = indexer_flops(case), attn_flops(case)
     res = {
@@ -311,7 +332,7 @@ def run_prefill(steps: int, warmup: int, dev, flush):
         torch.cuda.synchronize(dev)
         if dsa.read_error(r.ws) != 0:
             raise RuntimeError(f"device fault bits set while timing the {mode} prefill indexer")
-        ms = statistics.mean(a.elapsed_time(b) for a, b in evk)
+        ms = statistics.median(a.elapsed_time(b) for a, b in evk)
         res["indexer_key_formats"][mode] = {"indexer_ms": round(ms, 3),
                                             "indexer_tflops": round(fi / (ms * 1e-3) / 1e12, 1)}
         del r
@@ -346,7 +367,7 @@ def run_key_formats(case, steps: int, dev, flush):
         torch.cuda.synchronize(dev)
         if dsa.read_error(ws) != 0:
             raise RuntimeError(f"device fault bits set while timing the {mode} indexer")
-        us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+        us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
         ib = indexer_bytes(c)
         res[mode] = {"indexer_us": round(us, 2), "indexer_bytes": ib, "gbs": round(ib / (us * 1e-6) / 1e9, 1),
                      "hbm_frac_of_" + kind: round(ib / (us * 1e-6) / 1e9 / peak, 4),
@@ -354,6 +375,118 @@ def run_key_formats(case, steps: int, dev, flush):
         del q_I, w, k_I, ksc, bt, sl, ws, idx
     torch.cuda.empty_cache()
     return res
+
+
+def _med_us(fn, steps: int, flush, stream) -> float:
+    """Median CUDA-event time of fn() in microseconds, L2 flushed (256 MiB write) before each call."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+
+
+def _hbm(nbytes: int, us: float, peak: float, kind: str) -> dict:
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"bytes": nbytes, "gbs": round(gbs, 1), "hbm_frac_of_" + kind: round(gbs / peak, 4)}
+
+
+def _tensor(flops: int, us: float, peak: float, kind: str) -> dict:
+    tf = flops / (us * 1e-6) / 1e12
+    return {"flops": flops, "tflops": round(tf, 1), "tensor_frac_of_" + kind: round(tf / peak, 4)}
+
+
+class _Rows:
+    """A contiguous range of query rows of a resident workload, as views (no copies)."""
+
+    def __init__(self, r: "Resident", lo: int, hi: int):
+        self.r, self.lo, self.hi = r, lo, hi
+        self.idx = r.idx[lo:hi]
+
+    def indexer(self):
+        import indexer_top_sparse_paged_gb300 as dsa
+        r = self.r
+        dsa.indexer_topk(r.dims, r.q_I[self.lo:self.hi], r.w[self.lo:self.hi], r.k_I, r.ksc, r.bt, r.sl,
+                         r.qs[self.lo:self.hi], r.qp[self.lo:self.hi], ws=r.ws, idx=self.idx)
+
+    def attn(self):
+        import indexer_top_sparse_paged_gb300 as dsa
+        r = self.r
+        dsa.sparse_attn(r.dims, r.q[self.lo:self.hi], r.kv, r.bt, r.sl, self.idx, r.case.spec.sm_scale,
+                        q_seq=r.qs[self.lo:self.hi], ws=r.ws, out=r.out[self.lo:self.hi], lse=r.lse[self.lo:self.hi])
+
+
+def run_workloads(steps: int, dev, flush) -> dict:
+    """The other named workloads at full size, each call timed on its own (median CUDA-event time,
+    L2 flushed before each call), with its algorithmic bytes or flops and the fraction of the
+    measured peak:
+      1  tiny decode, fp32 (L = 2048, K = 256): launch- and latency-bound, reported in microseconds;
+      3  1M-token decode with FP8 indexer keys: HBM-bound;
+      5  mixed serving batch (64 decode rows, contexts log-uniform in [1K, 256K], plus one 2048-token
+         chunk at 128K, FP8 keys): the whole step (one indexer call and one attention call over all
+         2112 rows), and its decode rows and chunk rows as separate calls."""
+    import indexer_top_sparse_paged_gb300 as dsa
+    hbm_peak, hk = measured_peaks()
+    tc_peak, tk = measured_tensor_peak()
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for n in (1, 3, 5):
+        t0 = time.time()
+        spec, seed = W.named(n)
+        case = W.generate(spec, seed)
+        gen_s = time.time() - t0
+        r = Resident(case, dev)
+        s = case.spec
+        for _ in range(3):
+            r.indexer()
+            r.attn()
+        torch.cuda.synchronize(dev)
+        if dsa.read_error(r.ws) != 0:
+            raise RuntimeError(f"device fault bits set during the warm-up of workload {n}")
+        res = {"workload": s.name, "T": s.T, "B": s.B, "K": s.K, "mode": s.mode, "generate_s": round(gen_s, 1)}
+        if n in (1, 3):
+            res["indexer_us"] = round(_med_us(r.indexer, steps, flush, stream), 2)
+            res["attn_us"] = round(_med_us(r.attn, steps, flush, stream), 2)
+
+            def step():
+                dsa.decode(r.dims, r.q_I, r.w, r.k_I, r.ksc, r.bt, r.sl, r.q, r.kv, s.sm_scale, ws=r.ws, idx=r.idx,
+                           out=r.out, lse=r.lse)
+            res["step_us"] = round(_med_us(step, steps, flush, stream), 2)
+            res["step_launches"] = dsa.last_launch_count()
+            ib, ab = indexer_bytes(case), attn_bytes(case)
+            res["step"] = _hbm(ib + ab, res["step_us"], hbm_peak, hk)
+            res["indexer"] = _hbm(ib, res["indexer_us"], hbm_peak, hk)
+            res["attn"] = _hbm(ab, res["attn_us"], hbm_peak, hk)
+        else:
+            n_dec = int(sum(1 for x in s.new_tokens if x == 1))
+            dec, chunk = _Rows(r, 0, n_dec), _Rows(r, n_dec, s.T)
+            res["total_step_us"] = round(_med_us(lambda: (r.indexer(), r.attn()), steps, flush, stream), 2)
+            res["total_indexer_us"] = round(_med_us(r.indexer, steps, flush, stream), 2)
+            res["total_attn_us"] = round(_med_us(r.attn, steps, flush, stream), 2)
+            drows = np.arange(n_dec)
+            d = {"rows": n_dec, "indexer_us": round(_med_us(dec.indexer, steps, flush, stream), 2),
+                 "attn_us": round(_med_us(dec.attn, steps, flush, stream), 2)}
+            d["step_us"] = round(_med_us(lambda: (dec.indexer(), dec.attn()), steps, flush, stream), 2)
+            d.update(_hbm(indexer_bytes(case, drows) + attn_bytes(case, drows), d["step_us"], hbm_peak, hk))
+            crows = np.arange(n_dec, s.T)
+            c = {"rows": s.T - n_dec, "indexer_us": round(_med_us(chunk.indexer, steps, flush, stream), 2),
+                 "attn_us": round(_med_us(chunk.attn, steps, flush, stream), 2)}
+            c["tokens_per_s"] = round(c["rows"] / ((c["indexer_us"] + c["attn_us"]) * 1e-6), 1)
+            c["indexer"] = _tensor(indexer_flops(case, crows), c["indexer_us"], tc_peak, tk)
+            c["attn"] = _tensor(attn_flops(case, crows), c["attn_us"], tc_peak, tk)
+            res["decode_rows"] = d
+            res["chunk_rows"] = c
+        if dsa.read_error(r.ws) != 0:
+            raise RuntimeError(f"device fault bits set while timing workload {n}")
+        out[str(n)] = res
+        del r, case
+        torch.cuda.empty_cache()
+    out["method"] = ("median CUDA-event time per call over %d calls, L2 flushed (256 MiB write) before each; "
+                     "bytes and flops are the method's own (every causal key once, the selected rows once)" % steps)
+    return out
 
 
 def run_ours(args, rank, world):
@@ -499,18 +632,19 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize(dev)
     if dsa.read_error(ws) != 0:
         raise RuntimeError("device fault bits set during the cache append")
-    app_us = statistics.mean(a.elapsed_time(b) for a, b in app_ev) * 1e3
+    app_us = statistics.median(a.elapsed_time(b) for a, b in app_ev) * 1e3
     app_bytes = 2 * s.T * (s.d_I + s.d) * 2  # new rows read + cache rows written (bf16)
 
     ib, ab = indexer_bytes(case), attn_bytes(case)
     step_bytes = ib + ab
-    total_ms, e2e_total = reduce_across_ranks([sum(step_ms), sum(e2e_ms)], "max", world, dev)
-    (job_bytes,) = reduce_across_ranks([step_bytes * args.steps], "sum", world, dev)
-    ms_per_step = total_ms / args.steps
-    value = job_throughput(job_bytes, total_ms)
-    e2e_value = job_throughput(job_bytes, e2e_total)
+    # per-step medians (CUDA events), the slowest rank's; the K bracketed steps' total beside them
+    total_ms, e2e_total, ms_per_step, e2e_med = reduce_across_ranks(
+        [sum(step_ms), sum(e2e_ms), statistics.median(step_ms), statistics.median(e2e_ms)], "max", world, dev)
+    (job_bytes,) = reduce_across_ranks([step_bytes], "sum", world, dev)
+    value = job_throughput(job_bytes, ms_per_step)
+    e2e_value = job_throughput(job_bytes, e2e_med)
     peak, peak_kind = measured_peaks()
-    idx_avg = statistics.mean(idx_ms)
+    idx_avg = statistics.median(idx_ms)
     achieved = ib / (idx_avg * 1e-3) / 1e9
     res = {
         "metric": METRIC,
@@ -521,6 +655,8 @@ def run_ours(args, rank, world):
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5),
         "us_per_step": round(ms_per_step * 1e3, 2),
+        "timing": "median of the K per-step CUDA-event times (slowest rank); mean over the K bracketed steps "
+                  f"{total_ms / args.steps * 1e3:.2f} us",
         "hbm_frac_of_" + peak_kind: round(value / world / peak, 4),
         "higher_is_better": True,
         "scaling": "weak",
@@ -530,13 +666,13 @@ def run_ours(args, rank, world):
         "config": {"workload": WORKLOAD, "global_batch": s.B * world, "seq_len": "16384..32768",
                    "parallelism": f"replicas x{world}", "l2": "flushed (256 MiB write) before every timed step",
                    "step_bytes": step_bytes, "indexer_bytes": ib, "attention_bytes": ab},
-        "breakdown_us": {"indexer_topk": round(idx_avg * 1e3, 2), "sparse_attn": round(statistics.mean(att_ms) * 1e3, 2)},
+        "breakdown_us": {"indexer_topk": round(idx_avg * 1e3, 2), "sparse_attn": round(statistics.median(att_ms) * 1e3, 2)},
         "roofline": {"kernel": "dsa_indexer_topk (indexer_tc_kernel + topk_merge)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                      "algorithmic_bytes_per_launch": ib},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_total / args.steps, 5)},
+                "ms_per_step": round(e2e_med, 5)},
         "gpu_launches": launches,
         "clocks": clocks,
         "cache_append": {"us": round(app_us, 2), "rows": s.T, "bytes": app_bytes,
@@ -545,6 +681,8 @@ def run_ours(args, rank, world):
     res["indexer_key_formats"] = run_key_formats(case, max(3, min(args.steps, 20)), dev, flush)
     if not args.no_prefill:
         res["prefill"] = run_prefill(max(3, min(args.steps, 10)), args.warmup, dev, flush)
+    if not args.no_workloads:
+        res["workloads"] = run_workloads(max(3, min(args.steps, 20)), dev, flush)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(case)
     return res
@@ -572,13 +710,20 @@ def time_oracle(sub, threads: int) -> float:
     return time.perf_counter() - t0
 
 
-def cpu_baseline(case, n_seq: int = 32):
+def cpu_baseline(case, n_seq: int = 32, n_seq_single: int = 8):
+    """The oracle as it stands on the host cores: all 32 decode rows with one thread per core, and
+    a sample of the rows on one thread."""
     threads = os.cpu_count() or 1
     sub = sample_case(case, n_seq)
     dt = time_oracle(sub, threads)
     b = indexer_bytes(sub) + attn_bytes(sub)
+    sub1 = sample_case(case, n_seq_single)
+    dt1 = time_oracle(sub1, 1)
+    b1 = indexer_bytes(sub1) + attn_bytes(sub1)
     return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n_seq} of the 32 decode sequences (indexer + Top-K + attention, fp64), {dt:.2f} s"}
+            "sample": f"{n_seq} of the 32 decode sequences (indexer + Top-K + attention, fp64), {dt:.2f} s",
+            "single_thread": {"value": round(b1 / dt1 / 1e9, 5), "unit": "GB/s", "cores": 1,
+                              "sample": f"the first {n_seq_single} of the 32 decode sequences, {dt1:.2f} s"}}
 
 
 def run_reference(args, rank, world):
@@ -664,6 +809,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill measurement")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the tiny, 1M-token and mixed-batch workloads (measured after the headline)")
     ap.add_argument("--profile", nargs="?", const="decode", choices=["decode", "prefill", "prefill-small", "decode-fp8", "decode-mx"],
                     help="only run --warmup + 1 steps of one case (a short command for ncu captures)")
     args = ap.parse_args()

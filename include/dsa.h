@@ -180,7 +180,7 @@ dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, con
  * consecutive rows in ascending position. fp32 / bf16 keys and all latent rows are copied. FP8
  * keys: every block that receives new tokens is requantised as a whole: with x = code * scale
  * (fp32) for its earlier tokens and the new keys' values, the block's scale becomes amax / 448
- * (1 when amax is 0) and each code RNE_e4m3(x / scale), saturating at +-448, all in fp32. Rows
+ * (1 when amax is 0) and each code RNE_e4m3(x / scale), saturating at +-448, all in fp32.
  * MXFP8 keys: each new key's groups of 32 are quantised on their own (as q_I is in the indexer),
  * writing its codes and its d_I / 32 scale bytes; no other row changes. Rows
  * with an invalid sequence, position or block-table entry are skipped and reported through the
@@ -257,8 +257,10 @@ dsa_status dsa_indexer_topk_hier(const dsa_dims* dims, const void* q_I, const fl
  * order them on one stream.
  * Returns DSA_ERR_TOO_LARGE, launching nothing, when the indexer's scratch (error word, work plan
  * and candidate lists: about (indexer CTAs + T) * K * 8 bytes, plus T * H_I * d_I * 2 bytes for
- * the quantised query in DSA_MXFP8) exceeds DSA_NOALLOC_SCRATCH_BYTES (for K = 2048: T <= 871
- * rows with the 64 x 128 bf16 indexer on 152 SMs);
+ * the quantised query in DSA_MXFP8) exceeds DSA_NOALLOC_SCRATCH_BYTES (for K = 2048: T <= 870
+ * rows with the 64 x 128 bf16 indexer on 152 SMs). This size check comes before the pointer checks,
+ * so a call with null buffers tells whether T rows fit without launching anything.
+ * T = 0 launches nothing and leaves the static scratch alone (only *fault_word is cleared);
  * DSA_ERR_LAUNCH when the set-up or a launch fails.
  */
 #define DSA_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -109,6 +109,20 @@ def _check(fn: str, status: int):
         raise DsaError(fn, status)
 
 
+def _check_out(dims: Dims, T: int, out, lse):
+    """The output buffers the library writes must have its dtype and size (it takes raw pointers)."""
+    odt = torch.float32 if dims.mode == MODES["f32"] else torch.bfloat16
+    if out.dtype != odt or out.numel() < T * dims.H * dims.d_v or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous {odt} tensor of T x H x d_v elements")
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() < T * dims.H or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 tensor of T x H elements")
+
+
+def _check_idx(dims: Dims, T: int, idx):
+    if idx.dtype != torch.int32 or idx.numel() < T * dims.K or not idx.is_contiguous():
+        raise ValueError("idx must be a contiguous int32 tensor of T x K elements")
+
+
 def workspace_size(dims: Dims, T: int) -> int:
     return int(lib().dsa_workspace_size(ctypes.byref(dims), T))
 
@@ -131,6 +145,7 @@ def indexer_topk(dims: Dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens
     T = q_I.shape[0]
     if idx is None:
         idx = torch.empty((T, dims.K), dtype=torch.int32, device=q_I.device)
+    _check_idx(dims, T, idx)
     st = lib().dsa_indexer_topk(ctypes.byref(dims), _p(q_I), _p(w), _p(k_I_cache), _p(k_I_scale), _p(block_table),
                                 _p(seq_lens), _p(q_seq), _p(q_pos), T, _p(idx), _p(ws), ws.numel(), _stream(stream))
     _check("dsa_indexer_topk", st)
@@ -147,6 +162,7 @@ def indexer_topk_noalloc(dims: Dims, q_I, w, k_I_cache, k_I_scale, block_table, 
     T = q_I.shape[0]
     if idx is None:
         idx = torch.empty((T, dims.K), dtype=torch.int32, device=q_I.device)
+    _check_idx(dims, T, idx)
     st = lib().dsa_indexer_topk_noalloc(ctypes.byref(dims), _p(q_I), _p(w), _p(k_I_cache), _p(k_I_scale),
                                         _p(block_table), _p(seq_lens), _p(q_seq), _p(q_pos), T, _p(idx),
                                         _p(fault_word), _stream(stream))
@@ -163,6 +179,7 @@ def sparse_attn(dims: Dims, q, kv_cache, block_table, seq_lens, idx, sm_scale: f
         out = torch.empty((T, dims.H, dims.d_v), dtype=odt, device=q.device)
     if lse is None:
         lse = torch.empty((T, dims.H), dtype=torch.float32, device=q.device)
+    _check_out(dims, T, out, lse)
     st = lib().dsa_sparse_attn(ctypes.byref(dims), _p(q), _p(kv_cache), _p(block_table), _p(seq_lens), _p(q_seq),
                                _p(idx), T, float(sm_scale), _p(out), _p(lse), _p(ws), ws.numel(), _stream(stream))
     _check("dsa_sparse_attn", st)
@@ -180,6 +197,9 @@ def decode(dims: Dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, q, k
         out = torch.empty((T, dims.H, dims.d_v), dtype=odt, device=q.device)
     if lse is None:
         lse = torch.empty((T, dims.H), dtype=torch.float32, device=q.device)
+    _check_out(dims, T, out, lse)
+    if idx is not None and (idx.dtype != torch.int32 or idx.numel() < T * dims.K or not idx.is_contiguous()):
+        raise ValueError("idx must be a contiguous int32 tensor of T x K elements")
     st = lib().dsa_decode(ctypes.byref(dims), _p(q_I), _p(w), _p(k_I_cache), _p(k_I_scale), _p(block_table),
                           _p(seq_lens), _p(q), _p(kv_cache), float(sm_scale), _p(idx), _p(out), _p(lse), _p(ws),
                           ws.numel(), _stream(stream))

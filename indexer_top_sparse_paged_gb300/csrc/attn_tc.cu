@@ -24,10 +24,11 @@
 // CTA (A operand from TMEM); shared memory holds the first query chunk, four row stages, two
 // exchange slots and the resolved rows of the split.
 //
-// Roles (320 threads per CTA): warps 0-3 softmax / epilogue (thread = head = TMEM lane), warps
-// 4-7 producers (gather rows; send the partial logits of their TMEM lane quarter), warp 8 TMEM
-// allocator + MMA issuer (+ the TMA loads of the query), warp 9 prefetches the CTA's columns of
-// every selected row into L2 at the start.
+// Roles (448 threads = 14 warps per CTA): warps 0-3 and 10-13 softmax / epilogue in two groups
+// (thread = head = TMEM lane; group 0 takes rows 0..31 of every tile and O columns 0..127, group 1
+// rows 32..63 and O columns 128..255), warps 4-7 producers (gather rows; send the partial logits
+// of their TMEM lane quarter), warp 8 TMEM allocator + MMA issuer (+ the TMA loads of the query),
+// warp 9 prefetches the CTA's columns of every selected row into L2 at the start.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 

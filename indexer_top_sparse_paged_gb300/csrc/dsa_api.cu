@@ -456,22 +456,27 @@ dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const
     if (st != DSA_OK) return st;
     if (T < 0) return DSA_ERR_INVALID_ARG;
     if (!q_seq && T != dims->B) return DSA_ERR_INVALID_ARG;
+    // the indexer uses the workspace regions up to the attention's (error word, plan, candidates);
+    // checked before the pointers, so that a size query with null buffers never launches anything
+    if (ws_layout(*dims, T, false).idx > kNoAllocScratchBytes) return DSA_ERR_TOO_LARGE;
     if (T > 0 && (!q_I || !w || !k_I_cache || !block_table || !seq_lens || !idx)) return DSA_ERR_INVALID_ARG;
     if (!scale_ok(dims, k_I_scale)) return DSA_ERR_INVALID_ARG;
     if (!aligned16(q_I) || !aligned16(w) || !aligned16(k_I_cache)) return DSA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(fault_word) & 3u) return DSA_ERR_INVALID_ARG;
-    // the indexer uses the workspace regions up to the attention's (error word, plan, candidates)
-    if (ws_layout(*dims, T, false).idx > kNoAllocScratchBytes) return DSA_ERR_TOO_LARGE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (T == 0) {  // no rows: no kernel and no scratch; only the caller's fault word is cleared
+        g_last_launches = 0;
+        if (fault_word && cudaMemsetAsync(fault_word, 0, sizeof(int32_t), s) != cudaSuccess) return DSA_ERR_LAUNCH;
+        return DSA_OK;
+    }
     void* ws = noalloc_scratch();
     if (!ws) return DSA_ERR_LAUNCH;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int launches = 0;
     // the error word is the only scratch that must start at zero (every other region is written
     // before it is read within the call)
     if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return DSA_ERR_LAUNCH;
-    if (T > 0)
-        st = run_indexer(dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, q_seq, q_pos, T, idx, ws, s,
-                         &launches, /*allow_prefill=*/false);
+    st = run_indexer(dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, q_seq, q_pos, T, idx, ws, s,
+                     &launches, /*allow_prefill=*/false);
     if (st == DSA_OK && fault_word &&
         cudaMemcpyAsync(fault_word, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
         st = DSA_ERR_LAUNCH;

@@ -159,3 +159,47 @@ def test_calls_with_no_rows_launch_nothing(L):
     st = L.dsa_sparse_attn(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, ctypes.c_float(0.04), FAKE, None,
                            FAKE, 1 << 30, None)
     assert st == 0 and L.dsa_last_launch_count() == 0
+    # the entry point without a workspace: no kernel, and its static scratch is not touched
+    st = L.dsa_indexer_topk_noalloc(ctypes.byref(d), FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, None,
+                                    None)
+    assert st == 0 and L.dsa_last_launch_count() == 0
+
+
+def _noalloc_prefix_bytes(T: int, K: int, G: int, mx: bool = False, H_I: int = 64, d_I: int = 128) -> int:
+    """Bytes of scratch the indexer path uses for T rows: the workspace regions before the
+    indices (error word, work plan, merge counters, candidate counts and lists, the MX query)."""
+    a256 = lambda x: (x + 255) // 256 * 256
+    off = 256
+    off = a256(off + 4 * (T + 1))                    # tile prefix
+    off = a256(off + 4 * (T + 1))                    # merge-group prefix
+    off = a256(off + 4 * 3 * (T + (G + 7) // 8 + 1))  # merge-tree counters
+    off = a256(off + 4 * (G + T))                    # candidate counts
+    off = a256(off + 8 * (G + T) * K)                # candidate lists
+    if mx:
+        off = a256(off + 2 * T * H_I * d_I)          # the MX-quantised query (bf16)
+    return off
+
+
+def _noalloc_rows_limit(K: int, G: int, mx: bool = False) -> int:
+    T = 0
+    while _noalloc_prefix_bytes(T + 1, K, G, mx) <= 16 << 20:
+        T += 1
+    return T
+
+
+def test_noalloc_row_limit_is_the_documented_one(L):
+    """The largest call dsa_indexer_topk_noalloc accepts follows from its scratch layout, and the
+    header states that number for K = 2048 on 152 SMs. The library is probed with null buffers:
+    a call over the limit is rejected as too large before its pointers are looked at, one within
+    the limit as an invalid argument -- neither launches anything."""
+    import torch
+    G = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+    for mode, K in (("bf16", 2048), ("bf16", 512), ("mxfp8", 2048)):
+        t_max = _noalloc_rows_limit(K, G, mode == "mxfp8")
+        for T, want in ((t_max, 1), (t_max + 1, 7)):
+            d = _dims(mode=mode, B=T, K=K)
+            st = L.dsa_indexer_topk_noalloc(ctypes.byref(d), None, None, None, None, None, None, None, None, T, None,
+                                            None, None)
+            assert st == want, (mode, K, T, st)
+    documented = re.search(r"K = 2048: T <= (\d+)[\s*]+rows", open(HEADER).read())
+    assert documented and int(documented.group(1)) == _noalloc_rows_limit(2048, 152)

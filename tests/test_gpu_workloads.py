@@ -46,12 +46,21 @@ def test_decode_1m_fp8_keys_full_size():
     assert np.array_equal(dout, out)
 
 
+def _spread_rows(lo: int, hi: int, n: int) -> np.ndarray:
+    """n rows spread over [lo, hi): both ends, and every position inside a group of four rows
+    (the prefill path scores rows 4g..4g+3 together) in turn."""
+    base = np.linspace(lo, hi - 4, n).astype(np.int64) // 4 * 4
+    rows = base + np.arange(n) % 4
+    return np.unique(np.concatenate([[lo, lo + 1, hi - 2, hi - 1], rows]))
+
+
 def test_chunked_prefill_2x4096_full_size():
     spec, seed = W.named(4)
     case = W.generate(spec, seed)
     T = spec.T
-    # first, last and interior rows of both chunks (every row of the sample has > K positions)
-    rows = np.unique(np.concatenate([np.linspace(0, T // 2 - 1, 7), np.linspace(T // 2, T - 1, 7)]).astype(np.int64))
+    # 2 x 68 rows: both ends of each chunk and every position inside a group of four
+    rows = np.concatenate([_spread_rows(0, T // 2, 64), _spread_rows(T // 2, T, 64)])
+    assert len(rows) >= 128 and set((rows % 4).tolist()) == {0, 1, 2, 3}
     _check_rows(case, rows)
 
 
@@ -59,13 +68,24 @@ def test_mixed_serving_batch_full_size():
     spec, seed = W.named(5)
     case = W.generate(spec, seed)
     n_dec = 64
-    rows = np.concatenate([np.arange(n_dec), n_dec + np.linspace(0, spec.T - n_dec - 1, 8).astype(np.int64)])
-    _check_rows(case, rows)
+    # every decode row and 68 rows of the 2048-row chunk (both ends, every group position)
+    chunk = _spread_rows(n_dec, spec.T, 64)
+    assert len(chunk) >= 64
+    _check_rows(case, np.concatenate([np.arange(n_dec), chunk]))
+
+
+@pytest.mark.parametrize("mode", ["bf16", "mxfp8"])
+def test_chunked_prefill_shrunk_every_row(mode):
+    """The chunked prefill shape shrunk to 2 x 256 new tokens on a 1024-token cached prefix (1280
+    in total): every row's index set and attention against the oracle."""
+    spec = W.prefill_chunk(B=2, new=256, total=1280, mode=mode)
+    case = W.generate(spec, seed=40)
+    _check_rows(case, np.arange(spec.T))
 
 
 def test_chunked_prefill_2x4096_mxfp8_full_size():
     spec, seed = W.named(4)
     case = W.generate(dataclasses.replace(spec, mode="mxfp8"), seed)
     T = spec.T
-    rows = np.array([0, 1, 2047, T // 2 - 1, T // 2, T // 2 + 3001, T - 1])
+    rows = np.concatenate([_spread_rows(0, T // 2, 16), _spread_rows(T // 2, T, 16)])
     _check_rows(case, rows)

@@ -8,7 +8,7 @@ import torch
 import indexer_top_sparse_paged_gb300 as dsa
 import workloads as W
 from cases import small_spec
-from gpu_helpers import Dev
+from gpu_helpers import Dev, assert_index_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +43,19 @@ def test_noalloc_matches_workspace_call_twice(which):
     assert np.array_equal(first, ref)
     assert np.array_equal(second, ref)
     assert dsa.last_launch_count() == ref_launches  # the same kernels as the workspace call
+
+
+def test_noalloc_prefill_shaped_rows_match_the_oracle():
+    """Several causal rows of one sequence (a chunk of new tokens): the workspace call scores them
+    on the prefill path, the call without a workspace on the decode kernels; both must follow the
+    oracle's index rule row by row."""
+    case = W.generate(small_spec("bf16", [3000, 2000], 512, new_tokens=[16, 8]), seed=306)
+    dev = Dev(case)
+    fw = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    idx = _noalloc(dev, fw)
+    assert int(fw.item()) == 0
+    assert_index_parity(case, idx)
+    assert_index_parity(case, dev.indexer())
 
 
 def test_noalloc_reports_faults_in_the_callers_word():
