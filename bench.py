@@ -80,7 +80,8 @@ def attn_bytes(case, rows=None) -> int:
     act = 4 if s.mode == "f32" else 2
     n_sel = int(np.minimum((case.q_pos[rows].astype(np.int64) + 1).clip(min=0), s.K).sum())
     T = len(rows)
-    b = n_sel * s.d * act                                       # gathered rows
+    row_b = s.d + 4 * ((s.d + 127) // 128) if s.kv == "fp8" else s.d * act  # FP8 record: codes + tile scales
+    b = n_sel * row_b                                           # gathered rows
     b += T * s.K * 4 + n_sel * 4                                # idx read + table entries
     b += T * s.H * s.d * act + T * s.H * s.d_v * act            # q, out
     b += T * s.H * 4                                            # lse
@@ -242,7 +243,8 @@ class Resident:
         import indexer_top_sparse_paged_gb300 as dsa
         s = case.spec
         self.case, self.dev = case, dev
-        self.dims = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K)
+        self.dims = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K,
+                                  kv=s.kv)
         self.q_I, self.w, self.k_I = to_dev(case.q_I, dev), to_dev(case.w, dev), to_dev(case.k_I, dev)
         self.ksc = to_dev(case.k_I_scale, dev) if case.k_I_scale is not None else None
         self.q, self.kv = to_dev(case.q, dev), to_dev(case.kv, dev)
@@ -489,6 +491,41 @@ def run_workloads(steps: int, dev, flush) -> dict:
     return out
 
 
+def run_latent_formats(case, steps: int, dev, flush) -> dict:
+    """The decode workload with its latent rows stored as FP8 records (e4m3 codes, one fp32 scale per
+    128 elements): the attention call alone, and the whole decode step with bf16 and with FP8
+    indexer keys (CUDA events, L2 flushed before each call, medians)."""
+    import indexer_top_sparse_paged_gb300 as dsa
+    peak, kind = measured_peaks()
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for keys in ("bf16", "bf16_kfp8"):
+        c = W.with_kv_format(case if keys == "bf16" else W.with_key_format(case, keys), "fp8")
+        r = Resident(c, dev)
+        s = c.spec
+
+        def step():
+            dsa.decode(r.dims, r.q_I, r.w, r.k_I, r.ksc, r.bt, r.sl, r.q, r.kv, s.sm_scale, ws=r.ws, idx=r.idx,
+                       out=r.out, lse=r.lse)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize(dev)
+        step_us = _med_us(step, steps, flush, stream)
+        ent = {"step_us": round(step_us, 2), "step_launches": dsa.last_launch_count()}
+        ent.update(_hbm(indexer_bytes(c) + attn_bytes(c), step_us, peak, kind))
+        if keys == "bf16":
+            au = _med_us(r.attn, steps, flush, stream)
+            ent["attn_us"] = round(au, 2)
+            ent["attn"] = _hbm(attn_bytes(c), au, peak, kind)
+        if dsa.read_error(r.ws) != 0:
+            raise RuntimeError("device fault bits set while timing the FP8 latent cache")
+        res["keys_" + keys] = ent
+        del r
+        torch.cuda.empty_cache()
+    res["record_bytes"] = dsa.kv_record_bytes(case.spec.d)
+    return res
+
+
 def run_ours(args, rank, world):
     import indexer_top_sparse_paged_gb300 as dsa
 
@@ -679,6 +716,7 @@ def run_ours(args, rank, world):
                          "note": "dsa_cache_append of the batch's new keys and latent rows (launch-bound at 32 rows)"},
     }
     res["indexer_key_formats"] = run_key_formats(case, max(3, min(args.steps, 20)), dev, flush)
+    res["latent_fp8"] = run_latent_formats(case, max(3, min(args.steps, 20)), dev, flush)
     if not args.no_prefill:
         res["prefill"] = run_prefill(max(3, min(args.steps, 10)), args.warmup, dev, flush)
     if not args.no_workloads:

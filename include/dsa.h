@@ -75,6 +75,22 @@ typedef enum {
 } dsa_mode;
 
 /*
+ * Flag OR-ed into dsa_dims.mode (with DSA_BF16, DSA_BF16_KFP8 or DSA_MXFP8): the latent cache
+ * kv_cache holds FP8 records instead of bf16 rows ("Day0 Inference Support ... on Huawei Ascend CANN
+ * Architecture" §3: FP8 block quantisation in the attention stage, an independent block of 128
+ * elements per token and head). A record is the d e4m3 codes of the row, then ceil(d / 128) fp32
+ * scales (tile j covers elements 128j .. 128j + 127, the last tile the remaining d mod 128), then
+ * zero bytes up to DSA_KV_FP8_RECORD_BYTES(d), a multiple of 16; element e of the row is
+ * code[e] * scale[e / 128]. The attention dequantises every element to bf16 (code * scale in fp32,
+ * rounded to nearest even) before its tensor-core products; q, out and lse keep their types.
+ * dsa_cache_append quantises each new latent row tile by tile, in fp32: scale = amax / 448 (1 when
+ * amax is 0), code = RNE_e4m3(x / scale), saturating at +-448. The indexer ignores the flag.
+ * Requires d % 16 == 0.
+ */
+#define DSA_KV_FP8 0x10
+#define DSA_KV_FP8_RECORD_BYTES(d) ((((d) + 4 * (((d) + 127) / 128)) + 15) / 16 * 16)
+
+/*
  * Problem dimensions.
  *   block_size must be 64 (tokens per physical cache block).
  *   DSA_F32:              H_I <= 64, d_I <= 256, d_I % 4 == 0, H <= 128, d <= 1024, d % 4 == 0, d_v <= d
@@ -85,7 +101,7 @@ typedef enum {
  *   1 <= K <= 2048.
  */
 typedef struct {
-    int32_t mode;       /* dsa_mode */
+    int32_t mode;       /* dsa_mode, optionally | DSA_KV_FP8 */
     int32_t B;          /* number of sequences (rows of block_table, entries of seq_lens) */
     int32_t max_blocks; /* block_table row length */
     int32_t num_blocks; /* physical blocks in k_I_cache and kv_cache */
@@ -141,7 +157,9 @@ dsa_status dsa_indexer_topk(const dsa_dims* dims, const void* q_I, const float* 
 /*
  * Sparse attention over the positions idx selects ("sparse flash attention").
  *   q          [T][H][d]            fp32 or bf16
- *   kv_cache   [num_blocks][64][d]  fp32 or bf16 shared latent rows (K = row, V = row[0:d_v])
+ *   kv_cache   [num_blocks][64][d]  fp32 or bf16 shared latent rows (K = row, V = row[0:d_v]);
+ *                                   with DSA_KV_FP8: [num_blocks][64][DSA_KV_FP8_RECORD_BYTES(d)] FP8
+ *                                   records (see DSA_KV_FP8)
  *   idx        [T][K]               int32 logical positions, -1 = empty slot (any order)
  *   sm_scale   softmax scale (usually 1/sqrt(d))
  *   out        [T][H][d_v]          fp32 (DSA_F32) or bf16 out
@@ -170,7 +188,7 @@ dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, con
  * quantised on the way in).
  *   k_I_new    [T][d_I]   fp32 (DSA_F32) or bf16 (the other modes; DSA_BF16_KFP8 and DSA_MXFP8: the
  *                         values to quantise)
- *   kv_new     [T][d]     fp32 or bf16 latent rows
+ *   kv_new     [T][d]     fp32 or bf16 latent rows (with DSA_KV_FP8: bf16, quantised into FP8 records)
  *   seq_lens   [B]        cached positions per sequence AFTER the append (new tokens included)
  *   q_seq, q_pos [T]      sequence and position of each new token, as in dsa_indexer_topk (NULL: one
  *                         token per sequence at position seq_lens - 1)

@@ -89,9 +89,22 @@ def lib():
     return _lib
 
 
+KV_FP8 = 0x10  # DSA_KV_FP8: the latent cache holds FP8 records (e4m3 codes, one fp32 scale per 128 elements)
+
+
+def kv_record_bytes(d: int) -> int:
+    """DSA_KV_FP8_RECORD_BYTES(d): bytes of one FP8 latent record."""
+    return (d + 4 * ((d + 127) // 128) + 15) // 16 * 16
+
+
 def make_dims(mode: str, B: int, max_blocks: int, num_blocks: int, H_I: int, d_I: int, H: int, d: int, d_v: int,
-              K: int, block_size: int = 64) -> Dims:
+              K: int, block_size: int = 64, kv: str = "act") -> Dims:
+    """kv="fp8" sets DSA_KV_FP8 (the latent cache holds FP8 records)."""
     m = MODES[mode] if isinstance(mode, str) else int(mode)
+    if kv == "fp8":
+        m |= KV_FP8
+    elif kv != "act":
+        raise ValueError(f"unknown latent-cache storage {kv!r}")
     return Dims(m, B, max_blocks, num_blocks, block_size, H_I, d_I, H, d, d_v, K)
 
 

@@ -5,8 +5,12 @@
 // out = sum_i p_i * row_i[0:d_v]: each warp accumulates every 8th row over 4 consecutive columns
 // per lane (128 columns per pass, vector loads), and the 8 warps' partial sums are added in shared
 // memory ("Day0 Inference Support ... on Huawei Ascend CANN Architecture" §1 and §2.1: the sparse
-// attention reads the main KV exactly at the selected indices).
+// attention reads the main KV exactly at the selected indices). With an FP8 latent cache (§3: FP8
+// block quantisation in the attention stage) every element read is code * its tile's scale, in
+// fp32.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "internal.h"
 
@@ -21,8 +25,51 @@ __device__ __forceinline__ float act_f(const void* p, int64_t i, bool bf16) {
 
 __device__ __forceinline__ uint16_t to_bf16_rn(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 
-template <bool BF16>
+// Latent-cache storage: fp32 rows, bf16 rows, or FP8 records (codes, then one fp32 scale per 128).
+enum KvKind { kKvF32 = 0, kKvBf16 = 1, kKvFp8 = 2 };
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);  // exact
+    return __half2float(*reinterpret_cast<const __half*>(&h));
+}
+
+// element e of latent row r
+template <int KV>
+__device__ __forceinline__ float kv_elem(const AttnArgs& a, int64_t r, int e) {
+    if (KV == kKvFp8) {
+        const uint8_t* rec = static_cast<const uint8_t*>(a.kv) + r * a.kv_rec;
+        return e4m3_to_f32(rec[e]) * *reinterpret_cast<const float*>(rec + a.d + 4 * (e >> 7));
+    }
+    return act_f(a.kv, r * a.d + e, KV == kKvBf16);
+}
+
+// elements c .. c + 3 of latent row r (c % 4 == 0, c + 3 < d: vector loads)
+template <int KV>
+__device__ __forceinline__ void kv_load4(const AttnArgs& a, int64_t r, int c, float (&v)[4]) {
+    if (KV == kKvFp8) {
+        const uint8_t* rec = static_cast<const uint8_t*>(a.kv) + r * a.kv_rec;
+        const uint32_t codes = *reinterpret_cast<const uint32_t*>(rec + c);
+        const float sc = *reinterpret_cast<const float*>(rec + a.d + 4 * (c >> 7));  // one tile: 128 % 4 == 0
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = e4m3_to_f32((codes >> (8 * k)) & 0xFFu) * sc;
+    } else if (KV == kKvBf16) {
+        const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.kv) + r * a.d + c);
+        v[0] = __uint_as_float(u.x << 16);
+        v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        v[2] = __uint_as_float(u.y << 16);
+        v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else {
+        const float4 f4 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.kv) + r * a.d + c);
+        v[0] = f4.x;
+        v[1] = f4.y;
+        v[2] = f4.z;
+        v[3] = f4.w;
+    }
+}
+
+template <int KV>
 __global__ void __launch_bounds__(kAttnSimtThreads) attn_simt_kernel(AttnArgs a) {
+    constexpr bool BF16 = KV != kKvF32;  // queries and outputs are bf16 with bf16 or FP8 latent rows
     extern __shared__ __align__(16) uint8_t smem[];
     const int d = a.d, K = a.K;
     float* q_s = reinterpret_cast<float*>(smem);  // [d]
@@ -72,7 +119,7 @@ __global__ void __launch_bounds__(kAttnSimtThreads) attn_simt_kernel(AttnArgs a)
             const float qe = q_s[e];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                if (rr[u] >= 0) dot[u] = fmaf(qe, act_f(a.kv, rr[u] * d + e, BF16), dot[u]);
+                if (rr[u] >= 0) dot[u] = fmaf(qe, kv_elem<KV>(a, rr[u], e), dot[u]);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -124,28 +171,15 @@ __global__ void __launch_bounds__(kAttnSimtThreads) attn_simt_kernel(AttnArgs a)
             const int64_t r = row_s[i];
             if (r < 0) continue;  // the same row for the whole warp
             const float p = z_s[i];
-            const int64_t e = r * d + c;
-            if (c + 3 < a.d_v) {  // d % 4 == 0 (fp32) / d % 8 == 0 (bf16): 16- / 8-byte aligned
+            if (c + 3 < a.d_v) {  // d % 4 == 0 (fp32) / d % 8 == 0 (bf16) / records 16-byte aligned
                 float v[4];
-                if (BF16) {
-                    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.kv) + e);
-                    v[0] = __uint_as_float(u.x << 16);
-                    v[1] = __uint_as_float(u.x & 0xFFFF0000u);
-                    v[2] = __uint_as_float(u.y << 16);
-                    v[3] = __uint_as_float(u.y & 0xFFFF0000u);
-                } else {
-                    const float4 f4 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.kv) + e);
-                    v[0] = f4.x;
-                    v[1] = f4.y;
-                    v[2] = f4.z;
-                    v[3] = f4.w;
-                }
+                kv_load4<KV>(a, r, c, v);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) acc[k] = fmaf(p, v[k], acc[k]);
             } else {
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    if (c + k < a.d_v) acc[k] = fmaf(p, act_f(a.kv, e + k, BF16), acc[k]);
+                    if (c + k < a.d_v) acc[k] = fmaf(p, kv_elem<KV>(a, r, c + k), acc[k]);
             }
         }
 #pragma unroll
@@ -170,13 +204,13 @@ bool launch_attn_simt(const AttnArgs& a, cudaStream_t s, int* launches) {
                         static_cast<size_t>(kAttnSimtThreads / 32) * 128 * 4;
     dim3 grid(a.H, a.T);
     const bool pdl = a.after_own_kernel != 0;
-    if (a.mode == DSA_F32) {
-        if (!set_max_dynamic_smem(reinterpret_cast<const void*>(attn_simt_kernel<false>), smem)) return false;
-        if (!launch_kernel(pdl, attn_simt_kernel<false>, grid, dim3(kAttnSimtThreads), smem, s, a)) return false;
-    } else {
-        if (!set_max_dynamic_smem(reinterpret_cast<const void*>(attn_simt_kernel<true>), smem)) return false;
-        if (!launch_kernel(pdl, attn_simt_kernel<true>, grid, dim3(kAttnSimtThreads), smem, s, a)) return false;
-    }
+    auto go = [&](auto kernel) {
+        return set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), smem) &&
+               launch_kernel(pdl, kernel, grid, dim3(kAttnSimtThreads), smem, s, a);
+    };
+    const bool ok = a.mode == DSA_F32 ? go(attn_simt_kernel<kKvF32>)
+                                      : (a.kv_fp8 ? go(attn_simt_kernel<kKvFp8>) : go(attn_simt_kernel<kKvBf16>));
+    if (!ok) return false;
     ++*launches;
     return true;
 }

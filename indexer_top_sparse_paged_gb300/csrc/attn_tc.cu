@@ -19,6 +19,11 @@
 //      maximum grows by more than 2^8) and writes P as bf16 over its S in tensor memory,
 //   5. accumulates O_r[128 x 256] += P . V_r with V_r = its 256 value columns (CTA 0: values
 //      0..255, CTA 1: values 256..511 -- both inside the columns it already holds).
+// With an FP8 latent cache (records of e4m3 codes with one fp32 scale per 128 elements; §3: FP8
+// block quantisation in the attention stage) step 1 gathers the codes of the CTA's columns into a
+// staging ring (cp.async, 16 codes per copy) and the same producer threads widen them into the bf16
+// operand stage, code * tile scale in fp32 rounded to bf16: the gathered bytes halve, the tensor-core
+// work is unchanged.
 // Split-K partials (m, l, O) are merged by attn_combine_kernel. Tensor memory holds the O
 // accumulator (256 fp32 columns), two S/P buffers and all but the first 64 query columns of the
 // CTA (A operand from TMEM); shared memory holds the first query chunk, four row stages, two
@@ -42,11 +47,14 @@ constexpr int kD = 576;
 constexpr int kDV = 512;
 constexpr int kDVH = 256;                     // value columns per CTA
 constexpr int kRows = 64;                     // gathered rows per tile
-constexpr int kStages = 4;
+constexpr int kStagesMax = 4;                 // bf16 operand stages (3 with an FP8 latent cache)
 constexpr int kChunkBytes = kRows * 128;      // [64 rows x 64 bf16]
 constexpr int kQChunkBytes = kHeads * 128;    // [128 heads x 64 bf16]
 constexpr int kMaxChunks = 5;                 // row chunks per CTA (CTA 0: 4, CTA 1: 5)
 constexpr int kStageBytes = kMaxChunks * kChunkBytes;
+constexpr int kRecBytes = DSA_KV_FP8_RECORD_BYTES(kD);  // an FP8 latent record: 576 codes + 5 scales + pad
+constexpr int kCodeStages = 2;                          // FP8 code staging ring
+constexpr int kCodeStageBytes = kRows * kMaxChunks * 64;  // 64 rows x up to 320 codes = 20 KB
 constexpr int kXBytes = kHeads * kRows * 2;   // one partial-logit tile (fp16, prescaled by 2^-8)
 constexpr float kXScale = 1.0f / 256.0f;      // partial logits travel as fp16(S_r * 2^-8)
 constexpr int kMaxRows = 2048;
@@ -59,7 +67,7 @@ constexpr uint32_t kIdescQK = idesc_f16(128, kRows, 1u, 0u, 0u);
 constexpr uint32_t kIdescPV = idesc_f16(128, kDVH, 1u, 0u, 1u);
 
 struct Smem {
-    uint64_t full[kStages], empty[kStages];
+    uint64_t full[kStagesMax], empty[kStagesMax];
     uint64_t s_full[2], p_full[2], s_free[2];
     uint64_t qfull, o_full, mma_done;
     uint64_t xfull[2], xempty[2];  // both arrived on by the peer: its partial landed / it consumed ours
@@ -68,15 +76,24 @@ struct Smem {
     int abort_flag;
 };
 
-constexpr size_t kOffQ = 0;
-constexpr size_t kOffKv = kOffQ + kQChunkBytes;
-constexpr size_t kOffX = kOffKv + static_cast<size_t>(kStages) * kStageBytes;  // received partials
-constexpr size_t kOffValid = kOffX + 2 * kXBytes;                                // 1 bit per selected row
-constexpr size_t kOffPhys = kOffValid + kMaxRows / 8;                             // physical row per selected row
-constexpr size_t kOffRed = kOffPhys + kMaxRows * sizeof(int32_t);  // softmax maxima / row sums
-constexpr size_t kOffCtl = kOffRed + 4 * kHeads * sizeof(float);
-constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(Smem);
-static_assert(kSmemBytes <= 232448, "attention shared memory over the limit");
+// Shared memory of one CTA: bf16 latent rows use four operand stages, FP8 records three plus the
+// code staging ring.
+template <bool kKv8>
+struct Layout {
+    static constexpr int kStages = kKv8 ? 3 : 4;
+    static constexpr size_t kOffQ = 0;
+    static constexpr size_t kOffKv = kOffQ + kQChunkBytes;
+    static constexpr size_t kOffCode = kOffKv + static_cast<size_t>(kStages) * kStageBytes;  // FP8 codes
+    static constexpr size_t kOffX = kOffCode + (kKv8 ? static_cast<size_t>(kCodeStages) * kCodeStageBytes : 0);
+    static constexpr size_t kOffValid = kOffX + 2 * kXBytes;                // 1 bit per selected row
+    static constexpr size_t kOffPhys = kOffValid + kMaxRows / 8;            // physical row per selected row
+    static constexpr size_t kOffRed = kOffPhys + kMaxRows * sizeof(int32_t);  // softmax maxima / row sums
+    static constexpr size_t kOffCtl = kOffRed + 4 * kHeads * sizeof(float);
+    static constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(Smem);
+};
+static_assert(Layout<false>::kSmemBytes <= 232448, "attention shared memory over the limit");
+static_assert(Layout<true>::kSmemBytes <= 232448, "FP8 attention shared memory over the limit");
+static_assert(4 * kQChunkBytes <= Layout<true>::kStages * kStageBytes, "query chunks are staged in the row stages");
 
 __host__ __device__ inline int split_rows(int K, int S) {
     const int per = (K + S - 1) / S;
@@ -95,8 +112,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+template <bool kKv8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
     attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap map_q) {
+    using Lay = Layout<kKv8>;
+    constexpr int kStages = Lay::kStages;
+    constexpr size_t kOffQ = Lay::kOffQ, kOffKv = Lay::kOffKv, kOffX = Lay::kOffX, kOffValid = Lay::kOffValid;
+    constexpr size_t kOffPhys = Lay::kOffPhys, kOffRed = Lay::kOffRed, kOffCtl = Lay::kOffCtl;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem + kOffQ);
@@ -233,10 +255,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         //  send(j):   once S(j) is in tensor memory, read the partial logits of heads 32pw..32pw+31,
         //             round them to fp16(S * 2^-8) and store them into the peer's exchange slot
         //             j & 1 (distributed shared memory; the peer's softmax frees the slot);
-        //  gather(t): once stage t % 4 is free, resolve rows 4g..4g+3 of tile t (lane g) to
-        //             physical cache rows and issue one TMA tile::gather4 per 64-column chunk
-        //             (chunk pw; CTA 1's chunk 4 also goes to pw = 0) into the 128-byte-swizzled
-        //             layout (rows with no position read as zeros).
+        //  gather(t): once stage t % 4 is free, copy rows pw, pw + 4, ... of tile t (their physical
+        //             cache rows were resolved up front) with 16-byte cp.async per lane (lane = chunk
+        //             lane / 8, 16-byte group lane % 8; CTA 1's fifth chunk from lanes 0..7) into the
+        //             128-byte-swizzled layout; rows with no position read as zeros.
+        //  FP8 records instead: issue(t) copies the tile's codes (16 per cp.async, groups spread
+        //             over the 128 producer threads) into code stage t % 2, and convert(t), once bf16
+        //             stage t % 3 is free, widens the codes the same thread copied, times their tile
+        //             scale, into it.
         const int pw = warp - 4;
         const int h = pw * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(pw * 32) << 16;
@@ -292,22 +318,108 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                 st_async_v4(dst + xoff(h, g), hp[4 * g], hp[4 * g + 1], hp[4 * g + 2], hp[4 * g + 3], peer_xfull + sb * 8);
             return true;
         };
-        bool ok = true;
-        for (int t = 0; ok && t < kStages - 1 && t < ntiles; ++t) ok = gather(t);
-        for (int j = 0; ok && j < ntiles; ++j) {
-            ok = send(j);
-            if (ok && j + kStages - 1 < ntiles) ok = gather(j + kStages - 1);
+        if constexpr (!kKv8) {
+            bool ok = true;
+            for (int t = 0; ok && t < kStages - 1 && t < ntiles; ++t) ok = gather(t);
+            for (int j = 0; ok && j < ntiles; ++j) {
+                ok = send(j);
+                if (ok && j + kStages - 1 < ntiles) ok = gather(j + kStages - 1);
+            }
+        } else {
+            constexpr int kPT = kProducers * 32;                    // producer threads
+            constexpr int kGPT = kCodeStageBytes / 16 / kPT;        // 16-code groups per thread and tile (<= 10)
+            const int gpr = nchunks * 4;                            // groups per row of this CTA: 16 or 20
+            const int ngroups = kRows * gpr;
+            const int pt = pw * 32 + lane;
+            const uint8_t* kvb = static_cast<const uint8_t*>(a.kv);
+            const uint32_t sCode = smem_u32(smem + Lay::kOffCode);
+            int issued = 0;
+            auto issue = [&](int tile) {
+                const uint32_t base = sCode + (tile % kCodeStages) * kCodeStageBytes;
+#pragma unroll
+                for (int k = 0; k < kGPT; ++k) {
+                    const int gi = pt + k * kPT;
+                    if (gi < ngroups) {
+                        const int r = gi / gpr, q = gi - r * gpr;
+                        const int p = phys_s[tile * kRows + r];
+                        const uint8_t* src = p >= 0 ? kvb + static_cast<int64_t>(p) * kRecBytes + c0 * 64 + q * 16 : kvb;
+                        cp_async16(base + gi * 16, src, p >= 0 ? 16u : 0u);  // 0: zero-fill
+                    }
+                }
+                cp_async_commit();
+                ++issued;
+            };
+            auto convert = [&](int tile) -> bool {
+                const int st = tile % kStages;
+                float sc[kGPT];
+#pragma unroll
+                for (int k = 0; k < kGPT; ++k) {  // the scales first: their loads overlap the waits
+                    const int gi = pt + k * kPT;
+                    sc[k] = 0.0f;
+                    if (gi < ngroups) {
+                        const int r = gi / gpr, q = gi - r * gpr;
+                        const int p = phys_s[tile * kRows + r];
+                        if (p >= 0)
+                            sc[k] = __ldg(reinterpret_cast<const float*>(kvb + static_cast<int64_t>(p) * kRecBytes + kD) +
+                                          ((c0 * 64 + q * 16) >> 7));
+                    }
+                }
+                const bool got = mbar_wait(smem_u32(&S.empty[st]), ((tile / kStages) & 1) ^ 1, abort_flag, a.err);
+                if (!__all_sync(0xFFFFFFFFu, got)) return false;
+                if (issued > tile + 1) cp_async_wait<1>();  // the tile's codes have landed (the next tile's may not)
+                else cp_async_wait<0>();
+                const uint8_t* codes = smem + Lay::kOffCode + (tile % kCodeStages) * kCodeStageBytes;
+                uint8_t* stage = smem + kOffKv + st * kStageBytes;
+#pragma unroll
+                for (int k = 0; k < kGPT; ++k) {
+                    const int gi = pt + k * kPT;
+                    if (gi < ngroups) {
+                        const int r = gi / gpr, q = gi - r * gpr;
+                        uint4 lo, hi;
+                        e4m3x16_to_bf16_scaled(*reinterpret_cast<const uint4*>(codes + gi * 16), sc[k], lo, hi);
+                        uint8_t* row = stage + (q >> 2) * kChunkBytes + r * 128;  // chunk q / 4
+                        const int g2 = 2 * (q & 3);
+                        *reinterpret_cast<uint4*>(row + ((g2 ^ (r & 7)) << 4)) = lo;
+                        *reinterpret_cast<uint4*>(row + (((g2 + 1) ^ (r & 7)) << 4)) = hi;
+                    }
+                }
+                fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
+                mbar_arrive(smem_u32(&S.full[st]));
+                return true;
+            };
+            bool ok = true;
+            for (int t = 0; t < kCodeStages && t < ntiles; ++t) issue(t);
+            for (int t = 0; ok && t < kStages - 1 && t < ntiles; ++t) {
+                ok = convert(t);
+                if (ok && t + kCodeStages < ntiles) issue(t + kCodeStages);
+            }
+            for (int j = 0; ok && j < ntiles; ++j) {
+                ok = send(j);
+                const int tt = j + kStages - 1;
+                if (ok && tt < ntiles) {
+                    ok = convert(tt);
+                    if (ok && tt + kCodeStages < ntiles) issue(tt + kCodeStages);
+                }
+            }
+            cp_async_wait<0>();  // nothing of this thread's is still in flight when the CTA exits
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------- L2 prefetch
         // Every valid selected row's columns of this CTA (4 or 5 lines of 128 B), requested up
         // front so that the gathers find them in L2.
-        const uint8_t* kv = static_cast<const uint8_t*>(a.kv) + c0 * 128;
         for (int row = lane; row < nrows; row += 32) {
             const int p = phys_s[row];
             if (p < 0) continue;
-            const uint8_t* rp = kv + static_cast<int64_t>(p) * (kD * 2);
-            for (int c = 0; c < nchunks; ++c) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + c * 128));
+            if constexpr (!kKv8) {
+                const uint8_t* rp = static_cast<const uint8_t*>(a.kv) + c0 * 128 + static_cast<int64_t>(p) * (kD * 2);
+                for (int c = 0; c < nchunks; ++c) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + c * 128));
+            } else {  // the record's codes of this CTA's columns and the scales
+                const uint8_t* rp = static_cast<const uint8_t*>(a.kv) + static_cast<int64_t>(p) * kRecBytes;
+                const int lo = c0 * 64, hi = lo + nchunks * 64;
+                for (int o = lo; o < hi; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + o));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + hi - 1));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + kD));
+            }
         }
     } else if (warp == 8) {
         // ------------------------------------------------------------- MMA issuer
@@ -592,16 +704,21 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 
 }  // namespace tcattn
 
+template <bool kKv8>
+static bool launch_attn_tc_typed(const AttnArgs& a, const CUtensorMap& map_q, cudaStream_t s) {
+    const size_t smem = tcattn::Layout<kKv8>::kSmemBytes;
+    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(tcattn::attn_tc_kernel<kKv8>), smem)) return false;
+    return launch_kernel(a.after_own_kernel != 0, tcattn::attn_tc_kernel<kKv8>, dim3(2 * a.S, a.T),
+                         dim3(tcattn::kThreads), smem, s, a, map_q);
+}
+
 bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches) {
     if (a.T == 0) return true;
     CUtensorMap map_q;
     if (!make_tmap_2d(&map_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tcattn::kD,
                       static_cast<uint64_t>(a.T) * tcattn::kHeads, tcattn::kD * 2, 64, 128))
         return false;
-    if (!set_max_dynamic_smem(reinterpret_cast<const void*>(tcattn::attn_tc_kernel), tcattn::kSmemBytes)) return false;
-    if (!launch_kernel(a.after_own_kernel != 0, tcattn::attn_tc_kernel, dim3(2 * a.S, a.T), dim3(tcattn::kThreads),
-                       tcattn::kSmemBytes, s, a, map_q))
-        return false;
+    if (!(a.kv_fp8 ? launch_attn_tc_typed<true>(a, map_q, s) : launch_attn_tc_typed<false>(a, map_q, s))) return false;
     ++*launches;
     if (a.S > 1) {
         if (!launch_kernel(true, tcattn::attn_combine_kernel, dim3(tcattn::kHeads, a.T), dim3(128), 0, s, a)) return false;
@@ -610,6 +727,6 @@ bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches) {
     return true;
 }
 
-size_t attn_tc_smem() { return tcattn::kSmemBytes; }
+size_t attn_tc_smem() { return tcattn::Layout<false>::kSmemBytes; }
 
 }  // namespace dsa

@@ -12,6 +12,10 @@
 // scale = amax / 448 (1 when amax is 0) and every code becomes RNE_e4m3(x / scale), saturating
 // at +-448. The new tokens of one block must be consecutive rows (ascending positions). MXFP8
 // keys have no block state: each new key's groups of 32 get their own E8M0 scale and codes.
+// An FP8 latent cache (DSA_KV_FP8) has no block state either: each new row becomes one record,
+// every 128-element tile quantised on its own (one warp per tile), in fp32: scale = amax / 448
+// (1 when amax is 0), code = RNE_e4m3(x / scale), saturating ("Day0 Inference Support ... on
+// Huawei Ascend CANN Architecture" §3: FP8 block quantisation in the attention stage).
 #include "internal.h"
 
 namespace dsa {
@@ -20,6 +24,7 @@ constexpr int kAppendThreads = 256;
 
 struct AppendArgs {
     int mode;
+    int kv_fp8;  // latent rows stored as FP8 records
     int B, max_blocks, num_blocks;
     int d_I, d;
     int T;
@@ -57,6 +62,40 @@ __device__ __forceinline__ float e4m3_value(uint8_t code) {
     return __half2float(*reinterpret_cast<const __half*>(&h));
 }
 
+// One FP8 latent record from a bf16 row of d elements (d % 16 == 0): warp w quantises tiles
+// w, w + 8, ...; lane l holds elements 4l .. 4l + 3 of the tile. The padding after the scales is
+// zeroed.
+__device__ void store_kv_record(uint8_t* rec, const uint16_t* x, int d) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ntiles = (d + 127) / 128;
+    for (int j = warp; j < ntiles; j += kAppendThreads / 32) {
+        const int e = 128 * j + 4 * lane;
+        const bool in = e < d;  // d % 16 == 0: a lane's 4 elements are all in or all out
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (in) {
+            const uint2 u = *reinterpret_cast<const uint2*>(x + e);
+            v[0] = __uint_as_float(u.x << 16);
+            v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+            v[2] = __uint_as_float(u.y << 16);
+            v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+        }
+        float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        if (in) {
+            uint32_t c = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                c |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(v[k] / scale, __NV_SATFINITE, __NV_E4M3)) << (8 * k);
+            *reinterpret_cast<uint32_t*>(rec + e) = c;
+        }
+        if (lane == 0) *reinterpret_cast<float*>(rec + d + 4 * j) = scale;
+    }
+    for (int i = d + 4 * ntiles + static_cast<int>(threadIdx.x); i < DSA_KV_FP8_RECORD_BYTES(d); i += kAppendThreads)
+        rec[i] = 0;
+}
+
 __global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(AppendArgs a) {
     __shared__ float red[kAppendThreads / 32];
     __shared__ int run_end;
@@ -69,8 +108,13 @@ __global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(AppendArgs
     }
     const int64_t row = static_cast<int64_t>(blk) * kBlock + pos % kBlock;
     const int act = a.mode == DSA_F32 ? 4 : 2;
-    copy_row(static_cast<uint8_t*>(a.kv_cache) + row * a.d * act, static_cast<const uint8_t*>(a.kv_new) + static_cast<int64_t>(t) * a.d * act,
-             a.d * act);
+    if (a.kv_fp8) {
+        store_kv_record(static_cast<uint8_t*>(a.kv_cache) + row * DSA_KV_FP8_RECORD_BYTES(a.d),
+                        static_cast<const uint16_t*>(a.kv_new) + static_cast<int64_t>(t) * a.d, a.d);
+    } else {
+        copy_row(static_cast<uint8_t*>(a.kv_cache) + row * a.d * act,
+                 static_cast<const uint8_t*>(a.kv_new) + static_cast<int64_t>(t) * a.d * act, a.d * act);
+    }
     if (a.mode == DSA_MXFP8) {  // every group of 32 of the new key is quantised on its own
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.k_new) + static_cast<int64_t>(t) * a.d_I);
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.k_cache) + row * a.d_I);
@@ -147,12 +191,13 @@ __global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(AppendArgs
     if (threadIdx.x == 0) static_cast<float*>(a.k_scale)[blk] = scale;
 }
 
-bool launch_cache_append(const dsa_dims& d, const void* k_new, const void* kv_new, const int32_t* block_table,
-                         const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T, void* k_cache,
-                         void* k_scale, void* kv_cache, int* err, cudaStream_t s, int* launches) {
+bool launch_cache_append(const dsa_dims& d, bool kv_fp8, const void* k_new, const void* kv_new,
+                         const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
+                         const int32_t* q_pos, int T, void* k_cache, void* k_scale, void* kv_cache, int* err,
+                         cudaStream_t s, int* launches) {
     if (T == 0) return true;
-    AppendArgs a{d.mode, d.B, d.max_blocks, d.num_blocks, d.d_I, d.d, T, k_new, kv_new, block_table, seq_lens,
-                 q_seq, q_pos, k_cache, k_scale, kv_cache, err};
+    AppendArgs a{d.mode, kv_fp8 ? 1 : 0, d.B, d.max_blocks, d.num_blocks, d.d_I, d.d, T, k_new, kv_new, block_table,
+                 seq_lens, q_seq, q_pos, k_cache, k_scale, kv_cache, err};
     if (!launch_kernel(false, cache_append_kernel, dim3(T), dim3(kAppendThreads), 0, s, a)) return false;
     ++*launches;
     return true;

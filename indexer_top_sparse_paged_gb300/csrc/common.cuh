@@ -258,7 +258,8 @@ struct TopkGroup {
     uint32_t bar_id;
     // uniform across the group (every thread computes the same values)
     uint32_t count = 0;
-    uint64_t theta = 0;  // admission threshold: keys below it cannot be in the Top-K
+    uint64_t theta = 0;  // admission threshold: keys below it are not admitted
+    uint64_t est = 0;    // the largest sample estimate applied to this candidate set (0: none)
     uint32_t parity = 0;
 
     __device__ __forceinline__ void sync() const { named_bar_sync(bar_id, NT); }
@@ -267,7 +268,28 @@ struct TopkGroup {
     __device__ void reset() {
         count = 0;
         theta = 0;
+        est = 0;
         sync();
+    }
+
+    // Collective: raises the admission threshold to the r-th largest key of the buffer (0 < r <
+    // count), which holds every valid key offered so far (a sample of the row). Unlike the
+    // thresholds of select(), this is an estimate of the row's K-th key, not a bound: whoever
+    // merges the row's candidate lists must check that at least K of them are >= every estimate
+    // used (then no key of the row's Top-K was turned away) and recompute the row otherwise. The
+    // buffer keeps all its keys.
+    __device__ void estimate(uint32_t r) {
+        sync();  // every push's writes to buf are visible
+        const uint32_t n = count;
+        const uint32_t per = (n + NT - 1) / NT;
+        const uint32_t c0 = min(n, tid * per), c1 = min(n, c0 + per);
+        const uint32_t cnt = c1 - c0;
+        uint64_t keys[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) keys[j] = (static_cast<uint32_t>(j) < cnt) ? buf[c0 + j] : 0ull;
+        const uint64_t e = reg_radix_threshold<NT, PER>(keys, cnt, r, hist, ctl, tid, bar_id);
+        if (e > theta) theta = e;
+        if (e > est) est = e;
     }
 
     // Collective: exclusive offset of this thread's predicate among the group and the total.
@@ -341,10 +363,14 @@ struct TopkGroup {
         count += total;
     }
 
-    // Collective: writes at most K keys (in position order) to `out`, their number to count_out.
-    __device__ void flush(uint64_t* out, int32_t* count_out) {
+    // Collective: writes at most K keys (in position order) to `out`, their number to count_out
+    // and the estimate the set was filtered with (0: none) to est_out.
+    __device__ void flush(uint64_t* out, int32_t* count_out, uint64_t* est_out) {
         const uint32_t kept = select_to(out);
-        if (tid == 0) *count_out = static_cast<int32_t>(kept);
+        if (tid == 0) {
+            *count_out = static_cast<int32_t>(kept);
+            *est_out = est;
+        }
     }
 };
 
@@ -482,6 +508,28 @@ __device__ __forceinline__ void store_bf16_row_mx(uint8_t* stage, int r, const u
 // kernel parameter blocks
 // ------------------------------------------------------------------------------------------------
 
+// Sample estimate of a row's K-th key (streaming Top-K of the decode indexer): after the first
+// kEstTiles tiles of a segment of at least kEstMinTiles tiles, the admission threshold rises to
+// the r-th largest of the sampled keys with r = ceil(sample * kEstMargin * K / n) (n = the row's
+// causal keys), at least kEstMinRank. With K / n of the row's keys above its K-th key, the r-th
+// sample key lies above that key only if the sample holds kEstMargin times its expected share of
+// them; for independent draws that is more than 9 standard deviations out at K / n = 0.085 (decode
+// rows of 24K keys) and far rarer for longer rows, where the rank floor dominates.
+constexpr int kEstTiles = 2;
+constexpr int kEstMinTiles = 8;
+constexpr float kEstMargin = 3.0f;
+constexpr uint32_t kEstMinRank = 16;
+
+// The rank of the estimate for a sample of `sample` valid keys of a row of n causal keys, or 0
+// when no estimate applies (it would admit nearly everything).
+__device__ __forceinline__ uint32_t estimate_rank(uint32_t sample, int n, int K) {
+    if (n <= K) return 0;
+    const float q = kEstMargin * static_cast<float>(K) / static_cast<float>(n);
+    uint32_t r = static_cast<uint32_t>(ceilf(q * static_cast<float>(sample)));
+    r = max(r, kEstMinRank);
+    return (q < 0.75f && r < sample) ? r : 0u;
+}
+
 struct IndexerArgs {
     int mode;
     int B, max_blocks, num_blocks;
@@ -500,6 +548,7 @@ struct IndexerArgs {
     int32_t* merge_count;  // [3][merge groups] finished children per merge-tree group (workspace)
     int32_t* slot_count;   // [G + T] (workspace)
     uint64_t* slots;       // [G + T][K] (workspace)
+    uint64_t* slot_est;    // [G + T] sample estimate each candidate list was filtered with, 0: none (workspace)
     int32_t* idx;          // [T][K] out
     int* err;              // device error word (workspace)
     int G;                 // indexer CTAs

@@ -97,6 +97,8 @@ WsLayout ws_layout(const dsa_dims& d, int T, bool allow_prefill) {
     off = align256(off + sizeof(int32_t) * (static_cast<size_t>(w.G) + T));
     w.slots = off;
     off = align256(off + sizeof(uint64_t) * (static_cast<size_t>(w.G) + T) * d.K);
+    w.slot_est = off;
+    off = align256(off + sizeof(uint64_t) * (static_cast<size_t>(w.G) + T));
     w.q_mx = off;
     if (d.mode == DSA_MXFP8) off = align256(off + sizeof(uint16_t) * static_cast<size_t>(T) * d.H_I * d.d_I);
     w.idx = off;
@@ -149,6 +151,17 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
 // ------------------------------------------------------------------------------------------------
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The public mode may carry DSA_KV_FP8 (the latent cache's storage); every kernel below takes the
+// indexer-key mode alone, and the attention and the cache append get the flag on its own.
+static dsa_status split_mode(const dsa_dims* in, dsa_dims* out, bool* kv8) {
+    if (!in) return DSA_ERR_INVALID_ARG;
+    *out = *in;
+    *kv8 = (in->mode & DSA_KV_FP8) != 0;
+    out->mode = in->mode & ~DSA_KV_FP8;
+    if (*kv8 && (out->mode == DSA_F32 || in->d % 16)) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
 
 static dsa_status check_common(const dsa_dims* d) {
     if (!d) return DSA_ERR_INVALID_ARG;
@@ -224,6 +237,7 @@ static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w
     a.merge_count = reinterpret_cast<int32_t*>(base + L.merge_count);
     a.slot_count = reinterpret_cast<int32_t*>(base + L.slot_count);
     a.slots = reinterpret_cast<uint64_t*>(base + L.slots);
+    a.slot_est = reinterpret_cast<uint64_t*>(base + L.slot_est);
     a.idx = idx;
     a.err = reinterpret_cast<int*>(base + L.err);
     a.G = L.G;
@@ -250,10 +264,10 @@ static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w
     return DSA_OK;
 }
 
-static dsa_status run_attn(const dsa_dims* d, const void* q, const void* kv_cache, const int32_t* block_table,
-                           const int32_t* seq_lens, const int32_t* q_seq, const int32_t* idx, int32_t T,
-                           float sm_scale, void* out, float* lse, void* ws, cudaStream_t stream, int* launches,
-                           bool after_own_kernel) {
+static dsa_status run_attn(const dsa_dims* d, bool kv8, const void* q, const void* kv_cache,
+                           const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
+                           const int32_t* idx, int32_t T, float sm_scale, void* out, float* lse, void* ws,
+                           cudaStream_t stream, int* launches, bool after_own_kernel) {
     const WsLayout L = ws_layout(*d, T);
     uint8_t* base = static_cast<uint8_t*>(ws);
     AttnArgs a{};
@@ -280,6 +294,8 @@ static dsa_status run_attn(const dsa_dims* d, const void* q, const void* kv_cach
     a.S = L.S;
     a.err = reinterpret_cast<int*>(base + L.err);
     a.after_own_kernel = after_own_kernel ? 1 : 0;
+    a.kv_fp8 = kv8 ? 1 : 0;
+    a.kv_rec = kv8 ? DSA_KV_FP8_RECORD_BYTES(d->d) : d->d * (d->mode == DSA_F32 ? 4 : 2);
     const bool ok = attn_uses_tc(*d) ? launch_attn_tc(a, stream, launches) : launch_attn_simt(a, stream, launches);
     return ok ? DSA_OK : DSA_ERR_LAUNCH;
 }
@@ -368,8 +384,12 @@ using namespace dsa;
 
 extern "C" {
 
-size_t dsa_workspace_size(const dsa_dims* dims, int32_t T) {
-    if (!dims || T < 0 || check_common(dims) != DSA_OK) return 0;
+size_t dsa_workspace_size(const dsa_dims* dims_in, int32_t T) {
+    dsa_dims D;
+    bool kv8;
+    if (!dims_in || split_mode(dims_in, &D, &kv8) != DSA_OK) return 0;
+    const dsa_dims* dims = &D;
+    if (T < 0 || check_common(dims) != DSA_OK) return 0;
     return ws_layout(*dims, T).total;
 }
 
@@ -379,10 +399,17 @@ dsa_status dsa_workspace_init(void* ws, size_t ws_bytes, dsa_stream_t stream) {
                                                                                               : DSA_ERR_LAUNCH;
 }
 
-dsa_status dsa_indexer_topk(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+dsa_status dsa_indexer_topk(const dsa_dims* dims_in, const void* q_I, const float* w, const void* k_I_cache,
                             const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                             const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx, void* ws,
                             size_t ws_bytes, dsa_stream_t stream) {
+    dsa_dims D;
+    bool kv8;
+    {
+        const dsa_status split = split_mode(dims_in, &D, &kv8);
+        if (split != DSA_OK) return split;
+    }
+    const dsa_dims* dims = &D;
     dsa_status st = check_indexer_dims(dims);
     if (st != DSA_OK) return st;
     if (T < 0) return DSA_ERR_INVALID_ARG;
@@ -400,9 +427,16 @@ dsa_status dsa_indexer_topk(const dsa_dims* dims, const void* q_I, const float* 
     return st;
 }
 
-dsa_status dsa_sparse_attn(const dsa_dims* dims, const void* q, const void* kv_cache, const int32_t* block_table,
+dsa_status dsa_sparse_attn(const dsa_dims* dims_in, const void* q, const void* kv_cache, const int32_t* block_table,
                            const int32_t* seq_lens, const int32_t* q_seq, const int32_t* idx, int32_t T,
                            float sm_scale, void* out, float* lse, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+    dsa_dims D;
+    bool kv8;
+    {
+        const dsa_status split = split_mode(dims_in, &D, &kv8);
+        if (split != DSA_OK) return split;
+    }
+    const dsa_dims* dims = &D;
     dsa_status st = check_attn_dims(dims);
     if (st != DSA_OK) return st;
     if (T < 0) return DSA_ERR_INVALID_ARG;
@@ -413,16 +447,23 @@ dsa_status dsa_sparse_attn(const dsa_dims* dims, const void* q, const void* kv_c
     if (st != DSA_OK) return st;
     int launches = 0;
     if (T > 0)
-        st = run_attn(dims, q, kv_cache, block_table, seq_lens, q_seq, idx, T, sm_scale, out, lse, ws,
+        st = run_attn(dims, kv8, q, kv_cache, block_table, seq_lens, q_seq, idx, T, sm_scale, out, lse, ws,
                       reinterpret_cast<cudaStream_t>(stream), &launches, false);
     g_last_launches = launches;
     return st;
 }
 
-dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+dsa_status dsa_decode(const dsa_dims* dims_in, const void* q_I, const float* w, const void* k_I_cache,
                       const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens, const void* q,
                       const void* kv_cache, float sm_scale, int32_t* idx, void* out, float* lse, void* ws,
                       size_t ws_bytes, dsa_stream_t stream) {
+    dsa_dims D;
+    bool kv8;
+    {
+        const dsa_status split = split_mode(dims_in, &D, &kv8);
+        if (split != DSA_OK) return split;
+    }
+    const dsa_dims* dims = &D;
     dsa_status st = check_indexer_dims(dims);
     if (st != DSA_OK) return st;
     st = check_attn_dims(dims);
@@ -442,16 +483,23 @@ dsa_status dsa_decode(const dsa_dims* dims, const void* q_I, const float* w, con
     st = run_indexer(dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, nullptr, nullptr, T, idx_buf, ws, s,
                      &launches);
     if (st == DSA_OK)
-        st = run_attn(dims, q, kv_cache, block_table, seq_lens, nullptr, idx_buf, T, sm_scale, out, lse, ws, s,
+        st = run_attn(dims, kv8, q, kv_cache, block_table, seq_lens, nullptr, idx_buf, T, sm_scale, out, lse, ws, s,
                       &launches, true);
     g_last_launches = launches;
     return st;
 }
 
-dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims_in, const void* q_I, const float* w, const void* k_I_cache,
                                     const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                                     const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx,
                                     int32_t* fault_word, dsa_stream_t stream) {
+    dsa_dims D;
+    bool kv8;
+    {
+        const dsa_status split = split_mode(dims_in, &D, &kv8);
+        if (split != DSA_OK) return split;
+    }
+    const dsa_dims* dims = &D;
     dsa_status st = check_indexer_dims(dims);
     if (st != DSA_OK) return st;
     if (T < 0) return DSA_ERR_INVALID_ARG;
@@ -484,10 +532,17 @@ dsa_status dsa_indexer_topk_noalloc(const dsa_dims* dims, const void* q_I, const
     return st;
 }
 
-dsa_status dsa_cache_append(const dsa_dims* dims, const void* k_I_new, const void* kv_new,
+dsa_status dsa_cache_append(const dsa_dims* dims_in, const void* k_I_new, const void* kv_new,
                             const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
                             const int32_t* q_pos, int32_t T, void* k_I_cache, void* k_I_scale, void* kv_cache,
                             void* ws, size_t ws_bytes, dsa_stream_t stream) {
+    dsa_dims D;
+    bool kv8;
+    {
+        const dsa_status split = split_mode(dims_in, &D, &kv8);
+        if (split != DSA_OK) return split;
+    }
+    const dsa_dims* dims = &D;
     dsa_status st = check_common(dims);
     if (st != DSA_OK) return st;
     if (T < 0 || dims->d_I <= 0 || dims->d <= 0) return DSA_ERR_INVALID_ARG;
@@ -501,21 +556,33 @@ dsa_status dsa_cache_append(const dsa_dims* dims, const void* k_I_new, const voi
         return DSA_ERR_INVALID_ARG;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return DSA_ERR_WORKSPACE;
     int launches = 0;
-    if (!launch_cache_append(*dims, k_I_new, kv_new, block_table, seq_lens, q_seq, q_pos, T, k_I_cache, k_I_scale,
-                             kv_cache, static_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream), &launches))
+    if (!launch_cache_append(*dims, kv8, k_I_new, kv_new, block_table, seq_lens, q_seq, q_pos, T, k_I_cache,
+                             k_I_scale, kv_cache, static_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream),
+                             &launches))
         st = DSA_ERR_LAUNCH;
     g_last_launches = launches;
     return st;
 }
 
-size_t dsa_hier_workspace_size(const dsa_dims* dims, int32_t T, int32_t n_sel) {
-    if (!dims || T <= 0 || n_sel <= 0 || n_sel > 2048 || check_common(dims) != DSA_OK) return 0;
+size_t dsa_hier_workspace_size(const dsa_dims* dims_in, int32_t T, int32_t n_sel) {
+    dsa_dims D;
+    bool kv8;
+    if (!dims_in || split_mode(dims_in, &D, &kv8) != DSA_OK) return 0;
+    const dsa_dims* dims = &D;
+    if (T <= 0 || n_sel <= 0 || n_sel > 2048 || check_common(dims) != DSA_OK) return 0;
     return hier_layout(*dims, T, n_sel).total;
 }
 
-dsa_status dsa_block_summaries(const dsa_dims* dims, const void* k_I_cache, const void* k_I_scale,
+dsa_status dsa_block_summaries(const dsa_dims* dims_in, const void* k_I_cache, const void* k_I_scale,
                                const int32_t* block_table, const int32_t* seq_lens, uint16_t* summaries, void* ws,
                                size_t ws_bytes, dsa_stream_t stream) {
+    dsa_dims D;
+    bool kv8;
+    {
+        const dsa_status split = split_mode(dims_in, &D, &kv8);
+        if (split != DSA_OK) return split;
+    }
+    const dsa_dims* dims = &D;
     dsa_status st = check_common(dims);
     if (st != DSA_OK) return st;
     if (dims->d_I <= 0) return DSA_ERR_INVALID_ARG;
@@ -531,10 +598,17 @@ dsa_status dsa_block_summaries(const dsa_dims* dims, const void* k_I_cache, cons
     return st;
 }
 
-dsa_status dsa_block_summaries_append(const dsa_dims* dims, const void* k_I_cache, const void* k_I_scale,
+dsa_status dsa_block_summaries_append(const dsa_dims* dims_in, const void* k_I_cache, const void* k_I_scale,
                                       const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
                                       const int32_t* q_pos, int32_t T, uint16_t* summaries, void* ws, size_t ws_bytes,
                                       dsa_stream_t stream) {
+    dsa_dims D;
+    bool kv8;
+    {
+        const dsa_status split = split_mode(dims_in, &D, &kv8);
+        if (split != DSA_OK) return split;
+    }
+    const dsa_dims* dims = &D;
     dsa_status st = check_common(dims);
     if (st != DSA_OK) return st;
     if (T < 0 || dims->d_I <= 0) return DSA_ERR_INVALID_ARG;
@@ -551,11 +625,18 @@ dsa_status dsa_block_summaries_append(const dsa_dims* dims, const void* k_I_cach
     return st;
 }
 
-dsa_status dsa_indexer_topk_hier(const dsa_dims* dims, const void* q_I, const float* w, const void* k_I_cache,
+dsa_status dsa_indexer_topk_hier(const dsa_dims* dims_in, const void* q_I, const float* w, const void* k_I_cache,
                                  const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                                  const int32_t* q_seq, const int32_t* q_pos, int32_t T, const uint16_t* summaries,
                                  int32_t n_sel, int32_t* idx, int32_t* blocks_out, void* ws, size_t ws_bytes,
                                  dsa_stream_t stream) {
+    dsa_dims D;
+    bool kv8;
+    {
+        const dsa_status split = split_mode(dims_in, &D, &kv8);
+        if (split != DSA_OK) return split;
+    }
+    const dsa_dims* dims = &D;
     dsa_status st = check_indexer_dims(dims);
     if (st != DSA_OK) return st;
     if (dims->mode == DSA_F32) return DSA_ERR_UNSUPPORTED;  // the coarse stage scores bf16 summaries with bf16 q_I

@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kSimtThreads) indexer_simt_kernel(IndexerArgs 
             topk.push(make_key(score, static_cast<uint32_t>(s)), valid);
         }
         const int64_t slot = static_cast<int64_t>(blockIdx.x) + t;
-        topk.flush(a.slots + slot * a.K, a.slot_count + slot);
+        topk.flush(a.slots + slot * a.K, a.slot_count + slot, a.slot_est + slot);
         topk.sync();
     }
 }

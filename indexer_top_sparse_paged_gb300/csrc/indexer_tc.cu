@@ -447,6 +447,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         uint32_t n_it = 0;
         while (it.next(seg)) {
             topk.reset();
+            const int n = row_len(a, seg.row);
+            const bool sampled = seg.tile1 - seg.tile0 >= kEstMinTiles;
             bool ok = true;
             for (int j = seg.tile0; j < seg.tile1; ++j, ++n_it) {
                 const uint32_t slot = n_it % kRing, ruse = n_it / kRing;
@@ -458,10 +460,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 if (lane == 0) mbar_arrive(smem_u32(&S.ring_empty[slot]));
                 const int s = j * kTileKeys + static_cast<int>(row);
                 topk.push(make_key(score, static_cast<uint32_t>(s)), valid);
+                if (sampled && j == seg.tile0 + kEstTiles - 1) {  // the segment's first tiles are the sample
+                    const uint32_t r = estimate_rank(topk.count, n, a.K);
+                    if (r) topk.estimate(r);
+                }
             }
             if (!ok) break;
             const int64_t slot = static_cast<int64_t>(blockIdx.x) + seg.row;
-            topk.flush(a.slots + slot * a.K, a.slot_count + slot);
+            topk.flush(a.slots + slot * a.K, a.slot_count + slot, a.slot_est + slot);
             topk.sync();
         }
     } else if (kFp8 && warp >= 6) {
@@ -508,6 +514,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             if (row < kHeads / 4)
                 reinterpret_cast<float4*>(S.w_s)[row] = reinterpret_cast<const float4*>(a.w + static_cast<int64_t>(t) * kHeads)[row];
             topk.reset();  // a group barrier: the weights are visible
+            const bool sampled = seg.tile1 - seg.tile0 >= kEstMinTiles;
             const float4* wv4 = reinterpret_cast<const float4*>(S.w_s);
             bool ok = true;
             const int32_t* bt = a.block_table + static_cast<int64_t>(row_seq(a, t)) * a.max_blocks;
@@ -565,10 +572,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 // a block whose table entry is invalid was never loaded: its keys do not count
                 const bool valid = s < n && blk_ok;
                 topk.push(make_key(score, static_cast<uint32_t>(s)), valid);
+                if (sampled && j == seg.tile0 + kEstTiles - 1) {  // the segment's first tiles are the sample
+                    const uint32_t r = estimate_rank(topk.count, n, a.K);
+                    if (r) topk.estimate(r);
+                }
             }
             if (!ok) break;
             const int64_t slot = static_cast<int64_t>(blockIdx.x) + t;
-            topk.flush(a.slots + slot * a.K, a.slot_count + slot);
+            topk.flush(a.slots + slot * a.K, a.slot_count + slot, a.slot_est + slot);
             topk.sync();
         }
     }

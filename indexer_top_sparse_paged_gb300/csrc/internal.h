@@ -30,6 +30,7 @@ struct WsLayout {
     size_t merge_count;  // int32 [3][T + G/8 + 1] finished children of the merge tree's groups (levels 2..4)
     size_t slot_count;   // int32 [G + T]
     size_t slots;        // uint64 [G + T][K]
+    size_t slot_est;     // uint64 [G + T] the sample estimate each list was filtered with
     size_t q_mx;         // bf16 [T][H_I][d_I] the MX-quantised q_I (DSA_MXFP8 only)
     size_t idx;          // int32 [T][K] (dsa_decode without a caller idx)
     size_t part_o;       // fp32 [T][S][H][d_v]
@@ -112,6 +113,8 @@ struct AttnArgs {
     int S;
     int* err;
     int after_own_kernel;  // 1: launched right after this library's kernel (dsa_decode) -> PDL
+    int kv_fp8;            // 1: kv holds FP8 records of kv_rec bytes (DSA_KV_FP8)
+    int kv_rec;            // bytes per latent row (record) in the cache
 };
 
 bool launch_attn_simt(const AttnArgs& a, cudaStream_t s, int* launches);
@@ -128,9 +131,10 @@ bool launch_hier_virtualize(int B, int max_blocks, int n_sel, int T, const int32
                             int32_t* vtable, int32_t* vlen, int32_t* blocks_out, cudaStream_t s, int* launches);
 bool launch_hier_remap(int T, int n_sel, int K, const int32_t* bidx, const int32_t* vidx, int32_t* idx, int* fine_err,
                        int* err, cudaStream_t s, int* launches);
-bool launch_cache_append(const dsa_dims& d, const void* k_new, const void* kv_new, const int32_t* block_table,
-                         const int32_t* seq_lens, const int32_t* q_seq, const int32_t* q_pos, int T, void* k_cache,
-                         void* k_scale, void* kv_cache, int* err, cudaStream_t s, int* launches);
+bool launch_cache_append(const dsa_dims& d, bool kv_fp8, const void* k_new, const void* kv_new,
+                         const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
+                         const int32_t* q_pos, int T, void* k_cache, void* k_scale, void* kv_cache, int* err,
+                         cudaStream_t s, int* launches);
 bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches);
 bool launch_wait_timeout(int* err, cudaStream_t s, int* launches);
 

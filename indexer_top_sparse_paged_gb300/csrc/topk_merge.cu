@@ -21,7 +21,10 @@ constexpr int kPlanThreads = 1024;
 constexpr int kMergeThreads = 512;
 constexpr int kMergeSmemKeys = 16384;  // candidates held in registers (32 per thread)
 constexpr int kMergeHistBytes = kMergeThreads / 32 * 256 * 4;  // one 256-bin histogram per warp
-constexpr int kMergeSmemBytes = kMergeHistBytes + kMergeSmemKeys * 8;  // + the row's candidates
+constexpr int kRescoreHeads = 64, kRescoreDim = 128;            // the tensor-core indexer's shape
+constexpr int kRescoreBytes = kRescoreHeads * kRescoreDim * 2 + kRescoreHeads * 4;  // a row's q_I (bf16) and w
+// per-warp histograms + the row's candidates + the recovery path's query and head weights
+constexpr int kMergeSmemBytes = kMergeHistBytes + kMergeSmemKeys * 8 + kRescoreBytes;
 
 // Exclusive scan of v over the block (kPlanThreads threads, in thread order), plus the total.
 __device__ __forceinline__ int plan_scan(int v, int* warp_sums, int& total) {
@@ -126,12 +129,101 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(IndexerArgs a) {
 constexpr int kPer = kMergeSmemKeys / kMergeThreads;  // candidates per thread held in registers
 static_assert(kMergeFanIn * 2048 <= kMergeSmemKeys, "a merge group must fit the registers");
 
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// The exact Top-K of row t, every causal key rescored on the CUDA cores and streamed through an
+// exact selection: the recovery path of a row whose sample estimates turned away keys of its Top-K
+// (TopkGroup::estimate). Only rows of the tensor-core decode indexer take estimates, so the keys
+// are 64 heads x 128 wide, bf16, FP8 e4m3 with a block scale or MXFP8 (q_I then holds the
+// quantised query, as the indexer used it). Writes idx row `out`: ascending positions, then -1.
+__device__ __noinline__ void rescore_row(const IndexerArgs& a, int t, int32_t* out, uint64_t* cand, uint32_t* hist,
+                                         TopkCtl* ctl, uint8_t* scratch, uint32_t tid) {
+    constexpr int H = kRescoreHeads, D = kRescoreDim;
+    uint32_t* q_s = reinterpret_cast<uint32_t*>(scratch);  // [H][D / 2] bf16 pairs
+    float* w_s = reinterpret_cast<float*>(scratch + H * D * 2);
+    const uint32_t* q = static_cast<const uint32_t*>(a.q_I) + static_cast<int64_t>(t) * H * (D / 2);
+    for (uint32_t i = tid; i < H * D / 2; i += kMergeThreads) q_s[i] = q[i];
+    if (tid < static_cast<uint32_t>(H)) w_s[tid] = a.w[static_cast<int64_t>(t) * H + tid];
+    TopkGroup<kMergeThreads, kPer> g{cand, hist, ctl, static_cast<uint32_t>(kMergeSmemKeys), static_cast<uint32_t>(a.K),
+                                     tid, 1};
+    g.reset();  // a group barrier: q_s and w_s are visible
+    const int b = row_seq(a, t);
+    const int n = row_len(a, t);
+    const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
+    for (int base = 0; base < n; base += kMergeThreads) {
+        const int s = base + static_cast<int>(tid);
+        int blk = -1;
+        if (s < n) {
+            blk = bt[s >> 6];
+            if (blk < 0 || blk >= a.num_blocks) {
+                atomicOr(a.err, DSA_FAULT_BLOCK_TABLE);
+                blk = -1;
+            }
+        }
+        float score = 0.0f;
+        if (blk >= 0) {
+            const int64_t row = static_cast<int64_t>(blk) * kBlock + (s & 63);
+            uint32_t kp[D / 2];  // the key as bf16 pairs (exact for every storage)
+            float sc = 1.0f;
+            if (a.mode == DSA_BF16) {
+                const uint4* src = static_cast<const uint4*>(a.k_I) + row * (D * 2 / 16);
+#pragma unroll
+                for (int c = 0; c < D * 2 / 16; ++c) {
+                    const uint4 v = src[c];
+                    kp[4 * c] = v.x;
+                    kp[4 * c + 1] = v.y;
+                    kp[4 * c + 2] = v.z;
+                    kp[4 * c + 3] = v.w;
+                }
+            } else {
+                const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.k_I) + row * D);
+                uint32_t mx = 0;
+                if (a.mode == DSA_MXFP8) mx = *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.k_I_scale) + row * (D / 32));
+                else sc = static_cast<const float*>(a.k_I_scale)[blk];
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                    uint4 lo, hi;
+                    if (a.mode == DSA_MXFP8) e4m3x16_to_bf16_scaled(src[c], e8m0_value((mx >> (8 * (c >> 1))) & 0xFFu), lo, hi);
+                    else e4m3x16_to_bf16(src[c], lo, hi);
+                    kp[8 * c] = lo.x;
+                    kp[8 * c + 1] = lo.y;
+                    kp[8 * c + 2] = lo.z;
+                    kp[8 * c + 3] = lo.w;
+                    kp[8 * c + 4] = hi.x;
+                    kp[8 * c + 5] = hi.y;
+                    kp[8 * c + 6] = hi.z;
+                    kp[8 * c + 7] = hi.w;
+                }
+            }
+#pragma unroll 1
+            for (int j = 0; j < H; ++j) {
+                const uint32_t* qj = q_s + j * (D / 2);
+                float d0 = 0.0f, d1 = 0.0f;
+#pragma unroll
+                for (int i = 0; i < D / 2; ++i) {
+                    const uint32_t qw = qj[i];
+                    d0 = fmaf(bf16_lo(qw), bf16_lo(kp[i]), d0);
+                    d1 = fmaf(bf16_hi(qw), bf16_hi(kp[i]), d1);
+                }
+                score = fmaf(w_s[j], fmaxf((d0 + d1) * sc, 0.0f), score);
+            }
+        }
+        g.push(make_key(score, static_cast<uint32_t>(s)), blk >= 0);
+    }
+    const uint32_t kept = g.select_to(cand);  // the K largest, in position order
+    g.sync();
+    for (uint32_t i = tid; i < static_cast<uint32_t>(a.K); i += kMergeThreads) out[i] = (i < kept) ? key_pos(cand[i]) : -1;
+}
+
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a) {
     extern __shared__ __align__(16) uint8_t merge_smem[];
     uint32_t* hist = reinterpret_cast<uint32_t*>(merge_smem);  // [16 warps][256]
     uint64_t* cand = reinterpret_cast<uint64_t*>(merge_smem + kMergeHistBytes);
+    uint8_t* rescore_scratch = merge_smem + kMergeHistBytes + kMergeSmemKeys * 8;
     __shared__ const uint64_t* span_ptr[kMergeFanIn];
     __shared__ uint32_t span_off[kMergeFanIn + 1];
+    __shared__ unsigned long long group_est;  // the largest sample estimate any of the group's lists used
     __shared__ uint32_t warp_tot[32];
     __shared__ TopkCtl ctl;
     __shared__ int row_found;
@@ -181,6 +273,13 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a
             bool has = lane < static_cast<uint32_t>(kMergeFanIn) && i < nprev;
             if (has && level == 1) has = tile_begin(c + 1, total, G) > tile_begin(c, total, G);
             const uint32_t cnt = has ? static_cast<uint32_t>(__ldcg(a.slot_count + c + t)) : 0u;
+            unsigned long long est = has ? static_cast<unsigned long long>(__ldcg(a.slot_est + c + t)) : 0ull;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, est, o);
+                est = other > est ? other : est;
+            }
+            if (lane == 0) group_est = est;
             const bool keep = cnt > 0;
             const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
             uint32_t x = cnt;  // inclusive scan of the counts
@@ -235,11 +334,26 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a
 #pragma unroll
         for (int j = 0; j < kPer; ++j) keys[j] = (static_cast<uint32_t>(j) < cnt) ? cand[c0 + j] : 0ull;
 
-        // 3. threshold: exactly K keys are >= thr (thr = 0 keeps every candidate when n <= K)
+        // 3. at the row's root, the sample estimates are checked: if at least K candidates are >=
+        //    every estimate used, no key of the row's Top-K was turned away (then the K largest
+        //    candidates are the row's Top-K); otherwise the row is rescored
+        const uint64_t est = group_est;
+        if (ncur == 1 && est != 0ull) {
+            uint32_t above = 0;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) above += (static_cast<uint32_t>(j) < cnt && keys[j] >= est) ? 1u : 0u;
+            uint32_t total_above;
+            group_excl_scan<kMergeThreads>(above, warp_tot, tid, 1, total_above);
+            if (total_above < K) {
+                rescore_row(a, t, out, cand, hist, &ctl, rescore_scratch, tid);
+                return;
+            }
+        }
+        // 4. threshold: exactly K keys are >= thr (thr = 0 keeps every candidate when n <= K)
         uint64_t thr = 0ull;
         if (n > K) thr = reg_radix_threshold<kMergeThreads, kPer>(keys, cnt, K, hist, &ctl, tid, 1);
 
-        // 4. the kept keys in candidate order (= ascending position), compacted in shared memory
+        // 5. the kept keys in candidate order (= ascending position), compacted in shared memory
         //    (over the staged candidates: every thread has its keys in registers) and written out
         //    with coalesced stores: the row's positions at the root, else the keys back over the
         //    group's first list
@@ -261,9 +375,12 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a
         const int64_t cdst = c_first + static_cast<int64_t>(g) * kMergeFanIn * stride;
         uint64_t* dst = a.slots + (cdst + t) * a.K;
         for (uint32_t i = tid; i < kept; i += kMergeThreads) dst[i] = cand[i];
-        if (tid == 0) a.slot_count[cdst + t] = static_cast<int32_t>(kept);
+        if (tid == 0) {
+            a.slot_count[cdst + t] = static_cast<int32_t>(kept);
+            a.slot_est[cdst + t] = est;  // the parent checks the estimates of all the row's lists
+        }
         block_sync();
-        // 5. the last of the parent's children to finish merges the parent's lists
+        // 6. the last of the parent's children to finish merges the parent's lists
         const int parent = g / kMergeFanIn;
         const int64_t left = ncur - static_cast<int64_t>(parent) * kMergeFanIn;
         const int children = left < kMergeFanIn ? static_cast<int>(left) : kMergeFanIn;

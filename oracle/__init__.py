@@ -22,8 +22,13 @@ return NumPy arrays:
   score of their mean key, then the indexer's Top-K over the tokens of the
   shortlisted blocks (Day-0 accelerator page §3.1; adaptation page §3.1).
 * :func:`cache_append` -- the caches after writing new tokens' indexer keys and
-  latent rows into their paged slots (FP8 keys: block requantisation), the step
-  before the path (Ascend adaptation page §2.2, cache-update flow).
+  latent rows into their paged slots (FP8 keys: block requantisation; FP8
+  latent rows: per-row tile quantisation), the step before the path (Ascend
+  adaptation page §2.2, cache-update flow).
+
+A case whose ``spec.kv`` is ``"fp8"`` stores its latent rows as FP8 records
+(Ascend CANN page §3, FP8 block quantisation in the attention stage): per row,
+the e4m3 codes, one fp32 scale per 128-element tile, zero padding to 16 bytes.
 
 Parity pins for every function live in ``tests/test_oracle_pins.py``.
 """
@@ -122,9 +127,17 @@ def mx_quantize32(v) -> tuple:
     return int(X), codes
 
 
+KV_FP8 = 16  # mode flag: latent rows stored as FP8 records (e4m3 codes + one fp32 scale per 128 elements)
+
+
+def kv_fp8(case) -> bool:
+    return getattr(case.spec, "kv", "act") == "fp8"
+
+
 def dims_of(case, K=None) -> ODims:
     s = case.spec
-    return ODims(MODES[s.mode], s.B, case.max_blocks, case.num_blocks, s.block_size, s.H_I, s.d_I, s.H, s.d,
+    mode = MODES[s.mode] | (KV_FP8 if kv_fp8(case) else 0)
+    return ODims(mode, s.B, case.max_blocks, case.num_blocks, s.block_size, s.H_I, s.d_I, s.H, s.d,
                  s.d_v, s.K if K is None else K)
 
 
@@ -196,7 +209,8 @@ def sparse_attn(case, idx, rows=None, sm_scale=None, threads=None):
     lse = np.zeros((T, s.H), dtype=np.float64)
     psum = np.zeros((T, s.H), dtype=np.float64)
     adt = np.float32 if s.mode == "f32" else np.uint16
-    keep = [_c(q, adt), _c(case.kv, adt), _c(case.block_table, np.int32), _c(case.seq_lens, np.int32),
+    kvdt = np.uint8 if kv_fp8(case) else adt
+    keep = [_c(q, adt), _c(case.kv, kvdt), _c(case.block_table, np.int32), _c(case.seq_lens, np.int32),
             _c(q_seq, np.int32)]
     rc = lib.oracle_sparse_attn(ctypes.byref(D), *[_ptr(a) for a in keep], _ptr(idx), idx.shape[1], T,
                                 s.sm_scale if sm_scale is None else float(sm_scale), _ptr(out), _ptr(lse),

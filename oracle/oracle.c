@@ -54,6 +54,15 @@
  * all-zero group; element = RNE_e4m3(v * 2^-X), saturating at +-448; value =
  * element * 2^X).  Attention stays bf16.
  *
+ * FP8 latent cache (flag 16 of mode, with any bf16 mode; "FP8 block quantization
+ * in the attention stage", Ascend CANN page §3: per token and head, independent
+ * blocks of 128 elements): every latent row is stored as one record of d e4m3
+ * codes, then ceil(d/128) fp32 scales (tile j covers elements 128j..128j+127;
+ * the last tile the remaining d mod 128 ones), then zero bytes up to a multiple
+ * of 16 bytes.  Element e of the row is code[e] * scale[e / 128].  Appending a
+ * row quantises each tile on its own, every step in fp32: scale = amax / 448
+ * (1 when amax is 0), code = RNE_e4m3(x / scale), saturating at +-448.
+ *
  * Input decoding:
  *  - bf16: the 16 bits are the top half of an IEEE binary32 (exact widening).
  *  - e4m3 (OCP 8-bit floating point spec, E4M3): sign, 4 exponent bits with
@@ -70,12 +79,28 @@
 #include <string.h>
 
 typedef struct {
-    int32_t mode; /* 0: fp32 everything; 1: bf16 (w fp32); 2: bf16 with e4m3 indexer keys; 3: MXFP8 indexer */
+    int32_t mode; /* 0: fp32 everything; 1: bf16 (w fp32); 2: bf16 with e4m3 indexer keys; 3: MXFP8 indexer;
+                   * + 16: FP8 latent cache (bf16 modes only) */
     int32_t B, max_blocks, num_blocks, block_size;
     int32_t H_I, d_I, H, d, d_v, K;
 } odims;
 
 enum { O_OK = 0, O_BAD_ARG = -1, O_BAD_IDX = -2, O_NOMEM = -3 };
+
+#define OMODE(D) ((D)->mode & 15)          /* storage of activations and indexer keys */
+#define KV_FP8(D) (((D)->mode & 16) != 0)  /* latent rows stored as FP8 records */
+
+/* a valid mode: 0..3, plus the FP8-latent-cache flag on the bf16 modes */
+static int mode_ok(const void* dims) {
+    const int m = *(const int32_t*)dims;
+    if (m & ~31) return 0;
+    if ((m & 15) > 3) return 0;
+    if ((m & 16) && (m & 15) == 0) return 0;
+    return 1;
+}
+
+/* bytes of one FP8 latent record: d codes, one fp32 scale per 128-element tile, padded to 16 */
+static size_t kv_record_bytes(int d) { return ((size_t)d + 4 * (size_t)((d + 127) / 128) + 15) / 16 * 16; }
 
 /* ------------------------------------------------------------------------- */
 /* exact decoders                                                            */
@@ -157,7 +182,16 @@ static double bf16_at(const void* p, size_t i) { return oracle_bf16_to_f64(((con
 
 /* value i of an activation / latent-cache tensor in the mode's storage type */
 static double act_at(const odims* D, const void* p, size_t i) {
-    return D->mode == 0 ? f32_at(p, i) : bf16_at(p, i);
+    return OMODE(D) == 0 ? f32_at(p, i) : bf16_at(p, i);
+}
+
+/* element e of latent row r: the activation type, or code * tile scale of an FP8 record */
+static double kv_at(const odims* D, const void* kv, int64_t r, int e) {
+    if (!KV_FP8(D)) return act_at(D, kv, (size_t)r * D->d + e);
+    const uint8_t* rec = (const uint8_t*)kv + (size_t)r * kv_record_bytes(D->d);
+    float scale;
+    memcpy(&scale, rec + D->d + 4 * (e / 128), sizeof scale);
+    return oracle_e4m3_to_f64(rec[e]) * (double)scale;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -261,7 +295,7 @@ static void score_item(void* vctx, int64_t item, void* scratch) {
             size_t i = ((size_t)t * D->H_I + j) * D->d_I + e;
             q[(size_t)j * D->d_I + e] = act_at(D, C->q_I, i);
         }
-    if (D->mode == 3)  /* the MXFP8 query: every group of 32 quantised and decoded */
+    if (OMODE(D) == 3)  /* the MXFP8 query: every group of 32 quantised and decoded */
         for (int j = 0; j < D->H_I; ++j)
             for (int g = 0; g < D->d_I / 32; ++g)
                 mx_roundtrip32((const uint16_t*)C->q_I + ((size_t)t * D->H_I + j) * D->d_I + 32 * g,
@@ -270,14 +304,14 @@ static void score_item(void* vctx, int64_t item, void* scratch) {
         int32_t blk;
         int64_t row = phys_row(D, C->block_table, b, s, &blk);
         if (row < 0) { C->bad = 1; C->S[C->row_off[t] + s] = NAN; continue; }
-        double scale = (D->mode == 2) ? (double)C->k_I_scale[blk] : 1.0;
+        double scale = (OMODE(D) == 2) ? (double)C->k_I_scale[blk] : 1.0;
         for (int e = 0; e < D->d_I; ++e) {
             size_t i = (size_t)row * D->d_I + e;
             double v;
-            if (D->mode == 0) v = f32_at(C->k_I, i);
-            else if (D->mode == 1) v = bf16_at(C->k_I, i);
+            if (OMODE(D) == 0) v = f32_at(C->k_I, i);
+            else if (OMODE(D) == 1) v = bf16_at(C->k_I, i);
             else v = oracle_e4m3_to_f64(((const uint8_t*)C->k_I)[i]);
-            if (D->mode == 3)  /* E8M0 byte of the key's group of 32 */
+            if (OMODE(D) == 3)  /* E8M0 byte of the key's group of 32 */
                 v = ldexp(v, (int)((const uint8_t*)C->k_I_scale)[(size_t)row * (D->d_I / 32) + e / 32] - 127);
             k[e] = v * scale;
         }
@@ -294,8 +328,8 @@ static void score_item(void* vctx, int64_t item, void* scratch) {
 
 static int check_dims(const odims* D) {
     if (!D || D->block_size <= 0 || D->H_I <= 0 || D->d_I <= 0 || D->K <= 0) return 0;
-    if (D->mode < 0 || D->mode > 3) return 0;
-    if (D->mode == 3 && D->d_I % 32) return 0;
+    if (!mode_ok(D)) return 0;
+    if (OMODE(D) == 3 && D->d_I % 32) return 0;
     return 1;
 }
 
@@ -335,7 +369,7 @@ int oracle_index_scores(const odims* D, const void* q_I, const float* w, const v
                         const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
                         const int32_t* q_pos, int T, int64_t row_stride, double* S, int threads) {
     if (!check_dims(D) || T < 0 || !check_rows(D, seq_lens, q_seq, q_pos, T)) return O_BAD_ARG;
-    if ((D->mode == 2 || D->mode == 3) && !k_I_scale) return O_BAD_ARG;
+    if ((OMODE(D) == 2 || OMODE(D) == 3) && !k_I_scale) return O_BAD_ARG;
     int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T > 0 ? T : 1));
     if (!off) return O_NOMEM;
     for (int t = 0; t < T; ++t) {
@@ -391,7 +425,7 @@ int oracle_indexer_topk(const odims* D, const void* q_I, const float* w, const v
                         const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
                         const int32_t* q_pos, int T, int32_t* idx, double* kth, int threads) {
     if (!check_dims(D) || T < 0 || !check_rows(D, seq_lens, q_seq, q_pos, T)) return O_BAD_ARG;
-    if ((D->mode == 2 || D->mode == 3) && !k_I_scale) return O_BAD_ARG;
+    if ((OMODE(D) == 2 || OMODE(D) == 3) && !k_I_scale) return O_BAD_ARG;
     int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T + 1));
     if (!off) return O_NOMEM;
     off[0] = 0;
@@ -434,7 +468,7 @@ static void attn_row(void* vctx, int64_t t, void* scratch) {
         if (s < 0 || s >= C->seq_lens[b]) { C->bad = 1; return; }
         int64_t r = phys_row(D, C->block_table, b, s, NULL);
         if (r < 0) { C->bad = 1; return; }
-        for (int e = 0; e < D->d; ++e) rows[(size_t)n * D->d + e] = act_at(D, C->kv, (size_t)r * D->d + e);
+        for (int e = 0; e < D->d; ++e) rows[(size_t)n * D->d + e] = kv_at(D, C->kv, r, e);
         ++n;
     }
     for (int h = 0; h < D->H; ++h) {
@@ -472,7 +506,7 @@ int oracle_sparse_attn(const odims* D, const void* q, const void* kv, const int3
                        const int32_t* seq_lens, const int32_t* q_seq, const int32_t* idx, int idx_stride, int T,
                        double sm_scale, double* out, double* lse, double* psum, int threads) {
     if (!D || D->H <= 0 || D->d <= 0 || D->d_v <= 0 || D->d_v > D->d || idx_stride <= 0 || T < 0) return O_BAD_ARG;
-    if (D->mode < 0 || D->mode > 3 || D->block_size <= 0) return O_BAD_ARG;
+    if (!mode_ok(D) || D->block_size <= 0) return O_BAD_ARG;
     for (int t = 0; t < T; ++t)
         if (q_seq[t] < 0 || q_seq[t] >= D->B) return O_BAD_ARG;
     attn_ctx C = {D, q, kv, block_table, seq_lens, q_seq, idx, idx_stride, sm_scale, out, lse, psum, 0};
@@ -501,9 +535,9 @@ int oracle_cache_append(const odims* D, const void* k_new, const void* kv_new, c
                         float* k_scale, void* kv_cache) {
     if (!check_dims(D) || T < 0 || D->block_size > 1024) return O_BAD_ARG;
     const int bs = D->block_size;
-    const size_t act = D->mode == 0 ? 4 : 2;
-    const size_t kb = D->mode == 0 ? 4 : (D->mode == 1 ? 2 : 1);
-    if (D->mode == 3 && D->d_I % 32) return O_BAD_ARG;
+    const size_t act = OMODE(D) == 0 ? 4 : 2;
+    const size_t kb = OMODE(D) == 0 ? 4 : (OMODE(D) == 1 ? 2 : 1);
+    if (OMODE(D) == 3 && D->d_I % 32) return O_BAD_ARG;
     for (int t = 0; t < T; ++t) {  /* validate first */
         int b;
         const int pos = append_pos(seq_lens, q_seq, q_pos, t, &b);
@@ -516,10 +550,28 @@ int oracle_cache_append(const odims* D, const void* k_new, const void* kv_new, c
         int b;
         const int pos = append_pos(seq_lens, q_seq, q_pos, t, &b);
         const int64_t row = (int64_t)block_table[(int64_t)b * D->max_blocks + pos / bs] * bs + pos % bs;
-        memcpy((char*)kv_cache + row * D->d * act, (const char*)kv_new + (int64_t)t * D->d * act, D->d * act);
-        if (D->mode <= 1)
+        if (KV_FP8(D)) {  /* FP8 latent record: each 128-element tile quantised on its own */
+            const size_t rb = kv_record_bytes(D->d);
+            uint8_t* rec = (uint8_t*)kv_cache + (size_t)row * rb;
+            const uint16_t* x = (const uint16_t*)kv_new + (int64_t)t * D->d;
+            memset(rec, 0, rb);
+            for (int j = 0; j < (D->d + 127) / 128; ++j) {
+                const int e0 = 128 * j, e1 = e0 + 128 < D->d ? e0 + 128 : D->d;
+                float amax = 0.0f;
+                for (int e = e0; e < e1; ++e) {
+                    const float v = fabsf((float)oracle_bf16_to_f64(x[e]));
+                    if (v > amax) amax = v;
+                }
+                const float tile_scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+                for (int e = e0; e < e1; ++e) rec[e] = oracle_f32_to_e4m3((float)oracle_bf16_to_f64(x[e]) / tile_scale);
+                memcpy(rec + D->d + 4 * j, &tile_scale, sizeof tile_scale);
+            }
+        } else {
+            memcpy((char*)kv_cache + row * D->d * act, (const char*)kv_new + (int64_t)t * D->d * act, D->d * act);
+        }
+        if (OMODE(D) <= 1)
             memcpy((char*)k_cache + row * D->d_I * kb, (const char*)k_new + (int64_t)t * D->d_I * kb, D->d_I * kb);
-        if (D->mode == 3) {  /* MXFP8 keys: each group of 32 quantised on its own (no block state) */
+        if (OMODE(D) == 3) {  /* MXFP8 keys: each group of 32 quantised on its own (no block state) */
             for (int g = 0; g < D->d_I / 32; ++g) {
                 float v[32];
                 for (int i = 0; i < 32; ++i)
@@ -529,7 +581,7 @@ int oracle_cache_append(const odims* D, const void* k_new, const void* kv_new, c
             }
         }
     }
-    if (D->mode != 2) return O_OK;
+    if (OMODE(D) != 2) return O_OK;
     /* FP8 keys: every block that receives new tokens, once (at its first new token) */
     uint8_t* codes = (uint8_t*)k_cache;
     const uint16_t* knew = (const uint16_t*)k_new;
@@ -620,9 +672,9 @@ int oracle_block_summaries(const odims* D, const void* k_I, const float* k_I_sca
                 for (int i = 0; i < cnt; ++i) {
                     const size_t e = ((size_t)blk * bs + i) * D->d_I + d;
                     float x;
-                    if (D->mode == 0) x = ((const float*)k_I)[e];
-                    else if (D->mode == 1) x = (float)oracle_bf16_to_f64(((const uint16_t*)k_I)[e]);
-                    else if (D->mode == 2) x = (float)oracle_e4m3_to_f64(((const uint8_t*)k_I)[e]) * k_I_scale[blk];
+                    if (OMODE(D) == 0) x = ((const float*)k_I)[e];
+                    else if (OMODE(D) == 1) x = (float)oracle_bf16_to_f64(((const uint16_t*)k_I)[e]);
+                    else if (OMODE(D) == 2) x = (float)oracle_e4m3_to_f64(((const uint8_t*)k_I)[e]) * k_I_scale[blk];
                     else x = ldexpf((float)oracle_e4m3_to_f64(((const uint8_t*)k_I)[e]),
                                     (int)((const uint8_t*)k_I_scale)[((size_t)blk * bs + i) * (D->d_I / 32) + d / 32] - 127);
                     acc = acc + x;

@@ -14,7 +14,8 @@ import torch
 import workloads as W
 
 
-def small_spec(mode: str, lens, K: int, new_tokens=None, H_I=None, d_I=None, H=None, d=None, d_v=None) -> W.Spec:
+def small_spec(mode: str, lens, K: int, new_tokens=None, H_I=None, d_I=None, H=None, d=None, d_v=None,
+               kv: str = "act") -> W.Spec:
     """Small shapes per mode (f32: 4x64 indexer, 8 heads d=128; bf16 modes: the full head counts)."""
     if mode == "f32":
         dims = dict(H_I=4, d_I=64, H=8, d=128, d_v=128)
@@ -25,7 +26,7 @@ def small_spec(mode: str, lens, K: int, new_tokens=None, H_I=None, d_I=None, H=N
             dims[k] = v
     lens = [int(x) for x in lens]
     nt = [1] * len(lens) if new_tokens is None else [int(x) for x in new_tokens]
-    return W.Spec(f"small_{mode}", mode, lens, nt, K=K, **dims)
+    return W.Spec(f"small_{mode}", mode, lens, nt, K=K, kv=kv, **dims)
 
 
 # ----------------------------------------------------------------------------
@@ -81,7 +82,18 @@ def logical_keys(case, b: int, n=None) -> np.ndarray:
     return act(case, logical_rows(case, b, case.k_I, None, n))
 
 
+def kv_fp8_decode(recs, d: int) -> np.ndarray:
+    """FP8 latent records -> row values in fp64: torch's e4m3 cast of the codes times the fp32 scale
+    of each element's 128-wide tile (the scales follow the d codes)."""
+    recs = np.ascontiguousarray(recs, dtype=np.uint8)
+    nt = (d + 127) // 128
+    sc = np.ascontiguousarray(recs[..., d: d + 4 * nt]).view(np.float32).astype(np.float64)
+    return np_e4m3(recs[..., :d]) * np.repeat(sc, 128, axis=-1)[..., :d]
+
+
 def logical_kv(case, b: int, n=None) -> np.ndarray:
+    if getattr(case.spec, "kv", "act") == "fp8":
+        return kv_fp8_decode(logical_rows(case, b, case.kv, None, n), case.spec.d)
     return act(case, logical_rows(case, b, case.kv, None, n))
 
 

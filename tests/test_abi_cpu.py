@@ -175,6 +175,7 @@ def _noalloc_prefix_bytes(T: int, K: int, G: int, mx: bool = False, H_I: int = 6
     off = a256(off + 4 * 3 * (T + (G + 7) // 8 + 1))  # merge-tree counters
     off = a256(off + 4 * (G + T))                    # candidate counts
     off = a256(off + 8 * (G + T) * K)                # candidate lists
+    off = a256(off + 8 * (G + T))                    # the sample estimate of each list
     if mx:
         off = a256(off + 2 * T * H_I * d_I)          # the MX-quantised query (bf16)
     return off
@@ -203,3 +204,20 @@ def test_noalloc_row_limit_is_the_documented_one(L):
             assert st == want, (mode, K, T, st)
     documented = re.search(r"K = 2048: T <= (\d+)[\s*]+rows", open(HEADER).read())
     assert documented and int(documented.group(1)) == _noalloc_rows_limit(2048, 152)
+
+
+def test_fp8_latent_flag_checks(L):
+    """DSA_KV_FP8 goes with the bf16 modes and rows of a multiple of 16 elements; the workspace does
+    not depend on it; other bits of the mode are rejected."""
+    fp8 = _dims(mode="bf16", kv="fp8")
+    assert fp8.mode == 1 | 0x10
+    assert L.dsa_workspace_size(ctypes.byref(fp8), 2) == L.dsa_workspace_size(ctypes.byref(_dims()), 2)
+    assert L.dsa_workspace_size(ctypes.byref(_dims(mode="f32", H_I=4, d_I=64, H=8, d=128, d_v=128, kv="fp8")), 2) == 0
+    assert L.dsa_workspace_size(ctypes.byref(_dims(d=584, kv="fp8")), 2) == 0          # 584 % 16 != 0
+    bad = _dims()
+    bad.mode = 1 | 0x20
+    assert L.dsa_workspace_size(ctypes.byref(bad), 2) == 0
+    st = L.dsa_sparse_attn(ctypes.byref(_dims(mode="f32", H_I=4, d_I=64, H=8, d=128, d_v=128, kv="fp8")), FAKE, FAKE,
+                           FAKE, FAKE, FAKE, FAKE, 2, ctypes.c_float(0.04), FAKE, None, FAKE, 1 << 30, None)
+    assert st == 2
+    assert dsa.kv_record_bytes(576) == 608 and dsa.kv_record_bytes(128) == 144 and dsa.kv_record_bytes(80) == 96

@@ -33,7 +33,7 @@ def _new_tokens(case, seed):
 
 def _gpu_append(case, k_new, kv_new, explicit_rows=True):
     s = case.spec
-    dims = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K)
+    dims = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K, kv=s.kv)
     k_I, kv = _t(case.k_I), _t(case.kv)
     scale = _t(case.k_I_scale) if case.k_I_scale is not None else None
     ws = dsa.workspace(dims, 1)
@@ -86,3 +86,14 @@ def test_append_fp8_mixed_chunk():
     spec = small_spec("bf16_kfp8", [1024, 3000, 9000, 16384], 64, new_tokens=[1, 1, 1, 2048])
     case = W.generate(spec, seed=206)
     _check(case, 207)
+
+
+@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8"])
+def test_append_fp8_latent_records(mode):
+    """FP8 latent cache: every new row becomes one record (each 128-element tile quantised on its
+    own, the scales after the codes, zero padding), byte for byte as the oracle writes it; decode
+    appends and a chunk that crosses blocks, at the tensor-core row width (576) and a small one."""
+    spec = small_spec(mode, [300, 1000, 77, 4096], 64, new_tokens=[150, 1, 13, 200], kv="fp8")
+    _check(W.generate(spec, seed=208), 209)
+    spec = small_spec(mode, [1, 64, 65, 700], 64, H=4, d=80, d_v=48, kv="fp8")
+    _check(W.generate(spec, seed=210), 211, explicit_rows=False)

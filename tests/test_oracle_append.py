@@ -140,3 +140,24 @@ def test_append_mx_quantises_each_new_key_on_its_own():
             if (blk, off) not in touched:
                 assert np.array_equal(k_I[blk, off], case.k_I[blk, off])
                 assert np.array_equal(scale[blk, off], case.k_I_scale[blk, off])
+
+
+def test_append_fp8_latent_rows_match_the_generators_quantisation():
+    """FP8 latent records: each new row's 128-element tiles quantised on their own (the generator's
+    NumPy/torch recipe applied to the bf16 row), bit for bit; no other record changes."""
+    spec = small_spec("bf16", [130, 64, 7], 64, new_tokens=[70, 1, 7], H_I=4, d_I=16, H=4, d=192, d_v=160,
+                      kv="fp8")
+    case = W.generate(spec, seed=37)
+    k_new, kv_new = _new_tokens(case, 38)
+    k_I, _, kv = oracle.cache_append(case, k_new, kv_new)
+    recs = W.to_kv_fp8_records(np_bf16(kv_new).astype(np.float32))
+    touched = set()
+    for t in range(spec.T):
+        blk, off = _slot(case, t)
+        assert np.array_equal(kv[blk, off], recs[t])
+        assert np.array_equal(k_I[blk, off], k_new[t])
+        touched.add((blk, off))
+    for blk in range(case.num_blocks):
+        for off in range(64):
+            if (blk, off) not in touched:
+                assert np.array_equal(kv[blk, off], case.kv[blk, off])

@@ -24,7 +24,7 @@ MUTANTS = {
     "transposed_query": ("dot += q[(size_t)j * D->d_I + e] * k[e];", "dot += q[(size_t)e * D->H_I + j] * k[e];"),
     "e4m3_bias_8": ("else v = ldexp(1.0 + (double)m / 8.0, e - 7);", "else v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
     "e4m3_no_subnormal": ("if (e == 0) v = ldexp((double)m, -9);", "if (e == 0) v = ldexp(1.0 + (double)m / 8.0, -7);"),
-    "no_block_scale": ("double scale = (D->mode == 2) ? (double)C->k_I_scale[blk] : 1.0;", "double scale = 1.0;"),
+    "no_block_scale": ("double scale = (OMODE(D) == 2) ? (double)C->k_I_scale[blk] : 1.0;", "double scale = 1.0;"),
     "not_causal_inclusive": ("if (s1 > pos + 1) s1 = pos + 1;", "if (s1 > pos) s1 = pos;"),
     "drop_sm_scale": ("z[i] = C->sm_scale * dot;", "z[i] = dot;"),
     "value_width_d_v": ("o[c] += p * rows[(size_t)i * D->d + c];", "o[c] += p * rows[(size_t)i * D->d_v + c];"),
@@ -42,12 +42,19 @@ MUTANTS = {
     "append_keeps_old_scale": ("const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;", "const float scale = old_scale;"),
     "append_wrong_slot": ("const int64_t row = (int64_t)block_table[(int64_t)b * D->max_blocks + pos / bs] * bs + pos % bs;",
                           "const int64_t row = (int64_t)block_table[(int64_t)b * D->max_blocks + pos / bs] * bs + (pos + 1) % bs;"),
-    "mx_query_not_quantised": ("    if (D->mode == 3)  /* the MXFP8 query", "    if (0)  /* the MXFP8 query"),
+    "mx_query_not_quantised": ("    if (OMODE(D) == 3)  /* the MXFP8 query", "    if (0)  /* the MXFP8 query"),
     "mx_scale_bias_126": ("e / 32] - 127);\n            k[e]", "e / 32] - 126);\n            k[e]"),
     "mx_first_group_scale_only": ("[(size_t)row * (D->d_I / 32) + e / 32] - 127);", "[(size_t)row * (D->d_I / 32)] - 127);"),
     "mx_exponent_is_ceil": ("X = (e - 1) - 8;", "X = e - 8;"),
     "mx_summary_first_group_scale": ("* (D->d_I / 32) + d / 32] - 127);", "* (D->d_I / 32)] - 127);"),
     "mx_append_quantises_group_0_everywhere": ("[(int64_t)t * D->d_I + 32 * g + i]);", "[(int64_t)t * D->d_I + i]);"),
+    "kv_fp8_tile_of_64": ("memcpy(&scale, rec + D->d + 4 * (e / 128), sizeof scale);",
+                          "memcpy(&scale, rec + D->d + 4 * ((e / 64) % ((D->d + 127) / 128)), sizeof scale);"),
+    "kv_fp8_ignores_scale": ("return oracle_e4m3_to_f64(rec[e]) * (double)scale;", "return oracle_e4m3_to_f64(rec[e]);"),
+    "kv_fp8_append_first_tile_amax": ("for (int e = e0; e < e1; ++e) {\n                    const float v = fabsf(",
+                                      "for (int e = 0; e < (D->d < 128 ? D->d : 128); ++e) {\n                    const float v = fabsf("),
+    "kv_fp8_append_scale_slot": ("memcpy(rec + D->d + 4 * j, &tile_scale, sizeof tile_scale);",
+                                 "memcpy(rec + D->d, &tile_scale, sizeof tile_scale);"),
     "mx_append_wrong_scale_row": ("((uint8_t*)k_scale)[row * (D->d_I / 32) + g] = (uint8_t)(X + 127);",
                                   "((uint8_t*)k_scale)[(row ^ 1) * (D->d_I / 32) + g] = (uint8_t)(X + 127);"),
 }
@@ -72,6 +79,10 @@ PIN_TESTS = [
     pins.test_mx_scores_equal_bf16_scores_of_the_decoded_values,
     app.test_append_mx_quantises_each_new_key_on_its_own,
     hier.test_planted_block_is_chosen,
+    pins.test_kv_fp8_attention_matches_brute_force,
+    pins.test_kv_fp8_single_row_is_its_decoded_values,
+    pins.test_kv_fp8_power_of_two_tile_scales_change_nothing,
+    app.test_append_fp8_latent_rows_match_the_generators_quantisation,
 ]
 
 

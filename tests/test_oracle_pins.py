@@ -405,3 +405,81 @@ def test_mx_scores_equal_bf16_scores_of_the_decoded_values():
     # and the query really was quantised: scores with the unquantised query differ
     bf.q_I = mx.q_I.copy()
     assert not np.array_equal(oracle.index_scores(bf), S_mx, equal_nan=True)
+
+
+# ------------------------------------------------------------------ FP8 latent cache (attention stage)
+# "FP8 block quantization in the attention stage" (Ascend CANN page §3): per token and head,
+# independent blocks of 128 elements. A latent row is one record: d e4m3 codes, one fp32 scale per
+# 128-element tile (the last tile holds the remaining d mod 128 elements), zero padding to 16 bytes.
+
+def _kv_fp8_case(lens, K, seed, d=192, d_v=160, H=4):
+    spec = small_spec("bf16", lens, K, H_I=4, d_I=16, H=H, d=d, d_v=d_v, kv="fp8")
+    return W.generate(spec, seed=seed)
+
+
+def test_kv_fp8_record_layout():
+    """The generator's records decode to the bf16 draw within e4m3 rounding, and each tile's largest
+    magnitude is stored as code 448 (scale = amax / 448)."""
+    case = _kv_fp8_case([130], 32, seed=60)
+    d = case.spec.d
+    assert case.kv.shape[-1] == W.kv_record_bytes(d) == 208   # 192 codes + 2 scales + 8 zero bytes
+    rec = case.kv[case.block_table[0, 0], 5]
+    assert np.all(rec[d + 8:] == 0)
+    vals = logical_kv(case, 0)[5]
+    for j, (e0, e1) in enumerate(((0, 128), (128, 192))):
+        assert np.max(np.abs(np_e4m3(rec[e0:e1]))) == 448.0
+        sc = float(rec[d + 4 * j: d + 4 * j + 4].view(np.float32)[0])
+        np.testing.assert_allclose(vals[e0:e1], np_e4m3(rec[e0:e1]) * sc, rtol=0, atol=0)
+
+
+def test_kv_fp8_attention_matches_brute_force():
+    """Oracle attention over FP8 records against NumPy on rows decoded with torch's e4m3 cast and the
+    tile scales (a second tile of 64 elements exercises the partial last tile)."""
+    case = _kv_fp8_case([5, 200, 700], 64, seed=61)
+    idx, _ = oracle.indexer_topk(case)
+    out, lse, psum = oracle.sparse_attn(case, idx)
+    for t in range(case.spec.T):
+        ref, ref_lse = brute_attn_row(case, t, idx[t])
+        np.testing.assert_allclose(out[t], ref, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse[t], ref_lse, rtol=1e-12)
+    np.testing.assert_allclose(psum, 1.0, atol=1e-12)
+
+
+def test_kv_fp8_single_row_is_its_decoded_values():
+    case = _kv_fp8_case([90], 16, seed=62)
+    idx = np.full((1, 16), -1, np.int32)
+    idx[0, 0] = 37
+    out, _, _ = oracle.sparse_attn(case, idx)
+    row = logical_kv(case, 0)[37, : case.spec.d_v]
+    assert np.array_equal(out[0], np.broadcast_to(row, out[0].shape))
+
+
+def test_kv_fp8_power_of_two_tile_scales_change_nothing():
+    """Halving every code of a tile and doubling its scale leaves every element's value, hence the
+    attention, bit-identical (codes whose halving is not exact are zeroed in both copies first);
+    doubling one tile's scale alone changes the output."""
+    case = _kv_fp8_case([300], 64, seed=63)
+    d, nt = case.spec.d, 2
+    codes = case.kv[..., :d].copy()
+    v = np_e4m3(codes)
+    exact_half = (np.abs(v) >= 2.0 ** -5) | (v == 0)              # exponent field >= 2: halving is exact
+    codes[~exact_half] = 0
+    a = case.kv.copy()
+    a[..., :d] = codes
+    b = a.copy()
+    b[..., :d] = W.to_e4m3_codes((np_e4m3(codes) / 2).astype(np.float32))
+    sc = np.ascontiguousarray(a[..., d: d + 4 * nt]).view(np.float32) * np.float32(2.0)
+    b[..., d: d + 4 * nt] = sc.view(np.uint8).reshape(b[..., d: d + 4 * nt].shape)
+    assert np.array_equal(np_e4m3(b[..., :d]) * 2, np_e4m3(a[..., :d]))
+    idx, _ = oracle.indexer_topk(case)
+    case.kv = a
+    out_a, lse_a, _ = oracle.sparse_attn(case, idx)
+    case.kv = b
+    out_b, lse_b, _ = oracle.sparse_attn(case, idx)
+    assert np.array_equal(out_a, out_b) and np.array_equal(lse_a, lse_b)
+    c = a.copy()
+    sc1 = np.ascontiguousarray(c[..., d + 4: d + 8]).view(np.float32) * np.float32(2.0)
+    c[..., d + 4: d + 8] = sc1.view(np.uint8).reshape(c[..., d + 4: d + 8].shape)   # tile 1 only
+    case.kv = c
+    out_c, _, _ = oracle.sparse_attn(case, idx)
+    assert not np.array_equal(out_c, out_a)

@@ -62,6 +62,7 @@ class Spec:
     block_size: int = BLOCK
     spare_blocks: int = 3
     meta: dict = field(default_factory=dict)
+    kv: str = "act"  # latent rows: "act" (the mode's activation type) | "fp8" (FP8 records, bf16 modes)
 
     @property
     def B(self) -> int:
@@ -136,6 +137,43 @@ def to_e4m3_codes(x: np.ndarray) -> np.ndarray:
     x = np.clip(np.asarray(x, dtype=np.float32), -448.0, 448.0)
     t = torch.from_numpy(np.ascontiguousarray(x)).to(torch.float8_e4m3fn)
     return t.view(torch.uint8).numpy()
+
+
+def kv_record_bytes(d: int) -> int:
+    """Bytes of one FP8 latent record: d e4m3 codes, one fp32 scale per 128 elements, padded to 16."""
+    return (d + 4 * ((d + 127) // 128) + 15) // 16 * 16
+
+
+def to_kv_fp8_records(x: np.ndarray) -> np.ndarray:
+    """fp32 rows ``[..., d]`` -> FP8 latent records ``[..., kv_record_bytes(d)]`` (uint8).
+
+    Each tile of 128 consecutive elements (the last one the remaining d mod 128) is quantised on its
+    own, in fp32: ``scale = amax / 448`` (1 when amax is 0), codes ``RNE_e4m3(x / scale)``
+    saturating at 448. A record holds the d codes, then the fp32 scales, then zero bytes.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    d = x.shape[-1]
+    nt = (d + 127) // 128
+    out = np.zeros(x.shape[:-1] + (kv_record_bytes(d),), dtype=np.uint8)
+    scales = np.empty(x.shape[:-1] + (nt,), dtype=np.float32)
+    for j in range(nt):
+        tile = x[..., 128 * j: min(d, 128 * j + 128)]
+        amax = np.abs(tile).max(axis=-1)
+        sc = (amax / np.float32(448.0)).astype(np.float32)
+        sc[sc == 0] = 1.0
+        scales[..., j] = sc
+        out[..., 128 * j: 128 * j + tile.shape[-1]] = to_e4m3_codes(tile / sc[..., None])
+    out[..., d: d + 4 * nt] = scales.view(np.uint8).reshape(x.shape[:-1] + (4 * nt,))
+    return out
+
+
+def kv_fp8_poison(d: int) -> np.ndarray:
+    """The record of an empty slot: every code 448 (0x7E), every scale 1."""
+    rec = np.zeros(kv_record_bytes(d), dtype=np.uint8)
+    rec[:d] = POISON_E4M3
+    nt = (d + 127) // 128
+    rec[d: d + 4 * nt] = np.ones(nt, np.float32).view(np.uint8)
+    return rec
 
 
 def to_mx_e4m3(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
@@ -228,7 +266,9 @@ def generate(spec: Spec, seed: int, chunk_blocks: int = 1024) -> Case:
     kdt = np.float32 if spec.mode == "f32" else (np.uint8 if fp8 or mx else np.uint16)
     vdt = np.float32 if spec.mode == "f32" else np.uint16
     k_I = np.empty((NB, bs, spec.d_I), dtype=kdt)
-    kv = np.empty((NB, bs, spec.d), dtype=vdt)
+    kv_fp8 = spec.kv == "fp8"
+    assert spec.kv in ("act", "fp8") and not (kv_fp8 and spec.mode == "f32")
+    kv = np.empty((NB, bs, kv_record_bytes(spec.d)), dtype=np.uint8) if kv_fp8 else np.empty((NB, bs, spec.d), dtype=vdt)
     scale = np.ones(NB, dtype=np.float32) if fp8 else None
     if mx:
         scale = np.full((NB, bs, spec.d_I // 32), 127, dtype=np.uint8)
@@ -249,11 +289,13 @@ def generate(spec: Spec, seed: int, chunk_blocks: int = 1024) -> Case:
             k_I[dst], scale[dst] = to_mx_e4m3(bf16_bits_to_f32(to_bf16_bits(kx)))
         else:
             k_I[dst] = _store(kx, spec.mode)
-        kv[dst] = _store(_normal(rng, (c1 - c0, bs, spec.d)), spec.mode)
+        vx = _normal(rng, (c1 - c0, bs, spec.d))
+        # FP8 latent rows: quantised from their bf16 values (what a cache append receives)
+        kv[dst] = to_kv_fp8_records(bf16_bits_to_f32(to_bf16_bits(vx))) if kv_fp8 else _store(vx, spec.mode)
 
     # poison: spare blocks and the tail slots of each sequence's last block
     kpois = np.uint8(POISON_E4M3) if fp8 or mx else _poison_value(spec.mode)
-    vpois = _poison_value(spec.mode)
+    vpois = kv_fp8_poison(spec.d) if kv_fp8 else _poison_value(spec.mode)
     spare = perm[n_logical:]
     k_I[spare] = kpois
     kv[spare] = vpois
@@ -298,6 +340,25 @@ def with_key_format(case: Case, mode: str) -> Case:
         codes = to_e4m3_codes(x / scale[:, None, None])
     codes[~valid] = POISON_E4M3
     return dataclasses.replace(case, spec=dataclasses.replace(case.spec, mode=mode), k_I=codes, k_I_scale=scale)
+
+
+def with_kv_format(case: Case, kv: str) -> Case:
+    """The same case with its bf16 latent rows re-stored as FP8 records (``kv="fp8"``): every tile of
+    128 elements of a row quantised on its own (``to_kv_fp8_records``); slots that hold no token get
+    the poison record. Every other input is shared with ``case``."""
+    import dataclasses
+    assert case.spec.mode != "f32" and case.spec.kv == "act" and kv == "fp8"
+    bs = case.spec.block_size
+    recs = to_kv_fp8_records(bf16_bits_to_f32(case.kv))
+    valid = np.zeros(case.kv.shape[:2], dtype=bool)
+    for b, L in enumerate(case.seq_lens.tolist()):
+        nblk = (L + bs - 1) // bs
+        blks = case.block_table[b, :nblk]
+        valid[blks] = True
+        if L % bs:
+            valid[blks[-1], L % bs:] = False
+    recs[~valid] = kv_fp8_poison(case.spec.d)
+    return dataclasses.replace(case, spec=dataclasses.replace(case.spec, kv=kv), kv=recs)
 
 
 def repage(case: Case, seed: int) -> Case:
