@@ -20,10 +20,10 @@
 //   5. accumulates O_r[128 x 256] += P . V_r with V_r = its 256 value columns (CTA 0: values
 //      0..255, CTA 1: values 256..511 -- both inside the columns it already holds).
 // With an FP8 latent cache (records of e4m3 codes with one fp32 scale per 128 elements; §3: FP8
-// block quantisation in the attention stage) step 1 gathers the codes of the CTA's columns into a
-// staging ring (cp.async, 16 codes per copy) and the same producer threads widen them into the bf16
-// operand stage, code * tile scale in fp32 rounded to bf16: the gathered bytes halve, the tensor-core
-// work is unchanged.
+// block quantisation in the attention stage) step 1 gathers the codes of the CTA's columns into the
+// upper half of the operand stage (cp.async, 16 codes per copy) and converter warps widen them in
+// place into bf16, code * tile scale in fp32 rounded to nearest even: the gathered bytes halve, the
+// tensor-core work is unchanged.
 // Split-K partials (m, l, O) are merged by attn_combine_kernel. Tensor memory holds the O
 // accumulator (256 fp32 columns), two S/P buffers and all but the first 64 query columns of the
 // CTA (A operand from TMEM); shared memory holds the first query chunk, four row stages, two
@@ -33,7 +33,9 @@
 // (thread = head = TMEM lane; group 0 takes rows 0..31 of every tile and O columns 0..127, group 1
 // rows 32..63 and O columns 128..255), warps 4-7 producers (gather rows; send the partial logits
 // of their TMEM lane quarter), warp 8 TMEM allocator + MMA issuer (+ the TMA loads of the query),
-// warp 9 prefetches the CTA's columns of every selected row into L2 at the start.
+// warp 9 prefetches the CTA's columns of every selected row into L2 at the start. With FP8
+// records (512 threads = 16 warps) the second softmax group is warps 9-12, warps 13-15 stage and
+// widen the codes, and the producers prefetch and then only send the partial logits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -47,19 +49,21 @@ constexpr int kD = 576;
 constexpr int kDV = 512;
 constexpr int kDVH = 256;                     // value columns per CTA
 constexpr int kRows = 64;                     // gathered rows per tile
-constexpr int kStagesMax = 4;                 // bf16 operand stages (3 with an FP8 latent cache)
+constexpr int kStagesMax = 4;                 // bf16 operand stages
 constexpr int kChunkBytes = kRows * 128;      // [64 rows x 64 bf16]
 constexpr int kQChunkBytes = kHeads * 128;    // [128 heads x 64 bf16]
 constexpr int kMaxChunks = 5;                 // row chunks per CTA (CTA 0: 4, CTA 1: 5)
 constexpr int kStageBytes = kMaxChunks * kChunkBytes;
 constexpr int kRecBytes = DSA_KV_FP8_RECORD_BYTES(kD);  // an FP8 latent record: 576 codes + 5 scales + pad
-constexpr int kCodeStages = 2;                          // FP8 code staging ring
-constexpr int kCodeStageBytes = kRows * kMaxChunks * 64;  // 64 rows x up to 320 codes = 20 KB
+constexpr int kCodeBytes = kRows * kMaxChunks * 64;     // FP8 codes of a tile: 64 rows x up to 320 = 20 KB
+constexpr int kCodeOff = kStageBytes - kCodeBytes;      // ... staged in the upper half of their operand stage
 constexpr int kXBytes = kHeads * kRows * 2;   // one partial-logit tile (fp16, prescaled by 2^-8)
 constexpr float kXScale = 1.0f / 256.0f;      // partial logits travel as fp16(S_r * 2^-8)
 constexpr int kMaxRows = 2048;
-constexpr int kThreads = 448;
-constexpr int kWarpSoftB = 10;  // second softmax group: warps 10..13
+constexpr int kThreads = 448;   // bf16 latent rows: 14 warps
+constexpr int kThreads8 = 512;  // FP8 records: 16 warps (the register file holds no more at 128 a thread)
+constexpr int kWarpConv = 13;   // FP8 converters: warps 13..15
+constexpr int kConvThreads = 96;
 constexpr int kProducers = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // S/P buffers at 256 and 320; Q chunks 32 apart
@@ -76,15 +80,14 @@ struct Smem {
     int abort_flag;
 };
 
-// Shared memory of one CTA: bf16 latent rows use four operand stages, FP8 records three plus the
-// code staging ring.
+// Shared memory of one CTA (the same for bf16 rows and FP8 records, whose codes are staged inside
+// their own operand stage).
 template <bool kKv8>
 struct Layout {
-    static constexpr int kStages = kKv8 ? 3 : 4;
+    static constexpr int kStages = 4;
     static constexpr size_t kOffQ = 0;
     static constexpr size_t kOffKv = kOffQ + kQChunkBytes;
-    static constexpr size_t kOffCode = kOffKv + static_cast<size_t>(kStages) * kStageBytes;  // FP8 codes
-    static constexpr size_t kOffX = kOffCode + (kKv8 ? static_cast<size_t>(kCodeStages) * kCodeStageBytes : 0);
+    static constexpr size_t kOffX = kOffKv + static_cast<size_t>(kStages) * kStageBytes;
     static constexpr size_t kOffValid = kOffX + 2 * kXBytes;                // 1 bit per selected row
     static constexpr size_t kOffPhys = kOffValid + kMaxRows / 8;            // physical row per selected row
     static constexpr size_t kOffRed = kOffPhys + kMaxRows * sizeof(int32_t);  // softmax maxima / row sums
@@ -93,7 +96,7 @@ struct Layout {
 };
 static_assert(Layout<false>::kSmemBytes <= 232448, "attention shared memory over the limit");
 static_assert(Layout<true>::kSmemBytes <= 232448, "FP8 attention shared memory over the limit");
-static_assert(4 * kQChunkBytes <= Layout<true>::kStages * kStageBytes, "query chunks are staged in the row stages");
+static_assert(kCodeBytes <= kStageBytes / 2, "FP8 codes fit the upper half of their stage");
 
 __host__ __device__ inline int split_rows(int K, int S) {
     const int per = (K + S - 1) / S;
@@ -113,8 +116,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 template <bool kKv8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKv8 ? kThreads8 : kThreads)
     attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap map_q) {
+    constexpr int kNT = kKv8 ? kThreads8 : kThreads;
+    constexpr int kWarpSoftB = kKv8 ? 9 : 10;  // second softmax group: warps 10..13 (FP8 records: 9..12)
     using Lay = Layout<kKv8>;
     constexpr int kStages = Lay::kStages;
     constexpr size_t kOffQ = Lay::kOffQ, kOffKv = Lay::kOffKv, kOffX = Lay::kOffX, kOffValid = Lay::kOffValid;
@@ -149,7 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(smem_u32(&S.full[i]), kProducers * 32);  // every producer thread's cp.async
+            mbar_init(smem_u32(&S.full[i]), kKv8 ? kConvThreads : kProducers * 32);  // every filling thread arrives
             mbar_init(smem_u32(&S.empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -191,11 +196,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
     // whose fault CTA 0 records) plus a validity bit per row for the softmax; all index loads are
     // issued before the dependent block-table loads
     {
-        constexpr int kPerThread = (kMaxRows + kThreads - 1) / kThreads;
+        constexpr int kPerThread = (kMaxRows + kNT - 1) / kNT;
         int sv[kPerThread];
 #pragma unroll
         for (int q = 0; q < kPerThread; ++q) {
-            const int i = (q * (kThreads / 32) + warp) * 32 + lane;
+            const int i = (q * (kNT / 32) + warp) * 32 + lane;
             sv[q] = (i < nrows) ? idx_row[i] : -1;
         }
         int blk[kPerThread];
@@ -204,7 +209,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             blk[q] = (sv[q] >= 0 && sv[q] < L && (sv[q] >> 6) < a.max_blocks) ? bt_row[sv[q] >> 6] : -1;
 #pragma unroll
         for (int q = 0; q < kPerThread; ++q) {
-            const int w0 = (q * (kThreads / 32) + warp) * 32;
+            const int w0 = (q * (kNT / 32) + warp) * 32;
             if (w0 >= ntiles * kRows) break;  // warp-uniform
             const int i = w0 + lane;
             int32_t p = -1;
@@ -247,6 +252,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
     block_sync();
     tc_fence_after();
 
+    // L2 prefetch of every valid selected row's columns of this CTA (4 or 5 lines of 128 B; FP8: the
+    // record's codes of these columns and its scales), requested up front so that the gathers find
+    // them in L2; thread i of n takes rows i, i + n, ...
+    auto prefetch_rows = [&](int i0, int n) {
+        for (int row = i0; row < nrows; row += n) {
+            const int p = phys_s[row];
+            if (p < 0) continue;
+            if constexpr (!kKv8) {
+                const uint8_t* rp = static_cast<const uint8_t*>(a.kv) + c0 * 128 + static_cast<int64_t>(p) * (kD * 2);
+                for (int c = 0; c < nchunks; ++c) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + c * 128));
+            } else {
+                const uint8_t* rp = static_cast<const uint8_t*>(a.kv) + static_cast<int64_t>(p) * kRecBytes;
+                const int lo = c0 * 64, hi = lo + nchunks * 64;
+                for (int o = lo; o < hi; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + o));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + hi - 1));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + kD));
+            }
+        }
+    };
     if (warp >= 4 && warp < 4 + kProducers) {
         // ------------------------------------------------------------- producers: gather + send
         // Producer warp pw (TMEM lane quarter pw) alternates two jobs, in an order that matches the
@@ -259,10 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         //             cache rows were resolved up front) with 16-byte cp.async per lane (lane = chunk
         //             lane / 8, 16-byte group lane % 8; CTA 1's fifth chunk from lanes 0..7) into the
         //             128-byte-swizzled layout; rows with no position read as zeros.
-        //  FP8 records instead: issue(t) copies the tile's codes (16 per cp.async, groups spread
-        //             over the 128 producer threads) into code stage t % 2, and convert(t), once bf16
-        //             stage t % 3 is free, widens the codes the same thread copied, times their tile
-        //             scale, into it.
+        //  With FP8 records the producers only send: four converter warps fill the stages.
         const int pw = warp - 4;
         const int h = pw * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(pw * 32) << 16;
@@ -325,102 +346,93 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                 ok = send(j);
                 if (ok && j + kStages - 1 < ntiles) ok = gather(j + kStages - 1);
             }
-        } else {
-            constexpr int kPT = kProducers * 32;                    // producer threads
-            constexpr int kGPT = kCodeStageBytes / 16 / kPT;        // 16-code groups per thread and tile (<= 10)
-            const int gpr = nchunks * 4;                            // groups per row of this CTA: 16 or 20
-            const int ngroups = kRows * gpr;
-            const int pt = pw * 32 + lane;
-            const uint8_t* kvb = static_cast<const uint8_t*>(a.kv);
-            const uint32_t sCode = smem_u32(smem + Lay::kOffCode);
-            int issued = 0;
-            auto issue = [&](int tile) {
-                const uint32_t base = sCode + (tile % kCodeStages) * kCodeStageBytes;
-#pragma unroll
-                for (int k = 0; k < kGPT; ++k) {
-                    const int gi = pt + k * kPT;
-                    if (gi < ngroups) {
-                        const int r = gi / gpr, q = gi - r * gpr;
-                        const int p = phys_s[tile * kRows + r];
-                        const uint8_t* src = p >= 0 ? kvb + static_cast<int64_t>(p) * kRecBytes + c0 * 64 + q * 16 : kvb;
-                        cp_async16(base + gi * 16, src, p >= 0 ? 16u : 0u);  // 0: zero-fill
-                    }
-                }
-                cp_async_commit();
-                ++issued;
-            };
-            auto convert = [&](int tile) -> bool {
-                const int st = tile % kStages;
-                float sc[kGPT];
-#pragma unroll
-                for (int k = 0; k < kGPT; ++k) {  // the scales first: their loads overlap the waits
-                    const int gi = pt + k * kPT;
-                    sc[k] = 0.0f;
-                    if (gi < ngroups) {
-                        const int r = gi / gpr, q = gi - r * gpr;
-                        const int p = phys_s[tile * kRows + r];
-                        if (p >= 0)
-                            sc[k] = __ldg(reinterpret_cast<const float*>(kvb + static_cast<int64_t>(p) * kRecBytes + kD) +
-                                          ((c0 * 64 + q * 16) >> 7));
-                    }
-                }
-                const bool got = mbar_wait(smem_u32(&S.empty[st]), ((tile / kStages) & 1) ^ 1, abort_flag, a.err);
-                if (!__all_sync(0xFFFFFFFFu, got)) return false;
-                if (issued > tile + 1) cp_async_wait<1>();  // the tile's codes have landed (the next tile's may not)
-                else cp_async_wait<0>();
-                const uint8_t* codes = smem + Lay::kOffCode + (tile % kCodeStages) * kCodeStageBytes;
-                uint8_t* stage = smem + kOffKv + st * kStageBytes;
-#pragma unroll
-                for (int k = 0; k < kGPT; ++k) {
-                    const int gi = pt + k * kPT;
-                    if (gi < ngroups) {
-                        const int r = gi / gpr, q = gi - r * gpr;
-                        uint4 lo, hi;
-                        e4m3x16_to_bf16_scaled(*reinterpret_cast<const uint4*>(codes + gi * 16), sc[k], lo, hi);
-                        uint8_t* row = stage + (q >> 2) * kChunkBytes + r * 128;  // chunk q / 4
-                        const int g2 = 2 * (q & 3);
-                        *reinterpret_cast<uint4*>(row + ((g2 ^ (r & 7)) << 4)) = lo;
-                        *reinterpret_cast<uint4*>(row + (((g2 + 1) ^ (r & 7)) << 4)) = hi;
-                    }
-                }
-                fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
-                mbar_arrive(smem_u32(&S.full[st]));
-                return true;
-            };
+        } else {  // FP8 records: the converter warps fill the stages; the producers prefetch, then send
+            prefetch_rows(pw * 32 + lane, kProducers * 32);
             bool ok = true;
-            for (int t = 0; t < kCodeStages && t < ntiles; ++t) issue(t);
-            for (int t = 0; ok && t < kStages - 1 && t < ntiles; ++t) {
-                ok = convert(t);
-                if (ok && t + kCodeStages < ntiles) issue(t + kCodeStages);
-            }
-            for (int j = 0; ok && j < ntiles; ++j) {
-                ok = send(j);
-                const int tt = j + kStages - 1;
-                if (ok && tt < ntiles) {
-                    ok = convert(tt);
-                    if (ok && tt + kCodeStages < ntiles) issue(tt + kCodeStages);
+            for (int j = 0; ok && j < ntiles; ++j) ok = send(j);
+        }
+    } else if (kKv8 && warp >= kWarpConv) {
+        // ------------------------------------------------------------- FP8 converters
+        // issue(t): once operand stage t % 4 is free, 16-byte cp.async of the codes of tile t (this
+        // CTA's columns; 16 codes per copy, groups spread over the 96 converter threads) into the
+        // stage's upper half, and each group's tile scale into registers; convert(t): every thread
+        // loads the codes it copied, the converters meet at a named barrier (the stage is then
+        // overwritten in place), and each widens its groups, times their scale, into the 128-byte-
+        // swizzled bf16 layout (code * scale in fp32, bf16 RNE). A tile is converted one tile after
+        // its copies were issued. Every converter takes every barrier, so a wait that gives up
+        // only stops the work.
+        constexpr int kPT = kConvThreads;
+        constexpr int kGPT = (kCodeBytes / 16 + kPT - 1) / kPT;  // 16-code groups per thread and tile (<= 14)
+        const int gpr = nchunks * 4;                               // groups per row of this CTA: 16 or 20
+        const int ngroups = kRows * gpr;
+        const int pt = (warp - kWarpConv) * 32 + lane;
+        const uint8_t* kvb = static_cast<const uint8_t*>(a.kv);
+        int issued = 0;
+        bool dead = false;
+        auto issue = [&](int tile, float (&sc)[kGPT]) {
+            const int st = tile % kStages;
+            const bool got = mbar_wait(smem_u32(&S.empty[st]), ((tile / kStages) & 1) ^ 1, abort_flag, a.err);
+            if (!__all_sync(0xFFFFFFFFu, got)) dead = true;
+            const uint32_t base = sKv + st * kStageBytes + kCodeOff;
+#pragma unroll
+            for (int k = 0; k < kGPT; ++k) {
+                const int gi = pt + k * kPT;
+                sc[k] = 0.0f;
+                if (!dead && gi < ngroups) {
+                    const int r = gi / gpr, q = gi - r * gpr;
+                    const int p = phys_s[tile * kRows + r];
+                    const uint8_t* rec = kvb + static_cast<int64_t>(p) * kRecBytes;
+                    cp_async16(base + gi * 16, p >= 0 ? rec + c0 * 64 + q * 16 : kvb, p >= 0 ? 16u : 0u);  // 0: zero-fill
+                    if (p >= 0) sc[k] = __ldg(reinterpret_cast<const float*>(rec + kD) + ((c0 * 64 + q * 16) >> 7));
                 }
             }
-            cp_async_wait<0>();  // nothing of this thread's is still in flight when the CTA exits
-        }
-    } else if (warp == 9) {
-        // ------------------------------------------------------------- L2 prefetch
-        // Every valid selected row's columns of this CTA (4 or 5 lines of 128 B), requested up
-        // front so that the gathers find them in L2.
-        for (int row = lane; row < nrows; row += 32) {
-            const int p = phys_s[row];
-            if (p < 0) continue;
-            if constexpr (!kKv8) {
-                const uint8_t* rp = static_cast<const uint8_t*>(a.kv) + c0 * 128 + static_cast<int64_t>(p) * (kD * 2);
-                for (int c = 0; c < nchunks; ++c) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + c * 128));
-            } else {  // the record's codes of this CTA's columns and the scales
-                const uint8_t* rp = static_cast<const uint8_t*>(a.kv) + static_cast<int64_t>(p) * kRecBytes;
-                const int lo = c0 * 64, hi = lo + nchunks * 64;
-                for (int o = lo; o < hi; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + o));
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + hi - 1));
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + kD));
+            cp_async_commit();
+            ++issued;
+        };
+        auto convert = [&](int tile, const float (&sc)[kGPT]) {
+            const int st = tile % kStages;
+            if (issued > tile + 1) cp_async_wait<1>();  // the tile's codes have landed (the next tile's may not)
+            else cp_async_wait<0>();
+            uint8_t* stage = smem + kOffKv + st * kStageBytes;
+            uint4 codes[kGPT];
+#pragma unroll
+            for (int k = 0; k < kGPT; ++k) {
+                const int gi = pt + k * kPT;
+                codes[k] = (!dead && gi < ngroups) ? *reinterpret_cast<const uint4*>(stage + kCodeOff + gi * 16)
+                                                   : make_uint4(0u, 0u, 0u, 0u);
+            }
+            dead = named_bar_or(5, kConvThreads, dead);  // every code is in registers: the stage may be overwritten
+            if (dead) return;
+#pragma unroll
+            for (int k = 0; k < kGPT; ++k) {
+                const int gi = pt + k * kPT;
+                if (gi < ngroups) {
+                    const int r = gi / gpr, q = gi - r * gpr;
+                    uint4 lo, hi;
+                    e4m3x16_to_bf16_scaled(codes[k], sc[k], lo, hi);
+                    uint8_t* row = stage + (q >> 2) * kChunkBytes + r * 128;  // chunk q / 4
+                    const int g2 = 2 * (q & 3);
+                    *reinterpret_cast<uint4*>(row + ((g2 ^ (r & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4*>(row + (((g2 + 1) ^ (r & 7)) << 4)) = hi;
+                }
+            }
+            fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
+            mbar_arrive(smem_u32(&S.full[st]));
+        };
+        // two tiles per iteration, so that each tile's scales sit in a statically named array
+        float sc0[kGPT], sc1[kGPT];
+        if (ntiles > 0) issue(0, sc0);
+        for (int t = 0; t < ntiles; t += 2) {
+            if (t + 1 < ntiles) issue(t + 1, sc1);
+            convert(t, sc0);
+            if (t + 1 < ntiles) {
+                if (t + 2 < ntiles) issue(t + 2, sc0);
+                convert(t + 1, sc1);
             }
         }
+        cp_async_wait<0>();  // nothing of this thread's is still in flight when the CTA exits
+    } else if (!kKv8 && warp == 9) {
+        prefetch_rows(lane, 32);
     } else if (warp == 8) {
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0 && ntiles > 0) {
@@ -472,7 +484,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             tc_commit(smem_u32(&S.mma_done));
             mbar_wait_drain(smem_u32(&S.mma_done), 0, a.err);
         }
-    } else if (warp < 4 || warp >= kWarpSoftB) {
+    } else if (warp < 4 || (warp >= kWarpSoftB && warp < kWarpSoftB + 4)) {
         // ------------------------------------------------------------- softmax + epilogue
         // Two warps per TMEM lane quarter: group 0 (warps 0-3) takes rows 0..31 of every tile and
         // O columns 0..127 of the CTA, group 1 (warps 10-13) rows 32..63 and O columns 128..255.
@@ -709,7 +721,7 @@ static bool launch_attn_tc_typed(const AttnArgs& a, const CUtensorMap& map_q, cu
     const size_t smem = tcattn::Layout<kKv8>::kSmemBytes;
     if (!set_max_dynamic_smem(reinterpret_cast<const void*>(tcattn::attn_tc_kernel<kKv8>), smem)) return false;
     return launch_kernel(a.after_own_kernel != 0, tcattn::attn_tc_kernel<kKv8>, dim3(2 * a.S, a.T),
-                         dim3(tcattn::kThreads), smem, s, a, map_q);
+                         dim3(kKv8 ? tcattn::kThreads8 : tcattn::kThreads), smem, s, a, map_q);
 }
 
 bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches) {
