@@ -803,7 +803,8 @@ def run_profile(args):
       prefill        the chunked prefill workload at full size (indexer + attention calls),
       prefill-small  2 x 2048 new tokens on 16,384 (a small case of the prefill kernels),
       decode-fp8     the default workload's keys stored as FP8 e4m3 with a per-block scale,
-      decode-mx      the default workload's keys stored as MXFP8."""
+      decode-mx      the default workload's keys stored as MXFP8,
+      decode-kv8     the default workload's latent rows stored as FP8 records."""
     import indexer_top_sparse_paged_gb300 as dsa
 
     dev = torch.device("cuda", 0)
@@ -822,8 +823,10 @@ def run_profile(args):
     case = W.generate(spec, seed)
     if args.profile in ("decode-fp8", "decode-mx"):
         case = W.with_key_format(case, "bf16_kfp8" if args.profile == "decode-fp8" else "mxfp8")
+    if args.profile == "decode-kv8":
+        case = W.with_kv_format(case, "fp8")
     s = case.spec
-    dims = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K)
+    dims = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K, kv=s.kv)
     q_I, w, k_I = to_dev(case.q_I, dev), to_dev(case.w, dev), to_dev(case.k_I, dev)
     ksc = to_dev(case.k_I_scale, dev) if case.k_I_scale is not None else None
     q, kv = to_dev(case.q, dev), to_dev(case.kv, dev)
@@ -849,7 +852,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill measurement")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the tiny, 1M-token and mixed-batch workloads (measured after the headline)")
-    ap.add_argument("--profile", nargs="?", const="decode", choices=["decode", "prefill", "prefill-small", "decode-fp8", "decode-mx"],
+    ap.add_argument("--profile", nargs="?", const="decode",
+                    choices=["decode", "prefill", "prefill-small", "decode-fp8", "decode-mx", "decode-kv8"],
                     help="only run --warmup + 1 steps of one case (a short command for ncu captures)")
     args = ap.parse_args()
     if args.profile:

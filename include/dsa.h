@@ -101,7 +101,7 @@ typedef enum {
  *   1 <= K <= 2048.
  */
 typedef struct {
-    int32_t mode;       /* dsa_mode, optionally | DSA_KV_FP8 */
+    int32_t mode;       /* dsa_mode, optionally | DSA_KV_FP8 | DSA_Q_MX_READY */
     int32_t B;          /* number of sequences (rows of block_table, entries of seq_lens) */
     int32_t max_blocks; /* block_table row length */
     int32_t num_blocks; /* physical blocks in k_I_cache and kv_cache */
@@ -209,6 +209,26 @@ dsa_status dsa_cache_append(const dsa_dims* dims, const void* k_I_new, const voi
                             const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
                             const int32_t* q_pos, int32_t T, void* k_I_cache, void* k_I_scale, void* kv_cache,
                             void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/*
+ * Indexer prolog: one launch that prepares the indexer's inputs for a step ("Day0 Inference Support
+ * ... on Huawei Ascend CANN Architecture" §2.2, Indexer Prolog: the query quantisation runs beside
+ * the other preparations instead of after them):
+ *  - the cache append of T_new new tokens, exactly as dsa_cache_append with the same arguments;
+ *  - with q_I_mx not NULL (DSA_MXFP8 only): the MXFP8 quantisation of the indexer query q_I
+ *    [T_q][H_I][d_I] (bf16), written to q_I_mx [T_q][H_I][d_I] as the exact bf16 values of its MX
+ *    elements (code * 2^X; the same rounding dsa_indexer_topk applies).
+ * Pass q_I_mx as q_I to dsa_indexer_topk / dsa_decode with DSA_Q_MX_READY in dims.mode: they then
+ * skip their own quantisation of the query (one launch fewer); the indices are the same, since
+ * quantising MX values again returns them unchanged. ws as for dsa_cache_append (only its error
+ * word is used). Either part may be empty (T_new = 0, or q_I_mx = NULL).
+ */
+#define DSA_Q_MX_READY 0x20
+dsa_status dsa_indexer_prolog(const dsa_dims* dims, const void* k_I_new, const void* kv_new,
+                              const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
+                              const int32_t* q_pos, int32_t T_new, void* k_I_cache, void* k_I_scale, void* kv_cache,
+                              const void* q_I, int32_t T_q, void* q_I_mx, void* ws, size_t ws_bytes,
+                              dsa_stream_t stream);
 
 /*
  * Hierarchical (coarse -> fine) index selection ("Engineering Path for Day-0 Adaptation ..." §3.1:

@@ -11,7 +11,8 @@ Entry points (same names as the C ABI):
 * :func:`sparse_attn` -- sparse attention over the rows ``idx`` selects.
 * :func:`decode` -- both, fused on one stream, for one query row per sequence.
 * :func:`cache_append` -- new tokens' indexer keys and latent rows into the paged caches (FP8 keys:
-  block requantisation).
+  block requantisation; FP8 latent rows: per-tile quantisation).
+* :func:`indexer_prolog` -- the cache append and the MXFP8 query quantisation in one launch.
 * :func:`block_summaries`, :func:`indexer_topk_hier` -- hierarchical (coarse -> fine) selection over
   per-block summary keys.
 * :func:`indexer_topk_noalloc` -- :func:`indexer_topk` with the library's static scratch instead of
@@ -73,6 +74,8 @@ def lib():
         L.dsa_indexer_topk_hier.argtypes = [D, P, P, P, P, P, P, P, P, I32, P, I32, P, P, P, SZ, P]
         L.dsa_cache_append.restype = ctypes.c_int
         L.dsa_cache_append.argtypes = [D, P, P, P, P, P, P, I32, P, P, P, P, SZ, P]
+        L.dsa_indexer_prolog.restype = ctypes.c_int
+        L.dsa_indexer_prolog.argtypes = [D, P, P, P, P, P, P, I32, P, P, P, P, I32, P, P, SZ, P]
         L.dsa_indexer_topk_noalloc.restype = ctypes.c_int
         L.dsa_indexer_topk_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, I32, P, P, P]
         L.dsa_read_error.restype = ctypes.c_int
@@ -90,6 +93,7 @@ def lib():
 
 
 KV_FP8 = 0x10  # DSA_KV_FP8: the latent cache holds FP8 records (e4m3 codes, one fp32 scale per 128 elements)
+Q_MX_READY = 0x20  # DSA_Q_MX_READY: q_I already holds MXFP8 values (from indexer_prolog)
 
 
 def kv_record_bytes(d: int) -> int:
@@ -98,9 +102,11 @@ def kv_record_bytes(d: int) -> int:
 
 
 def make_dims(mode: str, B: int, max_blocks: int, num_blocks: int, H_I: int, d_I: int, H: int, d: int, d_v: int,
-              K: int, block_size: int = 64, kv: str = "act") -> Dims:
-    """kv="fp8" sets DSA_KV_FP8 (the latent cache holds FP8 records)."""
+              K: int, block_size: int = 64, kv: str = "act", q_ready: bool = False) -> Dims:
+    """kv="fp8" sets DSA_KV_FP8 (the latent cache holds FP8 records); q_ready sets DSA_Q_MX_READY."""
     m = MODES[mode] if isinstance(mode, str) else int(mode)
+    if q_ready:
+        m |= Q_MX_READY
     if kv == "fp8":
         m |= KV_FP8
     elif kv != "act":
@@ -228,6 +234,25 @@ def cache_append(dims: Dims, k_I_new, kv_new, block_table, seq_lens, k_I_cache, 
                                 _p(q_pos), T, _p(k_I_cache), _p(k_I_scale), _p(kv_cache), _p(ws), ws.numel(),
                                 _stream(stream))
     _check("dsa_cache_append", st)
+
+
+def indexer_prolog(dims: Dims, k_I_new, kv_new, block_table, seq_lens, k_I_cache, k_I_scale, kv_cache, q_I=None,
+                   q_seq=None, q_pos=None, *, ws, q_out=None, stream=None):
+    """One launch: the cache append of the new tokens (as cache_append) and, when q_I is given
+    (DSA_MXFP8), its MXFP8 quantisation into q_out (returned; bf16, q_I's shape)."""
+    T_new = 0 if kv_new is None else kv_new.shape[0]
+    T_q = 0
+    if q_I is not None:
+        T_q = q_I.shape[0]
+        if q_out is None:
+            q_out = torch.empty_like(q_I)
+        if q_out.dtype != torch.bfloat16 or q_out.numel() < q_I.numel() or not q_out.is_contiguous():
+            raise ValueError("q_out must be a contiguous bf16 tensor of q_I's size")
+    st = lib().dsa_indexer_prolog(ctypes.byref(dims), _p(k_I_new), _p(kv_new), _p(block_table), _p(seq_lens),
+                                  _p(q_seq), _p(q_pos), T_new, _p(k_I_cache), _p(k_I_scale), _p(kv_cache), _p(q_I), T_q,
+                                  _p(q_out), _p(ws), ws.numel(), _stream(stream))
+    _check("dsa_indexer_prolog", st)
+    return q_out
 
 
 def summaries_buffer(dims: Dims, device="cuda") -> torch.Tensor:

@@ -96,10 +96,10 @@ __device__ void store_kv_record(uint8_t* rec, const uint16_t* x, int d) {
         rec[i] = 0;
 }
 
-__global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(AppendArgs a) {
+// New token t's rows into the paged caches (the whole CTA).
+__device__ void append_token(const AppendArgs& a, int t) {
     __shared__ float red[kAppendThreads / 32];
     __shared__ int run_end;
-    const int t = blockIdx.x;
     int b, pos;
     const int blk = append_block(a, t, b, pos);
     if (blk < 0) {
@@ -191,6 +191,23 @@ __global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(AppendArgs
     if (threadIdx.x == 0) static_cast<float*>(a.k_scale)[blk] = scale;
 }
 
+__global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(AppendArgs a) { append_token(a, blockIdx.x); }
+
+// Indexer prolog: the cache append of the step's new tokens (CTAs 0 .. T - 1) and, in the same
+// launch, the MXFP8 quantisation of the indexer query (the other CTAs, one group of 32 elements per
+// thread, written as its exact bf16 values to q_out) -- the two independent preparations the
+// indexer needs ("Day0 Inference Support ... on Huawei Ascend CANN Architecture" §2.2, Indexer
+// Prolog: Q quantisation runs beside the other preparations instead of after them).
+__global__ void __launch_bounds__(kAppendThreads)
+    indexer_prolog_kernel(AppendArgs a, const uint16_t* __restrict__ q, uint16_t* __restrict__ q_out, int64_t q_groups) {
+    if (static_cast<int>(blockIdx.x) < a.T) {
+        append_token(a, blockIdx.x);
+        return;
+    }
+    const int64_t g = static_cast<int64_t>(blockIdx.x - a.T) * kAppendThreads + threadIdx.x;
+    if (g < q_groups) mx_quantize_group32(q + g * 32, q_out + g * 32);
+}
+
 bool launch_cache_append(const dsa_dims& d, bool kv_fp8, const void* k_new, const void* kv_new,
                          const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
                          const int32_t* q_pos, int T, void* k_cache, void* k_scale, void* kv_cache, int* err,
@@ -199,6 +216,22 @@ bool launch_cache_append(const dsa_dims& d, bool kv_fp8, const void* k_new, cons
     AppendArgs a{d.mode, kv_fp8 ? 1 : 0, d.B, d.max_blocks, d.num_blocks, d.d_I, d.d, T, k_new, kv_new, block_table,
                  seq_lens, q_seq, q_pos, k_cache, k_scale, kv_cache, err};
     if (!launch_kernel(false, cache_append_kernel, dim3(T), dim3(kAppendThreads), 0, s, a)) return false;
+    ++*launches;
+    return true;
+}
+
+bool launch_indexer_prolog(const dsa_dims& d, bool kv_fp8, const void* k_new, const void* kv_new,
+                           const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
+                           const int32_t* q_pos, int T, void* k_cache, void* k_scale, void* kv_cache, const void* q_I,
+                           void* q_out, int64_t q_elements, int* err, cudaStream_t s, int* launches) {
+    const int64_t q_groups = q_out ? q_elements / 32 : 0;
+    const int64_t q_ctas = (q_groups + kAppendThreads - 1) / kAppendThreads;
+    if (T == 0 && q_ctas == 0) return true;
+    AppendArgs a{d.mode, kv_fp8 ? 1 : 0, d.B, d.max_blocks, d.num_blocks, d.d_I, d.d, T, k_new, kv_new, block_table,
+                 seq_lens, q_seq, q_pos, k_cache, k_scale, kv_cache, err};
+    if (!launch_kernel(false, indexer_prolog_kernel, dim3(static_cast<unsigned>(T + q_ctas)), dim3(kAppendThreads), 0, s,
+                       a, static_cast<const uint16_t*>(q_I), static_cast<uint16_t*>(q_out), q_groups))
+        return false;
     ++*launches;
     return true;
 }

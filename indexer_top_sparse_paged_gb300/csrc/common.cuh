@@ -467,6 +467,36 @@ __device__ __forceinline__ int mx_encode32(const uint32_t (&w)[16], uint32_t (&c
     return X;
 }
 
+// One group of 32 bf16 values (64 bytes at src, 16-byte aligned) -> their MXFP8 values as bf16
+// (exact: code * 2^X), at dst: the MX quantisation of a query group for the tensor-core indexer.
+__device__ __forceinline__ void mx_quantize_group32(const uint16_t* src, uint16_t* dst) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = s4[i];
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+    uint32_t codes[8];
+    const int X = mx_encode32(w, codes);
+    const float up = e8m0_value(static_cast<uint32_t>(X + 127));  // 2^X
+    uint32_t o[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {  // element pair 2i, 2i + 1: bytes 2(i % 2), 2(i % 2) + 1 of code word i / 2
+        const __nv_fp8x2_storage_t c = static_cast<__nv_fp8x2_storage_t>((codes[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
+        const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(c, __NV_E4M3);
+        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));  // .x = the lower code
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v.x * up, v.y * up);
+        o[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+}
+
 // 16 e4m3 codes times the power of two f -> 16 bf16. The fp32 products are exact (at most 4
 // significant bits, magnitudes >= 2^-136); so is their bf16 rounding unless a value lies below
 // bf16's normal range (an MX exponent under -117).

@@ -158,10 +158,14 @@ static dsa_status split_mode(const dsa_dims* in, dsa_dims* out, bool* kv8) {
     if (!in) return DSA_ERR_INVALID_ARG;
     *out = *in;
     *kv8 = (in->mode & DSA_KV_FP8) != 0;
-    out->mode = in->mode & ~DSA_KV_FP8;
+    out->mode = in->mode & ~(DSA_KV_FP8 | DSA_Q_MX_READY);
     if (*kv8 && (out->mode == DSA_F32 || in->d % 16)) return DSA_ERR_UNSUPPORTED;
+    if ((in->mode & DSA_Q_MX_READY) && out->mode != DSA_MXFP8) return DSA_ERR_UNSUPPORTED;
     return DSA_OK;
 }
+
+// DSA_Q_MX_READY: q_I already holds the MXFP8 values (dsa_indexer_prolog wrote them).
+static bool q_mx_ready(const dsa_dims* in) { return (in->mode & DSA_Q_MX_READY) != 0; }
 
 static dsa_status check_common(const dsa_dims* d) {
     if (!d) return DSA_ERR_INVALID_ARG;
@@ -212,7 +216,7 @@ static dsa_status check_ws(const dsa_dims* d, int T, void* ws, size_t ws_bytes) 
 static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w, const void* k_I_cache,
                               const void* k_I_scale, const int32_t* block_table, const int32_t* seq_lens,
                               const int32_t* q_seq, const int32_t* q_pos, int32_t T, int32_t* idx, void* ws,
-                              cudaStream_t stream, int* launches, bool allow_prefill = true) {
+                              cudaStream_t stream, int* launches, bool allow_prefill = true, bool q_ready = false) {
     const WsLayout L = ws_layout(*d, T, allow_prefill);
     uint8_t* base = static_cast<uint8_t*>(ws);
     IndexerArgs a{};
@@ -246,7 +250,7 @@ static dsa_status run_indexer(const dsa_dims* d, const void* q_I, const float* w
     a.gemm_tile_prefix = reinterpret_cast<int32_t*>(base + L.gemm_tile_prefix);
     a.scores = reinterpret_cast<float*>(base + L.scores);
     a.G2 = device_sm_count();
-    if (d->mode == DSA_MXFP8) {  // the quantised query first; the indexer kernels read it as bf16
+    if (d->mode == DSA_MXFP8 && !q_ready) {  // the quantised query first; the indexer kernels read it as bf16
         void* q_mx = base + L.q_mx;
         if (!launch_mx_quantize_q(q_I, q_mx, static_cast<int64_t>(T) * d->H_I * d->d_I, stream, launches))
             return DSA_ERR_LAUNCH;
@@ -422,7 +426,7 @@ dsa_status dsa_indexer_topk(const dsa_dims* dims_in, const void* q_I, const floa
     int launches = 0;
     if (T > 0)
         st = run_indexer(dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, q_seq, q_pos, T, idx, ws,
-                         reinterpret_cast<cudaStream_t>(stream), &launches);
+                         reinterpret_cast<cudaStream_t>(stream), &launches, true, q_mx_ready(dims_in));
     g_last_launches = launches;
     return st;
 }
@@ -481,7 +485,7 @@ dsa_status dsa_decode(const dsa_dims* dims_in, const void* q_I, const float* w, 
     int launches = 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     st = run_indexer(dims, q_I, w, k_I_cache, k_I_scale, block_table, seq_lens, nullptr, nullptr, T, idx_buf, ws, s,
-                     &launches);
+                     &launches, true, q_mx_ready(dims_in));
     if (st == DSA_OK)
         st = run_attn(dims, kv8, q, kv_cache, block_table, seq_lens, nullptr, idx_buf, T, sm_scale, out, lse, ws, s,
                       &launches, true);
@@ -559,6 +563,45 @@ dsa_status dsa_cache_append(const dsa_dims* dims_in, const void* k_I_new, const 
     if (!launch_cache_append(*dims, kv8, k_I_new, kv_new, block_table, seq_lens, q_seq, q_pos, T, k_I_cache,
                              k_I_scale, kv_cache, static_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream),
                              &launches))
+        st = DSA_ERR_LAUNCH;
+    g_last_launches = launches;
+    return st;
+}
+
+dsa_status dsa_indexer_prolog(const dsa_dims* dims_in, const void* k_I_new, const void* kv_new,
+                              const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
+                              const int32_t* q_pos, int32_t T_new, void* k_I_cache, void* k_I_scale, void* kv_cache,
+                              const void* q_I, int32_t T_q, void* q_I_mx, void* ws, size_t ws_bytes,
+                              dsa_stream_t stream) {
+    dsa_dims D;
+    bool kv8;
+    {
+        const dsa_status split = split_mode(dims_in, &D, &kv8);
+        if (split != DSA_OK) return split;
+    }
+    const dsa_dims* dims = &D;
+    dsa_status st = check_common(dims);
+    if (st != DSA_OK) return st;
+    if (T_new < 0 || T_q < 0 || dims->d_I <= 0 || dims->d <= 0) return DSA_ERR_INVALID_ARG;
+    if (!q_seq && T_new != dims->B) return DSA_ERR_INVALID_ARG;
+    if (T_new > 0 && (!k_I_new || !kv_new || !block_table || !seq_lens || !k_I_cache || !kv_cache))
+        return DSA_ERR_INVALID_ARG;
+    if (!scale_ok(dims, k_I_scale)) return DSA_ERR_INVALID_ARG;
+    const int act = dims->mode == DSA_F32 ? 4 : 2;
+    if ((dims->d * act) % 16 || (dims->d_I * act) % 16) return DSA_ERR_UNSUPPORTED;
+    if (dims->mode == DSA_MXFP8 && dims->d_I % 32) return DSA_ERR_UNSUPPORTED;
+    if (!aligned16(k_I_new) || !aligned16(kv_new) || !aligned16(k_I_cache) || !aligned16(kv_cache))
+        return DSA_ERR_INVALID_ARG;
+    if (q_I_mx) {  // the query quantisation: MXFP8 only, both buffers [T_q][H_I][d_I] bf16
+        if (dims->mode != DSA_MXFP8) return DSA_ERR_UNSUPPORTED;
+        if (T_q > 0 && (!q_I || !aligned16(q_I) || !aligned16(q_I_mx))) return DSA_ERR_INVALID_ARG;
+    }
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < 256) return DSA_ERR_WORKSPACE;
+    int launches = 0;
+    const int64_t q_elements = q_I_mx ? static_cast<int64_t>(T_q) * dims->H_I * dims->d_I : 0;
+    if (!launch_indexer_prolog(*dims, kv8, k_I_new, kv_new, block_table, seq_lens, q_seq, q_pos, T_new, k_I_cache,
+                               k_I_scale, kv_cache, q_I, q_I_mx, q_elements, static_cast<int*>(ws),
+                               reinterpret_cast<cudaStream_t>(stream), &launches))
         st = DSA_ERR_LAUNCH;
     g_last_launches = launches;
     return st;

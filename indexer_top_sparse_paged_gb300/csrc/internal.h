@@ -135,6 +135,10 @@ bool launch_cache_append(const dsa_dims& d, bool kv_fp8, const void* k_new, cons
                          const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
                          const int32_t* q_pos, int T, void* k_cache, void* k_scale, void* kv_cache, int* err,
                          cudaStream_t s, int* launches);
+bool launch_indexer_prolog(const dsa_dims& d, bool kv_fp8, const void* k_new, const void* kv_new,
+                           const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_seq,
+                           const int32_t* q_pos, int T, void* k_cache, void* k_scale, void* kv_cache, const void* q_I,
+                           void* q_out, int64_t q_elements, int* err, cudaStream_t s, int* launches);
 bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches);
 bool launch_wait_timeout(int* err, cudaStream_t s, int* launches);
 

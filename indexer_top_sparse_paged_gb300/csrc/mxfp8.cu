@@ -17,31 +17,7 @@ __global__ void __launch_bounds__(kMxThreads)
     griddep_launch_dependents();  // the indexer may start its prologue (it waits for this grid)
     const int64_t g = static_cast<int64_t>(blockIdx.x) * kMxThreads + threadIdx.x;
     if (g >= groups) return;
-    const uint4* src = reinterpret_cast<const uint4*>(q + g * 32);
-    uint32_t w[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint4 v = src[i];
-        w[4 * i] = v.x;
-        w[4 * i + 1] = v.y;
-        w[4 * i + 2] = v.z;
-        w[4 * i + 3] = v.w;
-    }
-    uint32_t codes[8];
-    const int X = mx_encode32(w, codes);
-    const float up = e8m0_value(static_cast<uint32_t>(X + 127));  // 2^X
-    uint32_t o[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {  // element pair 2i, 2i + 1: bytes 2(i % 2), 2(i % 2) + 1 of code word i / 2
-        const __nv_fp8x2_storage_t c = static_cast<__nv_fp8x2_storage_t>((codes[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
-        const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(c, __NV_E4M3);
-        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));  // .x = the lower code
-        const __nv_bfloat162 b = __floats2bfloat162_rn(v.x * up, v.y * up);
-        o[i] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(out + g * 32);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    mx_quantize_group32(q + g * 32, out + g * 32);
 }
 
 bool launch_mx_quantize_q(const void* q_I, void* out, int64_t elements, cudaStream_t s, int* launches) {

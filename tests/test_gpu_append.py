@@ -9,7 +9,7 @@ import torch
 import indexer_top_sparse_paged_gb300 as dsa
 import oracle
 import workloads as W
-from cases import small_spec
+from cases import np_bf16, np_e4m3, small_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -97,3 +97,50 @@ def test_append_fp8_latent_records(mode):
     _check(W.generate(spec, seed=208), 209)
     spec = small_spec(mode, [1, 64, 65, 700], 64, H=4, d=80, d_v=48, kv="fp8")
     _check(W.generate(spec, seed=210), 211, explicit_rows=False)
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "bf16_kfp8"])
+def test_indexer_prolog_is_the_append_and_the_query_quantisation_in_one_launch(mode):
+    """dsa_indexer_prolog: the caches byte for byte as the oracle's append, the MX query (MXFP8) bit
+    for bit as the oracle's OCP MX quantisation, one launch; the indexer fed the prepared query
+    (DSA_Q_MX_READY) gives the same indices with one launch fewer."""
+    spec = small_spec(mode, [300, 1000, 77, 4096], 256, new_tokens=[1, 1, 1, 1])
+    case = W.generate(spec, seed=212)
+    k_new, kv_new = _new_tokens(case, 213)
+    s = case.spec
+    dims = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K)
+    k_I, kv = _t(case.k_I), _t(case.kv)
+    scale = _t(case.k_I_scale)
+    ws = dsa.workspace(dims, s.T)
+    q_I = _t(case.q_I).view(torch.bfloat16)
+    mx = mode == "mxfp8"
+    q_out = dsa.indexer_prolog(dims, _t(k_new).view(torch.bfloat16), _t(kv_new).view(torch.bfloat16),
+                               _t(case.block_table), _t(case.seq_lens), k_I, scale, kv, q_I=q_I if mx else None, ws=ws)
+    torch.cuda.synchronize()
+    assert dsa.read_error(ws) == 0
+    assert dsa.last_launch_count() == 1
+    ok, osc, okv = oracle.cache_append(case, k_new, kv_new)
+    assert np.array_equal(kv.cpu().numpy().view(case.kv.dtype), okv)
+    assert np.array_equal(k_I.cpu().numpy().view(case.k_I.dtype), ok)
+    assert np.array_equal(scale.cpu().numpy().view(osc.dtype), osc)
+    if not mx:
+        return
+    # the query: every group of 32 quantised by the oracle, decoded exactly, as bf16 bits
+    qf = np_bf16(case.q_I).astype(np.float32).reshape(-1, 32)
+    want = np.empty_like(qf)
+    for g in range(qf.shape[0]):
+        X, codes = oracle.mx_quantize32(qf[g])
+        want[g] = np_e4m3(codes) * 2.0 ** X
+    got = q_out.view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1, 32)
+    assert np.array_equal(got, W.to_bf16_bits(want))
+    # the indexer on the appended caches: the prepared query with DSA_Q_MX_READY, and the raw query
+    bt, sl = _t(case.block_table), _t(case.seq_lens)
+    w = _t(case.w)
+    idx_raw = dsa.indexer_topk(dims, q_I, w, k_I, scale, bt, sl, ws=ws)
+    n_raw = dsa.last_launch_count()
+    ready = dsa.make_dims(s.mode, s.B, case.max_blocks, case.num_blocks, s.H_I, s.d_I, s.H, s.d, s.d_v, s.K,
+                          q_ready=True)
+    idx_ready = dsa.indexer_topk(ready, q_out, w, k_I, scale, bt, sl, ws=ws)
+    assert dsa.last_launch_count() == n_raw - 1
+    torch.cuda.synchronize()
+    assert torch.equal(idx_raw, idx_ready)
