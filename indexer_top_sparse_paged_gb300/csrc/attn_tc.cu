@@ -7,7 +7,7 @@
 // divides the latent dimension: CTA 0 owns columns 0..255, CTA 1 owns columns 256..575, so every
 // selected row is gathered from memory exactly once. For every tile of 64 gathered rows each CTA
 //   1. gathers only its columns of the 64 rows (the index list, resolved once to physical cache
-//      rows, drives 16-byte cp.async row copies by four producer warps straight into the
+//      rows, drives 16-byte cp.async row copies by seven warps straight into the
 //      128-byte-swizzled layout the tensor core reads; four row stages),
 //   2. computes its partial logits S_r[128 heads x 64 rows] = Q[:, cols_r] . R[:, cols_r]^T with
 //      tcgen05 (M = 128 heads, N = 64 rows; an MMA of N < 64 would leave the tensor pipe idle),
@@ -29,13 +29,14 @@
 // CTA (A operand from TMEM); shared memory holds the first query chunk, four row stages, two
 // exchange slots and the resolved rows of the split.
 //
-// Roles (448 threads = 14 warps per CTA): warps 0-3 and 10-13 softmax / epilogue in two groups
+// Roles (512 threads = 16 warps per CTA): warps 0-3 and 9-12 softmax / epilogue in two groups
 // (thread = head = TMEM lane; group 0 takes rows 0..31 of every tile and O columns 0..127, group 1
-// rows 32..63 and O columns 128..255), warps 4-7 producers (gather rows; send the partial logits
-// of their TMEM lane quarter), warp 8 TMEM allocator + MMA issuer (+ the TMA loads of the query),
-// warp 9 prefetches the CTA's columns of every selected row into L2 at the start. With FP8
-// records (512 threads = 16 warps) the second softmax group is warps 9-12, warps 13-15 stage and
-// widen the codes, and the producers prefetch and then only send the partial logits.
+// rows 32..63 and O columns 128..255), warps 4-7 producers (send the partial logits of their TMEM
+// lane quarter; bf16 rows: gather a quarter of each tile), warp 8 TMEM allocator + MMA issuer
+// (+ the TMA loads of the query), warps 13-15 fill the operand stages (bf16 rows: cp.async
+// gathers of the other three quarters, with L2 prefetches of later tiles' rows in windows of 12
+// tiles; FP8 records: stage the codes and widen them in place, the producers having requested
+// every record into L2 at the start).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -60,10 +61,10 @@ constexpr int kCodeOff = kStageBytes - kCodeBytes;      // ... staged in the upp
 constexpr int kXBytes = kHeads * kRows * 2;   // one partial-logit tile (fp16, prescaled by 2^-8)
 constexpr float kXScale = 1.0f / 256.0f;      // partial logits travel as fp16(S_r * 2^-8)
 constexpr int kMaxRows = 2048;
-constexpr int kThreads = 448;   // bf16 latent rows: 14 warps
-constexpr int kThreads8 = 512;  // FP8 records: 16 warps (the register file holds no more at 128 a thread)
-constexpr int kWarpConv = 13;   // FP8 converters: warps 13..15
-constexpr int kConvThreads = 96;
+constexpr int kThreads = 512;     // 16 warps (the register file holds no more at 128 registers a thread)
+constexpr int kWarpFill = 13;     // the operand-stage fillers: warps 13..15
+constexpr int kFillThreads = 96;
+constexpr int kFillRows = 48;     // bf16 rows: the fillers gather rows 0..47 of a tile, the producers 48..63
 constexpr int kProducers = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // S/P buffers at 256 and 320; Q chunks 32 apart
@@ -116,10 +117,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 template <bool kKv8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKv8 ? kThreads8 : kThreads)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
     attn_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap map_q) {
-    constexpr int kNT = kKv8 ? kThreads8 : kThreads;
-    constexpr int kWarpSoftB = kKv8 ? 9 : 10;  // second softmax group: warps 10..13 (FP8 records: 9..12)
+    constexpr int kNT = kThreads;
+    constexpr int kWarpSoftB = 9;  // second softmax group: warps 9..12
     using Lay = Layout<kKv8>;
     constexpr int kStages = Lay::kStages;
     constexpr size_t kOffQ = Lay::kOffQ, kOffKv = Lay::kOffKv, kOffX = Lay::kOffX, kOffValid = Lay::kOffValid;
@@ -154,7 +155,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKv8 ? kThreads8 : k
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(smem_u32(&S.full[i]), kKv8 ? kConvThreads : kProducers * 32);  // every filling thread arrives
+            mbar_init(smem_u32(&S.full[i]), kKv8 ? kFillThreads : kFillThreads + kProducers * 32);  // every filling thread arrives
             mbar_init(smem_u32(&S.empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -252,11 +253,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKv8 ? kThreads8 : k
     block_sync();
     tc_fence_after();
 
-    // L2 prefetch of every valid selected row's columns of this CTA (4 or 5 lines of 128 B; FP8: the
-    // record's codes of these columns and its scales), requested up front so that the gathers find
-    // them in L2; thread i of n takes rows i, i + n, ...
-    auto prefetch_rows = [&](int i0, int n) {
-        for (int row = i0; row < nrows; row += n) {
+    // L2 prefetch of the valid selected rows i0, i0 + n, ... < i1: this CTA's columns (4 or 5 lines of
+    // 128 B; FP8: the record's codes of these columns and its scales), requested ahead so that the
+    // gathers find them in L2
+    auto prefetch_rows = [&](int i0, int i1, int n) {
+        for (int row = i0; row < i1; row += n) {
             const int p = phys_s[row];
             if (p < 0) continue;
             if constexpr (!kKv8) {
@@ -272,45 +273,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKv8 ? kThreads8 : k
         }
     };
     if (warp >= 4 && warp < 4 + kProducers) {
-        // ------------------------------------------------------------- producers: gather + send
-        // Producer warp pw (TMEM lane quarter pw) alternates two jobs, in an order that matches the
-        // tensor pipe's (QK(j + 1) is issued right after PV(j - 1), which frees the stage of tile
-        // j + 3), so neither job waits behind the other:
-        //  send(j):   once S(j) is in tensor memory, read the partial logits of heads 32pw..32pw+31,
-        //             round them to fp16(S * 2^-8) and store them into the peer's exchange slot
-        //             j & 1 (distributed shared memory; the peer's softmax frees the slot);
-        //  gather(t): once stage t % 4 is free, copy rows pw, pw + 4, ... of tile t (their physical
-        //             cache rows were resolved up front) with 16-byte cp.async per lane (lane = chunk
-        //             lane / 8, 16-byte group lane % 8; CTA 1's fifth chunk from lanes 0..7) into the
-        //             128-byte-swizzled layout; rows with no position read as zeros.
-        //  With FP8 records the producers only send: four converter warps fill the stages.
+        // ------------------------------------------------------------- producers: send
+        // Producer warp pw (TMEM lane quarter pw; with FP8 records after requesting its share of
+        // the selected records into L2; with bf16 rows it also gathers rows 48 + pw, 52 + pw, ... of
+        // every tile) for every tile j
+        //  send(j):   once S(j) is in tensor memory, reads the partial logits of heads 32pw..32pw+31,
+        //             rounds them to fp16(S * 2^-8) and stores them into the peer's exchange slot
+        //             j & 1 (distributed shared memory; the peer's softmax frees the slot).
+        // A gather waits only for a stage that the tensor pipe frees before the next S, so a partial
+        // leaves as soon as its MMA has completed.
         const int pw = warp - 4;
         const int h = pw * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(pw * 32) << 16;
         const uint32_t peer_x = mapa_shared(sX, peer);
         const uint32_t peer_xfull = mapa_shared(smem_u32(&S.xfull[0]), peer);  // [1] at +8
-        const uint8_t* kv = static_cast<const uint8_t*>(a.kv) + c0 * 128;
-        const int c = lane >> 3, g = lane & 7;  // chunk and 16-byte group this lane copies
-        auto gather = [&](int tile) -> bool {
-            const int st = tile % kStages;
-            const bool got = mbar_wait(smem_u32(&S.empty[st]), ((tile / kStages) & 1) ^ 1, abort_flag, a.err);
-            if (!__all_sync(0xFFFFFFFFu, got)) return false;
-            const uint32_t base = sKv + st * kStageBytes;
-#pragma unroll 4
-            for (int k = 0; k < kRows / kProducers; ++k) {
-                const int r = kProducers * k + pw;
-                const int p = phys_s[tile * kRows + r];
-                const uint8_t* src = p >= 0 ? kv + static_cast<int64_t>(p) * (kD * 2) : kv;
-                const uint32_t nb = p >= 0 ? 16u : 0u;  // 0: zero-fill
-                const uint32_t rowoff = static_cast<uint32_t>(r * 128);
-                cp_async16(base + c * kChunkBytes + rowoff + ((g ^ (r & 7)) << 4), src + (p >= 0 ? c * 128 + g * 16 : 0), nb);
-                if (nchunks == 5 && lane < 8)
-                    cp_async16(base + 4 * kChunkBytes + rowoff + ((lane ^ (r & 7)) << 4),
-                               src + (p >= 0 ? 4 * 128 + lane * 16 : 0), nb);
-            }
-            cp_async_arrive_noinc(smem_u32(&S.full[st]));  // once this thread's copies have landed
-            return true;
-        };
         auto send = [&](int j) -> bool {
             const int sb = j & 1;
             const bool got = mbar_wait(smem_u32(&S.s_full[sb]), (j >> 1) & 1, abort_flag, a.err);
@@ -339,19 +315,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKv8 ? kThreads8 : k
                 st_async_v4(dst + xoff(h, g), hp[4 * g], hp[4 * g + 1], hp[4 * g + 2], hp[4 * g + 3], peer_xfull + sb * 8);
             return true;
         };
-        if constexpr (!kKv8) {
+        if constexpr (kKv8) {
+            prefetch_rows(pw * 32 + lane, nrows, kProducers * 32);
             bool ok = true;
-            for (int t = 0; ok && t < kStages - 1 && t < ntiles; ++t) ok = gather(t);
+            for (int j = 0; ok && j < ntiles; ++j) ok = send(j);
+        } else {
+            // bf16 rows: rows 48..63 of every tile are the producers' (4 per warp), gathered as
+            // the fillers gather theirs, in the gaps between sends: gather(t) runs once stage t % 4
+            // is free, three tiles ahead, in the order the tensor pipe frees the stages
+            const uint8_t* kv = static_cast<const uint8_t*>(a.kv) + c0 * 128;
+            const int c = lane >> 3, g = lane & 7;  // chunk and 16-byte group this lane copies
+            auto gather = [&](int tile) -> bool {
+                const int st = tile % kStages;
+                const bool got = mbar_wait(smem_u32(&S.empty[st]), ((tile / kStages) & 1) ^ 1, abort_flag, a.err);
+                if (!__all_sync(0xFFFFFFFFu, got)) return false;
+                const uint32_t base = sKv + st * kStageBytes;
+#pragma unroll
+                for (int k = 0; k < kRows / 4 / kProducers; ++k) {
+                    const int r = kFillRows + kProducers * k + pw;
+                    const int p = phys_s[tile * kRows + r];
+                    const uint8_t* src = p >= 0 ? kv + static_cast<int64_t>(p) * (kD * 2) : kv;
+                    const uint32_t nb = p >= 0 ? 16u : 0u;  // 0: zero-fill
+                    const uint32_t rowoff = static_cast<uint32_t>(r * 128);
+                    cp_async16(base + c * kChunkBytes + rowoff + ((g ^ (r & 7)) << 4), src + (p >= 0 ? c * 128 + g * 16 : 0), nb);
+                    if (nchunks == 5 && lane < 8)
+                        cp_async16(base + 4 * kChunkBytes + rowoff + ((lane ^ (r & 7)) << 4),
+                                   src + (p >= 0 ? 4 * 128 + lane * 16 : 0), nb);
+                }
+                cp_async_arrive_noinc(smem_u32(&S.full[st]));  // once this thread's copies have landed
+                return true;
+            };
+            bool ok = true;
+            for (int t0 = 0; ok && t0 < kStages - 1 && t0 < ntiles; ++t0) ok = gather(t0);
             for (int j = 0; ok && j < ntiles; ++j) {
                 ok = send(j);
                 if (ok && j + kStages - 1 < ntiles) ok = gather(j + kStages - 1);
             }
-        } else {  // FP8 records: the converter warps fill the stages; the producers prefetch, then send
-            prefetch_rows(pw * 32 + lane, kProducers * 32);
-            bool ok = true;
-            for (int j = 0; ok && j < ntiles; ++j) ok = send(j);
+            cp_async_wait<0>();  // nothing of this thread's is still in flight when the CTA exits
         }
-    } else if (kKv8 && warp >= kWarpConv) {
+    } else if (!kKv8 && warp >= kWarpFill) {
+        // ------------------------------------------------------------- bf16 row gathers
+        // Filler warp fw copies rows fw, fw + 3, ... < 48 of tile t once stage t % 4 is free: 16-byte
+        // cp.async per lane (lane = chunk lane / 8, 16-byte group lane % 8; CTA 1's fifth chunk
+        // from lanes 0..7) into the 128-byte-swizzled layout, from the physical cache rows
+        // resolved up front; rows with no position read as zeros. The fillers run up to four
+        // tiles ahead of the tensor core. They also request rows into L2 ahead of their copies, in
+        // windows of 12 tiles: tiles 4..15 once the first four tiles are issued (the stages start
+        // free; issued earlier, those requests would queue ahead of the first tiles' copies), then
+        // every 8 tiles the 12 tiles from 5 ahead on. Per-tile requests a few tiles ahead leave the
+        // copies waiting on HBM; all of a long split's rows at once overrun L2 when many CTAs read
+        // rows of one long context.
+        const int fw = warp - kWarpFill;
+        const uint8_t* kv = static_cast<const uint8_t*>(a.kv) + c0 * 128;
+        const int c = lane >> 3, g = lane & 7;  // chunk and 16-byte group this lane copies
+        const int last_free = min(kStages, ntiles) - 1;
+        for (int tile = 0; tile < ntiles; ++tile) {
+            const int st = tile % kStages;
+            const bool got = mbar_wait(smem_u32(&S.empty[st]), ((tile / kStages) & 1) ^ 1, abort_flag, a.err);
+            if (!__all_sync(0xFFFFFFFFu, got)) break;
+            const uint32_t base = sKv + st * kStageBytes;
+#pragma unroll 2
+            for (int r = fw; r < kFillRows; r += kFillThreads / 32) {
+                const int p = phys_s[tile * kRows + r];
+                const uint8_t* src = p >= 0 ? kv + static_cast<int64_t>(p) * (kD * 2) : kv;
+                const uint32_t nb = p >= 0 ? 16u : 0u;  // 0: zero-fill
+                const uint32_t rowoff = static_cast<uint32_t>(r * 128);
+                cp_async16(base + c * kChunkBytes + rowoff + ((g ^ (r & 7)) << 4), src + (p >= 0 ? c * 128 + g * 16 : 0), nb);
+                if (nchunks == 5 && lane < 8)
+                    cp_async16(base + 4 * kChunkBytes + rowoff + ((lane ^ (r & 7)) << 4),
+                               src + (p >= 0 ? 4 * 128 + lane * 16 : 0), nb);
+            }
+            cp_async_arrive_noinc(smem_u32(&S.full[st]));  // once this thread's copies have landed
+            if (tile >= last_free && (tile - last_free) % 8 == 0) {  // the next L2 window (see above)
+                const int w0 = tile == last_free ? kStages : tile + 5;
+                prefetch_rows(w0 * kRows + fw * 32 + lane, min(nrows, (w0 + 12) * kRows), kFillThreads);
+            }
+        }
+        cp_async_wait<0>();  // nothing of this thread's is still in flight when the CTA exits
+    } else if (kKv8 && warp >= kWarpFill) {
         // ------------------------------------------------------------- FP8 converters
         // issue(t): once operand stage t % 4 is free, 16-byte cp.async of the codes of tile t (this
         // CTA's columns; 16 codes per copy, groups spread over the 96 converter threads) into the
@@ -361,11 +402,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKv8 ? kThreads8 : k
         // swizzled bf16 layout (code * scale in fp32, bf16 RNE). A tile is converted one tile after
         // its copies were issued. Every converter takes every barrier, so a wait that gives up
         // only stops the work.
-        constexpr int kPT = kConvThreads;
+        constexpr int kPT = kFillThreads;
         constexpr int kGPT = (kCodeBytes / 16 + kPT - 1) / kPT;  // 16-code groups per thread and tile (<= 14)
         const int gpr = nchunks * 4;                               // groups per row of this CTA: 16 or 20
         const int ngroups = kRows * gpr;
-        const int pt = (warp - kWarpConv) * 32 + lane;
+        const int pt = (warp - kWarpFill) * 32 + lane;
         const uint8_t* kvb = static_cast<const uint8_t*>(a.kv);
         int issued = 0;
         bool dead = false;
@@ -401,7 +442,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKv8 ? kThreads8 : k
                 codes[k] = (!dead && gi < ngroups) ? *reinterpret_cast<const uint4*>(stage + kCodeOff + gi * 16)
                                                    : make_uint4(0u, 0u, 0u, 0u);
             }
-            dead = named_bar_or(5, kConvThreads, dead);  // every code is in registers: the stage may be overwritten
+            dead = named_bar_or(5, kFillThreads, dead);  // every code is in registers: the stage may be overwritten
             if (dead) return;
 #pragma unroll
             for (int k = 0; k < kGPT; ++k) {
@@ -431,8 +472,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKv8 ? kThreads8 : k
             }
         }
         cp_async_wait<0>();  // nothing of this thread's is still in flight when the CTA exits
-    } else if (!kKv8 && warp == 9) {
-        prefetch_rows(lane, 32);
     } else if (warp == 8) {
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0 && ntiles > 0) {
@@ -721,7 +760,7 @@ static bool launch_attn_tc_typed(const AttnArgs& a, const CUtensorMap& map_q, cu
     const size_t smem = tcattn::Layout<kKv8>::kSmemBytes;
     if (!set_max_dynamic_smem(reinterpret_cast<const void*>(tcattn::attn_tc_kernel<kKv8>), smem)) return false;
     return launch_kernel(a.after_own_kernel != 0, tcattn::attn_tc_kernel<kKv8>, dim3(2 * a.S, a.T),
-                         dim3(kKv8 ? tcattn::kThreads8 : tcattn::kThreads), smem, s, a, map_q);
+                         dim3(tcattn::kThreads), smem, s, a, map_q);
 }
 
 bool launch_attn_tc(const AttnArgs& a, cudaStream_t s, int* launches) {

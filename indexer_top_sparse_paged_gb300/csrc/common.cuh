@@ -545,8 +545,11 @@ __device__ __forceinline__ void store_bf16_row_mx(uint8_t* stage, int r, const u
 // sample key lies above that key only if the sample holds kEstMargin times its expected share of
 // them; for independent draws that is more than 9 standard deviations out at K / n = 0.085 (decode
 // rows of 24K keys) and far rarer for longer rows, where the rank floor dominates.
+// Segments shorter than kEstMinTiles end too soon after their sample for the estimate's select to
+// pay for itself (measured: batch-32 decode rows split into segments of 8..15 tiles took longer
+// with an estimate than without).
 constexpr int kEstTiles = 2;
-constexpr int kEstMinTiles = 8;
+constexpr int kEstMinTiles = 16;
 constexpr float kEstMargin = 3.0f;
 constexpr uint32_t kEstMinRank = 16;
 

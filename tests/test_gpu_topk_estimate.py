@@ -68,7 +68,7 @@ def _planted_segment_start(case, n_front: int = 256, alpha: float = 30.0):
         t = int(np.searchsorted(prefix, x, side="right") - 1)
         p0, p1 = int(prefix[t]), int(prefix[t + 1])
         owners = ((p1 - 1 + 1) * G - 1) // total - ((p0 + 1) * G - 1) // total + 1
-        if x > p0 and min(tb(c + 1), p1) - x >= 8 and owners <= 8:
+        if x > p0 and min(tb(c + 1), p1) - x >= 16 and owners <= 8:  # a segment long enough to be sampled
             s0 = (x - p0) * 128
             bs = case.spec.block_size
             u = (case.w[t][:, None].astype(np.float64) * np_bf16(case.q_I[t])).sum(0)
