@@ -313,9 +313,11 @@ struct TopkGroup {
         return off + __popc(ballot & ((1u << lane) - 1u));
     }
 
-    // Collective: writes the min(count, K) largest keys of buf, in buffer (= position) order, to
-    // dst (shared or global; may be buf itself) and returns how many. Each thread loads its
-    // contiguous chunk into registers first, so writing over buf is safe.
+    // Collective: writes the min(count, K) largest keys of buf that are >= the admission threshold,
+    // in buffer (= position) order, to dst (shared or global; may be buf itself) and returns how
+    // many. Each thread loads its contiguous chunk into registers first, so writing over buf is
+    // safe. The keys below the threshold are those of an estimate's sample: dropping them is safe
+    // under the merge's estimate check (it counts only keys >= the largest estimate).
     __device__ uint32_t select_to(uint64_t* dst, int max_passes = 64) {
         sync();  // every push's writes to buf are visible
         const uint32_t n = count;
@@ -327,6 +329,7 @@ struct TopkGroup {
         for (int j = 0; j < PER; ++j) keys[j] = (static_cast<uint32_t>(j) < cnt) ? buf[c0 + j] : 0ull;
         uint64_t thr = 0ull;
         if (n > K) thr = reg_radix_threshold<NT, PER>(keys, cnt, K, hist, ctl, tid, bar_id, max_passes);
+        if (theta > thr) thr = theta;  // keys below the admission threshold (e.g. a sample's) never qualify
         uint32_t mine = 0;
 #pragma unroll
         for (int j = 0; j < PER; ++j) mine += (static_cast<uint32_t>(j) < cnt && keys[j] >= thr) ? 1u : 0u;
@@ -336,7 +339,7 @@ struct TopkGroup {
         for (int j = 0; j < PER; ++j) {
             if (static_cast<uint32_t>(j) < cnt && keys[j] >= thr) dst[o++] = keys[j];
         }
-        if (n > K) theta = thr;
+        theta = thr;
         return kept;
     }
 
@@ -540,27 +543,29 @@ __device__ __forceinline__ void store_bf16_row_mx(uint8_t* stage, int r, const u
 
 // Sample estimate of a row's K-th key (streaming Top-K of the decode indexer): after the first
 // kEstTiles tiles of a segment of at least kEstMinTiles tiles, the admission threshold rises to
-// the r-th largest of the sampled keys with r = ceil(sample * kEstMargin * K / n) (n = the row's
-// causal keys), at least kEstMinRank. With K / n of the row's keys above its K-th key, the r-th
-// sample key lies above that key only if the sample holds kEstMargin times its expected share of
-// them; for independent draws that is more than 9 standard deviations out at K / n = 0.085 (decode
-// rows of 24K keys) and far rarer for longer rows, where the rank floor dominates.
+// the r-th largest of the sampled keys. The sample's count X of keys from the row's Top-K is
+// hypergeometric with mean mu = sample * K / n (n = the row's causal keys), and the r-th sample key
+// lies above the row's K-th key only if X >= r. r = ceil(mu + 6.5 sqrt(mu) + 6) keeps that
+// probability below 4e-11 for every row length (the exact tail, evaluated for rows of 2K to 4M keys
+// and samples of 256 to 512 keys) while admitting as few keys as that allows; a fixed multiple of
+// mu admits more keys on short rows and fails far more often on rows of 30K to 130K keys, where mu
+// is small. No estimate applies when it would admit three quarters of the keys or more. A sample
+// of four tiles (512 keys) puts r closer to mu than two tiles do: measured, the batch-32 decode
+// indexer call 79 -> 74 us and the 1M-key row 113 -> 102 us (with the flush dropping the sample's
+// keys below the estimate).
 // Segments shorter than kEstMinTiles end too soon after their sample for the estimate's select to
 // pay for itself (measured: batch-32 decode rows split into segments of 8..15 tiles took longer
 // with an estimate than without).
-constexpr int kEstTiles = 2;
+constexpr int kEstTiles = 4;
 constexpr int kEstMinTiles = 16;
-constexpr float kEstMargin = 3.0f;
-constexpr uint32_t kEstMinRank = 16;
 
 // The rank of the estimate for a sample of `sample` valid keys of a row of n causal keys, or 0
-// when no estimate applies (it would admit nearly everything).
+// when no estimate applies.
 __device__ __forceinline__ uint32_t estimate_rank(uint32_t sample, int n, int K) {
     if (n <= K) return 0;
-    const float q = kEstMargin * static_cast<float>(K) / static_cast<float>(n);
-    uint32_t r = static_cast<uint32_t>(ceilf(q * static_cast<float>(sample)));
-    r = max(r, kEstMinRank);
-    return (q < 0.75f && r < sample) ? r : 0u;
+    const float mu = static_cast<float>(sample) * static_cast<float>(K) / static_cast<float>(n);
+    const uint32_t r = static_cast<uint32_t>(ceilf(mu + 6.5f * sqrtf(mu) + 6.0f));
+    return (4 * r < 3 * sample) ? r : 0u;
 }
 
 struct IndexerArgs {

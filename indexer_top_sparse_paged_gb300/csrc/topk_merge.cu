@@ -352,6 +352,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(IndexerArgs a
         // 4. threshold: exactly K keys are >= thr (thr = 0 keeps every candidate when n <= K)
         uint64_t thr = 0ull;
         if (n > K) thr = reg_radix_threshold<kMergeThreads, kPer>(keys, cnt, K, hist, &ctl, tid, 1);
+        if (est > thr) thr = est;  // keys below an estimate the row used never reach its Top-K (see 3.)
 
         // 5. the kept keys in candidate order (= ascending position), compacted in shared memory
         //    (over the staged candidates: every thread has its keys in registers) and written out

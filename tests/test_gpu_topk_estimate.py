@@ -4,8 +4,9 @@ a segment's sample is not representative of the row, the merge finds fewer than 
 above the estimates and recomputes the row exactly. Both outcomes must match the fp64 oracle.
 
 The planted rows put keys with very large scores in the first two tiles of a 200,000-key row, so
-the first segment's estimate lies far above the row's K-th key and that segment turns away the
-ordinary keys that belong to the row's Top-K."""
+the first segment's estimate (the r-th largest of its first four tiles, r far below the 256
+planted keys) lies far above the row's K-th key and that segment turns away the ordinary keys
+that belong to the row's Top-K."""
 import numpy as np
 import pytest
 
