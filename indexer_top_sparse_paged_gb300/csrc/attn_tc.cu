@@ -73,6 +73,7 @@ constexpr uint32_t kIdescPV = idesc_f16(128, kDVH, 1u, 0u, 1u);
 
 struct Smem {
     uint64_t full[kStagesMax], empty[kStagesMax];
+    uint64_t codes_full[kStagesMax];  // FP8 records: a tile's codes have landed in its stage
     uint64_t s_full[2], p_full[2], s_free[2];
     uint64_t qfull, o_full, mma_done;
     uint64_t xfull[2], xempty[2];  // both arrived on by the peer: its partial landed / it consumed ours
@@ -157,6 +158,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         for (int i = 0; i < kStages; ++i) {
             mbar_init(smem_u32(&S.full[i]), kKv8 ? kFillThreads : kFillThreads + kProducers * 32);  // every filling thread arrives
             mbar_init(smem_u32(&S.empty[i]), 1);
+            mbar_init(smem_u32(&S.codes_full[i]), kProducers * 32);  // FP8 records: every producer thread arrives
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&S.s_full[i]), 1);
@@ -316,9 +318,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             return true;
         };
         if constexpr (kKv8) {
-            prefetch_rows(pw * 32 + lane, nrows, kProducers * 32);
+            // FP8 records: the producers copy the codes of this CTA's columns of every tile into the
+            // upper half of its stage (rows pw, pw + 4, ...: lane q < 16 or 20 copies 16-byte group q
+            // of the row, group index row * groups-per-row + q; rows with no position read as
+            // zeros), three tiles ahead, in the gaps between sends, as for bf16 rows; the filler
+            // warps widen them. L2 prefetches of later tiles' records go out in windows of 12
+            // tiles once the first three tiles' copies are queued.
+            const int gpr = nchunks * 4;
+            const uint8_t* kvb = static_cast<const uint8_t*>(a.kv);
+            auto gather_codes = [&](int tile) -> bool {
+                const int st = tile % kStages;
+                const bool got = mbar_wait(smem_u32(&S.empty[st]), ((tile / kStages) & 1) ^ 1, abort_flag, a.err);
+                if (!__all_sync(0xFFFFFFFFu, got)) return false;
+                const uint32_t base = sKv + st * kStageBytes + kCodeOff;
+#pragma unroll 4
+                for (int k = 0; k < kRows / kProducers; ++k) {
+                    const int r = kProducers * k + pw;
+                    const int p = phys_s[tile * kRows + r];
+                    if (lane < gpr)
+                        cp_async16(base + (r * gpr + lane) * 16,
+                                   p >= 0 ? kvb + static_cast<int64_t>(p) * kRecBytes + c0 * 64 + lane * 16 : kvb,
+                                   p >= 0 ? 16u : 0u);
+                }
+                cp_async_arrive_noinc(smem_u32(&S.codes_full[st]));  // once this thread's copies have landed
+                return true;
+            };
+            int pf_end = min(kStages - 1, ntiles);  // tiles below pf_end are copied or requested
+            auto prefetch_window = [&]() {           // the records of the next 12 tiles
+                prefetch_rows(pf_end * kRows + pw * 32 + lane, min(nrows, (pf_end + 12) * kRows), kProducers * 32);
+                pf_end += 12;
+            };
             bool ok = true;
-            for (int j = 0; ok && j < ntiles; ++j) ok = send(j);
+            for (int t0 = 0; ok && t0 < pf_end; ++t0) ok = gather_codes(t0);
+            prefetch_window();
+            for (int j = 0; ok && j < ntiles; ++j) {
+                ok = send(j);
+                const int tn = j + kStages - 1;
+                if (ok && tn < ntiles) {
+                    ok = gather_codes(tn);
+                    if (pf_end < ntiles && pf_end - tn <= 5) prefetch_window();  // the next window, ahead of its copies
+                }
+            }
+            cp_async_wait<0>();  // nothing of this thread's is still in flight when the CTA exits
         } else {
             // bf16 rows: rows 48..63 of every tile are the producers' (4 per warp), gathered as
             // the fillers gather theirs, in the gaps between sends: gather(t) runs once stage t % 4
@@ -394,46 +435,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         cp_async_wait<0>();  // nothing of this thread's is still in flight when the CTA exits
     } else if (kKv8 && warp >= kWarpFill) {
         // ------------------------------------------------------------- FP8 converters
-        // issue(t): once operand stage t % 4 is free, 16-byte cp.async of the codes of tile t (this
-        // CTA's columns; 16 codes per copy, groups spread over the 96 converter threads) into the
-        // stage's upper half, and each group's tile scale into registers; convert(t): every thread
-        // loads the codes it copied, the converters meet at a named barrier (the stage is then
-        // overwritten in place), and each widens its groups, times their scale, into the 128-byte-
-        // swizzled bf16 layout (code * scale in fp32, bf16 RNE). A tile is converted one tile after
-        // its copies were issued. Every converter takes every barrier, so a wait that gives up
-        // only stops the work.
+        // convert(t): once tile t's codes have landed in the upper half of its stage (the producers
+        // copy them), every thread loads the 16-code groups it converts, the converters meet at a
+        // named barrier (the stage is then overwritten in place), and each widens its groups, times
+        // their tile scale, into the 128-byte-swizzled bf16 layout (code * scale in fp32, bf16
+        // RNE). Each group's scale is loaded one tile ahead. Every converter takes every barrier,
+        // so a wait that gives up only stops the work.
         constexpr int kPT = kFillThreads;
         constexpr int kGPT = (kCodeBytes / 16 + kPT - 1) / kPT;  // 16-code groups per thread and tile (<= 14)
         const int gpr = nchunks * 4;                               // groups per row of this CTA: 16 or 20
         const int ngroups = kRows * gpr;
         const int pt = (warp - kWarpFill) * 32 + lane;
         const uint8_t* kvb = static_cast<const uint8_t*>(a.kv);
-        int issued = 0;
         bool dead = false;
-        auto issue = [&](int tile, float (&sc)[kGPT]) {
-            const int st = tile % kStages;
-            const bool got = mbar_wait(smem_u32(&S.empty[st]), ((tile / kStages) & 1) ^ 1, abort_flag, a.err);
-            if (!__all_sync(0xFFFFFFFFu, got)) dead = true;
-            const uint32_t base = sKv + st * kStageBytes + kCodeOff;
+        auto load_scales = [&](int tile, float (&sc)[kGPT]) {
 #pragma unroll
             for (int k = 0; k < kGPT; ++k) {
                 const int gi = pt + k * kPT;
                 sc[k] = 0.0f;
-                if (!dead && gi < ngroups) {
+                if (gi < ngroups) {
                     const int r = gi / gpr, q = gi - r * gpr;
                     const int p = phys_s[tile * kRows + r];
-                    const uint8_t* rec = kvb + static_cast<int64_t>(p) * kRecBytes;
-                    cp_async16(base + gi * 16, p >= 0 ? rec + c0 * 64 + q * 16 : kvb, p >= 0 ? 16u : 0u);  // 0: zero-fill
-                    if (p >= 0) sc[k] = __ldg(reinterpret_cast<const float*>(rec + kD) + ((c0 * 64 + q * 16) >> 7));
+                    if (p >= 0)
+                        sc[k] = __ldg(reinterpret_cast<const float*>(kvb + static_cast<int64_t>(p) * kRecBytes + kD) +
+                                      ((c0 * 64 + q * 16) >> 7));
                 }
             }
-            cp_async_commit();
-            ++issued;
         };
         auto convert = [&](int tile, const float (&sc)[kGPT]) {
             const int st = tile % kStages;
-            if (issued > tile + 1) cp_async_wait<1>();  // the tile's codes have landed (the next tile's may not)
-            else cp_async_wait<0>();
+            const bool got = mbar_wait(smem_u32(&S.codes_full[st]), (tile / kStages) & 1, abort_flag, a.err);
+            if (!__all_sync(0xFFFFFFFFu, got)) dead = true;
             uint8_t* stage = smem + kOffKv + st * kStageBytes;
             uint4 codes[kGPT];
 #pragma unroll
@@ -462,12 +494,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         };
         // two tiles per iteration, so that each tile's scales sit in a statically named array
         float sc0[kGPT], sc1[kGPT];
-        if (ntiles > 0) issue(0, sc0);
+        if (ntiles > 0) load_scales(0, sc0);
         for (int t = 0; t < ntiles; t += 2) {
-            if (t + 1 < ntiles) issue(t + 1, sc1);
+            if (t + 1 < ntiles) load_scales(t + 1, sc1);
             convert(t, sc0);
             if (t + 1 < ntiles) {
-                if (t + 2 < ntiles) issue(t + 2, sc0);
+                if (t + 2 < ntiles) load_scales(t + 2, sc0);
                 convert(t + 1, sc1);
             }
         }
