@@ -35,8 +35,8 @@
 // lane quarter; bf16 rows: gather a quarter of each tile), warp 8 TMEM allocator + MMA issuer
 // (+ the TMA loads of the query), warps 13-15 fill the operand stages (bf16 rows: cp.async
 // gathers of the other three quarters, with L2 prefetches of later tiles' rows in windows of 12
-// tiles; FP8 records: stage the codes and widen them in place, the producers having requested
-// every record into L2 at the start).
+// tiles when rows are split; FP8 records: widen the codes that the producers copied into the
+// stage).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -323,7 +323,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             // of the row, group index row * groups-per-row + q; rows with no position read as
             // zeros), three tiles ahead, in the gaps between sends, as for bf16 rows; the filler
             // warps widen them. L2 prefetches of later tiles' records go out in windows of 12
-            // tiles once the first three tiles' copies are queued.
+            // tiles once the first three tiles' copies are queued (when the call splits its rows).
             const int gpr = nchunks * 4;
             const uint8_t* kvb = static_cast<const uint8_t*>(a.kv);
             auto gather_codes = [&](int tile) -> bool {
@@ -350,7 +350,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
             };
             bool ok = true;
             for (int t0 = 0; ok && t0 < pf_end; ++t0) ok = gather_codes(t0);
-            prefetch_window();
+            if (a.S == 1) pf_end = ntiles;  // one split per row: no L2 prefetch (as for bf16 rows)
+            else prefetch_window();
             for (int j = 0; ok && j < ntiles; ++j) {
                 ok = send(j);
                 const int tn = j + kStages - 1;
@@ -400,12 +401,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         // cp.async per lane (lane = chunk lane / 8, 16-byte group lane % 8; CTA 1's fifth chunk
         // from lanes 0..7) into the 128-byte-swizzled layout, from the physical cache rows
         // resolved up front; rows with no position read as zeros. The fillers run up to four
-        // tiles ahead of the tensor core. They also request rows into L2 ahead of their copies, in
-        // windows of 12 tiles: tiles 4..15 once the first four tiles are issued (the stages start
-        // free; issued earlier, those requests would queue ahead of the first tiles' copies), then
-        // every 8 tiles the 12 tiles from 5 ahead on. Per-tile requests a few tiles ahead leave the
-        // copies waiting on HBM; all of a long split's rows at once overrun L2 when many CTAs read
-        // rows of one long context.
+        // tiles ahead of the tensor core. When the call splits its rows (S > 1: few rows, each
+        // CTA's rows its own) they also request rows into L2 ahead of their copies, in windows of 12
+        // tiles: tiles 4..15 once the first four tiles are issued (the stages start free; issued
+        // earlier, those requests would queue ahead of the first tiles' copies), then every 8 tiles
+        // the 12 tiles from 5 ahead on. Per-tile requests a few tiles ahead leave the copies waiting
+        // on HBM. With one split per row (T >= 76 on 152 SMs: prefill chunks, whose rows share most
+        // of their selected cache rows with other CTAs') no prefetch: measured, it cost 16% in a
+        // 2048-row chunk over one 131K-token context and 6% in a 2 x 4096-row prefill.
         const int fw = warp - kWarpFill;
         const uint8_t* kv = static_cast<const uint8_t*>(a.kv) + c0 * 128;
         const int c = lane >> 3, g = lane & 7;  // chunk and 16-byte group this lane copies
@@ -427,7 +430,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                                src + (p >= 0 ? 4 * 128 + lane * 16 : 0), nb);
             }
             cp_async_arrive_noinc(smem_u32(&S.full[st]));  // once this thread's copies have landed
-            if (tile >= last_free && (tile - last_free) % 8 == 0) {  // the next L2 window (see above)
+            if (a.S > 1 && tile >= last_free && (tile - last_free) % 8 == 0) {  // the next L2 window (see above)
                 const int w0 = tile == last_free ? kStages : tile + 5;
                 prefetch_rows(w0 * kRows + fw * 32 + lane, min(nrows, (w0 + 12) * kRows), kFillThreads);
             }
