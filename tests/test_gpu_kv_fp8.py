@@ -46,6 +46,13 @@ def test_prefill_rows():
     _check(W.generate(spec, seed=222))
 
 
+def test_prefill_rows_one_split_per_row():
+    """Enough rows (T = 100) that every row gets one split of 16 tiles: the path without L2
+    prefetches, where the producers copy every tile's codes between their sends."""
+    spec = small_spec("bf16", [6000, 4500], 1024, new_tokens=[60, 40], kv="fp8")
+    _check(W.generate(spec, seed=225), rows=list(range(0, 100, 7)))
+
+
 def test_cuda_core_shapes():
     """Small head shapes run on the CUDA cores: a row of 80 elements is one partial tile, a row of
     272 two full tiles and one of 16."""
