@@ -15,8 +15,9 @@
 //      store it into the other CTA's shared memory with st.async (completion counted in bytes on
 //      the receiver's mbarrier; the sender never waits); the softmax adds the two rounded
 //      partials, which both CTAs do with identical operands, so both see the same logits,
-//   4. runs the online softmax (one thread per head, lazy rescaling of O when a head's running
-//      maximum grows by more than 2^8) and writes P as bf16 over its S in tensor memory,
+//   4. runs the online softmax (two threads per head, one per half of the tile's rows, sharing the
+//      running maximum; lazy rescaling of O when a head's running maximum grows by more than
+//      2^8) and writes P as bf16 over its S in tensor memory,
 //   5. accumulates O_r[128 x 256] += P . V_r with V_r = its 256 value columns (CTA 0: values
 //      0..255, CTA 1: values 256..511 -- both inside the columns it already holds).
 // With an FP8 latent cache (records of e4m3 codes with one fp32 scale per 128 elements; §3: FP8
