@@ -35,7 +35,7 @@
 // rows 32..63 and O columns 128..255), warps 4-7 producers (send the partial logits of their TMEM
 // lane quarter; bf16 rows: gather a quarter of each tile), warp 8 TMEM allocator + MMA issuer
 // (+ the TMA loads of the query), warps 13-15 fill the operand stages (bf16 rows: cp.async
-// gathers of the other three quarters, with L2 prefetches of later tiles' rows in windows of 12
+// gathers of the other three quarters, with L2 prefetches of later tiles' rows in windows of 8
 // tiles when rows are split; FP8 records: widen the codes that the producers copied into the
 // stage).
 #include <cuda_bf16.h>
@@ -403,11 +403,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
         // from lanes 0..7) into the 128-byte-swizzled layout, from the physical cache rows
         // resolved up front; rows with no position read as zeros. The fillers run up to four
         // tiles ahead of the tensor core. When the call splits its rows (S > 1: few rows, each
-        // CTA's rows its own) they also request rows into L2 ahead of their copies, in windows of 12
-        // tiles: tiles 4..15 once the first four tiles are issued (the stages start free; issued
-        // earlier, those requests would queue ahead of the first tiles' copies), then every 8 tiles
-        // the 12 tiles from 5 ahead on. Per-tile requests a few tiles ahead leave the copies waiting
-        // on HBM. With one split per row (T >= 76 on 152 SMs: prefill chunks, whose rows share most
+        // CTA's rows its own) they also request rows into L2 ahead of their copies, in windows of 8
+        // tiles: tiles 4..11 once the first four tiles are issued (the stages start free; issued
+        // earlier, those requests would queue ahead of the first tiles' copies), then window k
+        // (tiles 4 + 8k ..) five tiles before its first copy. Per-tile requests a few tiles ahead
+        // leave the copies waiting on HBM; windows of 12 tiles queued more than the copies needed
+        // (52.2 -> 50.1 us at batch 32 with 8). With one split per row (T >= 76 on 152 SMs: prefill chunks, whose rows share most
         // of their selected cache rows with other CTAs') no prefetch: measured, it cost 16% in a
         // 2048-row chunk over one 131K-token context and 6% in a 2 x 4096-row prefill.
         const int fw = warp - kWarpFill;
@@ -431,9 +432,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads)
                                src + (p >= 0 ? 4 * 128 + lane * 16 : 0), nb);
             }
             cp_async_arrive_noinc(smem_u32(&S.full[st]));  // once this thread's copies have landed
-            if (a.S > 1 && tile >= last_free && (tile - last_free) % 8 == 0) {  // the next L2 window (see above)
+            if (a.S > 1 && (tile == last_free || (tile > last_free && (tile + 1) % 8 == 0))) {  // the next window
                 const int w0 = tile == last_free ? kStages : tile + 5;
-                prefetch_rows(w0 * kRows + fw * 32 + lane, min(nrows, (w0 + 12) * kRows), kFillThreads);
+                prefetch_rows(w0 * kRows + fw * 32 + lane, min(nrows, (w0 + 8) * kRows), kFillThreads);
             }
         }
         cp_async_wait<0>();  // nothing of this thread's is still in flight when the CTA exits
