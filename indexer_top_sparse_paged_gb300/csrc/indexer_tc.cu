@@ -12,14 +12,16 @@
 // paged cache; "Engineering Path for Day-0 Adaptation ..." §3.1: the scoring reuses a matrix
 // multiplication).
 //
-// Roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
-// warps 2..5 = epilogue (TMEM lane quarter = warp % 4). Pipelines: 5 smem stages of 32 KB (the
-// HBM round trip under full load is ~3.7 us: 160 KB in flight per SM keeps it busy), 4 TMEM
-// accumulators of 64 columns, one query buffer.
+// Roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer, warps 2..5 =
+// scoring (TMEM lane quarter = warp % 4), warps 6..9 = streaming Top-K, fed by a ring of 16 score
+// tiles in shared memory. Pipelines: 3 smem stages of 32 KB (96 KB in flight per SM keeps the
+// stream at full rate; deeper rings only lengthen HBM's queue), 4 TMEM accumulators of 64
+// columns, one query buffer.
 //
 // FP8 keys (320 threads): the TMA lands the e4m3 codes of a tile (16 KB) in a staging ring of 6
-// stages, and four more warps (6..9, one key row per thread) widen them to bf16 in the swizzled
-// operand layout of a 2-stage ring that the MMA reads. Every e4m3 value is exactly a bf16 value,
+// stages, warps 6..9 (one key row per thread) widen them to bf16 in the swizzled operand layout
+// of a 2-stage ring that the MMA reads, and warps 2..5 both score and select (no score ring).
+// Every e4m3 value is exactly a bf16 value,
 // so the product is still exact-input bf16 x bf16 -> fp32; the block's scale multiplies the
 // accumulator in the epilogue, before the ReLU:
 //     S[s] = sum_j w_j * max(0, scale_blk * D[s, j]).
