@@ -124,10 +124,38 @@ def measured_tensor_peak():
 TRAFFIC_SOURCES = ("dsa_api.cu", "internal.h", "common.cuh", "ptx.cuh", "indexer_tc.cu", "topk_merge.cu")
 
 
+def code_only(src: str) -> str:
+    """C/C++/CUDA source without its comments, trailing blanks and empty lines (string and
+    character literals are kept whole), so that a comment edit leaves the digest unchanged."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_digest() -> str:
+    """SHA-256 prefix over the code (comments removed) of every source of the measured call."""
     h = hashlib.sha256()
     for f in TRAFFIC_SOURCES:
-        h.update(open(os.path.join(ROOT, "indexer_top_sparse_paged_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "indexer_top_sparse_paged_gb300", "csrc", f), encoding="utf-8").read()
+        h.update(code_only(src).encode())
     return h.hexdigest()[:16]
 
 
