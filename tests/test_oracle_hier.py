@@ -56,7 +56,7 @@ def _brute_hier(case, t, n_sel):
     return np.sort(pos[order]), blocks
 
 
-@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8"])
+@pytest.mark.parametrize("mode", ["bf16", "bf16_kfp8", "mxfp8"])
 def test_hierarchical_matches_brute_force(mode):
     spec = small_spec(mode, [700, 2000, 130], 96, H_I=4, d_I=32, new_tokens=[1, 3, 1])
     case = W.generate(spec, seed=402)
