@@ -115,7 +115,16 @@ def make_dims(mode: str, B: int, max_blocks: int, num_blocks: int, H_I: int, d_I
 
 
 def _p(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """The device address of a tensor argument (None: NULL). The library reads and writes densely
+    packed data through raw device pointers, so a strided view or a host tensor is refused here:
+    passed on, it would be read with the wrong layout or dereferenced on the GPU as a bad address."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous (the library reads densely packed rows)")
+    if not t.is_cuda:
+        raise ValueError("tensor arguments must be CUDA tensors (the library takes device pointers)")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream=None):

@@ -221,3 +221,29 @@ def test_fp8_latent_flag_checks(L):
                            FAKE, FAKE, FAKE, FAKE, 2, ctypes.c_float(0.04), FAKE, None, FAKE, 1 << 30, None)
     assert st == 2
     assert dsa.kv_record_bytes(576) == 608 and dsa.kv_record_bytes(128) == 144 and dsa.kv_record_bytes(80) == 96
+
+
+def test_binding_refuses_host_and_strided_tensors(L):
+    """The binding hands raw device pointers to the library: a host tensor or a strided view is
+    refused in Python, before anything reaches the library or a GPU."""
+    import torch
+    d = _dims(B=1, K=64)
+    T = 1
+    ws = torch.zeros(1024, dtype=torch.uint8)
+    q_I = torch.zeros((T, 64, 128), dtype=torch.bfloat16)
+    w = torch.zeros((T, 64), dtype=torch.float32)
+    k_I = torch.zeros((8, 64, 128), dtype=torch.bfloat16)
+    bt = torch.zeros((1, 4), dtype=torch.int32)
+    sl = torch.ones(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        dsa.indexer_topk(d, q_I, w, k_I, None, bt, sl, ws=ws)
+    with pytest.raises(ValueError, match="contiguous"):
+        dsa.indexer_topk(d, q_I.transpose(1, 2), w, k_I, None, bt, sl, ws=ws)
+    q = torch.zeros((T, 128, 576), dtype=torch.bfloat16)
+    kv = torch.zeros((8, 64, 576), dtype=torch.bfloat16)
+    idx = torch.zeros((T, 64), dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        dsa.sparse_attn(d, q, kv, bt, sl, idx, 0.04, ws=ws)
+    with pytest.raises(ValueError, match="contiguous"):
+        dsa.decode(d, q_I[:, ::2], w, k_I, None, bt, sl, q, kv, 0.04, ws=ws)
+    assert L.dsa_last_launch_count() == 0
