@@ -9,7 +9,10 @@
 //        keys held in registers. A group that covers the whole row writes its positions in
 //        ascending order, then -1 up to K; any other group writes its keys back over its first
 //        list, and the last of 8 sibling groups to finish (a counter per parent group) goes on
-//        to merge the parent's lists, up to the row's root ("Engineering Path for Day-0
+//        to merge the parent's lists, up to the row's root. Lists of long segments were
+//        filtered by a sample estimate of the row's K-th key; the root checks that at least K
+//        candidates reach every estimate used and otherwise selects the row again from all of
+//        its keys (rescore_row) ("Engineering Path for Day-0
 //        Adaptation ..." §3.1: Top-K filtering over large candidate sets is split to match the
 //        hardware's thread organisation; "Adapting GPU Software Stacks ..." §3.1: the index
 //        format is aligned with the attention that consumes it, so no reordering is needed).
