@@ -17,6 +17,16 @@ Entry points (same names as the C ABI):
   per-block summary keys.
 * :func:`indexer_topk_noalloc` -- :func:`indexer_topk` with the library's static scratch instead of
   a workspace, for callers that cannot allocate device memory.
+
+Every tensor argument is a contiguous CUDA tensor in the layout ``include/dsa.h`` gives; the
+calls are enqueued on the current stream (or ``stream=``). A decode step over a batch of B
+sequences, bf16 everywhere, 64 indexer heads of 128, 128 heads over 576-wide latent rows::
+
+    dims = make_dims("bf16", B, max_blocks, num_blocks, H_I=64, d_I=128, H=128, d=576, d_v=512, K=2048)
+    ws = workspace(dims, B)                      # sized for calls of B rows (the library checks it)
+    idx, out, lse = decode(dims, q_I, w, k_I_cache, None, block_table, seq_lens, q, kv_cache,
+                           576 ** -0.5, ws=ws)  # idx [B][K] int32, out [B][128][512] bf16
+    assert read_error(ws) == 0                   # device-side fault bits (synchronises)
 """
 from __future__ import annotations
 
