@@ -87,3 +87,23 @@ def test_planted_block_is_chosen():
     idx, blocks = oracle.hierarchical_topk(case, n_sel=1)
     assert blocks[0].tolist() == [7]
     assert np.all((idx[0] >= 7 * 64) & (idx[0] < 8 * 64))
+
+
+def test_equal_keys_take_the_lowest_blocks_and_positions():
+    """Every key equal: all summaries score alike and so do all tokens, so the coarse stage keeps
+    the lowest blocks and the fine stage the lowest positions, never past the row's own position
+    (the 70-token sequence's rows have fewer causal tokens than K)."""
+    spec = small_spec("bf16", [300, 200, 70], 100, new_tokens=[3, 2, 3], H_I=4, d_I=32)
+    case = W.generate(spec, seed=405)
+    case.k_I[...] = 0x3F80  # bf16 1.0
+    n_sel = 2
+    idx, blocks = oracle.hierarchical_topk(case, n_sel=n_sel)
+    short_rows = 0
+    for t in range(spec.T):
+        n = int(case.q_pos[t]) + 1
+        nb = min(n_sel, (n + 63) // 64)
+        assert blocks[t].tolist() == list(range(nb)) + [-1] * (n_sel - nb)
+        m = min(spec.K, nb * 64, n)
+        short_rows += m < spec.K
+        assert idx[t].tolist() == list(range(m)) + [-1] * (spec.K - m)
+    assert short_rows == 3

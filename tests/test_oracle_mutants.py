@@ -107,3 +107,49 @@ def test_mutant_is_caught(name, tmp_path):
     finally:
         oracle._lib = saved
     assert caught, f"no pin caught mutant {name}"
+
+
+# The coarse -> fine composition of hierarchical selection is Python (oracle.hierarchical_topk over
+# the C indexer); its mutants are planted in a copy of that function's source.
+PY_MUTANTS = {
+    "hier_no_causal_cut": ("min((b + 1) * bs, n)", "(b + 1) * bs"),
+    "hier_fine_ties_to_higher": ("order = np.lexsort((pos, -sc))[: s.K]", "order = np.lexsort((-pos, -sc))[: s.K]"),
+    "hier_first_blocks_not_best": ("bl = np.sort(bidx[r][bidx[r] >= 0])", "bl = np.arange(min(n_sel, (n + bs - 1) // bs))"),
+    "hier_positions_in_score_order": ("chosen = np.sort(pos[order])", "chosen = pos[order]"),
+}
+
+HIER_PINS = [
+    lambda: [hier.test_hierarchical_matches_brute_force(m) for m in ("bf16", "bf16_kfp8", "mxfp8")],
+    hier.test_all_blocks_kept_reproduces_the_exact_topk,
+    hier.test_planted_block_is_chosen,
+    hier.test_equal_keys_take_the_lowest_blocks_and_positions,
+]
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_python_mutant_is_caught(name, monkeypatch):
+    import inspect
+    old, new = PY_MUTANTS[name]
+    src = inspect.getsource(oracle.hierarchical_topk)
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    ns = dict(vars(oracle))
+    exec(src.replace(old, new), ns)
+    monkeypatch.setattr(oracle, "hierarchical_topk", ns["hierarchical_topk"])
+    caught = []
+    for fn in HIER_PINS:
+        try:
+            fn()
+        except (AssertionError, IndexError, ValueError):
+            caught.append(getattr(fn, "__name__", "lambda"))
+    assert caught, f"no pin caught mutant {name}"
+
+
+def test_python_mutant_harness_control(monkeypatch):
+    """An unmodified copy of the function, made the same way, passes every pin (so a caught
+    mutant is caught by its mutation, not by the copying)."""
+    import inspect
+    ns = dict(vars(oracle))
+    exec(inspect.getsource(oracle.hierarchical_topk), ns)
+    monkeypatch.setattr(oracle, "hierarchical_topk", ns["hierarchical_topk"])
+    for fn in HIER_PINS:
+        fn()
