@@ -107,3 +107,23 @@ def test_equal_keys_take_the_lowest_blocks_and_positions():
         short_rows += m < spec.K
         assert idx[t].tolist() == list(range(m)) + [-1] * (spec.K - m)
     assert short_rows == 3
+
+
+def test_block_past_the_row_is_never_chosen():
+    """Every row has the same query and block 4 (positions 256..299) is given keys aligned with it:
+    with n_sel = 1 the rows at positions 256.. choose block 4, and the rows before it, for which
+    that block lies past their causal limit, choose another."""
+    spec = small_spec("bf16", [300], 16, new_tokens=[100], H_I=4, d_I=32)
+    case = W.generate(spec, seed=406)
+    case.q_I[:] = case.q_I[0]
+    case.w[:] = case.w[0]
+    u = (case.w[0][:, None].astype(np.float64) * np_bf16(case.q_I[0])).sum(0)
+    u /= np.linalg.norm(u)
+    blk = int(case.block_table[0, 4])
+    case.k_I[blk] = W.to_bf16_bits((np_bf16(case.k_I[blk]) + 20.0 * u).astype(np.float32))
+    idx, blocks = oracle.hierarchical_topk(case, n_sel=1)
+    pos = case.q_pos.astype(int)
+    assert np.all(blocks[pos >= 256, 0] == 4)
+    assert np.all(blocks[pos < 256, 0] <= pos[pos < 256] // 64)
+    assert np.all(idx[pos < 256] < 256)
+    assert (pos < 256).sum() == 56 and (pos >= 256).sum() == 44

@@ -109,13 +109,20 @@ def test_mutant_is_caught(name, tmp_path):
     assert caught, f"no pin caught mutant {name}"
 
 
-# The coarse -> fine composition of hierarchical selection is Python (oracle.hierarchical_topk over
-# the C indexer); its mutants are planted in a copy of that function's source.
+# The coarse -> fine composition of hierarchical selection is Python (oracle.summary_case and
+# oracle.hierarchical_topk over the C indexer); its mutants are planted in a copy of one
+# function's source, which replaces that function in the module.
 PY_MUTANTS = {
-    "hier_no_causal_cut": ("min((b + 1) * bs, n)", "(b + 1) * bs"),
-    "hier_fine_ties_to_higher": ("order = np.lexsort((pos, -sc))[: s.K]", "order = np.lexsort((-pos, -sc))[: s.K]"),
-    "hier_first_blocks_not_best": ("bl = np.sort(bidx[r][bidx[r] >= 0])", "bl = np.arange(min(n_sel, (n + bs - 1) // bs))"),
-    "hier_positions_in_score_order": ("chosen = np.sort(pos[order])", "chosen = pos[order]"),
+    "hier_no_causal_cut": ("hierarchical_topk", "min((b + 1) * bs, n)", "(b + 1) * bs"),
+    "hier_fine_ties_to_higher": ("hierarchical_topk", "order = np.lexsort((pos, -sc))[: s.K]",
+                                 "order = np.lexsort((-pos, -sc))[: s.K]"),
+    "hier_first_blocks_not_best": ("hierarchical_topk", "bl = np.sort(bidx[r][bidx[r] >= 0])",
+                                   "bl = np.arange(min(n_sel, (n + bs - 1) // bs))"),
+    "hier_positions_in_score_order": ("hierarchical_topk", "chosen = np.sort(pos[order])", "chosen = pos[order]"),
+    "hier_coarse_sees_next_block": ("summary_case", "q_pos=(case.q_pos // bs).astype(np.int32)",
+                                    "q_pos=(case.q_pos // bs + 1).astype(np.int32)"),
+    "hier_coarse_block_rounded_up": ("summary_case", "q_pos=(case.q_pos // bs).astype(np.int32)",
+                                     "q_pos=np.minimum((case.q_pos + bs - 1) // bs, lens[case.q_seq] - 1).astype(np.int32)"),
 }
 
 HIER_PINS = [
@@ -123,33 +130,38 @@ HIER_PINS = [
     hier.test_all_blocks_kept_reproduces_the_exact_topk,
     hier.test_planted_block_is_chosen,
     hier.test_equal_keys_take_the_lowest_blocks_and_positions,
+    hier.test_block_past_the_row_is_never_chosen,
 ]
+
+
+def _patched(monkeypatch, fn_name: str, old: str = "", new: str = ""):
+    """Replaces oracle.<fn_name> with a copy of its source (with old -> new), compiled against the
+    module's globals, so the module's other functions call the copy."""
+    import inspect
+    src = inspect.getsource(getattr(oracle, fn_name))
+    if old:
+        assert src.count(old) == 1, f"mutation anchor {old!r} not found exactly once"
+    ns = dict(vars(oracle))
+    exec(src.replace(old, new) if old else src, ns)
+    monkeypatch.setattr(oracle, fn_name, ns[fn_name])
 
 
 @pytest.mark.parametrize("name", sorted(PY_MUTANTS))
 def test_python_mutant_is_caught(name, monkeypatch):
-    import inspect
-    old, new = PY_MUTANTS[name]
-    src = inspect.getsource(oracle.hierarchical_topk)
-    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
-    ns = dict(vars(oracle))
-    exec(src.replace(old, new), ns)
-    monkeypatch.setattr(oracle, "hierarchical_topk", ns["hierarchical_topk"])
+    _patched(monkeypatch, *PY_MUTANTS[name])
     caught = []
     for fn in HIER_PINS:
         try:
             fn()
-        except (AssertionError, IndexError, ValueError):
+        except (AssertionError, IndexError, RuntimeError, ValueError):
             caught.append(getattr(fn, "__name__", "lambda"))
     assert caught, f"no pin caught mutant {name}"
 
 
-def test_python_mutant_harness_control(monkeypatch):
+@pytest.mark.parametrize("fn_name", ["hierarchical_topk", "summary_case"])
+def test_python_mutant_harness_control(fn_name, monkeypatch):
     """An unmodified copy of the function, made the same way, passes every pin (so a caught
     mutant is caught by its mutation, not by the copying)."""
-    import inspect
-    ns = dict(vars(oracle))
-    exec(inspect.getsource(oracle.hierarchical_topk), ns)
-    monkeypatch.setattr(oracle, "hierarchical_topk", ns["hierarchical_topk"])
+    _patched(monkeypatch, fn_name)
     for fn in HIER_PINS:
         fn()
